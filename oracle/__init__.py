@@ -1,0 +1,153 @@
+"""Plain float64 CPU oracle for batched speculative verification (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package. The CUDA library never touches it, and it never touches
+the CUDA library: the two share no code. The arithmetic lives in ``sv_oracle.c``
+(sequential float64 loops, one element at a time); this module compiles it with
+gcc and marshals numpy arrays through ctypes.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+(brute-force output distribution at small V, greedy argmax, q == p, closed-form
+acceptance rate, hand-computed golden cases, schedule invariants and brute force).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_ACCEPT_TIE = 1
+FLAG_CDF_EDGE = 2
+FLAG_TINY_PROB = 4
+FLAG_SMALL_RESIDUAL = 8
+FLAG_INVALID = 16
+NEAR_TIE_MASK = FLAG_ACCEPT_TIE | FLAG_CDF_EDGE | FLAG_TINY_PROB | FLAG_SMALL_RESIDUAL
+
+OK, ERR_ARG, ERR_INPUT = 0, -1, -5
+
+
+def build(force: bool = False) -> str:
+    """Compile sv_oracle.c into liboracle.so (plain C, -O2, OpenMP over requests)."""
+    with _lock:
+        if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+        ):
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path):
+    """Open a compiled oracle and declare its signatures."""
+    lib = ctypes.CDLL(path)
+    vp, i32p, f64p, f32p = (ctypes.c_void_p,) * 4
+    lib.oracle_schedule.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                    ctypes.c_longlong, i32p, f64p, i32p]
+    lib.oracle_schedule.restype = ctypes.c_int
+    common = [vp, vp, ctypes.c_int, i32p, i32p]
+    tail = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    outs = [i32p, i32p, f64p, f64p, i32p, ctypes.c_int]
+    lib.oracle_verify.argtypes = common + [f32p] + tail + [ctypes.c_float] + outs
+    lib.oracle_verify.restype = ctypes.c_int
+    lib.oracle_verify_u64.argtypes = common + [f64p] + tail + [ctypes.c_double] + outs
+    lib.oracle_verify_u64.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(_LIB_PATH)
+    return _lib
+
+
+def build_variant(source_text: str, path: str):
+    """Compile a modified copy of the oracle source to ``path`` and open it. Used only
+    by the tests that plant a mistake in the oracle to show that the pins catch it."""
+    src = path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", path,
+                    "-lm"], check=True)
+    return _bind(path)
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def schedule(conf, tau: float, token_budget: int, lib=None):
+    """Confidence schedule. conf: [B,K] float32 in [0,1].
+
+    Returns dict(out_len [B] int32, surv [B,K] float64, l0 [B] int32, status int).
+    """
+    conf = np.ascontiguousarray(conf, dtype=np.float32)
+    B, K = conf.shape
+    out_len = np.zeros(B, np.int32)
+    surv = np.zeros((B, K), np.float64)
+    l0 = np.zeros(B, np.int32)
+    rc = (lib or _load()).oracle_schedule(_ptr(conf), B, K, float(tau), int(token_budget),
+                                          _ptr(out_len), _ptr(surv), _ptr(l0))
+    return {"out_len": out_len, "surv": surv, "l0": l0, "status": rc}
+
+
+def _logits(a):
+    """numpy float32 -> (array, dtype 0); numpy uint16/int16 bf16 bits -> (array, 1)."""
+    if a is None:
+        return None, None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, 0
+    if a.dtype in (np.uint16, np.int16):
+        return a.view(np.uint16), 1
+    raise TypeError(f"logits must be float32 or bf16 bits (uint16), got {a.dtype}")
+
+
+def verify(target, draft, draft_tok, verify_len, uniforms, temperature: float,
+           nthreads: int = 1, diag: bool = True, u64: bool = False, lib=None):
+    """Batched verification.
+
+    target [B,K+1,V] and draft [B,K,V]: float32, or bf16 given as uint16 bit patterns.
+    draft_tok [B,K] int32, verify_len [B] int32, uniforms [B,K+1] float32 (float64 when
+    ``u64``; only the brute-force tests use that). Returns dict(out_tok, out_accepted,
+    p, q, flags, status).
+    """
+    t, dt = _logits(target)
+    d, dd = _logits(draft)
+    if d is not None and dd != dt:
+        raise TypeError("target and draft logits must share a dtype")
+    B, K1, V = t.shape
+    K = K1 - 1
+    tok = np.ascontiguousarray(draft_tok, dtype=np.int32)
+    vlen = np.ascontiguousarray(verify_len, dtype=np.int32)
+    u = None
+    if uniforms is not None:
+        u = np.ascontiguousarray(uniforms, dtype=np.float64 if u64 else np.float32)
+    out_tok = np.zeros((B, K + 1), np.int32)
+    out_acc = np.zeros(B, np.int32)
+    p = np.zeros((B, K), np.float64) if diag else None
+    q = np.zeros((B, K), np.float64) if diag else None
+    flags = np.zeros(B, np.int32)
+    lib = lib or _load()
+    fn = lib.oracle_verify_u64 if u64 else lib.oracle_verify
+    rc = fn(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(vlen), _ptr(u), B, K, V, float(temperature),
+            _ptr(out_tok), _ptr(out_acc), _ptr(p), _ptr(q), _ptr(flags), int(nthreads))
+    return {"out_tok": out_tok, "out_accepted": out_acc, "p": p, "q": q, "flags": flags,
+            "status": rc}

@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for batched speculative verification.
+
+This module is shared by the tests, the benchmark and the smoke check; it feeds the
+same tensors to the CUDA library and to the CPU oracle. It holds none of the
+method's arithmetic: no softmax, no acceptance test, no survival product. Draft
+tokens are drawn from softmax(draft/T) with the Gumbel-max construction
+(argmax of logits/T plus Gumbel noise), which needs no normaliser.
+
+Workload shapes follow the DSpark pages' serving settings: Qwen3-8B's vocabulary of
+151,936 entries and DeepSeek-V4's 129,280, 1-512 concurrent requests, draft blocks of
+4-16 tokens. No benchmark dataset is involved; every value is drawn here from a seed.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+QWEN3_VOCAB = 151_936
+DSV4_VOCAB = 129_280
+
+_CHUNK_ELEMS = 1 << 26  # bound on the temporaries of one generation chunk
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def verify_inputs(B, K, V, *, dtype=torch.bfloat16, temperature=1.0, target_sigma=3.0,
+                  draft_sigma=1.0, peak_prob=0.0, peak_height=12.0, verify_len="full",
+                  seed=0, device="cpu"):
+    """Inputs of one verification call.
+
+    target [B,K+1,V] ~ N(0, target_sigma^2); each target row independently gets
+    +peak_height at one uniform index with probability peak_prob. draft [B,K,V] =
+    target rows 0..K-1 (before rounding) + N(0, sigma_b^2), sigma_b = draft_sigma (a
+    scalar or a length-B sequence). Both are rounded to ``dtype``. draft_tok[b,k] is a
+    sample of softmax(draft[b,k]/T) from the rounded draft logits (argmax at T == 0).
+    verify_len: "full" (= K), "uniform" (U{1..K}), or an int sequence of length B.
+    uniforms [B,K+1] ~ U[0,1) float32.
+    """
+    g = _gen(device, seed)
+    sig = torch.as_tensor(draft_sigma, dtype=torch.float32).reshape(-1)
+    if sig.numel() == 1:
+        sig = sig.expand(B)
+    assert sig.numel() == B
+    sig = sig.to(device)
+    target = torch.empty((B, K + 1, V), dtype=dtype, device=device)
+    draft = torch.empty((B, K, V), dtype=dtype, device=device)
+    tok = torch.empty((B, K), dtype=torch.int32, device=device)
+    rb = max(1, _CHUNK_ELEMS // ((K + 1) * V))
+    for b0 in range(0, B, rb):
+        b1 = min(B, b0 + rb)
+        n = b1 - b0
+        t32 = torch.randn((n, K + 1, V), generator=g, device=device) * target_sigma
+        if peak_prob > 0.0:
+            hit = torch.rand((n, K + 1), generator=g, device=device) < peak_prob
+            where = torch.randint(0, V, (n, K + 1), generator=g, device=device)
+            t32.scatter_add_(2, where.unsqueeze(-1), (hit.float() * peak_height).unsqueeze(-1))
+        noise = torch.randn((n, K, V), generator=g, device=device) * sig[b0:b1].view(n, 1, 1)
+        d32 = t32[:, :K, :] + noise
+        del noise
+        target[b0:b1] = t32.to(dtype)
+        draft[b0:b1] = d32.to(dtype)
+        del t32, d32
+        d = draft[b0:b1].float()
+        if temperature > 0.0:
+            e = torch.rand((n, K, V), generator=g, device=device).clamp_min_(1e-30)
+            gumbel = -torch.log(-torch.log(e))
+            del e
+            tok[b0:b1] = torch.argmax(d / temperature + gumbel, dim=-1).to(torch.int32)
+            del gumbel
+        else:
+            tok[b0:b1] = torch.argmax(d, dim=-1).to(torch.int32)
+        del d
+    if isinstance(verify_len, str) and verify_len == "full":
+        vlen = torch.full((B,), K, dtype=torch.int32, device=device)
+    elif isinstance(verify_len, str) and verify_len == "uniform":
+        vlen = torch.randint(1, K + 1, (B,), generator=g, device=device).to(torch.int32)
+    else:
+        vlen = torch.as_tensor(list(verify_len), dtype=torch.int32).to(device)
+        assert vlen.numel() == B
+    uniforms = torch.rand((B, K + 1), generator=g, device=device, dtype=torch.float32)
+    return {"target": target, "draft": draft, "draft_tok": tok, "verify_len": vlen,
+            "uniforms": uniforms}
+
+
+def confidences(B, K, *, a=8.0, b=2.0, decay=0.93, seed=0):
+    """Per-position draft confidences c[b,k] = Beta(a,b) draw * decay**(k+1), float32.
+
+    Positions are 1-based in the exponent (the first position is scaled by decay once).
+    """
+    rng = np.random.default_rng(int(seed))
+    draws = rng.beta(a, b, size=(B, K))
+    scale = decay ** np.arange(1, K + 1, dtype=np.float64)
+    return torch.from_numpy((draws * scale[None, :]).astype(np.float32))
+
+
+def to_oracle(t):
+    """torch tensor -> numpy array in the form the oracle takes (bf16 as uint16 bits)."""
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+# ----------------------------------------------------------------------------------
+# Named workloads. Each returns (kwargs for verify_inputs, extra) for a seed.
+# ----------------------------------------------------------------------------------
+
+def tiny_fp32(seed=0, device="cpu"):
+    """B=4, K=4, V=1024, fp32; target N(0,2^2), draft noise N(0,0.5^2); T=1; L=K."""
+    return verify_inputs(4, 4, 1024, dtype=torch.float32, temperature=1.0, target_sigma=2.0,
+                         draft_sigma=0.5, seed=seed, device=device)
+
+
+def qwen3_verify(temperature, seed=0, device="cpu", B=32, K=8):
+    """B=32, K=8, V=151,936 bf16; target N(0,3^2) with rows peaked (+12) w.p. 0.2;
+    draft noise N(0,1); L=K."""
+    return verify_inputs(B, K, QWEN3_VOCAB, dtype=torch.bfloat16, temperature=temperature,
+                         target_sigma=3.0, draft_sigma=1.0, peak_prob=0.2, peak_height=12.0,
+                         seed=seed, device=device)
+
+
+def ragged_sigmas(B):
+    """Draft noise 0.5 for the first half of the requests, 1.5 for the second."""
+    return [0.5 if b < B // 2 else 1.5 for b in range(B)]
+
+
+def ragged_schedule(seed=0, device="cpu", B=256, K=16):
+    """B=256, K=16, V=151,936 bf16, T=1; confidences Beta(8,2)*0.93^k; draft noise 0.5
+    for the first half of the requests and 1.5 for the second. The verify lengths come
+    from the schedule, so the caller supplies them; the inputs here carry L=K."""
+    inp = verify_inputs(B, K, QWEN3_VOCAB, dtype=torch.bfloat16, temperature=1.0,
+                        target_sigma=3.0, draft_sigma=ragged_sigmas(B), seed=seed,
+                        device=device)
+    inp["conf"] = confidences(B, K, seed=seed).to(device)
+    return inp
+
+
+def large_batch(seed=0, device="cpu", B=512):
+    """B=512, K=8, V=129,280 bf16, T=0.7; target N(0,3^2), draft noise N(0,1);
+    verify lengths U{1..8}."""
+    return verify_inputs(B, 8, DSV4_VOCAB, dtype=torch.bfloat16, temperature=0.7,
+                         target_sigma=3.0, draft_sigma=1.0, verify_len="uniform", seed=seed,
+                         device=device)
+
+
+def sweep_point(B, K, seed=0, device="cpu"):
+    """Roofline sweep point: V=151,936 bf16, T=1, draft noise 1.0, full-length blocks."""
+    return verify_inputs(B, K, QWEN3_VOCAB, dtype=torch.bfloat16, temperature=1.0,
+                         target_sigma=3.0, draft_sigma=1.0, seed=seed, device=device)
+
+
+SWEEP_B = (1, 4, 8, 16, 32, 64, 128)
+SWEEP_K = (4, 8, 16)
+
+
+def logit_bytes(verify_len, V, elem_bytes, greedy=False):
+    """Algorithmic logit bytes one verification call must read: per request (L+1)
+    target rows, plus L draft rows unless greedy."""
+    L = torch.as_tensor(verify_len).to(torch.int64).clamp_min(0)
+    rows = (L + 1) if greedy else (2 * L + 1)
+    return int(rows.sum().item()) * V * elem_bytes
+

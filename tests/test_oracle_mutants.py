@@ -1,0 +1,77 @@
+"""Plant plausible mistakes in a copy of the oracle (CPU only) and check that the pins
+fail on each. This shows the pins can tell a right oracle from a wrong one."""
+import os
+
+import numpy as np
+import pytest
+
+from test_oracle_verify import lossless_error
+
+MUTANTS = {
+    "residual sign q-p": (
+        "r[v] = p[v] - q[v] > 0.0 ? p[v] - q[v] : 0.0;",
+        "r[v] = q[v] - p[v] > 0.0 ? q[v] - p[v] : 0.0;"),
+    "accept ratio inverted": ("if (uk * qx < px) {", "if (uk * px < qx) {"),
+    "temperature multiplies": (
+        "p[v] = exp((logit_at(base, dtype, off + (size_t)v) - M) / T);",
+        "p[v] = exp((logit_at(base, dtype, off + (size_t)v) - M) * T);"),
+    "bonus from the wrong row": (
+        "row_softmax(tgt, dtype, (trow0 + L) * (size_t)V, V, T, Mt[L], p);",
+        "row_softmax(tgt, dtype, (trow0 + L - 1) * (size_t)V, V, T, Mt[L - 1], p);"),
+    "terminal sample reuses the accept uniform": (
+        "const double uK = u[(size_t)b * (K + 1) + K];",
+        "const double uK = u[(size_t)b * (K + 1) + k];"),
+    "inverse CDF one bucket late": ("            return v;\n", "            return v + 1 < V ? v + 1 : v;\n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_lossless_pin_catches(oracle_mod, tmp_path, name):
+    old, new = MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    T = 0.5 if "temperature" in name else 1.0
+    assert lossless_error(oracle_mod, T, 0, lib=lib) > 1e-3
+
+
+SCHED_MUTANTS = {
+    "strict tau comparison": ("if (run >= (double)tau) n = k + 1;", "if (run > (double)tau) n = k + 1;"),
+    "no floor of one": ("if (n < 1) n = 1;", "if (n < 0) n = 1;"),
+    "tie-break on k reversed": ("if (a->k != b->k) return a->k < b->k ? -1 : 1;",
+                                "if (a->k != b->k) return a->k > b->k ? -1 : 1;"),
+    "survival ascending": ("if (a->s != b->s) return a->s > b->s ? -1 : 1;",
+                           "if (a->s != b->s) return a->s < b->s ? -1 : 1;"),
+    "floors never first": ("int floor_first = token_budget >= B;", "int floor_first = 0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCHED_MUTANTS))
+def test_schedule_pins_catch(oracle_mod, tmp_path, name):
+    import test_oracle_schedule as ts
+
+    old, new = SCHED_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+
+    class Shim:
+        def __getattr__(self, a):
+            return getattr(oracle_mod, a)
+
+        def schedule(self, conf, tau, budget):
+            return oracle_mod.schedule(conf, tau, budget, lib=lib)
+
+    shim = Shim()
+    failed = 0
+    tests = [lambda: ts.test_golden_variable_length_draft(shim),
+             lambda: ts.test_truncation_rule_of_the_guide_sketch(shim),
+             lambda: ts.test_tie_break_prefers_earlier_positions_then_lower_requests(shim)]
+    tests += [lambda s=s: ts.test_budget_trim_bruteforce(shim, s) for s in range(40)]
+    tests += [lambda s=s: ts.test_budget_invariants(shim, s) for s in range(20)]
+    for t in tests:
+        try:
+            t()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name
