@@ -1,0 +1,178 @@
+/*
+ * specverify.h -- C-ABI of libspecverify: batched, lossless verification of drafted
+ * token blocks, and the confidence schedule that sets how many drafted tokens of each
+ * request go to verification. GB300 (sm_103a) only.
+ *
+ * The method is DSpark's ("confidence-scheduled, semi-autoregressive speculative
+ * decoding"). Sources, cited by page title and section:
+ *  [DD] "DSpark Deep Dive: How DeepSeek Squeezed an 85% Speedup Out of Inference
+ *       Without Touching a Single Model Weight" (fuyuan7.com)
+ *  [GD] "DSpark Guide: Confidence Speculative Decoding in LLMs" (aifetchly)
+ *  [TP] perchy.ai "Technology", engine 01, "Verified by the target"
+ *
+ * Conventions for every call
+ *  - Pointers named *_d are DEVICE pointers owned by the caller; tensors are dense,
+ *    row-major, and aligned to their element size. Nothing is allocated per call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL means
+ *    the legacy default stream). A return of SV_OK means the work was enqueued.
+ *  - Arguments the host can check are checked before anything is enqueued; a bad
+ *    argument returns SV_ERR_ARG / SV_ERR_SHAPE / SV_ERR_DTYPE / SV_ERR_WORKSPACE
+ *    and enqueues nothing. Errors in device-resident data (NaN or +inf logits, a
+ *    row of -inf, a token outside [0,V), a verify length outside [0,K], a uniform
+ *    outside [0,1), a confidence outside [0,1]) cannot be seen by the host: the
+ *    kernels mark the affected request (out_accepted = -1, its out_tok row = -1; or
+ *    out_len = 0 for the schedule) and set a sticky bit in the workspace status
+ *    word, readable with sv_get_status. Kernels never trap.
+ *  - A workspace serves one call at a time: calls that share a workspace must be
+ *    ordered on one stream. Calls on different workspaces may run concurrently.
+ *  - Grids depend only on (B, K, V, dtype, greedy), and device-resident lengths are
+ *    read on the device, so a call sequence can be captured in a CUDA graph and
+ *    replayed with new data in the same buffers.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sv_status {
+    SV_OK = 0,
+    SV_ERR_ARG = -1,          /* null pointer, non-finite or out-of-range scalar */
+    SV_ERR_SHAPE = -2,        /* B, K or V outside the supported range */
+    SV_ERR_DTYPE = -3,        /* unknown sv_dtype */
+    SV_ERR_CUDA = -4,         /* a CUDA runtime call failed (launch, attribute query) */
+    SV_ERR_DEVICE_INPUT = -5, /* (status word) invalid device-resident data was seen */
+    SV_ERR_TIMEOUT = -6,      /* (status word) a bounded device wait gave up */
+    SV_ERR_WORKSPACE = -7     /* workspace missing, too small or misaligned */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Supported sizes. */
+#define SV_MAX_B 4096         /* requests per verify call */
+#define SV_MAX_K 32           /* drafted positions per request */
+#define SV_MAX_V (1 << 24)    /* vocabulary entries */
+#define SV_MAX_SCHED_B 8192   /* requests per schedule call */
+#define SV_MAX_SCHED_BK 16384 /* B*K per schedule call */
+
+/*
+ * sv_workspace_bytes: size of the device workspace needed by sv_schedule and
+ * sv_verify for shapes up to (B, K, V), for either dtype (0 for an unsupported
+ * shape). The caller allocates it (256-byte aligned) and zeroes it once with
+ * sv_workspace_init before first use; every call leaves it ready for the next call,
+ * of any shape that fits, including after device-side errors.
+ */
+size_t sv_workspace_bytes(int B, int K, int V);
+
+/* Zero a workspace on `stream` (one cudaMemsetAsync). */
+sv_status sv_workspace_init(void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_schedule: per-request verify lengths from per-position draft confidences.
+ * [GD "2. Confidence-Scheduled Dynamic Verification"; DD "Variable-Length Drafts",
+ *  "The Optimization Logic", "GPU-Resident Scheduling", "The Full Scheduling Pipeline"]
+ *
+ *  conf_d     [B,K] float32, c_{b,k} in [0,1]: calibrated probability that drafted
+ *             token k of request b is accepted.
+ *  tau        survival threshold in [0,1].
+ *  token_budget  global cap (>= 0) on sum_b out_len[b] (drafted tokens sent to
+ *             verification; the +1 target row per request is not counted).
+ *  out_len_d  [B] int32 result L_b.
+ *
+ *  1. Prefix survival S_{b,k} = c_{b,0} * ... * c_{b,k}, computed left to right in
+ *     float64 (the product of per-position survival, [GD] C_k).
+ *  2. L0_b = max(1, #{k : S_{b,k} >= tau}) (truncate at the first C_k < tau, keep
+ *     at least one token [GD "Hands-On Implementation"]; 1 <= L <= K [DD]).
+ *  3. If sum_b L0_b > token_budget, keep the token_budget highest-ranked positions
+ *     among the tau-survivors and drop the rest, lowest marginal survival first.
+ *     Rank: guaranteed floor positions (b,0) first when token_budget >= B; then S
+ *     descending, position k ascending, request b ascending. When token_budget < B
+ *     the floor positions compete like the others and a request can get L_b = 0.
+ *     Kept positions always form a prefix of each request's block.
+ *  One CTA; a few microseconds. Device errors: a confidence outside [0,1] or NaN
+ *  sets SV_ERR_DEVICE_INPUT in the status word and writes out_len = 0 everywhere.
+ *  Limits: 1 <= K <= SV_MAX_K, 0 <= B <= SV_MAX_SCHED_B, B*K <= SV_MAX_SCHED_BK.
+ *  The workspace needs only its 256-byte header (any size from sv_workspace_bytes).
+ */
+sv_status sv_schedule(const float *conf_d, int B, int K, float tau, int token_budget,
+                      int32_t *out_len_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_verify: standard speculative rejection sampling over a batch of drafted blocks.
+ * [DD "Speculative Decoding From First Principles" / "The Speculative Decoding
+ *  Solution"; GD "1. The Mathematics of Suffix Decay"; TP "Verified by the target"]
+ *
+ *  target_d   [B, K+1, V] target logits (dtype), row k = target prediction for the
+ *             position of drafted token k; row L_b is the bonus position.
+ *  draft_d    [B, K, V] draft logits (dtype). Not read when temperature == 0 (may be
+ *             NULL then).
+ *  draft_tok_d [B, K] int32 drafted tokens x_{b,k}.
+ *  verify_len_d [B] int32 L_b in [0, K] (for example sv_schedule's out_len; rows
+ *             past L_b are never read, so only the verified prefix must hold data).
+ *  uniforms_d [B, K+1] float32 in [0,1): u_{b,k} (k < K) drives the accept test of
+ *             drafted token k; u_{b,K} drives the terminal sample. Not read when
+ *             temperature == 0 (may be NULL then).
+ *  temperature  T >= 0. p_k = softmax(target_k / T), q_k = softmax(draft_k / T).
+ *             T == 0 selects greedy verification; otherwise 1e-6 <= T <= 1e6.
+ *  out_tok_d  [B, K+1] int32: x_{b,0..j-1}, then the terminal token y, then -1.
+ *  out_accepted_d [B] int32: j, the number of accepted drafted tokens (or -1).
+ *
+ *  Per request: accept x_k iff u_k * q_k(x_k) < p_k(x_k), i.e. with probability
+ *  min(1, p/q); j = first rejected position, or L_b. If j < L_b the terminal token
+ *  is the inverse-CDF sample of max(0, p_j - q_j) (normalised) at u_{b,K}: the
+ *  smallest v with u*Z < r_0 + ... + r_v; if that residual has no mass left the
+ *  sample is taken from p_j instead. If j == L_b it is the inverse-CDF sample of
+ *  p_{L_b} at u_{b,K} (bonus token). At T == 0: accept iff x_k is the lowest-index
+ *  argmax of target row k, and the terminal token is the argmax of row j. The
+ *  emitted tokens follow the target distribution exactly.
+ *  Arithmetic: fp32 softmax statistics; the terminal inverse CDF is accumulated in
+ *  float64 over compensated fp32 sums.
+ *  Limits: 0 <= B <= SV_MAX_B, 1 <= K <= SV_MAX_K, 1 <= V <= SV_MAX_V.
+ */
+sv_status sv_verify(const void *target_d, const void *draft_d, sv_dtype dtype,
+                    const int32_t *draft_tok_d, const int32_t *verify_len_d,
+                    const float *uniforms_d, int B, int K, int V, float temperature,
+                    int32_t *out_tok_d, int32_t *out_accepted_d, void *ws_d,
+                    size_t ws_bytes, void *stream);
+
+/*
+ * sv_verify_diag: sv_verify plus diagnostics (same decisions, same arguments).
+ *  out_p_d, out_q_d [B, K] float32 or NULL: p_k(x_k) and q_k(x_k) for k < L_b
+ *           (NaN for k >= L_b, and at T == 0).
+ *  accept_count_d [K] uint32 or NULL: for each position k, atomically adds the
+ *           number of requests whose drafted token k was accepted.
+ *  tested_count_d [K] uint32 or NULL: adds the number of requests that tested
+ *           position k (k <= j and k < L_b). accept/tested is the per-position
+ *           acceptance rate the online calibration of [DD "Online Calibration"]
+ *           compares against the predicted confidence.
+ */
+sv_status sv_verify_diag(const void *target_d, const void *draft_d, sv_dtype dtype,
+                         const int32_t *draft_tok_d, const int32_t *verify_len_d,
+                         const float *uniforms_d, int B, int K, int V, float temperature,
+                         int32_t *out_tok_d, int32_t *out_accepted_d, float *out_p_d,
+                         float *out_q_d, uint32_t *accept_count_d, uint32_t *tested_count_d,
+                         void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_get_status: wait for `stream`, then read the sticky status word of the
+ * workspace into *status_out (SV_OK, SV_ERR_DEVICE_INPUT or SV_ERR_TIMEOUT; the most
+ * severe seen since the last clear). clear != 0 resets it to SV_OK.
+ * Returns SV_OK or the error of the copy.
+ */
+sv_status sv_get_status(void *ws_d, void *stream, int clear, int32_t *status_out);
+
+/* Static string for a status code. */
+const char *sv_status_string(sv_status s);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,175 @@
+"""Python binding of libspecverify (GB300 / sm_103a).
+
+Argument marshalling only: every step of the schedule and of verification runs in the
+CUDA kernels of libspecverify.so, called through its C-ABI (include/specverify.h).
+PyTorch provides device memory and streams. There is no CPU fallback: without the
+built library, or without a CUDA device, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+_lib = None
+
+SV_OK, SV_ERR_ARG, SV_ERR_SHAPE, SV_ERR_DTYPE = 0, -1, -2, -3
+SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE = -4, -5, -6, -7
+SV_F32, SV_BF16 = 0, 1
+SV_MAX_B, SV_MAX_K = 4096, 32
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Open libspecverify.so (building it first when it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libspecverify.so is not built; run __graft_entry__.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.sv_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.sv_workspace_bytes.restype = sz
+    lib.sv_workspace_init.argtypes = [vp, sz, vp]
+    lib.sv_workspace_init.restype = i32
+    lib.sv_schedule.argtypes = [vp, i32, i32, f32, i32, vp, vp, sz, vp]
+    lib.sv_schedule.restype = i32
+    lib.sv_verify.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
+    lib.sv_verify.restype = i32
+    lib.sv_verify_diag.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp,
+                                   vp, vp, vp, sz, vp]
+    lib.sv_verify_diag.restype = i32
+    lib.sv_get_status.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.sv_get_status.restype = i32
+    lib.sv_status_string.argtypes = [i32]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_version.argtypes = []
+    lib.sv_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().sv_status_string(int(code)).decode()
+
+
+def _check(fn, code):
+    if code != SV_OK:
+        raise SpecVerifyError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+class Workspace:
+    """Device workspace for shapes up to (B, K, V); zeroed once at creation."""
+
+    def __init__(self, B, K, V, device=None, stream=None):
+        self.nbytes = int(load().sv_workspace_bytes(int(B), int(K), int(V)))
+        if self.nbytes == 0:
+            raise ValueError(f"unsupported workspace shape B={B} K={K} V={V}")
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buf.data_ptr()) % 256
+        self.t = self.buf[off: off + self.nbytes]
+        _check("sv_workspace_init",
+               load().sv_workspace_init(_ptr(self.t), self.nbytes, _stream(stream)))
+
+    def status(self, stream=None, clear=False) -> int:
+        out = ctypes.c_int32(0)
+        _check("sv_get_status", load().sv_get_status(_ptr(self.t), _stream(stream), int(clear),
+                                                     ctypes.byref(out)))
+        return int(out.value)
+
+
+def sv_schedule(conf, tau, token_budget, ws: Workspace, out_len=None, stream=None):
+    """Verify lengths [B] int32 from confidences [B,K] float32 (see specverify.h)."""
+    conf = _dev(conf, "conf", torch.float32)
+    B, K = conf.shape
+    if out_len is None:
+        out_len = torch.empty(B, dtype=torch.int32, device=conf.device)
+    _dev(out_len, "out_len", torch.int32)
+    _check("sv_schedule", load().sv_schedule(_ptr(conf), B, K, float(tau), int(token_budget),
+                                             _ptr(out_len), _ptr(ws.t), ws.nbytes,
+                                             _stream(stream)))
+    return out_len
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise ValueError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def sv_verify(target, draft, draft_tok, verify_len, uniforms, temperature, ws: Workspace,
+              out_tok=None, out_accepted=None, diag=False, accept_count=None,
+              tested_count=None, stream=None):
+    """Rejection-sampling verification (see specverify.h).
+
+    target [B,K+1,V], draft [B,K,V] (bf16 or fp32; draft/uniforms may be None at T=0),
+    draft_tok [B,K] int32, verify_len [B] int32, uniforms [B,K+1] float32.
+    Returns (out_tok [B,K+1], out_accepted [B]) and, with diag=True, also (p, q) [B,K].
+    """
+    target = _dev(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    draft = _dev(draft, "draft", target.dtype)
+    draft_tok = _dev(draft_tok, "draft_tok", torch.int32)
+    verify_len = _dev(verify_len, "verify_len", torch.int32)
+    uniforms = _dev(uniforms, "uniforms", torch.float32)
+    dev = target.device
+    if out_tok is None:
+        out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_accepted is None:
+        out_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    lib = load()
+    if diag or accept_count is not None or tested_count is not None:
+        p = torch.empty((B, K), dtype=torch.float32, device=dev) if diag else None
+        q = torch.empty((B, K), dtype=torch.float32, device=dev) if diag else None
+        rc = lib.sv_verify_diag(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tok),
+                                _ptr(verify_len), _ptr(uniforms), B, K, V, float(temperature),
+                                _ptr(out_tok), _ptr(out_accepted), _ptr(p), _ptr(q),
+                                _ptr(accept_count), _ptr(tested_count), _ptr(ws.t), ws.nbytes,
+                                _stream(stream))
+        _check("sv_verify_diag", rc)
+        return (out_tok, out_accepted, p, q) if diag else (out_tok, out_accepted)
+    rc = lib.sv_verify(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tok),
+                       _ptr(verify_len), _ptr(uniforms), B, K, V, float(temperature),
+                       _ptr(out_tok), _ptr(out_accepted), _ptr(ws.t), ws.nbytes, _stream(stream))
+    _check("sv_verify", rc)
+    return out_tok, out_accepted

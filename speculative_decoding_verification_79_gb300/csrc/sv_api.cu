@@ -1,0 +1,174 @@
+// sv_api.cu -- the C-ABI boundary of libspecverify: argument checks, workspace
+// layout, launches. Declarations and contracts are in include/specverify.h.
+#include <atomic>
+#include <cmath>
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+static int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t sv_workspace_bytes(int B, int K, int V) {
+  if (B < 0 || K < 1 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return 0;
+  return ws_layout(B > SV_MAX_B ? SV_MAX_B : B, K, V).total;
+}
+
+sv_status sv_workspace_init(void* ws_d, size_t ws_bytes, void* stream) {
+  if (!ws_d || ws_bytes < sizeof(WsHeader) || !aligned(ws_d, 256)) return SV_ERR_WORKSPACE;
+  if (cudaMemsetAsync(ws_d, 0, ws_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+sv_status sv_schedule(const float* conf_d, int B, int K, float tau, int token_budget,
+                      int32_t* out_len_d, void* ws_d, size_t ws_bytes, void* stream) {
+  if (B < 0 || B > SV_MAX_SCHED_B || K < 1 || K > SV_MAX_K || (long long)B * K > SV_MAX_SCHED_BK)
+    return SV_ERR_SHAPE;
+  if (!(tau >= 0.f && tau <= 1.f) || token_budget < 0) return SV_ERR_ARG;
+  if (!ws_d || ws_bytes < sizeof(WsHeader) || !aligned(ws_d, 256)) return SV_ERR_WORKSPACE;
+  if (B == 0) return SV_OK;
+  if (!conf_d || !out_len_d || !aligned(conf_d, 4) || !aligned(out_len_d, 4)) return SV_ERR_ARG;
+  const cudaError_t e =
+      launch_schedule(conf_d, B, K, tau, token_budget, out_len_d, static_cast<WsHeader*>(ws_d),
+                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dtype,
+                         const int32_t* draft_tok_d, const int32_t* verify_len_d,
+                         const float* uniforms_d, int B, int K, int V, float temperature,
+                         int32_t* out_tok_d, int32_t* out_accepted_d, float* out_p_d,
+                         float* out_q_d, uint32_t* accept_count_d, uint32_t* tested_count_d,
+                         void* ws_d, size_t ws_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B > SV_MAX_B || K < 1 || K > SV_MAX_K || V < 1 || V > SV_MAX_V)
+    return SV_ERR_SHAPE;
+  const bool greedy = temperature == 0.f;
+  if (!std::isfinite(temperature) || temperature < 0.f ||
+      (!greedy && (temperature < 1e-6f || temperature > 1e6f)))
+    return SV_ERR_ARG;
+  const WsLayout L = ws_layout(B, K, V);
+  if (!ws_d || !aligned(ws_d, 256) || ws_bytes < L.total) return SV_ERR_WORKSPACE;
+  if (B == 0) return SV_OK;
+  const size_t eb = dtype == SV_BF16 ? 2 : 4;
+  if (!target_d || !draft_tok_d || !verify_len_d || !out_tok_d || !out_accepted_d)
+    return SV_ERR_ARG;
+  if (!greedy && (!draft_d || !uniforms_d)) return SV_ERR_ARG;
+  if (!aligned(target_d, eb) || (draft_d && !aligned(draft_d, eb)) || !aligned(draft_tok_d, 4) ||
+      !aligned(verify_len_d, 4) || (uniforms_d && !aligned(uniforms_d, 4)) ||
+      !aligned(out_tok_d, 4) || !aligned(out_accepted_d, 4) || (out_p_d && !aligned(out_p_d, 4)) ||
+      (out_q_d && !aligned(out_q_d, 4)) || (accept_count_d && !aligned(accept_count_d, 4)) ||
+      (tested_count_d && !aligned(tested_count_d, 4)))
+    return SV_ERR_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return SV_ERR_CUDA;
+
+  unsigned char* ws = static_cast<unsigned char*>(ws_d);
+  VerifyArgs A;
+  A.tgt = target_d;
+  A.drf = draft_d;
+  A.tok = draft_tok_d;
+  A.vlen = verify_len_d;
+  A.uni = uniforms_d;
+  A.B = B;
+  A.K = K;
+  A.V = V;
+  {
+    const double ad = greedy ? 0.0 : 1.4426950408889634 / (double)temperature;
+    A.a = (float)ad;
+    A.a_lo = (float)(ad - (double)A.a);
+  }
+  A.P = pieces_per_row(V, (int)eb);
+  A.E = SLOT_BYTES / (int)eb;
+  A.R = resid_pieces(V, (int)eb);
+  A.E2 = SLOT_BYTES / 2 / (int)eb;
+  A.RS = L.RS;
+  A.Rmax = L.Rmax;
+  A.out_tok = out_tok_d;
+  A.out_acc = out_accepted_d;
+  A.out_p = out_p_d;
+  A.out_q = out_q_d;
+  A.acc_cnt = accept_count_d;
+  A.tst_cnt = tested_count_d;
+  A.hdr = reinterpret_cast<WsHeader*>(ws);
+  A.t_row = reinterpret_cast<uint32_t*>(ws + L.t_row);
+  A.t_req = reinterpret_cast<uint32_t*>(ws + L.t_req);
+  A.t_res = reinterpret_cast<uint32_t*>(ws + L.t_res);
+  A.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
+  A.part = reinterpret_cast<float2*>(ws + L.part);
+  A.rpart = reinterpret_cast<double*>(ws + L.rpart);
+
+  // One persistent CTA per SM, fewer when the batch cannot feed them all.
+  const long long max_pieces = (long long)B * (greedy ? K + 1 : 2 * K + 1) * A.P;
+  const long long want = (max_pieces + Q1_BATCH - 1) / Q1_BATCH;
+  const int grid = (int)(want < sms ? want : sms);
+  const cudaError_t e =
+      launch_verify(A, dtype == SV_BF16, greedy, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_verify(const void* target_d, const void* draft_d, sv_dtype dtype,
+                    const int32_t* draft_tok_d, const int32_t* verify_len_d,
+                    const float* uniforms_d, int B, int K, int V, float temperature,
+                    int32_t* out_tok_d, int32_t* out_accepted_d, void* ws_d, size_t ws_bytes,
+                    void* stream) {
+  return sv_verify_diag(target_d, draft_d, dtype, draft_tok_d, verify_len_d, uniforms_d, B, K, V,
+                        temperature, out_tok_d, out_accepted_d, nullptr, nullptr, nullptr,
+                        nullptr, ws_d, ws_bytes, stream);
+}
+
+sv_status sv_get_status(void* ws_d, void* stream, int clear, int32_t* status_out) {
+  if (!ws_d || !status_out) return SV_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, ws_d, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  *status_out = (bits & ST_TIMEOUT) ? SV_ERR_TIMEOUT
+                : (bits & ST_DEVICE_INPUT) ? SV_ERR_DEVICE_INPUT
+                                           : SV_OK;
+  if (clear) {
+    if (cudaMemsetAsync(ws_d, 0, sizeof(bits), st) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}
+
+const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_ARG: return "invalid argument";
+    case SV_ERR_SHAPE: return "unsupported shape";
+    case SV_ERR_DTYPE: return "unsupported dtype";
+    case SV_ERR_CUDA: return "CUDA runtime error";
+    case SV_ERR_DEVICE_INPUT: return "invalid device-resident input";
+    case SV_ERR_TIMEOUT: return "device wait timed out";
+    case SV_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+  }
+  return "unknown status";
+}
+
+int sv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+// sv_common.cuh -- device helpers, kernel arguments and the workspace layout shared
+// by the libspecverify kernels (sm_103a only).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// Tuning constants of the fused verify kernel.
+// One persistent CTA per SM: one producer warp issues 1-D bulk copies (TMA) of
+// row pieces into a ring of shared-memory slots; NCW consumer warps each own
+// SLOTS_PER_WARP slots and reduce whole pieces on their own.
+// ---------------------------------------------------------------------------
+constexpr int SLOT_BYTES = 8192;
+constexpr int NCW = 12;
+constexpr int SLOTS_PER_WARP = 2;
+constexpr int NSLOT = NCW * SLOTS_PER_WARP;
+constexpr int NTHREADS = 32 * (NCW + 1);
+constexpr int Q1_BATCH = 8;                      // pieces claimed per atomic on the work counter
+constexpr int MBOX = 64;                         // terminal-job mailbox entries per CTA
+constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz: bound on any wait
+
+// Status word bits (sticky, in the workspace header).
+constexpr uint32_t ST_DEVICE_INPUT = 1u;
+constexpr uint32_t ST_TIMEOUT = 2u;
+
+// ---------------------------------------------------------------------------
+// Workspace layout (computed identically on host and device from B, K, V).
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t status;    // ST_* bits
+  uint32_t q1_next;   // verify: next unclaimed stream piece
+  uint32_t cta_done;  // verify: CTAs that have finished
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct WsLayout {
+  size_t t_row, t_req, t_res;  // uint32 tickets: [B*RS], [B], [B]
+  size_t rowstat;              // float2 [B*RS]
+  size_t part;                 // float2 [B*RS*Pmax]
+  size_t rpart;                // double [B*Rmax]
+  size_t total;
+  int RS, Pmax, Rmax;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Pieces per row for element size `eb`: SLOT_BYTES per stream piece, half a slot per
+// row for terminal-job pieces (a residual piece carries the same range of two rows).
+__host__ __device__ inline int pieces_per_row(int V, int eb) {
+  const int E = SLOT_BYTES / eb;
+  return (V + E - 1) / E;
+}
+__host__ __device__ inline int resid_pieces(int V, int eb) {
+  const int E2 = SLOT_BYTES / 2 / eb;
+  return (V + E2 - 1) / E2;
+}
+
+// The ticket counters sit at fixed offsets sized for the library maxima, so that calls
+// of different shapes sharing one workspace never find another call's data where they
+// expect a counter. Every counter is back to zero when a call ends.
+constexpr size_t TICKET_ROW_WORDS = (size_t)SV_MAX_B * (2 * SV_MAX_K + 1);
+constexpr size_t TICKET_BYTES = 4 * (TICKET_ROW_WORDS + 2 * (size_t)SV_MAX_B);
+
+__host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
+  WsLayout L;
+  L.RS = 2 * K + 1;
+  L.Pmax = pieces_per_row(V, 4);  // fp32 needs the most pieces
+  L.Rmax = resid_pieces(V, 4);
+  const size_t nb = (size_t)(B > 0 ? B : 1);
+  L.t_row = sizeof(WsHeader);
+  L.t_req = L.t_row + 4 * TICKET_ROW_WORDS;
+  L.t_res = L.t_req + 4 * (size_t)SV_MAX_B;
+  size_t off = align_up(sizeof(WsHeader) + TICKET_BYTES, 256);
+  L.rowstat = off; off = align_up(off + 8 * nb * L.RS, 256);
+  L.part = off;    off = align_up(off + 8 * nb * L.RS * (size_t)L.Pmax, 256);
+  L.rpart = off;   off = align_up(off + 8 * nb * (size_t)L.Rmax, 256);
+  L.total = off;
+  return L;
+}
+
+// Arguments of the fused verify kernel (built by the C-ABI layer).
+struct VerifyArgs {
+  const void* tgt;
+  const void* drf;
+  const int32_t* tok;
+  const int32_t* vlen;
+  const float* uni;
+  int B, K, V;
+  float a;     // log2(e) / T rounded to fp32, T > 0
+  float a_lo;  // log2(e) / T - a (the rounding error of a)
+  int P;       // stream pieces per row
+  int E;       // elements per stream piece
+  int R;       // terminal-job pieces per request
+  int E2;      // elements per terminal-job piece (per row)
+  int RS;      // row slots per request, 2K+1
+  int Rmax;    // stride of the terminal-partial array
+  int32_t* out_tok;
+  int32_t* out_acc;
+  float* out_p;
+  float* out_q;
+  uint32_t* acc_cnt;
+  uint32_t* tst_cnt;
+  WsHeader* hdr;
+  uint32_t* t_row;
+  uint32_t* t_req;
+  uint32_t* t_res;
+  float2* rowstat;
+  float2* part;
+  double* rpart;
+};
+
+cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st);
+cudaError_t launch_schedule(const float* conf, int B, int K, float tau, int budget,
+                            int32_t* out_len, WsHeader* hdr, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+// Non-blocking probe: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Potentially blocking probe (the hardware may suspend the thread for a short,
+// system-defined time before returning false).
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 2^x on the special-function unit (hardware approximation).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max that returns NaN when either input is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Lane-wise max of two packed bf16 pairs, NaN-propagating.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ bool finitef(float x) { return fabsf(x) <= 3.402823466e38f; }
+
+}  // namespace sv

@@ -1,0 +1,189 @@
+// sv_schedule.cu -- GPU-resident confidence schedule (sm_103a).
+//
+// Computes per-request verify lengths from per-position draft confidences, on the
+// device, in one small launch (DSpark Deep Dive, "GPU-Resident Scheduling": the
+// scheduling decision is a CUDA kernel that reads the confidence scores and writes a
+// verification length per request, with no CPU round trip).
+//
+//  1. S_{b,k} = c_{b,0} * ... * c_{b,k} in float64, left to right (DSpark Guide,
+//     "2. Confidence-Scheduled Dynamic Verification": prefix survival C_k).
+//  2. L0_b = max(1, #{k : S_{b,k} >= tau}) (truncate at the first C_k < tau, keep at
+//     least one token; DSpark Guide sketch, DSpark Deep Dive "Variable-Length Drafts").
+//  3. If sum L0 > budget: keep the budget best positions (floor positions first when
+//     budget >= B; then S descending, k ascending, b ascending), found by an MSB-first
+//     radix select on the 64-bit patterns of S (order-preserving for S >= 0) and a
+//     k-major prefix count that ranks positions tied with the threshold
+//     (DSpark Deep Dive, "The Optimization Logic").
+// One CTA of 1024 threads; everything lives in shared memory.
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr int SCHED_THREADS = 1024;
+
+struct ScheduleArgs {
+  const float* conf;
+  int B, K;
+  float tau;
+  int budget;
+  int32_t* out_len;
+  WsHeader* hdr;
+};
+
+__device__ __forceinline__ unsigned long long surv_key(double s) {
+  return static_cast<unsigned long long>(__double_as_longlong(s == 0.0 ? 0.0 : s));
+}
+
+__global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const ScheduleArgs A) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  const int B = A.B, K = A.K, N = B * K;
+  double* S = reinterpret_cast<double*>(dsm);  // [B*K], request-major
+  int* L0 = reinterpret_cast<int*>(S + N);     // [B]
+  int* cnt = L0 + B;                           // [B] kept competing positions
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ unsigned int s_rem;
+  __shared__ int s_scan[32];
+  __shared__ unsigned long long s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // 1-2. survival products and tau-lengths, one thread per request.
+  bool bad = false;
+  unsigned long long my_total = 0;
+  for (int b = tid; b < B; b += SCHED_THREADS) {
+    double run = 1.0;
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+      const float c = A.conf[(size_t)b * K + k];
+      if (!(c >= 0.f && c <= 1.f)) bad = true;
+      run = run * static_cast<double>(c);
+      S[(size_t)b * K + k] = run;
+      if (run >= static_cast<double>(A.tau)) n = k + 1;
+    }
+    if (n < 1) n = 1;
+    L0[b] = n;
+    cnt[b] = 0;
+    my_total += n;
+  }
+  if (tid == 0) s_total = 0;
+  if (__syncthreads_or(bad)) {
+    for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = 0;
+    if (tid == 0) atomicOr(&A.hdr->status, ST_DEVICE_INPUT);
+    return;
+  }
+  atomicAdd(&s_total, my_total);
+  __syncthreads();
+  const long long total = static_cast<long long>(s_total);
+  if (total <= A.budget) {
+    for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = L0[b];
+    return;
+  }
+  const bool floor_first = A.budget >= B;
+  const int lo = floor_first ? 1 : 0;
+  const unsigned int bud = static_cast<unsigned int>(floor_first ? A.budget - B : A.budget);
+  if (bud == 0) {
+    for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = lo;
+    return;
+  }
+
+  // 3a. Radix select: the bud-th largest key among competing positions
+  // (lo <= k < L0_b). Their count exceeds bud because total > budget.
+  if (tid == 0) {
+    s_prefix = 0ull;
+    s_rem = bud;
+  }
+  unsigned long long mask = 0ull;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += SCHED_THREADS) hist[i] = 0u;
+    __syncthreads();
+    const unsigned long long pre = s_prefix;
+    for (int i = tid; i < N; i += SCHED_THREADS) {
+      const int b = i / K, k = i - b * K;
+      if (k < lo || k >= L0[b]) continue;
+      const unsigned long long key = surv_key(S[i]);
+      if ((key & mask) != pre) continue;
+      atomicAdd(&hist[(key >> shift) & 255ull], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned int acc = 0, rem = s_rem;
+      int d = 255;
+      for (; d > 0; --d) {
+        if (acc + hist[d] >= rem) break;
+        acc += hist[d];
+      }
+      s_rem = rem - acc;
+      s_prefix = pre | (static_cast<unsigned long long>(d) << shift);
+    }
+    mask |= 255ull << shift;
+    __syncthreads();
+  }
+  const unsigned long long thr = s_prefix;
+  const unsigned int need = s_rem;  // how many keys equal to thr are kept
+
+  // 3b. Keys above the threshold are kept; ties with it are ranked in k-major order
+  // (k ascending, then b ascending) by a block-wide prefix count.
+  const int per = (N + SCHED_THREADS - 1) / SCHED_THREADS;
+  const int i0 = min(N, tid * per), i1 = min(N, i0 + per);  // k-major index range
+  int my_ties = 0;
+  for (int i = i0; i < i1; ++i) {
+    const int k = i / B, b = i - k * B;
+    if (k < lo || k >= L0[b]) continue;
+    const unsigned long long key = surv_key(S[(size_t)b * K + k]);
+    if (key > thr)
+      atomicAdd(&cnt[b], 1);
+    else if (key == thr)
+      ++my_ties;
+  }
+  int incl = my_ties;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = s_scan[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    s_scan[lane] = v;
+  }
+  __syncthreads();
+  int rank = incl - my_ties + (warp ? s_scan[warp - 1] : 0);
+  for (int i = i0; i < i1; ++i) {
+    const int k = i / B, b = i - k * B;
+    if (k < lo || k >= L0[b]) continue;
+    if (surv_key(S[(size_t)b * K + k]) == thr) {
+      if (static_cast<unsigned int>(rank) < need) atomicAdd(&cnt[b], 1);
+      ++rank;
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = lo + cnt[b];
+}
+
+static size_t schedule_smem_bytes(int B, int K) {
+  return (size_t)B * K * sizeof(double) + 2 * (size_t)B * sizeof(int);
+}
+
+cudaError_t launch_schedule(const float* conf, int B, int K, float tau, int budget,
+                            int32_t* out_len, WsHeader* hdr, cudaStream_t st) {
+  const size_t smem = schedule_smem_bytes(B, K);
+  static bool attr_set = false;  // idempotent if two threads race here
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        sv_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)schedule_smem_bytes(SV_MAX_SCHED_B, SV_MAX_SCHED_BK / SV_MAX_SCHED_B));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  ScheduleArgs A{conf, B, K, tau, budget, out_len, hdr};
+  sv_schedule_kernel<<<1, SCHED_THREADS, smem, st>>>(A);
+  return cudaGetLastError();
+}
+
+}  // namespace sv
