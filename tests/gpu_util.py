@@ -1,0 +1,91 @@
+"""Helpers for the GPU parity tests: run the CUDA path and the oracle on the same
+seeded inputs and compare them element by element."""
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+NTHREADS = max(1, min(32, os.cpu_count() or 1))
+
+# Probabilities p_k(x_k), q_k(x_k): the kernel works in fp32 on the same (exactly
+# widened) inputs as the float64 oracle, so both dtypes are held to 1e-5 relative,
+# the bound stated for fp32 inputs (bf16's stated bound, 2e-3, is looser).
+P_RTOL = 1e-5
+
+# Running totals over the full-size parity tests: verified positions, requests flagged
+# as near-ties by the oracle (windows of 1e-5 on the accept ratio and on the inverse-CDF
+# position), and flagged requests on which the GPU actually decided differently.
+TOTALS = {"positions": 0, "flagged": 0, "mismatch": 0}
+
+
+def to_dev(inp, device="cuda"):
+    return {k: (v.to(device) if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+
+def run_gpu(sv, g, T, ws=None, diag=True):
+    B, K1, V = g["target"].shape
+    ws = ws or sv.Workspace(B, K1 - 1, V, device=g["target"].device)
+    out = sv.sv_verify(g["target"], g["draft"] if T > 0 else None, g["draft_tok"],
+                       g["verify_len"], g["uniforms"] if T > 0 else None, T, ws, diag=diag)
+    torch.cuda.synchronize()
+    res = {"out_tok": out[0].cpu().numpy(), "out_accepted": out[1].cpu().numpy()}
+    if diag:
+        res["p"] = out[2].cpu().numpy()
+        res["q"] = out[3].cpu().numpy()
+    res["status"] = ws.status(clear=True)
+    return res
+
+
+def run_oracle(inp, T, idx=None, diag=True):
+    sel = (lambda t: t[idx]) if idx is not None else (lambda t: t)
+    return oracle.verify(synth.to_oracle(sel(inp["target"])),
+                         synth.to_oracle(sel(inp["draft"])) if T > 0 else None,
+                         sel(inp["draft_tok"]).cpu().numpy(), sel(inp["verify_len"]).cpu().numpy(),
+                         sel(inp["uniforms"]).cpu().numpy() if T > 0 else None, T,
+                         nthreads=NTHREADS, diag=diag)
+
+
+def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
+    """Bit-exact decisions outside flagged near-ties; p/q within P_RTOL.
+    Returns (flagged requests, verified positions, flagged requests that differ)."""
+    acc, tok = gpu["out_accepted"], gpu["out_tok"]
+    if idx is not None:
+        acc, tok = acc[idx], tok[idx]
+    L = np.asarray(verify_len)
+    flagged = (ref["flags"] & oracle.NEAR_TIE_MASK) != 0
+    ok = ~flagged
+    bad = np.nonzero(ok & (acc != ref["out_accepted"]))[0]
+    assert bad.size == 0, (f"accepted mismatch at requests {bad[:10]}: gpu {acc[bad[:10]]} "
+                           f"ref {ref['out_accepted'][bad[:10]]}")
+    rows = np.nonzero(ok & (tok != ref["out_tok"]).any(axis=1))[0]
+    assert rows.size == 0, (f"token mismatch at requests {rows[:10]}: gpu {tok[rows[:3]]} "
+                            f"ref {ref['out_tok'][rows[:3]]}")
+    if check_p and T > 0 and "p" in gpu:
+        gp, gq = gpu["p"], gpu["q"]
+        if idx is not None:
+            gp, gq = gp[idx], gq[idx]
+        valid = (ref["flags"] & oracle.FLAG_INVALID) == 0
+        K = gp.shape[1]
+        mask = (np.arange(K)[None, :] < np.clip(L, 0, K)[:, None]) & valid[:, None]
+        for name, g, r in (("p", gp, ref["p"]), ("q", gq, ref["q"])):
+            err = np.abs(g[mask].astype(np.float64) - r[mask])
+            lim = P_RTOL * np.abs(r[mask]) + 1e-30
+            assert (err <= lim).all(), f"{name} rel err {np.max(err / (np.abs(r[mask]) + 1e-300))}"
+    positions = int((np.clip(L, 0, None) + 1).sum())
+    differ = flagged & ((acc != ref["out_accepted"]) | (tok != ref["out_tok"]).any(axis=1))
+    for b in np.nonzero(differ)[0][:5]:
+        print(f"[near-ties] differs: request {b} flags {ref['flags'][b]} gpu acc {acc[b]} "
+              f"tok {tok[b].tolist()} ref acc {ref['out_accepted'][b]} "
+              f"tok {ref['out_tok'][b].tolist()}")
+    return int(flagged.sum()), positions, int(differ.sum())
+
+
+def account(name, nf, npos, nmis):
+    TOTALS["positions"] += npos
+    TOTALS["flagged"] += nf
+    TOTALS["mismatch"] += nmis
+    print(f"[near-ties] {name}: {nf} flagged requests, {nmis} of them decided differently, "
+          f"{npos} positions")

@@ -1,0 +1,100 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, and exports every
+function that include/*.h declares; host-side argument checks reject bad calls before
+anything touches a device."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(sv_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import speculative_decoding_verification_79_gb300 as sv
+
+    return sv.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
+              "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import speculative_decoding_verification_79_gb300 as sv
+
+    out = subprocess.run(["nm", "-D", "--defined-only", sv.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    missing = _declared() - exported
+    assert not missing, missing
+    for n in _declared():
+        assert hasattr(lib, n)
+
+
+def test_host_argument_checks(lib):
+    """Rejected before any device work; no GPU is needed for these."""
+    import speculative_decoding_verification_79_gb300 as sv
+
+    assert lib.sv_workspace_bytes(64, 8, 151936) > 0
+    assert lib.sv_workspace_bytes(-1, 8, 10) == 0
+    assert lib.sv_workspace_bytes(4, 0, 10) == 0
+    assert lib.sv_workspace_bytes(4, 33, 10) == 0
+    fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails its checks first
+    n = lib.sv_workspace_bytes(4, 4, 100)
+    args = lambda dt=1, B=4, K=4, V=100, T=1.0, ws=fake, nb=n, tgt=fake, drf=fake: (  # noqa: E731
+        tgt, drf, dt, fake, fake, fake, B, K, V, T, fake, fake, ws, nb, None)
+    assert lib.sv_verify(*args(dt=7)) == sv.SV_ERR_DTYPE
+    assert lib.sv_verify(*args(K=0)) == sv.SV_ERR_SHAPE
+    assert lib.sv_verify(*args(K=33)) == sv.SV_ERR_SHAPE
+    assert lib.sv_verify(*args(B=5000)) == sv.SV_ERR_SHAPE
+    for T in (-1.0, float("nan"), float("inf"), 1e-9):
+        assert lib.sv_verify(*args(T=T)) == sv.SV_ERR_ARG
+    assert lib.sv_verify(*args(nb=n - 1)) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_verify(*args(ws=ctypes.c_void_p(264))) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_verify(*args(tgt=None)) == sv.SV_ERR_ARG
+    assert lib.sv_verify(*args(drf=None)) == sv.SV_ERR_ARG
+    assert lib.sv_verify(*args(dt=0, tgt=ctypes.c_void_p(258))) == sv.SV_ERR_ARG
+    assert lib.sv_verify(*args(B=0)) == sv.SV_OK
+    assert lib.sv_schedule(fake, 4, 4, 1.5, 10, fake, fake, n, None) == sv.SV_ERR_ARG
+    assert lib.sv_schedule(fake, 4, 4, float("nan"), 10, fake, fake, n, None) == sv.SV_ERR_ARG
+    assert lib.sv_schedule(fake, 4, 4, 0.3, -1, fake, fake, n, None) == sv.SV_ERR_ARG
+    assert lib.sv_schedule(fake, 9000, 1, 0.3, 10, fake, fake, n, None) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule(fake, 4096, 8, 0.3, 10, fake, fake, n, None) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule(fake, 4, 4, 0.3, 10, fake, None, n, None) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_schedule(fake, 0, 4, 0.3, 10, fake, fake, n, None) == sv.SV_OK
+    assert sv.status_string(sv.SV_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_workspace_layout_is_shape_independent_for_counters(lib):
+    """Counters live at fixed offsets, so any workspace holds at least that region."""
+    small = lib.sv_workspace_bytes(1, 1, 1)
+    assert small >= 4 * (4096 * 65 + 2 * 4096)
+
+
+def test_no_fallback_without_cuda():
+    """The product path fails loudly when CUDA is unavailable (no CPU fallback)."""
+    import torch
+
+    import speculative_decoding_verification_79_gb300 as sv
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(Exception):
+        sv.Workspace(4, 4, 100)
