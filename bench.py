@@ -1,0 +1,467 @@
+"""Benchmark of the DSpark verification hot path on one GB300 (or N replicas).
+
+One step = the whole hot path on one batch: sv_schedule (survival products, tau cut,
+budget check) then sv_verify (fused rejection-sampling verification) for B=64
+requests x K=8 drafted tokens over a 151,936-entry vocabulary in bf16 at T=1 (draft
+noise 1.0, full-length blocks: tau=0, budget=B*K). Inputs are synthetic and seeded.
+
+Prints one JSON line (rank 0). `value` is verified draft tokens per second with the
+inputs resident in HBM; `e2e` is the same metric through the public calls with the
+inputs copied from pinned host memory every step and the results copied back.
+`--impl reference` times the float64 CPU oracle on the same workload instead.
+`--sweep` prints one line per point of the B x K roofline sweep.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/sec and logit GB/s (fraction of GB300 HBM peak), 1 GPU"
+UNIT = "verified draft tokens/s"
+B_DEF, K_DEF, V_DEF, T_DEF = 64, 8, 151_936, 1.0
+GRAPH_STEPS = 100
+PROFILE = os.path.join(ROOT, "profiles", "sv_verify_B64_K8_V151936_bf16_T1.md")
+
+
+def _rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sha():
+    """Hash of the CUDA sources; ties a committed ncu summary to the kernel it measured."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_79_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def _profiled_traffic():
+    """DRAM bytes per launch of the verify kernel from the committed ncu summary, when it
+    was taken on the current kernel sources; else None."""
+    if not os.path.exists(PROFILE):
+        return None
+    txt = open(PROFILE).read()
+    m = re.search(r"kernel sources sha:\s*([0-9a-f]+)", txt)
+    t = re.search(r"dram bytes per launch \(full workload\):\s*([0-9]+)", txt)
+    if not m or not t or m.group(1) != kernel_sha():
+        return None
+    return int(t.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the sampler start before the timed region
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [[c.strip() for c in r] for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _inputs(B, K, V, T, seed, device):
+    import synth
+
+    inp = synth.verify_inputs(B, K, V, dtype=torch.bfloat16, temperature=T, target_sigma=3.0,
+                              draft_sigma=1.0, seed=seed, device=device)
+    inp["conf"] = synth.confidences(B, K, seed=seed).to(device)
+    return inp
+
+
+def run_gpu(args):
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    rank, world, local = _rank()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    B, K, V, T = args.B, args.K, args.V, args.T
+    tau, budget = 0.0, B * K  # full-length blocks: nothing truncated, nothing trimmed
+    sets = [_inputs(B, K, V, T, 1000 * rank + s, dev) for s in range(2)]  # 2 sets > L2
+    ws = sv.Workspace(B, K, V, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_acc = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def step(i, evs=None):
+        g = sets[i & 1]
+        if evs is not None:
+            evs[0].record(st)
+        sv.sv_schedule(g["conf"], tau, budget, ws, out_len=out_len, stream=st)
+        if evs is not None:
+            evs[1].record(st)
+        sv.sv_verify(g["target"], g["draft"], g["draft_tok"], out_len, g["uniforms"], T, ws,
+                     out_tok=out_tok, out_accepted=out_acc, stream=st)
+        if evs is not None:
+            evs[2].record(st)
+
+    # Warm-up (eager), then capture GRAPH_STEPS steps with per-launch events.
+    st.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(st):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    st.synchronize()
+    n_graph = min(GRAPH_STEPS, args.steps)
+    try:  # event-record nodes inside the graph time every launch of the last replay
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+               for _ in range(n_graph)]
+    except TypeError:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_graph)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for i in range(n_graph):
+            step(i, evs[i])
+    rem = args.steps % n_graph
+    graph_rem = None
+    if rem:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem, stream=st):
+            for i in range(rem):
+                step(i)
+    for _ in range(2):  # graph warm-up
+        graph.replay()
+    st.synchronize()
+    if ws.status(stream=st) != sv.SV_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    reps = args.steps // n_graph
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(dev.index if world == 1 else local) as clk:
+        t0.record(st)
+        for _ in range(reps):
+            graph.replay()
+        if graph_rem is not None:
+            graph_rem.replay()
+        t1.record(st)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    clocks = clk.summary()
+    try:
+        ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        sch_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        timing_src = f"event-record nodes in the graph, last of {reps} replays"
+    except RuntimeError:
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_graph)]
+        with torch.cuda.stream(st):
+            for i in range(n_graph):
+                step(i, ev2[i])
+        st.synchronize()
+        ver_ms = [e[1].elapsed_time(e[2]) for e in ev2]
+        sch_ms = [e[0].elapsed_time(e[1]) for e in ev2]
+        timing_src = "eager launches with CUDA events right after the timed region"
+    if ws.status(stream=st) != sv.SV_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    L = out_len.cpu()
+    tokens_per_step = int(L.sum().item())
+    bytes_per_launch = synth.logit_bytes(L, V, 2, greedy=(T == 0.0))
+    value = tokens_per_step * args.steps * world / (elapsed_ms / 1e3)
+    ver_avg = sum(ver_ms) / len(ver_ms)
+    peak, peak_kind = _peaks()
+    achieved = bytes_per_launch / (ver_avg / 1e3) / 1e9
+
+    e2e = run_e2e(args, sv, sets[0], ws, dev, tau, budget) if args.e2e_steps > 0 else None
+    cpu = cpu_baseline(args) if (rank == 0 and not args.no_cpu) else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"schedule + verify, B={B} K={K} V={V} bf16 T={T}, draft noise "
+                               "1.0, full-length blocks (tau=0, budget=B*K)",
+                   "B": B, "K": K, "V": V, "temperature": T, "per_gpu_batch": B,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: two alternating input sets of "
+                         f"{bytes_per_launch / 1e6:.0f} MB each (L2 129 MB)",
+                   "timing": f"CUDA graph of {n_graph} steps replayed; CUDA events"},
+        "logit_gbs": bytes_per_launch * args.steps * world / (elapsed_ms / 1e3) / 1e9,
+        "verify_us_avg": ver_avg * 1e3, "schedule_us_avg": sum(sch_ms) / len(sch_ms) * 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                     "kernel": "sv_verify_kernel<bf16, T>0>",
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "per_launch_timing": timing_src},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, sv, g, ws, dev, tau, budget):
+    """Public calls with host inputs: per step H2D of the step's inputs from pinned
+    memory, schedule + verify, D2H of the emitted tokens and accepted counts."""
+    B, K = args.B, args.K
+    host = {k: g[k].cpu().pin_memory() for k in ("target", "draft", "draft_tok", "uniforms",
+                                                  "conf")}
+    dbuf = {k: torch.empty_like(g[k]) for k in host}
+    out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    h_tok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    st = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_tok.numel() * 4 + h_acc.numel() * 4
+
+    def one():
+        with torch.cuda.stream(st):
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            sv.sv_schedule(dbuf["conf"], tau, budget, ws, out_len=out_len, stream=st)
+            sv.sv_verify(dbuf["target"], dbuf["draft"], dbuf["draft_tok"], out_len,
+                         dbuf["uniforms"], args.T, ws, out_tok=out_tok, out_accepted=out_acc,
+                         stream=st)
+            h_tok.copy_(out_tok, non_blocking=True)
+            h_acc.copy_(out_acc, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    st.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    st.synchronize()
+    dt = time.perf_counter() - t0
+    tokens = int(out_len.sum().item()) * args.e2e_steps
+    return {"value": tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": dt / args.e2e_steps * 1e3}
+
+
+def _oracle_args(inp, vlen=None):
+    import synth
+
+    return [synth.to_oracle(inp["target"]), synth.to_oracle(inp["draft"]),
+            inp["draft_tok"].numpy(), inp["verify_len"].numpy() if vlen is None else vlen,
+            inp["uniforms"].numpy()]
+
+
+def cpu_baseline(args):
+    """The float64 oracle, as it stands, on a bounded sample of the same workload (some
+    of the B requests), on all host cores; scaled to verified draft tokens/s."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    inp = _inputs(1, args.K, args.V, args.T, 7, "cpu")
+    t0 = time.perf_counter()
+    oracle.verify(*_oracle_args(inp), args.T, nthreads=1, diag=False)
+    one = time.perf_counter() - t0
+    n_req = max(1, min(args.B, int(args.cpu_seconds * cores / max(one, 1e-6))))
+    inp = _inputs(n_req, args.K, args.V, args.T, 8, "cpu")
+    conf = inp["conf"].numpy()
+    threads = min(cores, n_req)
+    t0 = time.perf_counter()
+    oracle.schedule(conf, 0.0, n_req * args.K)
+    oracle.verify(*_oracle_args(inp), args.T, nthreads=threads, diag=False)
+    dt = time.perf_counter() - t0
+    return {"value": n_req * args.K / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_req} of the {args.B} requests (K={args.K}, V={args.V}, bf16 inputs, "
+                      f"T={args.T}), schedule + verify, {dt:.2f} s wall on {threads} threads"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle on the host cores, each step a bounded sample of the
+    workload sized so that warm-up plus the timed steps take about two minutes."""
+    rank, world, _ = _rank()
+    if rank != 0:
+        return
+    import oracle
+
+    cores = os.cpu_count() or 1
+    n_steps = args.steps + min(args.warmup, 3)
+    per_step = 120.0 / max(1, n_steps)
+    inp = _inputs(1, args.K, args.V, args.T, 2, "cpu")
+    vl1 = torch.ones(1, dtype=torch.int32).numpy()
+    t0 = time.perf_counter()
+    oracle.verify(*_oracle_args(inp, vl1), args.T, nthreads=1, diag=False)
+    t_l1 = time.perf_counter() - t0  # one request, one drafted position (3 rows)
+    t_full = t_l1 * (2 * args.K + 1) / 3.0
+    if per_step >= t_full:
+        n_req = max(1, min(args.B, int(per_step * cores / t_full)))
+        L = args.K
+    else:
+        n_req = 1
+        L = max(1, min(args.K, int((per_step / t_l1 * 3.0 - 1.0) / 2.0)))
+    inp = _inputs(n_req, args.K, args.V, args.T, 3, "cpu")
+    conf = inp["conf"].numpy()
+    a = _oracle_args(inp, torch.full((n_req,), L, dtype=torch.int32).numpy())
+    threads = min(cores, n_req)
+
+    def step():
+        oracle.schedule(conf, 0.0, n_req * args.K)
+        oracle.verify(*a, args.T, nthreads=threads, diag=False)
+
+    for _ in range(min(args.warmup, 3)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = n_req * L * args.steps / dt
+    sample = (f"{n_req} of the {args.B} requests per step with verify length {L} (K={args.K}, "
+              f"V={args.V}, bf16 inputs, T={args.T}), schedule + verify")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"schedule + verify, B={args.B} K={args.K} V={args.V} bf16 "
+                               f"T={args.T}", "B": args.B, "K": args.K, "V": args.V},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_sweep(args):
+    """One JSON line per roofline sweep point (verify kernel only, CUDA events, L2
+    flushed between launches by a 256 MB memset)."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    peak, _ = _peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    temps = [args.T] if args.sweep_T is None else [float(x) for x in args.sweep_T.split(",")]
+    for T in temps:
+        for K in synth.SWEEP_K:
+            for B in synth.SWEEP_B:
+                g = synth.sweep_point(B, K, seed=0, device=dev)
+                ws = sv.Workspace(B, K, synth.QWEN3_VOCAB, device=dev)
+                for _ in range(3):
+                    sv.sv_verify(g["target"], g["draft"], g["draft_tok"], g["verify_len"],
+                                 g["uniforms"], T, ws)
+                times = []
+                for _ in range(args.sweep_reps):
+                    flush.zero_()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    sv.sv_verify(g["target"], g["draft"], g["draft_tok"], g["verify_len"],
+                                 g["uniforms"], T, ws)
+                    e1.record()
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                t = statistics.median(times) / 1e3
+                nbytes = synth.logit_bytes(g["verify_len"].cpu(), synth.QWEN3_VOCAB, 2,
+                                           greedy=(T == 0.0))
+                print(json.dumps({"sweep": True, "T": T, "B": B, "K": K, "us": t * 1e6,
+                                  "tokens_per_s": B * K / t, "gbs": nbytes / t / 1e9,
+                                  "frac": nbytes / t / 1e9 / peak, "bytes": nbytes}), flush=True)
+                del g, ws
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--B", type=int, default=B_DEF)
+    ap.add_argument("--K", type=int, default=K_DEF)
+    ap.add_argument("--V", type=int, default=V_DEF)
+    ap.add_argument("--T", type=float, default=T_DEF)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-T", default=None)
+    ap.add_argument("--sweep-reps", type=int, default=30)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
