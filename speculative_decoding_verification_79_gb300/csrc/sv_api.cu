@@ -118,6 +118,7 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   A.part = reinterpret_cast<float2*>(ws + L.part);
   A.rpart = reinterpret_cast<double*>(ws + L.rpart);
+  A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);
 
   // One persistent CTA per SM, fewer when the batch cannot feed them all.
   const long long max_pieces = (long long)B * (greedy ? K + 1 : 2 * K + 1) * A.P;

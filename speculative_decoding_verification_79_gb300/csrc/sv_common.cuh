@@ -23,7 +23,7 @@ constexpr int SLOTS_PER_WARP = 2;
 constexpr int NSLOT = NCW * SLOTS_PER_WARP;
 constexpr int NTHREADS = 32 * (NCW + 1);
 constexpr int Q1_BATCH = 8;                      // pieces claimed per atomic on the work counter
-constexpr int MBOX = 64;                         // terminal-job mailbox entries per CTA
+constexpr int TERM_WARPS = 8;                    // warps per CTA of the terminal kernel
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz: bound on any wait
 
 // Status word bits (sticky, in the workspace header).
@@ -41,19 +41,31 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// Terminal-sample job of one request, written by the deciding warp of the stream
+// kernel and read by the terminal kernel: the residual max(0, p_j - q_j) over rows
+// t_j and d_j, a plain sample of p over target row j (the bonus row L), or nothing
+// (an invalid request, or greedy verification).
+enum : int { J_NONE = -1, J_RESID = 0, J_BONUS = 1 };
+struct __align__(32) TermJob {
+  int kind, j;
+  float MAt, invSt, MAd, invSd;  // fl(M*a) and 1/S of target row j and draft row j
+  int pad[2];
+};
+
 struct WsLayout {
   size_t t_row, t_req, t_res;  // uint32 tickets: [B*RS], [B], [B]
   size_t rowstat;              // float2 [B*RS]
   size_t part;                 // float2 [B*RS*Pmax]
   size_t rpart;                // double [B*Rmax]
+  size_t jobs;                 // TermJob [B]
   size_t total;
   int RS, Pmax, Rmax;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Pieces per row for element size `eb`: SLOT_BYTES per stream piece, half a slot per
-// row for terminal-job pieces (a residual piece carries the same range of two rows).
+// Pieces per row for element size `eb`: SLOT_BYTES per stream piece; terminal-sample
+// pieces are half as long (a residual piece covers the same range of two rows).
 __host__ __device__ inline int pieces_per_row(int V, int eb) {
   const int E = SLOT_BYTES / eb;
   return (V + E - 1) / E;
@@ -82,6 +94,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
   L.rowstat = off; off = align_up(off + 8 * nb * L.RS, 256);
   L.part = off;    off = align_up(off + 8 * nb * L.RS * (size_t)L.Pmax, 256);
   L.rpart = off;   off = align_up(off + 8 * nb * (size_t)L.Rmax, 256);
+  L.jobs = off;    off = align_up(off + sizeof(TermJob) * nb, 256);
   L.total = off;
   return L;
 }
@@ -115,6 +128,7 @@ struct VerifyArgs {
   float2* rowstat;
   float2* part;
   double* rpart;
+  TermJob* jobs;
 };
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st);

@@ -4,27 +4,27 @@
 // (DSpark Deep Dive, "The Speculative Decoding Solution"; DSpark Guide, "1. The
 // Mathematics of Suffix Decay"; perchy.ai Technology, "Verified by the target").
 //
-// Design (one launch, one persistent CTA per SM, no CPU round trip):
-//  * Work list: every active logit row of the batch (request b: target rows 0..L_b,
-//    and at T > 0 draft rows 0..L_b-1) cut into fixed pieces of SLOT_BYTES. Pieces
-//    are ordered request-major and claimed in batches from one atomic counter, so
-//    a request's rows are streamed close together in time.
-//  * Producer warp: one lane issues 1-D bulk copies (cp.async.bulk, TMA) of each
-//    piece into a shared-memory slot and signals an mbarrier with the byte count.
-//  * Consumer warps: each owns two slots and reduces whole pieces: online softmax
-//    (running max + sum of 2^(z*log2e/T - max)) at T > 0, or (max, lowest argmax) at
-//    T == 0. The piece result goes to the workspace; an atomic ticket per row and per
-//    request elects the last arriving warp, which combines the row, and then the
-//    request: p_k(x_k), q_k(x_k), the accept tests u*q < p, a ballot for the first
-//    rejection j, the outputs.
-//  * Terminal sample at T > 0: the deciding warp posts a job to its CTA's producer,
-//    which streams the terminal rows again (t_j and d_j for a residual sample, or the
-//    bonus row t_L; they were read microseconds earlier and are L2-resident) through
-//    the same slots. Each job piece is summed with compensated fp32 arithmetic and
-//    reduced in float64; the last piece locates the token by inverse CDF (float64
-//    prefix over piece sums, one piece re-scanned in float64).
-//  * Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
-//    status word, lets its copies in flight land, and returns.
+// Two launches on the caller's stream, no CPU round trip:
+//  1. sv_verify_kernel, one persistent CTA per SM. Work list: every active logit row
+//     of the batch (request b: target rows 0..L_b, and at T > 0 draft rows
+//     0..L_b-1) cut into pieces of SLOT_BYTES, ordered request-major and claimed in
+//     batches from one atomic counter. A producer warp issues 1-D bulk copies
+//     (cp.async.bulk, TMA) of each piece into a shared-memory slot guarded by an
+//     mbarrier; consumer warps each own two slots and reduce whole pieces: online
+//     softmax (running max + sum of 2^(z*log2e/T - max)) at T > 0, or (max, lowest
+//     argmax) at T == 0. Each piece result is published with a release-ordered
+//     atomic ticket whose value the warp inspects only after waiting for its next
+//     slot, so the round trip hides behind the next piece. The warp completing a
+//     row combines it; the warp completing a request decides it: p_k(x_k), q_k(x_k),
+//     the accept tests u*q < p, a ballot for the first rejection j, the outputs,
+//     and (T > 0) the terminal-sample job of the request.
+//  2. sv_terminal_kernel (T > 0 only): one warp per (request, piece) task sums the
+//     terminal weights of a piece of the terminal rows (residual max(0, p_j - q_j),
+//     or p of the bonus row) with compensated fp32 arithmetic, reduced in float64;
+//     the last piece of a request locates the token by inverse CDF at u_{b,K}
+//     (float64 prefix over piece sums, one piece re-scanned in float64).
+//  Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
+//  status word, lets its copies in flight land, and returns.
 #include <cfloat>
 #include <climits>
 
@@ -32,12 +32,7 @@
 
 namespace sv {
 
-enum : int { K_STREAM = 0, K_JOB = 1, K_STOP = 2 };
-
-// Terminal-sample jobs: the residual max(0, p_j - q_j) over rows t_j and d_j, or a
-// plain sample of p over one target row (the bonus row, or row j when the residual
-// has no mass left).
-enum : int { J_RESID = 0, J_BONUS = 1 };
+enum : int { K_STREAM = 0, K_STOP = 2 };
 
 // A contiguous run of elements of one row, split by 16-byte alignment into a head
 // read directly from global memory, a body copied to shared memory, and a tail
@@ -48,28 +43,16 @@ struct Seg {
 };
 
 struct __align__(16) SlotMeta {
-  int kind, b, r, p;  // r: row slot (stream) or terminal row j / L (job piece)
+  int kind, b, r, p;  // request, row slot, piece
   int e0;             // first element of the piece within its row
-  int direct;         // job piece: 1 = rows read straight from global memory
-  int jkind;          // job piece: J_RESID or J_BONUS
-  int pad0;
-  Seg s0, s1;
-  float MAt, invSt, MAd, invSd;
-};
-
-struct Job {
-  int b, j, jkind;
-  float MAt, invSt, MAd, invSd;
+  int pad[3];
+  Seg s0;
 };
 
 struct Shared {
   SlotMeta meta[NSLOT];
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
-  Job mbox[MBOX];
-  int mbox_flag[MBOX];
-  int mbox_tail;
-  int mbox_head;
   int abort_flag;
   int last_cta;
   int total_rows;
@@ -306,10 +289,6 @@ __device__ __forceinline__ int L_of_rows(int nrows, bool greedy) {
   return greedy ? nrows - 1 : (nrows - 1) / 2;
 }
 
-__device__ __forceinline__ void proxy_fence_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ void raise_status(const VerifyArgs& A, uint32_t bits) { atomicOr(&A.hdr->status, bits); }
 
 // Bounded wait on an mbarrier phase; false on abort or timeout.
@@ -326,105 +305,36 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const Veri
   return true;
 }
 
-// Copy n elements of a row (starting at src) into shared memory at dst (16-byte
-// aligned). Vector loads when src is 16-byte aligned.
-template <typename T>
-__device__ void stage_row(unsigned char* dst, const T* src, int n, int lane) {
-  constexpr int eb = sizeof(T);
-  T* d = reinterpret_cast<T*>(dst);
-  if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-    const int nv = n * eb / 16;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll 4
-    for (int i = lane; i < nv; i += 32) d4[i] = __ldg(s4 + i);
-    for (int e = nv * 16 / eb + lane; e < n; e += 32) d[e] = src[e];
-  } else {
-    for (int e = lane; e < n; e += 32) d[e] = src[e];
-  }
-}
 
-__device__ __forceinline__ float smem_logit(const unsigned char* base, int e, float) {
-  return reinterpret_cast<const float*>(base)[e];
-}
-__device__ __forceinline__ float smem_logit(const unsigned char* base, int e, uint16_t) {
-  return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(base)[e]) << 16);
-}
-
-// Inverse-CDF step inside one staged piece of n elements: the smallest element v
-// with target < cum(v), cum in float64 over fp32 weights w(v) evaluated identically
-// by every lane. Falls back to the last positive-weight element when rounding leaves
-// target past the end of the piece.
-template <typename WF>
-__device__ int locate_in_piece(WF wf, int n, double target, int lane) {
-  const int c = (n + 31) / 32;
-  const int v0 = lane * c, v1 = min(n, v0 + c);
-  float hs = 0.f, hc = 0.f;
-  int lastpos = -1;
-  for (int v = v0; v < v1; ++v) {
-    const float w = wf(v);
-    two_sum(hs, hc, w);
-    if (w > 0.f) lastpos = v;
-  }
-  const double ls = (double)hs + (double)hc;
-  const double incl = warp_incl_scan_d(ls, lane);
-  const unsigned hit = __ballot_sync(FULL, target < incl);
-  int y = -1;
-  if (hit) {
-    const int ln = __ffs(hit) - 1;
-    if (lane == ln) {
-      double cum = incl - ls;
-      for (int v = v0; v < v1; ++v) {
-        cum += (double)wf(v);
-        if (target < cum) {
-          y = v;
-          break;
-        }
-      }
-      if (y < 0) y = lastpos;
-    }
-    y = __shfl_sync(FULL, y, ln);
-  }
-  if (y < 0) {  // past the end by rounding: last positive weight of the piece
-    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-    y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : 0;
-  }
-  return y;
+// Release-ordered atomic add (GPU scope): earlier stores of this thread become
+// visible to whoever observes the new count.
+__device__ __forceinline__ uint32_t atom_add_release(uint32_t* addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
 }
 
 __device__ void emit_invalid(const VerifyArgs& A, int b, int lane) {
   int32_t* ot = A.out_tok + (size_t)b * (A.K + 1);
   for (int k = lane; k <= A.K; k += 32) ot[k] = -1;
+  const float nan = __int_as_float(0x7fc00000);
   if (A.out_p)
-    for (int k = lane; k < A.K; k += 32) A.out_p[(size_t)b * A.K + k] = __int_as_float(0x7fc00000);
+    for (int k = lane; k < A.K; k += 32) A.out_p[(size_t)b * A.K + k] = nan;
   if (A.out_q)
-    for (int k = lane; k < A.K; k += 32) A.out_q[(size_t)b * A.K + k] = __int_as_float(0x7fc00000);
+    for (int k = lane; k < A.K; k += 32) A.out_q[(size_t)b * A.K + k] = nan;
   if (lane == 0) {
     A.out_acc[b] = -1;
+    A.jobs[b].kind = J_NONE;
     raise_status(A, ST_DEVICE_INPUT);
   }
 }
 
-// Post a terminal-sample job to this CTA's producer (one lane).
-__device__ void post_job(Shared& S, const VerifyArgs& A, const Job& J) {
-  const int idx = atomicAdd(&S.mbox_tail, 1);
-  const long long t0 = clock64();
-  while (idx - *reinterpret_cast<volatile int*>(&S.mbox_head) >= MBOX) {
-    if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return;
-    if (clock64() - t0 > WAIT_CYCLES) {
-      S.abort_flag = 1;
-      raise_status(A, ST_TIMEOUT);
-      return;
-    }
-  }
-  S.mbox[idx & (MBOX - 1)] = J;
-  __threadfence_block();
-  *reinterpret_cast<volatile int*>(&S.mbox_flag[idx & (MBOX - 1)]) = 1;
-}
-
 // Decision for one request at T > 0 (one warp).
 template <typename T>
-__device__ void decide_sample(const VerifyArgs& A, Shared& S, int b, int L, int lane) {
+__device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   const int K = A.K, V = A.V;
   const size_t rb = (size_t)b * A.RS;
   float p = __int_as_float(0x7fc00000), q = p, MAt = 0.f, MAd = 0.f, iSt = 0.f, iSd = 0.f;
@@ -464,26 +374,30 @@ __device__ void decide_sample(const VerifyArgs& A, Shared& S, int b, int L, int 
   int32_t* ot = A.out_tok + (size_t)b * (K + 1);
   for (int k = lane; k <= K; k += 32)
     if (k != j) ot[k] = (k < j) ? x : -1;
-  if (lane == 0) A.out_acc[b] = j;
   if (A.out_p && lane < K) A.out_p[(size_t)b * K + lane] = p;
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = q;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
-  Job J;
-  J.b = b;
-  J.j = j;
-  if (j == L) {  // every draft accepted: bonus sample from p_L
-    J.jkind = J_BONUS;
-    J.MAt = sL.x * A.a;
-    J.invSt = J.MAd = J.invSd = 0.f;
-  } else {  // first rejection at j: residual sample
-    J.jkind = J_RESID;
-    J.MAt = __shfl_sync(FULL, MAt, j & 31);
-    J.invSt = __shfl_sync(FULL, iSt, j & 31);
-    J.MAd = __shfl_sync(FULL, MAd, j & 31);
-    J.invSd = __shfl_sync(FULL, iSd, j & 31);
+  const float jMAt = __shfl_sync(FULL, MAt, j & 31), jSt = __shfl_sync(FULL, iSt, j & 31);
+  const float jMAd = __shfl_sync(FULL, MAd, j & 31), jSd = __shfl_sync(FULL, iSd, j & 31);
+  if (lane == 0) {
+    A.out_acc[b] = j;
+    TermJob J;
+    J.j = j;
+    if (j == L) {  // every draft accepted: bonus sample from p_L
+      J.kind = J_BONUS;
+      J.MAt = sL.x * A.a;
+      J.invSt = J.MAd = J.invSd = 0.f;
+    } else {  // first rejection at j: residual sample
+      J.kind = J_RESID;
+      J.MAt = jMAt;
+      J.invSt = jSt;
+      J.MAd = jMAd;
+      J.invSd = jSd;
+    }
+    J.pad[0] = J.pad[1] = 0;
+    A.jobs[b] = J;
   }
-  if (lane == 0) post_job(S, A, J);
 }
 
 // Decision for one request at T == 0 (one warp): argmax matching.
@@ -511,19 +425,27 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   if (j == L) y = __float_as_int(sL.y);
   int32_t* ot = A.out_tok + (size_t)b * (K + 1);
   for (int k = lane; k <= K; k += 32) ot[k] = (k < j) ? x : (k == j ? y : -1);
-  if (lane == 0) A.out_acc[b] = j;
   const float nan = __int_as_float(0x7fc00000);
   if (A.out_p && lane < K) A.out_p[(size_t)b * K + lane] = nan;
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = nan;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
+  if (lane == 0) {
+    A.out_acc[b] = j;
+    A.jobs[b].kind = J_NONE;
+  }
 }
 
-// Process one stream piece; on completion of its row (and request) do the row
-// combine (and the decision).
+// A piece whose ticket value has not been inspected yet.
+struct Pending {
+  int valid, b, r;
+  uint32_t old;  // ticket value returned to lane 0
+};
+
+// Reduce one stream piece to its partial, publish it, and return the pending ticket.
 template <typename T, bool GREEDY>
-__device__ void stream_piece(const VerifyArgs& A, Shared& S, const SlotMeta& M,
-                             unsigned char* slot, const int* prefix, int lane) {
+__device__ Pending stream_piece(const VerifyArgs& A, const SlotMeta& M, const unsigned char* slot,
+                                int lane) {
   constexpr int VEC = ET<T>::VEC;
   const Seg& sg = M.s0;
   const T* g = reinterpret_cast<const T*>(sg.g);
@@ -553,19 +475,29 @@ __device__ void stream_piece(const VerifyArgs& A, Shared& S, const SlotMeta& M,
     soft_warp(m, s, a, lane);
     res = make_float2(m, s);
   }
-  const int b = M.b, r = M.r, P = A.P;
-  const size_t rowid = (size_t)b * A.RS + r;
-  uint32_t old = 0;
+  Pending pd;
+  pd.valid = 1;
+  pd.b = M.b;
+  pd.r = M.r;
+  pd.old = 0;
   if (lane == 0) {
-    A.part[rowid * P + M.p] = res;
-    __threadfence();
-    old = atomicAdd(A.t_row + rowid, 1u);
+    const size_t rowid = (size_t)M.b * A.RS + M.r;
+    A.part[rowid * A.P + M.p] = res;
+    pd.old = atom_add_release(A.t_row + rowid, 1u);
   }
-  old = __shfl_sync(FULL, old, 0);
-  if (old != (uint32_t)(P - 1)) return;
+  return pd;
+}
 
-  // Last piece of this row: combine the row.
+// Inspect a pending ticket: the warp that completed a row combines it, the warp that
+// completed a request decides it.
+template <typename T, bool GREEDY>
+__device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix, int lane) {
+  const uint32_t old = __shfl_sync(FULL, pd.old, 0);
+  const int P = A.P;
+  if (old != (uint32_t)(P - 1)) return;
   __threadfence();
+  const int b = pd.b;
+  const size_t rowid = (size_t)b * A.RS + pd.r;
   const float2* pr = A.part + rowid * P;
   float2 rs;
   if (GREEDY) {
@@ -594,163 +526,25 @@ __device__ void stream_piece(const VerifyArgs& A, Shared& S, const SlotMeta& M,
     rs = make_float2(m, s);
   }
   const int nrows = prefix[b + 1] - prefix[b];
+  uint32_t o2 = 0;
   if (lane == 0) {
     A.rowstat[rowid] = rs;
     A.t_row[rowid] = 0;
-    __threadfence();
-    old = atomicAdd(A.t_req + b, 1u);
+    o2 = atom_add_release(A.t_req + b, 1u);
   }
-  old = __shfl_sync(FULL, old, 0);
-  if (old != (uint32_t)(nrows - 1)) return;
-
-  // Last row of this request: decide.
+  o2 = __shfl_sync(FULL, o2, 0);
+  if (o2 != (uint32_t)(nrows - 1)) return;
   __threadfence();
   if (lane == 0) A.t_req[b] = 0;
   const int L = L_of_rows(nrows, GREEDY);
   if (GREEDY)
     decide_greedy(A, b, L, lane);
   else
-    decide_sample<T>(A, S, b, L, lane);
-}
-
-// Terminal-sample weights of one element: residual max(0, p - q), or the
-// unnormalised target weight 2^(z*a - MA) of a plain sample.
-struct TermW {
-  float a, a_lo, MAt, iSt, MAd, iSd;
-  bool resid;
-  __device__ __forceinline__ float operator()(float zt, float zd) const {
-    const float et = exp2_precise(zt, a, a_lo, MAt);
-    if (!resid) return et;
-    return fmaxf(et * iSt - exp2_precise(zd, a, a_lo, MAd) * iSd, 0.f);
-  }
-};
-
-// Process one terminal-job piece: compensated sum of its weights, reduced in fp64.
-// The last piece of a request locates the terminal token by inverse CDF at u_{b,K}
-// (float64 prefix over the piece sums, then one piece re-scanned in float64).
-template <typename T>
-__device__ void job_piece(const VerifyArgs& A, Shared& S, const SlotMeta& M, unsigned char* slot,
-                          int lane) {
-  constexpr int VEC = ET<T>::VEC;
-  const bool resid = M.jkind == J_RESID;
-  const TermW W{A.a, A.a_lo, M.MAt, M.invSt, M.MAd, M.invSd, resid};
-  float hs = 0.f, hc = 0.f;
-  const int n = M.s0.n;
-  if (!M.direct) {
-    const uint4* t4 = reinterpret_cast<const uint4*>(slot);
-    const uint4* d4 = reinterpret_cast<const uint4*>(slot + SLOT_BYTES / 2);
-    const int nv = n / VEC;
-    for (int i = lane; i < nv; i += 32) {
-      const uint4 vt = t4[i];
-      const uint4 vd = resid ? d4[i] : vt;
-      if (VEC == 8) {
-        two_sum(hs, hc, W(bf_lo(vt.x), bf_lo(vd.x)));
-        two_sum(hs, hc, W(bf_hi(vt.x), bf_hi(vd.x)));
-        two_sum(hs, hc, W(bf_lo(vt.y), bf_lo(vd.y)));
-        two_sum(hs, hc, W(bf_hi(vt.y), bf_hi(vd.y)));
-        two_sum(hs, hc, W(bf_lo(vt.z), bf_lo(vd.z)));
-        two_sum(hs, hc, W(bf_hi(vt.z), bf_hi(vd.z)));
-        two_sum(hs, hc, W(bf_lo(vt.w), bf_lo(vd.w)));
-        two_sum(hs, hc, W(bf_hi(vt.w), bf_hi(vd.w)));
-      } else {
-        two_sum(hs, hc, W(__uint_as_float(vt.x), __uint_as_float(vd.x)));
-        two_sum(hs, hc, W(__uint_as_float(vt.y), __uint_as_float(vd.y)));
-        two_sum(hs, hc, W(__uint_as_float(vt.z), __uint_as_float(vd.z)));
-        two_sum(hs, hc, W(__uint_as_float(vt.w), __uint_as_float(vd.w)));
-      }
-    }
-  } else {
-    const T* gt = reinterpret_cast<const T*>(M.s0.g);
-    const T* gd = resid ? reinterpret_cast<const T*>(M.s1.g) : gt;
-    for (int e = lane; e < n; e += 32) two_sum(hs, hc, W(ld_logit(gt + e), ld_logit(gd + e)));
-  }
-  const double acc = warp_sum_d((double)hs + (double)hc, lane);
-  const int b = M.b;
-  uint32_t old = 0;
-  if (lane == 0) {
-    A.rpart[(size_t)b * A.Rmax + M.p] = acc;
-    __threadfence();
-    old = atomicAdd(A.t_res + b, 1u);
-  }
-  old = __shfl_sync(FULL, old, 0);
-  if (old != (uint32_t)(A.R - 1)) return;
-
-  // Last piece of this job: locate the terminal token.
-  __threadfence();
-  if (lane == 0) A.t_res[b] = 0;
-  const int R = A.R, j = M.r, K = A.K;
-  const double uK = (double)__ldg(A.uni + (size_t)b * (K + 1) + K);
-  const double* rp = A.rpart + (size_t)b * A.Rmax;
-  const int c = (R + 31) / 32;
-  const int p0 = lane * c, p1 = min(R, p0 + c);
-  double ls = 0.0;
-  int lastpos = -1;
-  for (int p = p0; p < p1; ++p) {
-    const double w = __ldcg(rp + p);
-    ls += w;
-    if (w > 0.0) lastpos = p;
-  }
-  const double incl = warp_incl_scan_d(ls, lane);
-  const double Z = __shfl_sync(FULL, incl, 31);
-  if (resid && (!(Z > 0.0) || !(Z < 1e300))) {
-    // No residual mass left (p == q up to rounding): sample p_j itself instead.
-    if (lane == 0) {
-      Job J;
-      J.b = b;
-      J.j = j;
-      J.jkind = J_BONUS;
-      J.MAt = M.MAt;
-      J.invSt = J.MAd = J.invSd = 0.f;
-      post_job(S, A, J);
-    }
-    return;
-  }
-  const double target = uK * Z;
-  const unsigned hit = __ballot_sync(FULL, target < incl);
-  int pstar = -1;
-  double base = 0.0;
-  if (hit) {
-    const int ln = __ffs(hit) - 1;
-    if (lane == ln) {
-      double cum = incl - ls;
-      for (int p = p0; p < p1; ++p) {
-        const double w = __ldcg(rp + p);
-        if (target < cum + w) {
-          pstar = p;
-          break;
-        }
-        cum += w;
-      }
-      if (pstar < 0) pstar = lastpos;
-      base = cum;
-    }
-    pstar = __shfl_sync(FULL, pstar, ln);
-    base = __shfl_sync(FULL, base, ln);
-  }
-  if (pstar < 0) {  // rounding put the target past the last piece
-    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-    const int ln = has ? 31 - __clz(has) : 0;
-    pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
-    base = target;
-  }
-  const int e0 = pstar * A.E2;
-  const int ne = min(A.E2, A.V - e0);
-  unsigned char* s1 = slot + SLOT_BYTES / 2;
-  stage_row<T>(slot, static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V + e0, ne, lane);
-  if (resid)
-    stage_row<T>(s1, static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V + e0, ne, lane);
-  __syncwarp();
-  auto wf = [&](int v) {
-    const float zt = smem_logit(slot, v, T());
-    return W(zt, resid ? smem_logit(s1, v, T()) : zt);
-  };
-  const int y = e0 + locate_in_piece(wf, ne, target - base, lane);
-  if (lane == 0) A.out_tok[(size_t)b * (K + 1) + j] = y;
-  proxy_fence_shared();
+    decide_sample<T>(A, b, L, lane);
 }
 
 // ---------------------------------------------------------------------------
-// Producer: one lane. Fills slots in per-warp alternation, terminal jobs first.
+// Producer: one lane. Fills the slots of the consumer warps in per-warp alternation.
 // ---------------------------------------------------------------------------
 template <typename T, bool GREEDY>
 __device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix) {
@@ -763,104 +557,15 @@ __device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, c
   for (int w = 0; w < NCW; ++w) fills[w] = 0;
   int wrr = 0;
 
-  // Work-list cursor.
   unsigned long long cur = atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH);
   unsigned long long nxt = (cur < total) ? atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH) : total;
   unsigned long long item = cur, item_end = min(cur + Q1_BATCH, total);
   int cb = -1, cr = 0, cp = 0, cL = 0, cn = 0;  // request, row slot, piece, L, rows
-
-  // Terminal job state.
-  bool job = false;
-  Job J{};
-  int jp = 0;
-  int mh = 0;  // mailbox head
-
   bool aborted = false;
-  long long idle_t0 = -1;
 
   while (true) {
-    if (*reinterpret_cast<volatile int*>(&S.abort_flag)) {
-      aborted = true;
-      break;
-    }
-    SlotMeta m;
-    bool have = false;
-    if (!job && *reinterpret_cast<volatile int*>(&S.mbox_flag[mh & (MBOX - 1)])) {
-      __threadfence_block();
-      J = S.mbox[mh & (MBOX - 1)];
-      *reinterpret_cast<volatile int*>(&S.mbox_flag[mh & (MBOX - 1)]) = 0;
-      ++mh;
-      *reinterpret_cast<volatile int*>(&S.mbox_head) = mh;
-      job = true;
-      jp = 0;
-    }
-    if (job) {
-      const int e0 = jp * A.E2;
-      const int n = min(A.E2, A.V - e0);
-      const T* tr = static_cast<const T*>(A.tgt) + ((size_t)J.b * (A.K + 1) + J.j) * A.V + e0;
-      m.kind = K_JOB;
-      m.jkind = J.jkind;
-      m.b = J.b;
-      m.r = J.j;
-      m.p = jp;
-      m.e0 = e0;
-      m.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
-      bool aligned_all = m.s0.head == 0 && m.s0.body == n;
-      if (J.jkind == J_RESID) {
-        const T* dr = static_cast<const T*>(A.drf) + ((size_t)J.b * A.K + J.j) * A.V + e0;
-        m.s1 = make_seg(reinterpret_cast<const unsigned char*>(dr), n, eb);
-        aligned_all = aligned_all && m.s1.head == 0 && m.s1.body == n;
-      }
-      m.direct = !aligned_all;
-      m.MAt = J.MAt;
-      m.invSt = J.invSt;
-      m.MAd = J.MAd;
-      m.invSd = J.invSd;
-      if (++jp == A.R) job = false;
-      have = true;
-    } else if (item < item_end) {
-      if (cb < 0) {  // locate the item's row: binary search over the prefix
-        const unsigned long long g = item / P;
-        cp = static_cast<int>(item - g * P);
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (static_cast<unsigned long long>(prefix[mid]) <= g)
-            lo = mid;
-          else
-            hi = mid - 1;
-        }
-        cb = lo;
-        cr = static_cast<int>(g - prefix[cb]);
-        cn = prefix[cb + 1] - prefix[cb];
-        cL = L_of_rows(cn, GREEDY);
-      }
-      const T* row = row_ptr<T>(A, cb, cr, cL);
-      const int e0 = cp * A.E;
-      const int n = min(A.E, A.V - e0);
-      m.kind = K_STREAM;
-      m.b = cb;
-      m.r = cr;
-      m.p = cp;
-      m.e0 = e0;
-      m.direct = 0;
-      m.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
-      have = true;
-      ++item;
-      if (++cp == P) {
-        cp = 0;
-        if (++cr == cn) {
-          cr = 0;
-          do {
-            ++cb;
-          } while (cb < B && prefix[cb + 1] == prefix[cb]);
-          if (cb < B) {
-            cn = prefix[cb + 1] - prefix[cb];
-            cL = L_of_rows(cn, GREEDY);
-          }
-        }
-      }
-    } else if (cur < total) {
+    if (item >= item_end) {
+      if (cur >= total) break;  // work list exhausted
       cur = nxt;
       item = cur;
       item_end = min(cur + Q1_BATCH, total);
@@ -868,39 +573,56 @@ __device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, c
       if (cur < total) nxt = atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH);
       continue;
     }
-
-    if (!have) {
-      // Nothing to issue: finish once every slot is released and no job is pending.
-      bool idle = true;
-      for (int w = 0; w < NCW && idle; ++w) {
-#pragma unroll
-        for (int i = 0; i < SLOTS_PER_WARP; ++i) {
-          const uint32_t ns = (fills[w] > (uint32_t)i) ? (fills[w] - i + 1) / 2 : 0;
-          if (ns && !mbar_test(&S.empty[2 * w + i], (ns - 1) & 1)) idle = false;
+    if (cb < 0) {  // locate the item's row: binary search over the prefix
+      const unsigned long long g = item / P;
+      cp = static_cast<int>(item - g * P);
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<unsigned long long>(prefix[mid]) <= g)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      cb = lo;
+      cr = static_cast<int>(g - prefix[cb]);
+      cn = prefix[cb + 1] - prefix[cb];
+      cL = L_of_rows(cn, GREEDY);
+    }
+    SlotMeta m;
+    const T* row = row_ptr<T>(A, cb, cr, cL);
+    const int e0 = cp * A.E;
+    const int n = min(A.E, A.V - e0);
+    m.kind = K_STREAM;
+    m.b = cb;
+    m.r = cr;
+    m.p = cp;
+    m.e0 = e0;
+    m.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
+    ++item;
+    if (++cp == P) {
+      cp = 0;
+      if (++cr == cn) {
+        cr = 0;
+        do {
+          ++cb;
+        } while (cb < B && prefix[cb + 1] == prefix[cb]);
+        if (cb < B) {
+          cn = prefix[cb + 1] - prefix[cb];
+          cL = L_of_rows(cn, GREEDY);
         }
       }
-      if (idle && !*reinterpret_cast<volatile int*>(&S.mbox_flag[mh & (MBOX - 1)])) break;
-      if (idle_t0 < 0) idle_t0 = clock64();
-      if (clock64() - idle_t0 > WAIT_CYCLES) {
-        S.abort_flag = 1;
-        raise_status(A, ST_TIMEOUT);
-        aborted = true;
-        break;
-      }
-      continue;
     }
-    idle_t0 = -1;
 
-    // Find a consumer warp whose next slot is free (polling, no sleeps).
+    // Find a consumer warp whose next slot is free (polling).
     int w = -1;
     const long long t0 = clock64();
     while (w < 0) {
       for (int c = 0; c < NCW; ++c) {
         const int ww = (wrr + c) % NCW;
         const uint32_t f = fills[ww];
-        const int s = 2 * ww + (f & 1);
         const uint32_t k = f >> 1;
-        if (k == 0 || mbar_test(&S.empty[s], (k - 1) & 1)) {
+        if (k == 0 || mbar_test(&S.empty[2 * ww + (f & 1)], (k - 1) & 1)) {
           w = ww;
           break;
         }
@@ -919,29 +641,42 @@ __device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, c
     }
     wrr = (w + 1) % NCW;
     const int s = 2 * w + (fills[w] & 1);
-    unsigned char* dst = slots + (size_t)s * SLOT_BYTES;
     S.meta[s] = m;
-    uint32_t tx = 0;
-    if (m.kind == K_STREAM) {
-      tx = m.s0.body * eb;
-    } else if (!m.direct) {
-      tx = (m.jkind == J_RESID ? 2 : 1) * m.s0.body * eb;
-    }
+    const uint32_t tx = m.s0.body * eb;
     if (tx) {
       mbar_arrive_expect_tx(&S.full[s], tx);
-      if (m.kind == K_STREAM) {
-        bulk_g2s(dst, m.s0.g + m.s0.head * eb, m.s0.body * eb, &S.full[s]);
-      } else {
-        bulk_g2s(dst, m.s0.g, m.s0.body * eb, &S.full[s]);
-        if (m.jkind == J_RESID)
-          bulk_g2s(dst + SLOT_BYTES / 2, m.s1.g, m.s1.body * eb, &S.full[s]);
-      }
+      bulk_g2s(slots + (size_t)s * SLOT_BYTES, m.s0.g + m.s0.head * eb, tx, &S.full[s]);
     } else {
       mbar_arrive(&S.full[s]);
     }
     ++fills[w];
   }
 
+  if (!aborted) {
+    // Stop slot to every consumer warp, once its next slot is free.
+    for (int w = 0; w < NCW; ++w) {
+      const uint32_t f = fills[w];
+      const int s = 2 * w + (f & 1);
+      const uint32_t k = f >> 1;
+      const long long t0 = clock64();
+      bool ok = true;
+      while (k != 0 && !mbar_test(&S.empty[s], (k - 1) & 1)) {
+        if (*reinterpret_cast<volatile int*>(&S.abort_flag) || clock64() - t0 > WAIT_CYCLES) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        S.abort_flag = 1;
+        raise_status(A, ST_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      S.meta[s].kind = K_STOP;
+      mbar_arrive(&S.full[s]);
+      ++fills[w];
+    }
+  }
   if (aborted) {
     // Let every copy in flight land before the CTA may exit.
     for (int w = 0; w < NCW; ++w)
@@ -952,36 +687,31 @@ __device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, c
         while (!mbar_test(&S.full[2 * w + i], (ns - 1) & 1) && clock64() - t0 < WAIT_CYCLES) {
         }
       }
-    return;
-  }
-  // Send every consumer warp its stop slot.
-  for (int w = 0; w < NCW; ++w) {
-    const int s = 2 * w + (fills[w] & 1);
-    S.meta[s].kind = K_STOP;
-    mbar_arrive(&S.full[s]);
-    ++fills[w];
   }
 }
 
 template <typename T, bool GREEDY>
-__device__ void consumer(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
-                         int w, int lane) {
+__device__ void consumer(const VerifyArgs& A, Shared& S, const unsigned char* slots,
+                         const int* prefix, int w, int lane) {
   uint32_t it = 0;
+  Pending pd;
+  pd.valid = 0;
   while (true) {
     const int s = 2 * w + (it & 1);
     const bool ok = wait_phase(&S.full[s], (it >> 1) & 1, S, A);
     if (!__all_sync(FULL, ok)) break;
+    if (pd.valid) {  // the previous piece's ticket has had a whole wait to come back
+      settle<T, GREEDY>(A, pd, prefix, lane);
+      pd.valid = 0;
+    }
     const SlotMeta M = S.meta[s];
     if (M.kind == K_STOP) break;
-    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
-    if (M.kind == K_STREAM)
-      stream_piece<T, GREEDY>(A, S, M, slot, prefix, lane);
-    else
-      job_piece<T>(A, S, M, slot, lane);
+    pd = stream_piece<T, GREEDY>(A, M, slots + (size_t)s * SLOT_BYTES, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
     ++it;
   }
+  if (pd.valid) settle<T, GREEDY>(A, pd, prefix, lane);
 }
 
 template <typename T, bool GREEDY>
@@ -1024,11 +754,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
   if (tid == 0) {
     S.total_rows = S.scan[NTHREADS / 32 - 1];
     prefix[B] = S.scan[NTHREADS / 32 - 1];
-    S.mbox_tail = 0;
-    S.mbox_head = 0;
     S.abort_flag = 0;
     S.last_cta = 0;
-    for (int i = 0; i < MBOX; ++i) S.mbox_flag[i] = 0;
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
@@ -1064,10 +791,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
     const bool dirty = (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) != 0;
     if (dirty) {
       for (size_t i = tid; i < TICKET_ROW_WORDS; i += NTHREADS) A.t_row[i] = 0;
-      for (int i = tid; i < SV_MAX_B; i += NTHREADS) {
-        A.t_req[i] = 0;
-        A.t_res[i] = 0;
-      }
+      for (int i = tid; i < SV_MAX_B; i += NTHREADS) A.t_req[i] = 0;
     }
     if (tid == 0) {
       A.hdr->q1_next = 0;
@@ -1077,7 +801,208 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
 }
 
 // ---------------------------------------------------------------------------
-// Host launcher (called from the C-ABI layer).
+// Terminal-sample kernel (T > 0).
+// ---------------------------------------------------------------------------
+
+// Weight of one element: residual max(0, p - q), or the unnormalised target weight
+// 2^(z*a - MA) of a plain sample.
+struct TermW {
+  float a, a_lo, MAt, iSt, MAd, iSd;
+  bool resid;
+  __device__ __forceinline__ float operator()(float zt, float zd) const {
+    const float et = exp2_precise(zt, a, a_lo, MAt);
+    if (!resid) return et;
+    return fmaxf(et * iSt - exp2_precise(zd, a, a_lo, MAd) * iSd, 0.f);
+  }
+};
+
+// Compensated sum over elements [0, n) of rows t (and d) with the weight W.
+template <typename T>
+__device__ void term_sum(const T* t, const T* d, int n, const TermW& W, int lane, float& hs,
+                         float& hc) {
+  constexpr int VEC = ET<T>::VEC;
+  const bool vec = ((reinterpret_cast<uintptr_t>(t) | reinterpret_cast<uintptr_t>(d)) & 15) == 0;
+  int done = 0;
+  if (vec) {
+    const int nv = n / VEC;
+    const uint4* t4 = reinterpret_cast<const uint4*>(t);
+    const uint4* d4 = reinterpret_cast<const uint4*>(d);
+#pragma unroll 2
+    for (int i = lane; i < nv; i += 32) {
+      const uint4 vt = __ldg(t4 + i);
+      const uint4 vd = W.resid ? __ldg(d4 + i) : vt;
+      if (VEC == 8) {
+        two_sum(hs, hc, W(bf_lo(vt.x), bf_lo(vd.x)));
+        two_sum(hs, hc, W(bf_hi(vt.x), bf_hi(vd.x)));
+        two_sum(hs, hc, W(bf_lo(vt.y), bf_lo(vd.y)));
+        two_sum(hs, hc, W(bf_hi(vt.y), bf_hi(vd.y)));
+        two_sum(hs, hc, W(bf_lo(vt.z), bf_lo(vd.z)));
+        two_sum(hs, hc, W(bf_hi(vt.z), bf_hi(vd.z)));
+        two_sum(hs, hc, W(bf_lo(vt.w), bf_lo(vd.w)));
+        two_sum(hs, hc, W(bf_hi(vt.w), bf_hi(vd.w)));
+      } else {
+        two_sum(hs, hc, W(__uint_as_float(vt.x), __uint_as_float(vd.x)));
+        two_sum(hs, hc, W(__uint_as_float(vt.y), __uint_as_float(vd.y)));
+        two_sum(hs, hc, W(__uint_as_float(vt.z), __uint_as_float(vd.z)));
+        two_sum(hs, hc, W(__uint_as_float(vt.w), __uint_as_float(vd.w)));
+      }
+    }
+    done = nv * VEC;
+  }
+  for (int e = done + lane; e < n; e += 32) two_sum(hs, hc, W(ld_logit(t + e), ld_logit(d + e)));
+}
+
+// Inverse-CDF step over elements [0, n) of rows t (and d): the smallest v with
+// target < cum(v), cum in float64 over the fp32 weights. Lanes take contiguous ranges;
+// falls back to the last positive-weight element when rounding leaves target past
+// the end.
+template <typename T>
+__device__ int locate_range(const T* t, const T* d, int n, const TermW& W, double target,
+                            int lane) {
+  const int c = (n + 31) / 32;
+  const int v0 = min(n, lane * c), v1 = min(n, v0 + c);
+  float hs = 0.f, hc = 0.f;
+  int lastpos = -1;
+  for (int v = v0; v < v1; ++v) {
+    const float w = W(ld_logit(t + v), ld_logit(d + v));
+    two_sum(hs, hc, w);
+    if (w > 0.f) lastpos = v;
+  }
+  const double ls = (double)hs + (double)hc;
+  const double incl = warp_incl_scan_d(ls, lane);
+  const unsigned hit = __ballot_sync(FULL, target < incl);
+  int y = -1;
+  if (hit) {
+    const int ln = __ffs(hit) - 1;
+    if (lane == ln) {
+      double cum = incl - ls;
+      for (int v = v0; v < v1; ++v) {
+        cum += (double)W(ld_logit(t + v), ld_logit(d + v));
+        if (target < cum) {
+          y = v;
+          break;
+        }
+      }
+      if (y < 0) y = lastpos;
+    }
+    y = __shfl_sync(FULL, y, ln);
+  }
+  if (y < 0) {
+    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
+    y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : 0;
+  }
+  return y;
+}
+
+// Locate the terminal token of request b from its R piece sums.
+template <typename T>
+__device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const TermW& W,
+                           int lane) {
+  const int R = A.R, K = A.K, j = J.j;
+  const T* trow = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V;
+  const T* drow = W.resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V : trow;
+  const double uK = (double)__ldg(A.uni + (size_t)b * (K + 1) + K);
+  const double* rp = A.rpart + (size_t)b * A.Rmax;
+  const int c = (R + 31) / 32;
+  const int p0 = min(R, lane * c), p1 = min(R, p0 + c);
+  double ls = 0.0;
+  int lastpos = -1;
+  for (int p = p0; p < p1; ++p) {
+    const double w = __ldcg(rp + p);
+    ls += w;
+    if (w > 0.0) lastpos = p;
+  }
+  const double incl = warp_incl_scan_d(ls, lane);
+  const double Z = __shfl_sync(FULL, incl, 31);
+  if (W.resid && (!(Z > 0.0) || !(Z < 1e300))) {
+    // No residual mass left (p == q up to rounding): sample p_j itself instead,
+    // over the whole row.
+    TermW Wp = W;
+    Wp.resid = false;
+    float hs = 0.f, hc = 0.f;
+    const int cc = (A.V + 31) / 32;
+    const int v0 = min(A.V, lane * cc), v1 = min(A.V, v0 + cc);
+    for (int v = v0; v < v1; ++v) {
+      const float z = ld_logit(trow + v);
+      two_sum(hs, hc, Wp(z, z));
+    }
+    const double Zp = warp_sum_d((double)hs + (double)hc, lane);
+    return locate_range<T>(trow, trow, A.V, Wp, uK * Zp, lane);
+  }
+  const double target = uK * Z;
+  const unsigned hit = __ballot_sync(FULL, target < incl);
+  int pstar = -1;
+  double base = 0.0;
+  if (hit) {
+    const int ln = __ffs(hit) - 1;
+    if (lane == ln) {
+      double cum = incl - ls;
+      for (int p = p0; p < p1; ++p) {
+        const double w = __ldcg(rp + p);
+        if (target < cum + w) {
+          pstar = p;
+          break;
+        }
+        cum += w;
+      }
+      if (pstar < 0) pstar = lastpos;
+      base = cum;
+    }
+    pstar = __shfl_sync(FULL, pstar, ln);
+    base = __shfl_sync(FULL, base, ln);
+  }
+  if (pstar < 0) {  // rounding put the target past the last piece
+    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
+    const int ln = has ? 31 - __clz(has) : 0;
+    pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
+    base = target;
+  }
+  const int e0 = pstar * A.E2;
+  const int ne = min(A.E2, A.V - e0);
+  return e0 + locate_range<T>(trow + e0, drow + e0, ne, W, target - base, lane);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * TERM_WARPS) sv_terminal_kernel(const VerifyArgs A) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * TERM_WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * TERM_WARPS;
+  const int R = A.R, K = A.K;
+  // After a timed-out stream kernel the job records may be stale: do nothing (the
+  // status word already reports the timeout).
+  if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return;
+  const long long total = (long long)A.B * R;
+  for (long long task = gw; task < total; task += nw) {
+    const int b = (int)(task / R), p = (int)(task - (long long)b * R);
+    const TermJob J = A.jobs[b];
+    if (J.kind == J_NONE) continue;
+    if (!((J.kind == J_RESID && J.j >= 0 && J.j < K) || (J.kind == J_BONUS && J.j >= 0 && J.j <= K)))
+      continue;
+    const bool resid = J.kind == J_RESID;
+    const TermW W{A.a, A.a_lo, J.MAt, J.invSt, J.MAd, J.invSd, resid};
+    const int e0 = p * A.E2;
+    const int n = min(A.E2, A.V - e0);
+    const T* t = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + J.j) * A.V + e0;
+    const T* d = resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + J.j) * A.V + e0 : t;
+    float hs = 0.f, hc = 0.f;
+    term_sum<T>(t, d, n, W, lane, hs, hc);
+    const double acc = warp_sum_d((double)hs + (double)hc, lane);
+    uint32_t old = 0;
+    if (lane == 0) {
+      A.rpart[(size_t)b * A.Rmax + p] = acc;
+      old = atom_add_release(A.t_res + b, 1u);
+    }
+    old = __shfl_sync(FULL, old, 0);
+    if (old != (uint32_t)(R - 1)) continue;
+    __threadfence();
+    if (lane == 0) A.t_res[b] = 0;
+    const int y = term_locate<T>(A, b, J, W, lane);
+    if (lane == 0) A.out_tok[(size_t)b * (K + 1) + J.j] = y;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers (called from the C-ABI layer).
 // ---------------------------------------------------------------------------
 template <typename T, bool GREEDY>
 static cudaError_t launch_t(const VerifyArgs& A, int grid, size_t dsmem, cudaStream_t st) {
@@ -1090,6 +1015,12 @@ static cudaError_t launch_t(const VerifyArgs& A, int grid, size_t dsmem, cudaStr
     attr_set = true;
   }
   sv_verify_kernel<T, GREEDY><<<grid, NTHREADS, dsmem, st>>>(A);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || GREEDY) return e;
+  const long long tasks = (long long)A.B * A.R;
+  const long long want = (tasks + TERM_WARPS - 1) / TERM_WARPS;
+  const int tgrid = (int)(want < 4LL * grid ? want : 4LL * grid);
+  sv_terminal_kernel<T><<<tgrid, 32 * TERM_WARPS, 0, st>>>(A);
   return cudaGetLastError();
 }
 

@@ -71,9 +71,17 @@ def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
         K = gp.shape[1]
         mask = (np.arange(K)[None, :] < np.clip(L, 0, K)[:, None]) & valid[:, None]
         for name, g, r in (("p", gp, ref["p"]), ("q", gq, ref["q"])):
-            err = np.abs(g[mask].astype(np.float64) - r[mask])
-            lim = P_RTOL * np.abs(r[mask]) + 1e-30
-            assert (err <= lim).all(), f"{name} rel err {np.max(err / (np.abs(r[mask]) + 1e-300))}"
+            err = np.abs(g.astype(np.float64) - r)
+            lim = P_RTOL * np.abs(r) + 1e-30
+            badm = mask & ~(err <= lim)
+            if badm.any():
+                rel = np.where(badm, err / (np.abs(r) + 1e-300), 0)
+                bb, kk = np.unravel_index(np.argmax(rel), rel.shape)
+                raise AssertionError(
+                    f"{name} rel err {rel[bb, kk]:.3e} at request {bb} position {kk}: gpu "
+                    f"{g[bb, kk]:.9e} ref {r[bb, kk]:.9e} (other: gpu p {gp[bb, kk]:.6e} "
+                    f"q {gq[bb, kk]:.6e}; ref p {ref['p'][bb, kk]:.6e} q {ref['q'][bb, kk]:.6e}); "
+                    f"{int(badm.sum())} elements over")
     positions = int((np.clip(L, 0, None) + 1).sum())
     differ = flagged & ((acc != ref["out_accepted"]) | (tok != ref["out_tok"]).any(axis=1))
     for b in np.nonzero(differ)[0][:5]:
