@@ -120,9 +120,9 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.rpart = reinterpret_cast<double*>(ws + L.rpart);
   A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);
 
-  // One persistent CTA per SM, fewer when the batch cannot feed them all.
+  // One persistent CTA per SM, fewer when the batch cannot give every warp a piece.
   const long long max_pieces = (long long)B * (greedy ? K + 1 : 2 * K + 1) * A.P;
-  const long long want = (max_pieces + Q1_BATCH - 1) / Q1_BATCH;
+  const long long want = (max_pieces + NCW - 1) / NCW;
   const int grid = (int)(want < sms ? want : sms);
   const cudaError_t e =
       launch_verify(A, dtype == SV_BF16, greedy, grid, static_cast<cudaStream_t>(stream));

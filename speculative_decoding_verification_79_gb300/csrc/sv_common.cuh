@@ -13,16 +13,15 @@ namespace sv {
 
 // ---------------------------------------------------------------------------
 // Tuning constants of the fused verify kernel.
-// One persistent CTA per SM: one producer warp issues 1-D bulk copies (TMA) of
-// row pieces into a ring of shared-memory slots; NCW consumer warps each own
-// SLOTS_PER_WARP slots and reduce whole pieces on their own.
+// One persistent CTA per SM of NCW warps; each warp owns SLOTS_PER_WARP shared-memory
+// slots, issues its own 1-D bulk copies (TMA) of row pieces into them and reduces
+// whole pieces on its own.
 // ---------------------------------------------------------------------------
 constexpr int SLOT_BYTES = 8192;
 constexpr int NCW = 12;
 constexpr int SLOTS_PER_WARP = 2;
 constexpr int NSLOT = NCW * SLOTS_PER_WARP;
-constexpr int NTHREADS = 32 * (NCW + 1);
-constexpr int Q1_BATCH = 8;                      // pieces claimed per atomic on the work counter
+constexpr int NTHREADS = 32 * NCW;
 constexpr int TERM_WARPS = 8;                    // warps per CTA of the terminal kernel
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz: bound on any wait
 
@@ -35,7 +34,7 @@ constexpr uint32_t ST_TIMEOUT = 2u;
 // ---------------------------------------------------------------------------
 struct WsHeader {
   uint32_t status;    // ST_* bits
-  uint32_t q1_next;   // verify: next unclaimed stream piece
+  uint32_t reserved;
   uint32_t cta_done;  // verify: CTAs that have finished
   uint32_t pad[61];
 };

@@ -7,15 +7,18 @@
 // Two launches on the caller's stream, no CPU round trip:
 //  1. sv_verify_kernel, one persistent CTA per SM. Work list: every active logit row
 //     of the batch (request b: target rows 0..L_b, and at T > 0 draft rows
-//     0..L_b-1) cut into pieces of SLOT_BYTES, ordered request-major and claimed in
-//     batches from one atomic counter. A producer warp issues 1-D bulk copies
-//     (cp.async.bulk, TMA) of each piece into a shared-memory slot guarded by an
-//     mbarrier; consumer warps each own two slots and reduce whole pieces: online
-//     softmax (running max + sum of 2^(z*log2e/T - max)) at T > 0, or (max, lowest
-//     argmax) at T == 0. Each piece result is published with a release-ordered
-//     atomic ticket whose value the warp inspects only after waiting for its next
-//     slot, so the round trip hides behind the next piece. The warp completing a
-//     row combines it; the warp completing a request decides it: p_k(x_k), q_k(x_k),
+//     0..L_b-1) cut into pieces of SLOT_BYTES, ordered request-major; every warp of
+//     the grid takes an equal contiguous range of it. Each warp owns SLOTS_PER_WARP
+//     shared-memory slots and is its own producer: lane 0 issues a 1-D bulk copy
+//     (cp.async.bulk, TMA) of the next piece into the slot the warp has just
+//     finished, guarded by an mbarrier, while the warp reduces the other slots.
+//     Pieces are reduced whole: online softmax (running max + sum of
+//     2^(z*log2e/T - max)) at T > 0, or (max, lowest argmax) at T == 0, and merged in
+//     registers while consecutive pieces belong to the same row. Each row segment is
+//     published with a release-ordered atomic ticket whose value the warp inspects
+//     only after its next wait, so the round trip stays off the critical path. The
+//     warp completing a row combines it; the warp completing a request decides it:
+//     p_k(x_k), q_k(x_k),
 //     the accept tests u*q < p, a ballot for the first rejection j, the outputs,
 //     and (T > 0) the terminal-sample job of the request.
 //  2. sv_terminal_kernel (T > 0 only): one warp per (request, piece) task sums the
@@ -52,7 +55,6 @@ struct __align__(16) SlotMeta {
 struct Shared {
   SlotMeta meta[NSLOT];
   uint64_t full[NSLOT];
-  uint64_t empty[NSLOT];
   int abort_flag;
   int last_cta;
   int total_rows;
@@ -81,12 +83,16 @@ constexpr unsigned FULL = 0xffffffffu;
 // Online softmax pieces. State (m, s): m = running max of the raw logits, s = sum of
 // 2^(z*a - fl(m*a)). Merging uses the same rounded fl(m*a) on both sides.
 // ---------------------------------------------------------------------------
+// The frame of a partial sum is the ROUNDED product fl(m*a); every product below is
+// rounded explicitly (__fmul_rn) so the compiler cannot fuse it into an FMA with the
+// following subtraction, which would rescale a sum already in the right frame by
+// 2^(m*a - fl(m*a)) once per merge level.
 __device__ __forceinline__ void soft_merge(float& m, float& s, float m2, float s2, float a) {
   const float mn = fmax_nan(m, m2);
   if (mn == -INFINITY) return;  // both empty
-  const float man = mn * a;
-  const float f1 = (m == -INFINITY) ? 0.f : ex2(m * a - man);
-  const float f2 = (m2 == -INFINITY) ? 0.f : ex2(m2 * a - man);
+  const float man = __fmul_rn(mn, a);
+  const float f1 = (m == -INFINITY) ? 0.f : ex2(__fmul_rn(m, a) - man);
+  const float f2 = (m2 == -INFINITY) ? 0.f : ex2(__fmul_rn(m2, a) - man);
   s = fmaf(s, f1, s2 * f2);
   m = mn;
 }
@@ -94,7 +100,7 @@ __device__ __forceinline__ void soft_merge(float& m, float& s, float m2, float s
 __device__ __forceinline__ void soft_rescale(float& m, float& ma, float& s, float lm, float a) {
   if (lm > m || lm != lm) {
     const float mn = fmax_nan(m, lm);
-    const float man = mn * a;
+    const float man = __fmul_rn(mn, a);
     s = s * ex2(ma - man);
     m = mn;
     ma = man;
@@ -348,8 +354,8 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
     ok = x >= 0 && x < V && finitef(st.x) && finitef(sd.x) && st.y > 0.f && finitef(st.y) &&
          sd.y > 0.f && finitef(sd.y) && u >= 0.f && u < 1.f;
     if (ok) {
-      MAt = st.x * A.a;
-      MAd = sd.x * A.a;
+      MAt = __fmul_rn(st.x, A.a);
+      MAd = __fmul_rn(sd.x, A.a);
       const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + lane) * V;
       const T* dr = static_cast<const T*>(A.drf) + ((size_t)b * K + lane) * V;
       const float et = exp2_precise(ld_logit(tr + x), A.a, A.a_lo, MAt);
@@ -386,7 +392,7 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
     J.j = j;
     if (j == L) {  // every draft accepted: bonus sample from p_L
       J.kind = J_BONUS;
-      J.MAt = sL.x * A.a;
+      J.MAt = __fmul_rn(sL.x, A.a);
       J.invSt = J.MAd = J.invSd = 0.f;
     } else {  // first rejection at j: residual sample
       J.kind = J_RESID;
@@ -436,23 +442,16 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   }
 }
 
-// A piece whose ticket value has not been inspected yet.
-struct Pending {
-  int valid, b, r;
-  uint32_t old;  // ticket value returned to lane 0
-};
-
-// Reduce one stream piece to its partial, publish it, and return the pending ticket.
+// Reduce one stream piece; every lane returns the piece's (max, sum) or (max, argmax).
 template <typename T, bool GREEDY>
-__device__ Pending stream_piece(const VerifyArgs& A, const SlotMeta& M, const unsigned char* slot,
-                                int lane) {
+__device__ float2 reduce_piece(const VerifyArgs& A, const SlotMeta& M, const unsigned char* slot,
+                               int lane, bool& bad_out) {
   constexpr int VEC = ET<T>::VEC;
   const Seg& sg = M.s0;
   const T* g = reinterpret_cast<const T*>(sg.g);
   const int tail = sg.n - sg.head - sg.body;
   const int nv = sg.body / VEC;
   const uint4* v4 = reinterpret_cast<const uint4*>(slot);
-  float2 res;
   if (GREEDY) {
     float best = -INFINITY;
     int idx = INT_MAX;
@@ -464,26 +463,67 @@ __device__ Pending stream_piece(const VerifyArgs& A, const SlotMeta& M, const un
     if (lane < tail)
       arg_add1(best, idx, bad, ld_logit(g + sg.head + sg.body + lane), base + sg.body + lane);
     arg_warp(best, idx, bad);
-    res = make_float2(bad ? __int_as_float(0x7fc00000) : best, __int_as_float(idx));
-  } else {
-    const float a = A.a;
-    float m = -INFINITY, ma = -INFINITY, s = 0.f;
-    if (lane < sg.head) soft_add1(m, ma, s, ld_logit(g + lane), a);
-#pragma unroll 4
-    for (int i = lane; i < nv; i += 32) soft_add_vec(m, ma, s, v4[i], a, T());
-    if (lane < tail) soft_add1(m, ma, s, ld_logit(g + sg.head + sg.body + lane), a);
-    soft_warp(m, s, a, lane);
-    res = make_float2(m, s);
+    bad_out = bad;
+    return make_float2(best, __int_as_float(idx));
   }
+  const float a = A.a;
+  float m = -INFINITY, ma = -INFINITY, s = 0.f;
+  if (lane < sg.head) soft_add1(m, ma, s, ld_logit(g + lane), a);
+#pragma unroll 4
+  for (int i = lane; i < nv; i += 32) soft_add_vec(m, ma, s, v4[i], a, T());
+  if (lane < tail) soft_add1(m, ma, s, ld_logit(g + sg.head + sg.body + lane), a);
+  soft_warp(m, s, a, lane);
+  bad_out = false;
+  return make_float2(m, s);
+}
+
+// Running partial of one row segment (consecutive pieces of one row handled by one
+// warp), identical in every lane.
+struct Segment {
+  int valid, b, r, p0, p1;  // pieces [p0, p1] of row slot r of request b
+  float2 acc;
+  bool bad;
+};
+
+// A published segment whose ticket value has not been inspected yet.
+struct Pending {
+  int valid, b, r, count;
+  uint32_t old;  // ticket value returned to lane 0
+};
+
+template <bool GREEDY>
+__device__ __forceinline__ void seg_merge(Segment& sg, float2 v, bool bad, float a) {
+  if (GREEDY) {
+    const int vi = __float_as_int(v.y), ai = __float_as_int(sg.acc.y);
+    if (v.x > sg.acc.x || (v.x == sg.acc.x && vi < ai)) sg.acc = v;
+    sg.bad = sg.bad || bad;
+  } else {
+    float m = sg.acc.x, s = sg.acc.y;
+    soft_merge(m, s, v.x, v.y, a);
+    sg.acc = make_float2(m, s);
+  }
+}
+
+// Publish a segment: its partial at slot p0, neutral partials at p0+1..p1, then a
+// release-ordered ticket increment by the number of pieces. Lane 0 writes everything.
+template <bool GREEDY>
+__device__ Pending publish(const VerifyArgs& A, const Segment& sg, int lane) {
   Pending pd;
   pd.valid = 1;
-  pd.b = M.b;
-  pd.r = M.r;
+  pd.b = sg.b;
+  pd.r = sg.r;
+  pd.count = sg.p1 - sg.p0 + 1;
   pd.old = 0;
   if (lane == 0) {
-    const size_t rowid = (size_t)M.b * A.RS + M.r;
-    A.part[rowid * A.P + M.p] = res;
-    pd.old = atom_add_release(A.t_row + rowid, 1u);
+    const size_t rowid = (size_t)sg.b * A.RS + sg.r;
+    float2* pr = A.part + rowid * A.P;
+    float2 v = sg.acc;
+    if (GREEDY && sg.bad) v.x = __int_as_float(0x7fc00000);
+    pr[sg.p0] = v;
+    const float2 neutral = GREEDY ? make_float2(-INFINITY, __int_as_float(INT_MAX))
+                                  : make_float2(-INFINITY, 0.f);
+    for (int q = sg.p0 + 1; q <= sg.p1; ++q) pr[q] = neutral;
+    pd.old = atom_add_release(A.t_row + rowid, (uint32_t)pd.count);
   }
   return pd;
 }
@@ -494,7 +534,7 @@ template <typename T, bool GREEDY>
 __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix, int lane) {
   const uint32_t old = __shfl_sync(FULL, pd.old, 0);
   const int P = A.P;
-  if (old != (uint32_t)(P - 1)) return;
+  if (old + (uint32_t)pd.count != (uint32_t)P) return;
   __threadfence();
   const int b = pd.b;
   const size_t rowid = (size_t)b * A.RS + pd.r;
@@ -544,174 +584,175 @@ __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix
 }
 
 // ---------------------------------------------------------------------------
-// Producer: one lane. Fills the slots of the consumer warps in per-warp alternation.
+// Per-warp work: a contiguous range [i0, i1) of the work list (equal shares), walked
+// by a cursor in lane 0 that issues the bulk copy of each piece into the warp's
+// next free slot.
 // ---------------------------------------------------------------------------
+struct Cursor {
+  unsigned long long cur, end;
+  int cb, cr, cp, cL, cn;  // request, row slot, piece, L, rows of the current item
+};
+
+template <bool GREEDY>
+__device__ void cursor_init(Cursor& c, const VerifyArgs& A, const int* prefix,
+                            unsigned long long i0, unsigned long long i1) {
+  c.cur = i0;
+  c.end = i1;
+  if (i0 >= i1) return;
+  const int P = A.P;
+  const unsigned long long g = i0 / P;
+  c.cp = static_cast<int>(i0 - g * P);
+  int lo = 0, hi = A.B - 1;
+  while (lo < hi) {  // last request whose prefix is <= g
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<unsigned long long>(prefix[mid]) <= g)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  c.cb = lo;
+  c.cr = static_cast<int>(g - prefix[lo]);
+  c.cn = prefix[lo + 1] - prefix[lo];
+  c.cL = L_of_rows(c.cn, GREEDY);
+}
+
+// Next piece of the warp's range into a slot: fills the slot's metadata and starts
+// its bulk copy. Returns false at the end of the range. Lane 0 only.
 template <typename T, bool GREEDY>
-__device__ void producer(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix) {
+__device__ bool issue_next(const VerifyArgs& A, Cursor& c, const int* prefix, SlotMeta& meta,
+                           uint64_t* full, unsigned char* slot) {
   constexpr int eb = sizeof(T);
   const int P = A.P, B = A.B;
+  if (c.cur >= c.end) return false;
+  const T* row = row_ptr<T>(A, c.cb, c.cr, c.cL);
+  const int e0 = c.cp * A.E;
+  const int n = min(A.E, A.V - e0);
+  meta.kind = K_STREAM;
+  meta.b = c.cb;
+  meta.r = c.cr;
+  meta.p = c.cp;
+  meta.e0 = e0;
+  meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
+  ++c.cur;
+  if (++c.cp == P) {
+    c.cp = 0;
+    if (++c.cr == c.cn) {
+      c.cr = 0;
+      do {
+        ++c.cb;
+      } while (c.cb < B && prefix[c.cb + 1] == prefix[c.cb]);
+      if (c.cb < B) {
+        c.cn = prefix[c.cb + 1] - prefix[c.cb];
+        c.cL = L_of_rows(c.cn, GREEDY);
+      }
+    }
+  }
+  const uint32_t tx = meta.s0.body * eb;
+  if (tx) {
+    mbar_arrive_expect_tx(full, tx);
+    bulk_g2s(slot, meta.s0.g + meta.s0.head * eb, tx, full);
+  } else {
+    mbar_arrive(full);
+  }
+  return true;
+}
+
+// One warp: its range of pieces through SLOTS_PER_WARP slots; each slot is refilled
+// right after the warp has reduced it.
+template <typename T, bool GREEDY>
+__device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
+                          int w, int lane) {
   const unsigned long long total =
-      static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(P);
-  uint32_t fills[NCW];
+      static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(A.P);
+  const unsigned long long nw = (unsigned long long)gridDim.x * NCW;
+  const unsigned long long gw = (unsigned long long)blockIdx.x * NCW + w;
+  const unsigned long long i0 = total * gw / nw, i1 = total * (gw + 1) / nw;
+  Cursor c;
+  int have[SLOTS_PER_WARP];
+  uint32_t cons[SLOTS_PER_WARP];
 #pragma unroll
-  for (int w = 0; w < NCW; ++w) fills[w] = 0;
-  int wrr = 0;
-
-  unsigned long long cur = atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH);
-  unsigned long long nxt = (cur < total) ? atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH) : total;
-  unsigned long long item = cur, item_end = min(cur + Q1_BATCH, total);
-  int cb = -1, cr = 0, cp = 0, cL = 0, cn = 0;  // request, row slot, piece, L, rows
+  for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+    have[q] = 0;
+    cons[q] = 0;
+  }
+  if (lane == 0) {
+    cursor_init<GREEDY>(c, A, prefix, i0, i1);
+#pragma unroll
+    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+      const int s = SLOTS_PER_WARP * w + q;
+      have[q] = issue_next<T, GREEDY>(A, c, prefix, S.meta[s], &S.full[s],
+                                      slots + (size_t)s * SLOT_BYTES);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < SLOTS_PER_WARP; ++q) have[q] = __shfl_sync(FULL, have[q], 0);
+  Pending pd;
+  pd.valid = 0;
+  Segment sg;
+  sg.valid = 0;
+  unsigned long long item = i0;
+  int k = 0;
   bool aborted = false;
-
-  while (true) {
-    if (item >= item_end) {
-      if (cur >= total) break;  // work list exhausted
-      cur = nxt;
-      item = cur;
-      item_end = min(cur + Q1_BATCH, total);
-      cb = -1;
-      if (cur < total) nxt = atomicAdd(&A.hdr->q1_next, (unsigned)Q1_BATCH);
-      continue;
-    }
-    if (cb < 0) {  // locate the item's row: binary search over the prefix
-      const unsigned long long g = item / P;
-      cp = static_cast<int>(item - g * P);
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<unsigned long long>(prefix[mid]) <= g)
-          lo = mid;
-        else
-          hi = mid - 1;
-      }
-      cb = lo;
-      cr = static_cast<int>(g - prefix[cb]);
-      cn = prefix[cb + 1] - prefix[cb];
-      cL = L_of_rows(cn, GREEDY);
-    }
-    SlotMeta m;
-    const T* row = row_ptr<T>(A, cb, cr, cL);
-    const int e0 = cp * A.E;
-    const int n = min(A.E, A.V - e0);
-    m.kind = K_STREAM;
-    m.b = cb;
-    m.r = cr;
-    m.p = cp;
-    m.e0 = e0;
-    m.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
-    ++item;
-    if (++cp == P) {
-      cp = 0;
-      if (++cr == cn) {
-        cr = 0;
-        do {
-          ++cb;
-        } while (cb < B && prefix[cb + 1] == prefix[cb]);
-        if (cb < B) {
-          cn = prefix[cb + 1] - prefix[cb];
-          cL = L_of_rows(cn, GREEDY);
-        }
-      }
-    }
-
-    // Find a consumer warp whose next slot is free (polling).
-    int w = -1;
-    const long long t0 = clock64();
-    while (w < 0) {
-      for (int c = 0; c < NCW; ++c) {
-        const int ww = (wrr + c) % NCW;
-        const uint32_t f = fills[ww];
-        const uint32_t k = f >> 1;
-        if (k == 0 || mbar_test(&S.empty[2 * ww + (f & 1)], (k - 1) & 1)) {
-          w = ww;
-          break;
-        }
-      }
-      if (w >= 0) break;
-      if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
-      if (clock64() - t0 > WAIT_CYCLES) {
-        S.abort_flag = 1;
-        raise_status(A, ST_TIMEOUT);
-        break;
-      }
-    }
-    if (w < 0) {
+  while (have[k]) {
+    const int s = SLOTS_PER_WARP * w + k;
+    const bool ok = wait_phase(&S.full[s], cons[k] & 1, S, A);
+    if (!__all_sync(FULL, ok)) {
       aborted = true;
       break;
     }
-    wrr = (w + 1) % NCW;
-    const int s = 2 * w + (fills[w] & 1);
-    S.meta[s] = m;
-    const uint32_t tx = m.s0.body * eb;
-    if (tx) {
-      mbar_arrive_expect_tx(&S.full[s], tx);
-      bulk_g2s(slots + (size_t)s * SLOT_BYTES, m.s0.g + m.s0.head * eb, tx, &S.full[s]);
-    } else {
-      mbar_arrive(&S.full[s]);
-    }
-    ++fills[w];
-  }
-
-  if (!aborted) {
-    // Stop slot to every consumer warp, once its next slot is free.
-    for (int w = 0; w < NCW; ++w) {
-      const uint32_t f = fills[w];
-      const int s = 2 * w + (f & 1);
-      const uint32_t k = f >> 1;
-      const long long t0 = clock64();
-      bool ok = true;
-      while (k != 0 && !mbar_test(&S.empty[s], (k - 1) & 1)) {
-        if (*reinterpret_cast<volatile int*>(&S.abort_flag) || clock64() - t0 > WAIT_CYCLES) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok) {
-        S.abort_flag = 1;
-        raise_status(A, ST_TIMEOUT);
-        aborted = true;
-        break;
-      }
-      S.meta[s].kind = K_STOP;
-      mbar_arrive(&S.full[s]);
-      ++fills[w];
-    }
-  }
-  if (aborted) {
-    // Let every copy in flight land before the CTA may exit.
-    for (int w = 0; w < NCW; ++w)
-      for (int i = 0; i < SLOTS_PER_WARP; ++i) {
-        const uint32_t ns = (fills[w] > (uint32_t)i) ? (fills[w] - i + 1) / 2 : 0;
-        if (!ns) continue;
-        const long long t0 = clock64();
-        while (!mbar_test(&S.full[2 * w + i], (ns - 1) & 1) && clock64() - t0 < WAIT_CYCLES) {
-        }
-      }
-  }
-}
-
-template <typename T, bool GREEDY>
-__device__ void consumer(const VerifyArgs& A, Shared& S, const unsigned char* slots,
-                         const int* prefix, int w, int lane) {
-  uint32_t it = 0;
-  Pending pd;
-  pd.valid = 0;
-  while (true) {
-    const int s = 2 * w + (it & 1);
-    const bool ok = wait_phase(&S.full[s], (it >> 1) & 1, S, A);
-    if (!__all_sync(FULL, ok)) break;
-    if (pd.valid) {  // the previous piece's ticket has had a whole wait to come back
+    if (pd.valid) {  // the previous segment's ticket has had a whole wait to come back
       settle<T, GREEDY>(A, pd, prefix, lane);
       pd.valid = 0;
     }
     const SlotMeta M = S.meta[s];
-    if (M.kind == K_STOP) break;
-    pd = stream_piece<T, GREEDY>(A, M, slots + (size_t)s * SLOT_BYTES, lane);
+    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
+    bool bad;
+    const float2 v = reduce_piece<T, GREEDY>(A, M, slot, lane, bad);
+    ++cons[k];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
-    ++it;
+    int h = 0;
+    if (lane == 0) {
+      // The slot's shared-memory reads are done; order them before the async-proxy
+      // write of the next copy into the same slot.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      h = issue_next<T, GREEDY>(A, c, prefix, S.meta[s], &S.full[s], slot);
+    }
+    have[k] = __shfl_sync(FULL, h, 0);
+    // Extend or start the row segment; publish at the row's last piece or the
+    // range's last piece.
+    if (sg.valid && sg.b == M.b && sg.r == M.r) {
+      seg_merge<GREEDY>(sg, v, bad, A.a);
+      sg.p1 = M.p;
+    } else {
+      sg.valid = 1;
+      sg.b = M.b;
+      sg.r = M.r;
+      sg.p0 = sg.p1 = M.p;
+      sg.acc = v;
+      sg.bad = bad;
+    }
+    ++item;
+    if (M.p == A.P - 1 || item == i1) {
+      if (pd.valid) {
+        settle<T, GREEDY>(A, pd, prefix, lane);
+        pd.valid = 0;
+      }
+      pd = publish<GREEDY>(A, sg, lane);
+      sg.valid = 0;
+    }
+    k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
   }
   if (pd.valid) settle<T, GREEDY>(A, pd, prefix, lane);
+  if (aborted) {
+    // Let this warp's copies in flight land before the CTA may exit.
+    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+      if (!have[q]) continue;
+      const long long t0 = clock64();
+      while (!mbar_test(&S.full[SLOTS_PER_WARP * w + q], cons[q] & 1) &&
+             clock64() - t0 < WAIT_CYCLES) {
+      }
+    }
+  }
 }
 
 template <typename T, bool GREEDY>
@@ -756,10 +797,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
     prefix[B] = S.scan[NTHREADS / 32 - 1];
     S.abort_flag = 0;
     S.last_cta = 0;
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
-    }
+    for (int s = 0; s < NSLOT; ++s) mbar_init(&S.full[s], 1);
     fence_mbar_init();
   }
   // Requests whose verify length is out of range have no rows: CTA 0 marks them.
@@ -771,14 +809,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
   }
   __syncthreads();
 
-  if (warp == NCW) {
-    if (lane == 0) producer<T, GREEDY>(A, S, slots, prefix);
-  } else {
-    consumer<T, GREEDY>(A, S, slots, prefix, warp, lane);
-  }
+  warp_loop<T, GREEDY>(A, S, slots, prefix, warp, lane);
   __syncthreads();
 
-  // The last CTA to finish resets the work counter (and, after an abort, every
+  // The last CTA to finish resets the CTA counter (and, after an abort, every
   // ticket) so the workspace is ready for the next call.
   if (tid == 0) {
     __threadfence();
@@ -793,10 +827,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
       for (size_t i = tid; i < TICKET_ROW_WORDS; i += NTHREADS) A.t_row[i] = 0;
       for (int i = tid; i < SV_MAX_B; i += NTHREADS) A.t_req[i] = 0;
     }
-    if (tid == 0) {
-      A.hdr->q1_next = 0;
-      A.hdr->cta_done = 0;
-    }
+    if (tid == 0) A.hdr->cta_done = 0;
   }
 }
 
