@@ -165,6 +165,31 @@ sv_status sv_verify_diag(const void *target_d, const void *draft_d, sv_dtype dty
  */
 sv_status sv_get_status(void *ws_d, void *stream, int clear, int32_t *status_out);
 
+/*
+ * sv_verify_static: sv_verify for callers that cannot allocate device memory -- for
+ * example code that runs while a CUDA graph is being captured in a mode that forbids
+ * cudaMalloc, or a plugin whose host application owns every allocation. The paper has
+ * no counterpart; this is a convenience of this library.
+ *
+ * Same arguments and results as sv_verify, without the workspace: the scratch is one
+ * device array inside the library, SV_STATIC_SCRATCH_BYTES long, that every GPU which
+ * loads the library holds until the process exits. Shapes whose workspace
+ * (sv_workspace_bytes(B, K, V)) exceeds that size return SV_ERR_WORKSPACE without
+ * doing anything. The call allocates nothing (no cudaMalloc, no cudaFree).
+ *  - The first call on each device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - Every call shares the one array and clears its counters first (an async memset
+ *    on `stream`), so calls whose work overlaps on the GPU -- on different streams, or
+ *    from different threads -- race and must not be issued; order them on one stream.
+ *  - The workspace status word is cleared by every call and is not readable through
+ *    this entry point; invalid device data still shows as out_accepted = -1.
+ */
+#define SV_STATIC_SCRATCH_BYTES (16u << 20)
+sv_status sv_verify_static(const void *target_d, const void *draft_d, sv_dtype dtype,
+                           const int32_t *draft_tok_d, const int32_t *verify_len_d,
+                           const float *uniforms_d, int B, int K, int V, float temperature,
+                           int32_t *out_tok_d, int32_t *out_accepted_d, void *stream);
+
 /* Static string for a status code. */
 const char *sv_status_string(sv_status s);
 
