@@ -17,9 +17,20 @@ namespace sv {
 // slots, issues its own 1-D bulk copies (TMA) of row pieces into them and reduces
 // whole pieces on its own.
 // ---------------------------------------------------------------------------
-constexpr int SLOT_BYTES = 8192;
-constexpr int NCW = 12;
-constexpr int SLOTS_PER_WARP = 2;
+#ifndef SV_SLOT_BYTES
+#define SV_SLOT_BYTES 8192
+#endif
+#ifndef SV_NCW
+#define SV_NCW 12
+#endif
+#ifndef SV_SLOTS_PER_WARP
+#define SV_SLOTS_PER_WARP 2
+#endif
+constexpr int SLOT_BYTES = SV_SLOT_BYTES;
+constexpr int NCW = SV_NCW;
+constexpr int SLOTS_PER_WARP = SV_SLOTS_PER_WARP;
+static_assert(SLOT_BYTES % 32 == 0 && NCW * SLOTS_PER_WARP * SLOT_BYTES <= 200 * 1024,
+              "slots must fit in shared memory next to the request prefix");
 constexpr int NSLOT = NCW * SLOTS_PER_WARP;
 constexpr int NTHREADS = 32 * NCW;
 constexpr int TERM_WARPS = 8;                    // warps per CTA of the terminal kernel

@@ -442,47 +442,126 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   }
 }
 
-// Reduce one stream piece; every lane returns the piece's (max, sum) or (max, argmax).
+// Per-lane running state of a row segment: (m, ma = fl(m*a), s) at T > 0, or
+// (best, idx, bad) at T == 0. Lanes accumulate independently over the segment's
+// pieces; the warp reduces the lanes once, when the segment is published.
+struct LaneState {
+  float m, ma, s;  // softmax; greedy uses m = best, s = idx bits
+  bool bad;
+};
+
+__device__ __forceinline__ void lane_reset(LaneState& st) {
+  st.m = -INFINITY;
+  st.ma = -INFINITY;
+  st.s = 0.f;
+  st.bad = false;
+}
+
+__device__ __forceinline__ float vec_max(uint4 v, uint16_t) {
+  const uint32_t mx = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+  return fmax_nan(bf_lo(mx), bf_hi(mx));
+}
+__device__ __forceinline__ float vec_max(uint4 v, float) {
+  return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                  fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+__device__ __forceinline__ uint32_t vmax_raw(uint32_t a, uint32_t b, uint16_t) {
+  return bmax2_nan(a, b);
+}
+
+// Sum of 2^(z*a - ma) over one uint4 of elements.
+__device__ __forceinline__ float vec_expsum(uint4 v, float a, float nma, uint16_t) {
+  const float e0 = ex2(fmaf(bf_lo(v.x), a, nma)), e1 = ex2(fmaf(bf_hi(v.x), a, nma));
+  const float e2 = ex2(fmaf(bf_lo(v.y), a, nma)), e3 = ex2(fmaf(bf_hi(v.y), a, nma));
+  const float e4 = ex2(fmaf(bf_lo(v.z), a, nma)), e5 = ex2(fmaf(bf_hi(v.z), a, nma));
+  const float e6 = ex2(fmaf(bf_lo(v.w), a, nma)), e7 = ex2(fmaf(bf_hi(v.w), a, nma));
+  return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
+}
+__device__ __forceinline__ float vec_expsum(uint4 v, float a, float nma, float) {
+  const float e0 = ex2(fmaf(__uint_as_float(v.x), a, nma));
+  const float e1 = ex2(fmaf(__uint_as_float(v.y), a, nma));
+  const float e2 = ex2(fmaf(__uint_as_float(v.z), a, nma));
+  const float e3 = ex2(fmaf(__uint_as_float(v.w), a, nma));
+  return (e0 + e1) + (e2 + e3);
+}
+
+// Index (0..VEC-1) of the first element of v equal to lm.
+__device__ __forceinline__ int vec_first(uint4 v, float lm, uint16_t) {
+  int e = 7;
+  if (bf_lo(v.w) == lm) e = 6;
+  if (bf_hi(v.z) == lm) e = 5;
+  if (bf_lo(v.z) == lm) e = 4;
+  if (bf_hi(v.y) == lm) e = 3;
+  if (bf_lo(v.y) == lm) e = 2;
+  if (bf_hi(v.x) == lm) e = 1;
+  if (bf_lo(v.x) == lm) e = 0;
+  return e;
+}
+__device__ __forceinline__ int vec_first(uint4 v, float lm, float) {
+  int e = 3;
+  if (__uint_as_float(v.z) == lm) e = 2;
+  if (__uint_as_float(v.y) == lm) e = 1;
+  if (__uint_as_float(v.x) == lm) e = 0;
+  return e;
+}
+
+// Fold one stream piece into the lane states: a max pass over the lane's vectors in
+// shared memory, one rescale, then an exp-sum pass (T > 0); or a max pass and, only
+// when a lane's piece maximum beats its running best, a search for its first index
+// (T == 0). Head and tail elements outside the bulk copy are read from global memory.
 template <typename T, bool GREEDY>
-__device__ float2 reduce_piece(const VerifyArgs& A, const SlotMeta& M, const unsigned char* slot,
-                               int lane, bool& bad_out) {
+__device__ void fold_piece(LaneState& st, const VerifyArgs& A, const SlotMeta& M,
+                           const unsigned char* slot, int lane) {
   constexpr int VEC = ET<T>::VEC;
   const Seg& sg = M.s0;
   const T* g = reinterpret_cast<const T*>(sg.g);
   const int tail = sg.n - sg.head - sg.body;
   const int nv = sg.body / VEC;
   const uint4* v4 = reinterpret_cast<const uint4*>(slot);
+  const int base = M.e0 + sg.head;
   if (GREEDY) {
-    float best = -INFINITY;
-    int idx = INT_MAX;
-    bool bad = false;
-    if (lane < sg.head) arg_add1(best, idx, bad, ld_logit(g + lane), M.e0 + lane);
-    const int base = M.e0 + sg.head;
+    int idx = __float_as_int(st.s);
+    if (lane < sg.head) arg_add1(st.m, idx, st.bad, ld_logit(g + lane), M.e0 + lane);
+    float lm = -INFINITY;
 #pragma unroll 4
-    for (int i = lane; i < nv; i += 32) arg_add_vec(best, idx, bad, v4[i], base + i * VEC, T());
+    for (int i = lane; i < nv; i += 32) lm = fmax_nan(lm, vec_max(v4[i], T()));
+    if (lm != lm) {
+      st.bad = true;
+    } else if (lm > st.m) {  // new best in this piece: its first occurrence
+      for (int i = lane; i < nv; i += 32) {
+        const uint4 v = v4[i];
+        if (vec_max(v, T()) == lm) {
+          idx = base + i * VEC + vec_first(v, lm, T());
+          break;
+        }
+      }
+      st.m = lm;
+    }
     if (lane < tail)
-      arg_add1(best, idx, bad, ld_logit(g + sg.head + sg.body + lane), base + sg.body + lane);
-    arg_warp(best, idx, bad);
-    bad_out = bad;
-    return make_float2(best, __int_as_float(idx));
+      arg_add1(st.m, idx, st.bad, ld_logit(g + sg.head + sg.body + lane), base + sg.body + lane);
+    st.s = __int_as_float(idx);
+    return;
   }
   const float a = A.a;
-  float m = -INFINITY, ma = -INFINITY, s = 0.f;
-  if (lane < sg.head) soft_add1(m, ma, s, ld_logit(g + lane), a);
+  if (lane < sg.head) soft_add1(st.m, st.ma, st.s, ld_logit(g + lane), a);
+  float lm = -INFINITY;
 #pragma unroll 4
-  for (int i = lane; i < nv; i += 32) soft_add_vec(m, ma, s, v4[i], a, T());
-  if (lane < tail) soft_add1(m, ma, s, ld_logit(g + sg.head + sg.body + lane), a);
-  soft_warp(m, s, a, lane);
-  bad_out = false;
-  return make_float2(m, s);
+  for (int i = lane; i < nv; i += 32) lm = fmax_nan(lm, vec_max(v4[i], T()));
+  soft_rescale(st.m, st.ma, st.s, lm, a);
+  if (st.m != -INFINITY) {
+    const float nma = -st.ma;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int i = lane; i < nv; i += 32) acc += vec_expsum(v4[i], a, nma, T());
+    st.s += acc;
+  }
+  if (lane < tail) soft_add1(st.m, st.ma, st.s, ld_logit(g + sg.head + sg.body + lane), a);
 }
 
 // Running partial of one row segment (consecutive pieces of one row handled by one
-// warp), identical in every lane.
+// warp).
 struct Segment {
   int valid, b, r, p0, p1;  // pieces [p0, p1] of row slot r of request b
-  float2 acc;
-  bool bad;
 };
 
 // A published segment whose ticket value has not been inspected yet.
@@ -491,23 +570,22 @@ struct Pending {
   uint32_t old;  // ticket value returned to lane 0
 };
 
+// Publish a segment: reduce the lane states, store the partial at slot p0 and
+// neutral partials at p0+1..p1, then a release-ordered ticket increment by the number
+// of pieces. Lane 0 writes everything.
 template <bool GREEDY>
-__device__ __forceinline__ void seg_merge(Segment& sg, float2 v, bool bad, float a) {
+__device__ Pending publish(const VerifyArgs& A, const Segment& sg, LaneState st, int lane) {
+  float2 v;
   if (GREEDY) {
-    const int vi = __float_as_int(v.y), ai = __float_as_int(sg.acc.y);
-    if (v.x > sg.acc.x || (v.x == sg.acc.x && vi < ai)) sg.acc = v;
-    sg.bad = sg.bad || bad;
+    int idx = __float_as_int(st.s);
+    bool bad = st.bad;
+    arg_warp(st.m, idx, bad);
+    v = make_float2(bad ? __int_as_float(0x7fc00000) : st.m, __int_as_float(idx));
   } else {
-    float m = sg.acc.x, s = sg.acc.y;
-    soft_merge(m, s, v.x, v.y, a);
-    sg.acc = make_float2(m, s);
+    float m = st.m, s = st.s;
+    soft_warp(m, s, A.a, lane);
+    v = make_float2(m, s);
   }
-}
-
-// Publish a segment: its partial at slot p0, neutral partials at p0+1..p1, then a
-// release-ordered ticket increment by the number of pieces. Lane 0 writes everything.
-template <bool GREEDY>
-__device__ Pending publish(const VerifyArgs& A, const Segment& sg, int lane) {
   Pending pd;
   pd.valid = 1;
   pd.b = sg.b;
@@ -517,8 +595,6 @@ __device__ Pending publish(const VerifyArgs& A, const Segment& sg, int lane) {
   if (lane == 0) {
     const size_t rowid = (size_t)sg.b * A.RS + sg.r;
     float2* pr = A.part + rowid * A.P;
-    float2 v = sg.acc;
-    if (GREEDY && sg.bad) v.x = __int_as_float(0x7fc00000);
     pr[sg.p0] = v;
     const float2 neutral = GREEDY ? make_float2(-INFINITY, __int_as_float(INT_MAX))
                                   : make_float2(-INFINITY, 0.f);
@@ -690,6 +766,9 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
   pd.valid = 0;
   Segment sg;
   sg.valid = 0;
+  LaneState st;
+  lane_reset(st);
+  if (GREEDY) st.s = __int_as_float(INT_MAX);
   unsigned long long item = i0;
   int k = 0;
   bool aborted = false;
@@ -706,8 +785,16 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
     }
     const SlotMeta M = S.meta[s];
     unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
-    bool bad;
-    const float2 v = reduce_piece<T, GREEDY>(A, M, slot, lane, bad);
+    if (!(sg.valid && sg.b == M.b && sg.r == M.r)) {  // a new row segment starts here
+      sg.valid = 1;
+      sg.b = M.b;
+      sg.r = M.r;
+      sg.p0 = M.p;
+      lane_reset(st);
+      if (GREEDY) st.s = __int_as_float(INT_MAX);
+    }
+    sg.p1 = M.p;
+    fold_piece<T, GREEDY>(st, A, M, slot, lane);
     ++cons[k];
     __syncwarp();
     int h = 0;
@@ -718,26 +805,14 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
       h = issue_next<T, GREEDY>(A, c, prefix, S.meta[s], &S.full[s], slot);
     }
     have[k] = __shfl_sync(FULL, h, 0);
-    // Extend or start the row segment; publish at the row's last piece or the
-    // range's last piece.
-    if (sg.valid && sg.b == M.b && sg.r == M.r) {
-      seg_merge<GREEDY>(sg, v, bad, A.a);
-      sg.p1 = M.p;
-    } else {
-      sg.valid = 1;
-      sg.b = M.b;
-      sg.r = M.r;
-      sg.p0 = sg.p1 = M.p;
-      sg.acc = v;
-      sg.bad = bad;
-    }
+    // Publish at the row's last piece or the range's last piece.
     ++item;
     if (M.p == A.P - 1 || item == i1) {
       if (pd.valid) {
         settle<T, GREEDY>(A, pd, prefix, lane);
         pd.valid = 0;
       }
-      pd = publish<GREEDY>(A, sg, lane);
+      pd = publish<GREEDY>(A, sg, st, lane);
       sg.valid = 0;
     }
     k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
@@ -847,55 +922,89 @@ struct TermW {
   }
 };
 
-// Compensated sum over elements [0, n) of rows t (and d) with the weight W.
+// Weights of the elements of one uint4 of t (and d).
 template <typename T>
-__device__ void term_sum(const T* t, const T* d, int n, const TermW& W, int lane, float& hs,
-                         float& hc) {
+__device__ __forceinline__ void vec_weights(const uint4 vt, const uint4 vd, const TermW& W,
+                                            float* w) {
+  if (ET<T>::VEC == 8) {
+    w[0] = W(bf_lo(vt.x), bf_lo(vd.x));
+    w[1] = W(bf_hi(vt.x), bf_hi(vd.x));
+    w[2] = W(bf_lo(vt.y), bf_lo(vd.y));
+    w[3] = W(bf_hi(vt.y), bf_hi(vd.y));
+    w[4] = W(bf_lo(vt.z), bf_lo(vd.z));
+    w[5] = W(bf_hi(vt.z), bf_hi(vd.z));
+    w[6] = W(bf_lo(vt.w), bf_lo(vd.w));
+    w[7] = W(bf_hi(vt.w), bf_hi(vd.w));
+  } else {
+    w[0] = W(__uint_as_float(vt.x), __uint_as_float(vd.x));
+    w[1] = W(__uint_as_float(vt.y), __uint_as_float(vd.y));
+    w[2] = W(__uint_as_float(vt.z), __uint_as_float(vd.z));
+    w[3] = W(__uint_as_float(vt.w), __uint_as_float(vd.w));
+  }
+}
+
+// Compensated total of the weights of elements [0, n) of rows t (and d), n <= E2;
+// with wbuf != nullptr the weights are also stored there (shared, per warp). Vector
+// loads are issued a half-piece at a time before use.
+template <typename T>
+__device__ double piece_weights(const T* t, const T* d, int n, const TermW& W, float* wbuf,
+                                int lane) {
   constexpr int VEC = ET<T>::VEC;
+  constexpr int HALF = SLOT_BYTES / 2 / 16 / 32 / 2;  // uint4 per lane per half-piece
   const bool vec = ((reinterpret_cast<uintptr_t>(t) | reinterpret_cast<uintptr_t>(d)) & 15) == 0;
+  float hs = 0.f, hc = 0.f;
   int done = 0;
   if (vec) {
     const int nv = n / VEC;
     const uint4* t4 = reinterpret_cast<const uint4*>(t);
     const uint4* d4 = reinterpret_cast<const uint4*>(d);
-#pragma unroll 2
-    for (int i = lane; i < nv; i += 32) {
-      const uint4 vt = __ldg(t4 + i);
-      const uint4 vd = W.resid ? __ldg(d4 + i) : vt;
-      if (VEC == 8) {
-        two_sum(hs, hc, W(bf_lo(vt.x), bf_lo(vd.x)));
-        two_sum(hs, hc, W(bf_hi(vt.x), bf_hi(vd.x)));
-        two_sum(hs, hc, W(bf_lo(vt.y), bf_lo(vd.y)));
-        two_sum(hs, hc, W(bf_hi(vt.y), bf_hi(vd.y)));
-        two_sum(hs, hc, W(bf_lo(vt.z), bf_lo(vd.z)));
-        two_sum(hs, hc, W(bf_hi(vt.z), bf_hi(vd.z)));
-        two_sum(hs, hc, W(bf_lo(vt.w), bf_lo(vd.w)));
-        two_sum(hs, hc, W(bf_hi(vt.w), bf_hi(vd.w)));
-      } else {
-        two_sum(hs, hc, W(__uint_as_float(vt.x), __uint_as_float(vd.x)));
-        two_sum(hs, hc, W(__uint_as_float(vt.y), __uint_as_float(vd.y)));
-        two_sum(hs, hc, W(__uint_as_float(vt.z), __uint_as_float(vd.z)));
-        two_sum(hs, hc, W(__uint_as_float(vt.w), __uint_as_float(vd.w)));
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint4 vt[HALF], vd[HALF];
+#pragma unroll
+      for (int u = 0; u < HALF; ++u) {
+        const int i = lane + 32 * (u + HALF * h);
+        if (i < nv) {
+          vt[u] = __ldg(t4 + i);
+          vd[u] = W.resid ? __ldg(d4 + i) : vt[u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < HALF; ++u) {
+        const int i = lane + 32 * (u + HALF * h);
+        if (i < nv) {
+          float w[VEC];
+          vec_weights<T>(vt[u], vd[u], W, w);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) two_sum(hs, hc, w[e]);
+          if (wbuf) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) wbuf[i * VEC + e] = w[e];
+          }
+        }
       }
     }
     done = nv * VEC;
   }
-  for (int e = done + lane; e < n; e += 32) two_sum(hs, hc, W(ld_logit(t + e), ld_logit(d + e)));
+  for (int e = done + lane; e < n; e += 32) {
+    const float w = W(ld_logit(t + e), ld_logit(d + e));
+    if (wbuf) wbuf[e] = w;
+    two_sum(hs, hc, w);
+  }
+  __syncwarp();
+  return warp_sum_d((double)hs + (double)hc, lane);
 }
 
-// Inverse-CDF step over elements [0, n) of rows t (and d): the smallest v with
-// target < cum(v), cum in float64 over the fp32 weights. Lanes take contiguous ranges;
-// falls back to the last positive-weight element when rounding leaves target past
-// the end.
-template <typename T>
-__device__ int locate_range(const T* t, const T* d, int n, const TermW& W, double target,
-                            int lane) {
+// Inverse-CDF step over weights wbuf[0, n): the smallest v with target < cum(v), cum
+// in float64. Lanes take contiguous ranges; falls back to the last positive weight
+// when rounding leaves target past the end.
+__device__ int locate_weights(const float* wbuf, int n, double target, int lane) {
   const int c = (n + 31) / 32;
   const int v0 = min(n, lane * c), v1 = min(n, v0 + c);
   float hs = 0.f, hc = 0.f;
   int lastpos = -1;
   for (int v = v0; v < v1; ++v) {
-    const float w = W(ld_logit(t + v), ld_logit(d + v));
+    const float w = wbuf[v];
     two_sum(hs, hc, w);
     if (w > 0.f) lastpos = v;
   }
@@ -908,7 +1017,7 @@ __device__ int locate_range(const T* t, const T* d, int n, const TermW& W, doubl
     if (lane == ln) {
       double cum = incl - ls;
       for (int v = v0; v < v1; ++v) {
-        cum += (double)W(ld_logit(t + v), ld_logit(d + v));
+        cum += (double)wbuf[v];
         if (target < cum) {
           y = v;
           break;
@@ -928,7 +1037,7 @@ __device__ int locate_range(const T* t, const T* d, int n, const TermW& W, doubl
 // Locate the terminal token of request b from its R piece sums.
 template <typename T>
 __device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const TermW& W,
-                           int lane) {
+                           float* wbuf, int lane) {
   const int R = A.R, K = A.K, j = J.j;
   const T* trow = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V;
   const T* drow = W.resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V : trow;
@@ -944,61 +1053,77 @@ __device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const T
     if (w > 0.0) lastpos = p;
   }
   const double incl = warp_incl_scan_d(ls, lane);
-  const double Z = __shfl_sync(FULL, incl, 31);
+  double Z = __shfl_sync(FULL, incl, 31);
+  TermW Wl = W;
+  bool whole_row = false;
   if (W.resid && (!(Z > 0.0) || !(Z < 1e300))) {
-    // No residual mass left (p == q up to rounding): sample p_j itself instead,
-    // over the whole row.
-    TermW Wp = W;
-    Wp.resid = false;
-    float hs = 0.f, hc = 0.f;
-    const int cc = (A.V + 31) / 32;
-    const int v0 = min(A.V, lane * cc), v1 = min(A.V, v0 + cc);
-    for (int v = v0; v < v1; ++v) {
-      const float z = ld_logit(trow + v);
-      two_sum(hs, hc, Wp(z, z));
+    // No residual mass left (p == q up to rounding): sample p_j itself instead, piece
+    // by piece over the whole row.
+    Wl.resid = false;
+    whole_row = true;
+    Z = 0.0;
+    for (int p = 0; p < R; ++p) {
+      const int e0 = p * A.E2;
+      Z += piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
+      __syncwarp();
     }
-    const double Zp = warp_sum_d((double)hs + (double)hc, lane);
-    return locate_range<T>(trow, trow, A.V, Wp, uK * Zp, lane);
   }
   const double target = uK * Z;
-  const unsigned hit = __ballot_sync(FULL, target < incl);
   int pstar = -1;
   double base = 0.0;
-  if (hit) {
-    const int ln = __ffs(hit) - 1;
-    if (lane == ln) {
-      double cum = incl - ls;
-      for (int p = p0; p < p1; ++p) {
-        const double w = __ldcg(rp + p);
-        if (target < cum + w) {
-          pstar = p;
-          break;
-        }
-        cum += w;
-      }
-      if (pstar < 0) pstar = lastpos;
-      base = cum;
+  if (whole_row) {
+    for (int p = 0; p < R && pstar < 0; ++p) {
+      const int e0 = p * A.E2;
+      const double w =
+          piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
+      __syncwarp();
+      if (target < base + w || p == R - 1) pstar = p;
+      else base += w;
     }
-    pstar = __shfl_sync(FULL, pstar, ln);
-    base = __shfl_sync(FULL, base, ln);
-  }
-  if (pstar < 0) {  // rounding put the target past the last piece
-    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-    const int ln = has ? 31 - __clz(has) : 0;
-    pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
-    base = target;
+  } else {
+    const unsigned hit = __ballot_sync(FULL, target < incl);
+    if (hit) {
+      const int ln = __ffs(hit) - 1;
+      if (lane == ln) {
+        double cum = incl - ls;
+        for (int p = p0; p < p1; ++p) {
+          const double w = __ldcg(rp + p);
+          if (target < cum + w) {
+            pstar = p;
+            break;
+          }
+          cum += w;
+        }
+        if (pstar < 0) pstar = lastpos;
+        base = cum;
+      }
+      pstar = __shfl_sync(FULL, pstar, ln);
+      base = __shfl_sync(FULL, base, ln);
+    }
+    if (pstar < 0) {  // rounding put the target past the last piece
+      const unsigned has = __ballot_sync(FULL, lastpos >= 0);
+      const int ln = has ? 31 - __clz(has) : 0;
+      pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
+      base = target;
+    }
   }
   const int e0 = pstar * A.E2;
   const int ne = min(A.E2, A.V - e0);
-  return e0 + locate_range<T>(trow + e0, drow + e0, ne, W, target - base, lane);
+  piece_weights<T>(trow + e0, drow + e0, ne, Wl, wbuf, lane);
+  return e0 + locate_weights(wbuf, ne, target - base, lane);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(32 * TERM_WARPS) sv_terminal_kernel(const VerifyArgs A) {
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * TERM_WARPS + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(32 * TERM_WARPS, 2) sv_terminal_kernel(const VerifyArgs A) {
+  extern __shared__ __align__(16) float wsm[];  // per warp: the weights of one piece
+  // Programmatic dependent launch: wait until the stream kernel has completed and its
+  // writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int gw = blockIdx.x * TERM_WARPS + wid;
   const int nw = gridDim.x * TERM_WARPS;
   const int R = A.R, K = A.K;
+  float* wbuf = wsm + (size_t)wid * (SLOT_BYTES / 2 / 2);
   // After a timed-out stream kernel the job records may be stale: do nothing (the
   // status word already reports the timeout).
   if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return;
@@ -1015,44 +1140,63 @@ __global__ void __launch_bounds__(32 * TERM_WARPS) sv_terminal_kernel(const Veri
     const int n = min(A.E2, A.V - e0);
     const T* t = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + J.j) * A.V + e0;
     const T* d = resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + J.j) * A.V + e0 : t;
-    float hs = 0.f, hc = 0.f;
-    term_sum<T>(t, d, n, W, lane, hs, hc);
-    const double acc = warp_sum_d((double)hs + (double)hc, lane);
+    const double acc = piece_weights<T>(t, d, n, W, nullptr, lane);
     uint32_t old = 0;
     if (lane == 0) {
       A.rpart[(size_t)b * A.Rmax + p] = acc;
       old = atom_add_release(A.t_res + b, 1u);
     }
     old = __shfl_sync(FULL, old, 0);
+    __syncwarp();
     if (old != (uint32_t)(R - 1)) continue;
     __threadfence();
     if (lane == 0) A.t_res[b] = 0;
-    const int y = term_locate<T>(A, b, J, W, lane);
+    const int y = term_locate<T>(A, b, J, W, wbuf, lane);
     if (lane == 0) A.out_tok[(size_t)b * (K + 1) + J.j] = y;
+    __syncwarp();
   }
 }
 
 // ---------------------------------------------------------------------------
 // Host launchers (called from the C-ABI layer).
 // ---------------------------------------------------------------------------
+// Terminal kernel shared memory: one piece of fp32 weights per warp (the largest
+// piece holds SLOT_BYTES / 2 / 2 bf16 elements).
+constexpr int TERM_SMEM = TERM_WARPS * (SLOT_BYTES / 2 / 2) * 4;
+
 template <typename T, bool GREEDY>
 static cudaError_t launch_t(const VerifyArgs& A, int grid, size_t dsmem, cudaStream_t st) {
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, GREEDY>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(NSLOT * SLOT_BYTES + 4 * (SV_MAX_B + 1) + 256));
+    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, GREEDY>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(NSLOT * SLOT_BYTES + 4 * (SV_MAX_B + 1) + 256));
     if (e != cudaSuccess) return e;
+    if (!GREEDY) {
+      e = cudaFuncSetAttribute(sv_terminal_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               TERM_SMEM);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   sv_verify_kernel<T, GREEDY><<<grid, NTHREADS, dsmem, st>>>(A);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || GREEDY) return e;
+  // The terminal kernel is a programmatic dependent launch: it may be scheduled while
+  // the stream kernel drains, and waits for its completion on the device.
   const long long tasks = (long long)A.B * A.R;
   const long long want = (tasks + TERM_WARPS - 1) / TERM_WARPS;
-  const int tgrid = (int)(want < 4LL * grid ? want : 4LL * grid);
-  sv_terminal_kernel<T><<<tgrid, 32 * TERM_WARPS, 0, st>>>(A);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(want < 4LL * grid ? want : 4LL * grid));
+  cfg.blockDim = dim3(32 * TERM_WARPS);
+  cfg.dynamicSmemBytes = TERM_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sv_terminal_kernel<T>, A);
 }
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st) {
