@@ -33,7 +33,6 @@ static_assert(SLOT_BYTES % 32 == 0 && NCW * SLOTS_PER_WARP * SLOT_BYTES <= 200 *
               "slots must fit in shared memory next to the request prefix");
 constexpr int NSLOT = NCW * SLOTS_PER_WARP;
 constexpr int NTHREADS = 32 * NCW;
-constexpr int TERM_WARPS = 8;                    // warps per CTA of the terminal kernel
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz: bound on any wait
 
 // Status word bits (sticky, in the workspace header).
@@ -47,18 +46,21 @@ struct WsHeader {
   uint32_t status;    // ST_* bits
   uint32_t reserved;
   uint32_t cta_done;  // verify: CTAs that have finished
-  uint32_t pad[61];
+  uint32_t grid_sync; // verify: CTAs done with the stream phase (T > 0)
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
-// Terminal-sample job of one request, written by the deciding warp of the stream
-// kernel and read by the terminal kernel: the residual max(0, p_j - q_j) over rows
+// Terminal-sample job of one request, written by the deciding warp in the stream
+// phase and read in the terminal phase: the residual max(0, p_j - q_j) over rows
 // t_j and d_j, a plain sample of p over target row j (the bonus row L), or nothing
 // (an invalid request, or greedy verification).
 enum : int { J_NONE = -1, J_RESID = 0, J_BONUS = 1 };
 struct __align__(32) TermJob {
   int kind, j;
-  float MAt, invSt, MAd, invSd;  // fl(M*a) and 1/S of target row j and draft row j
+  // Target and draft rows j: raw maximum M and 2^(M*a - fl(M*a)) / S, the inverse
+  // row sum in the frame of the exact maximum.
+  float MAt, invSt, MAd, invSd;
   int pad[2];
 };
 

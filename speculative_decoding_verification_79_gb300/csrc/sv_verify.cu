@@ -4,8 +4,9 @@
 // (DSpark Deep Dive, "The Speculative Decoding Solution"; DSpark Guide, "1. The
 // Mathematics of Suffix Decay"; perchy.ai Technology, "Verified by the target").
 //
-// Two launches on the caller's stream, no CPU round trip:
-//  1. sv_verify_kernel, one persistent CTA per SM. Work list: every active logit row
+// One launch on the caller's stream, no CPU round trip: sv_verify_kernel, one
+// persistent CTA per SM, in two phases.
+//  1. Stream phase. Work list: every active logit row
 //     of the batch (request b: target rows 0..L_b, and at T > 0 draft rows
 //     0..L_b-1) cut into pieces of SLOT_BYTES, ordered request-major; every warp of
 //     the grid takes an equal contiguous range of it. Each warp owns SLOTS_PER_WARP
@@ -21,11 +22,13 @@
 //     p_k(x_k), q_k(x_k),
 //     the accept tests u*q < p, a ballot for the first rejection j, the outputs,
 //     and (T > 0) the terminal-sample job of the request.
-//  2. sv_terminal_kernel (T > 0 only): one warp per (request, piece) task sums the
-//     terminal weights of a piece of the terminal rows (residual max(0, p_j - q_j),
-//     or p of the bonus row) with compensated fp32 arithmetic, reduced in float64;
-//     the last piece of a request locates the token by inverse CDF at u_{b,K}
-//     (float64 prefix over piece sums, one piece re-scanned in float64).
+//  2. Terminal phase (T > 0 only), after a grid-wide barrier (the launch is
+//     cooperative, so all CTAs are resident): the (request, piece) tasks of the
+//     terminal rows (residual max(0, p_j - q_j), or p of the bonus row) are split
+//     over all warps and copied through the same slots; each sums its piece's weights
+//     with compensated fp32 arithmetic, reduced in float64; the last piece of a
+//     request locates the token by inverse CDF at u_{b,K} (float64 prefix over piece
+//     sums, one piece re-scanned in float64).
 //  Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
 //  status word, lets its copies in flight land, and returns.
 #include <cfloat>
@@ -35,7 +38,7 @@
 
 namespace sv {
 
-enum : int { K_STREAM = 0, K_STOP = 2 };
+enum : int { K_STREAM = 0, K_TERM = 1 };
 
 // A contiguous run of elements of one row, split by 16-byte alignment into a head
 // read directly from global memory, a body copied to shared memory, and a tail
@@ -46,16 +49,20 @@ struct Seg {
 };
 
 struct __align__(16) SlotMeta {
-  int kind, b, r, p;  // request, row slot, piece
+  int kind, b, r, p;  // request, row slot (stream) or terminal row (terminal), piece
   int e0;             // first element of the piece within its row
-  int pad[3];
-  Seg s0;
+  int direct;         // terminal piece: 1 = rows read straight from global memory
+  int jkind;          // terminal piece: J_RESID or J_BONUS
+  int pad;
+  Seg s0, s1;         // stream piece: s0; terminal piece: target (s0) and draft (s1)
+  float Mt, iSt, Md, iSd;
 };
 
 struct Shared {
   SlotMeta meta[NSLOT];
   uint64_t full[NSLOT];
   int abort_flag;
+  int grid_ok;
   int last_cta;
   int total_rows;
   int scan[32];
@@ -157,17 +164,27 @@ __device__ __forceinline__ void soft_warp(float& m, float& s, float a, int lane)
 
 // 2^(z*(a + a_lo) - MA) with the exponent carried to about twice fp32 precision:
 // y = z*a - MA split as y_hi + y_lo (exact product error by fma, TwoSum error of
-// the difference), then 2^y = 2^y_hi * (1 + y_lo*ln2). Used where single values or
-// terminal-sample weights must agree closely with float64.
+// the difference), then 2^y = 2^y_hi * (1 + y_lo*ln2). Explicit roundings keep the
+// compiler from fusing the pieces.
 __device__ __forceinline__ float exp2_precise(float z, float a, float a_lo, float MA) {
-  const float ph = z * a;
+  const float ph = __fmul_rn(z, a);
   const float pl = fmaf(z, a, -ph);  // exact error of the product
-  const float yh = ph - MA;
-  const float bp = yh - ph;  // TwoSum error of ph - MA
-  const float el = (ph - (yh - bp)) + (-MA - bp);
+  const float yh = __fsub_rn(ph, MA);
+  const float bp = __fsub_rn(yh, ph);  // TwoSum error of ph - MA
+  const float el = __fadd_rn(__fsub_rn(ph, __fsub_rn(yh, bp)), __fsub_rn(-MA, bp));
   const float yl = fmaf(z, a_lo, pl + el);
   const float e = ex2(yh);
   return fmaf(e, yl * 0.6931471805599453f, e);
+}
+
+// 2^((z - M)*(a + a_lo)) for a row maximum M: z - M is exact for bf16 logits (and
+// nearly so for fp32), the product is split as above; -inf logits give 0.
+__device__ __forceinline__ float exp2_diff(float z, float M, float a, float a_lo) {
+  const float d = __fsub_rn(z, M);
+  const float yh = __fmul_rn(d, a);
+  const float yl = fmaf(d, a_lo, fmaf(d, a, -yh));
+  const float e = ex2(yh);
+  return (d == -INFINITY) ? 0.f : fmaf(e, yl * 0.6931471805599453f, e);
 }
 
 // ---------------------------------------------------------------------------
@@ -312,6 +329,13 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const Veri
 }
 
 
+// Acquire-ordered load (GPU scope).
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // Release-ordered atomic add (GPU scope): earlier stores of this thread become
 // visible to whoever observes the new count.
 __device__ __forceinline__ uint32_t atom_add_release(uint32_t* addr, uint32_t v) {
@@ -384,21 +408,27 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = q;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
-  const float jMAt = __shfl_sync(FULL, MAt, j & 31), jSt = __shfl_sync(FULL, iSt, j & 31);
-  const float jMAd = __shfl_sync(FULL, MAd, j & 31), jSd = __shfl_sync(FULL, iSd, j & 31);
+  // Terminal-sample job. Weights are computed as 2^((z - M)*a) against the exact
+  // maximum, so each inverse row sum absorbs the frame offset 2^(M*a - fl(M*a)).
+  const float jM = (lane < L) ? __ldcg(A.rowstat + rb + lane).x : 0.f;
+  const float jMd = (lane < L) ? __ldcg(A.rowstat + rb + L + 1 + lane).x : 0.f;
+  const float cSt = iSt * ex2(fmaf(jM, A.a, -MAt));
+  const float cSd = iSd * ex2(fmaf(jMd, A.a, -MAd));
+  const float jMt = __shfl_sync(FULL, jM, j & 31), jSt = __shfl_sync(FULL, cSt, j & 31);
+  const float jMdd = __shfl_sync(FULL, jMd, j & 31), jSd = __shfl_sync(FULL, cSd, j & 31);
   if (lane == 0) {
     A.out_acc[b] = j;
     TermJob J;
     J.j = j;
     if (j == L) {  // every draft accepted: bonus sample from p_L
       J.kind = J_BONUS;
-      J.MAt = __fmul_rn(sL.x, A.a);
+      J.MAt = sL.x;
       J.invSt = J.MAd = J.invSd = 0.f;
     } else {  // first rejection at j: residual sample
       J.kind = J_RESID;
-      J.MAt = jMAt;
+      J.MAt = jMt;
       J.invSt = jSt;
-      J.MAd = jMAd;
+      J.MAd = jMdd;
       J.invSd = jSd;
     }
     J.pad[0] = J.pad[1] = 0;
@@ -737,7 +767,7 @@ __device__ bool issue_next(const VerifyArgs& A, Cursor& c, const int* prefix, Sl
 // right after the warp has reduced it.
 template <typename T, bool GREEDY>
 __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
-                          int w, int lane) {
+                          int w, int lane, uint32_t* cons) {
   const unsigned long long total =
       static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(A.P);
   const unsigned long long nw = (unsigned long long)gridDim.x * NCW;
@@ -745,12 +775,8 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
   const unsigned long long i0 = total * gw / nw, i1 = total * (gw + 1) / nw;
   Cursor c;
   int have[SLOTS_PER_WARP];
-  uint32_t cons[SLOTS_PER_WARP];
 #pragma unroll
-  for (int q = 0; q < SLOTS_PER_WARP; ++q) {
-    have[q] = 0;
-    cons[q] = 0;
-  }
+  for (int q = 0; q < SLOTS_PER_WARP; ++q) have[q] = 0;
   if (lane == 0) {
     cursor_init<GREEDY>(c, A, prefix, i0, i1);
 #pragma unroll
@@ -830,95 +856,20 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
   }
 }
 
-template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs A) {
-  extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ Shared S;
-  unsigned char* slots = dsm;
-  int* prefix = reinterpret_cast<int*>(dsm + (size_t)NSLOT * SLOT_BYTES);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int B = A.B;
-
-  // Exclusive prefix of active rows per request (every CTA computes the same one).
-  const int per = (B + NTHREADS - 1) / NTHREADS;
-  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += nrows_of(A, b, GREEDY);
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) S.scan[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int v = (lane < NTHREADS / 32) ? S.scan[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULL, v, o);
-      if (lane >= o) v += y;
-    }
-    if (lane < NTHREADS / 32) S.scan[lane] = v;
-  }
-  __syncthreads();
-  int run = incl - local + (warp ? S.scan[warp - 1] : 0);
-  for (int b = b0; b < b1; ++b) {
-    prefix[b] = run;
-    run += nrows_of(A, b, GREEDY);
-  }
-  if (tid == 0) {
-    S.total_rows = S.scan[NTHREADS / 32 - 1];
-    prefix[B] = S.scan[NTHREADS / 32 - 1];
-    S.abort_flag = 0;
-    S.last_cta = 0;
-    for (int s = 0; s < NSLOT; ++s) mbar_init(&S.full[s], 1);
-    fence_mbar_init();
-  }
-  // Requests whose verify length is out of range have no rows: CTA 0 marks them.
-  if (blockIdx.x == 0) {
-    for (int b = warp; b < B; b += NTHREADS / 32) {
-      const int L = A.vlen[b];
-      if (L < 0 || L > A.K) emit_invalid(A, b, lane);
-    }
-  }
-  __syncthreads();
-
-  warp_loop<T, GREEDY>(A, S, slots, prefix, warp, lane);
-  __syncthreads();
-
-  // The last CTA to finish resets the CTA counter (and, after an abort, every
-  // ticket) so the workspace is ready for the next call.
-  if (tid == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(&A.hdr->cta_done, 1u);
-    S.last_cta = (old == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (S.last_cta) {
-    __threadfence();
-    const bool dirty = (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) != 0;
-    if (dirty) {
-      for (size_t i = tid; i < TICKET_ROW_WORDS; i += NTHREADS) A.t_row[i] = 0;
-      for (int i = tid; i < SV_MAX_B; i += NTHREADS) A.t_req[i] = 0;
-    }
-    if (tid == 0) A.hdr->cta_done = 0;
-  }
-}
-
 // ---------------------------------------------------------------------------
-// Terminal-sample kernel (T > 0).
+// Terminal sample (T > 0): weights, piece sums, inverse-CDF location.
 // ---------------------------------------------------------------------------
 
 // Weight of one element: residual max(0, p - q), or the unnormalised target weight
-// 2^(z*a - MA) of a plain sample.
+// 2^((z - M)*a) of a plain sample. Mt, Md are the raw row maxima; iSt, iSd the
+// inverse row sums in that frame.
 struct TermW {
-  float a, a_lo, MAt, iSt, MAd, iSd;
+  float a, a_lo, Mt, iSt, Md, iSd;
   bool resid;
   __device__ __forceinline__ float operator()(float zt, float zd) const {
-    const float et = exp2_precise(zt, a, a_lo, MAt);
+    const float et = exp2_diff(zt, Mt, a, a_lo);
     if (!resid) return et;
-    return fmaxf(et * iSt - exp2_precise(zd, a, a_lo, MAd) * iSd, 0.f);
+    return fmaxf(et * iSt - exp2_diff(zd, Md, a, a_lo) * iSd, 0.f);
   }
 };
 
@@ -1113,90 +1064,297 @@ __device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const T
   return e0 + locate_weights(wbuf, ne, target - base, lane);
 }
 
+// ---------------------------------------------------------------------------
+// Terminal phase (T > 0), after every CTA has finished its stream work: the terminal
+// piece tasks (request b, piece p) are split in equal contiguous ranges over all warps
+// and fed through the same slots. Each task sums the weights of its piece (compensated
+// fp32, reduced in float64); the task completing a request locates its token.
+// ---------------------------------------------------------------------------
+
+// Next terminal task of the warp's range that has a job, into a slot (lane 0 only).
+// Returns false at the end of the range.
 template <typename T>
-__global__ void __launch_bounds__(32 * TERM_WARPS, 2) sv_terminal_kernel(const VerifyArgs A) {
-  extern __shared__ __align__(16) float wsm[];  // per warp: the weights of one piece
-  // Programmatic dependent launch: wait until the stream kernel has completed and its
-  // writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int gw = blockIdx.x * TERM_WARPS + wid;
-  const int nw = gridDim.x * TERM_WARPS;
+__device__ bool issue_term(const VerifyArgs& A, long long& tc, long long t1, SlotMeta& meta,
+                           uint64_t* full, unsigned char* slot) {
+  constexpr int eb = sizeof(T);
   const int R = A.R, K = A.K;
-  float* wbuf = wsm + (size_t)wid * (SLOT_BYTES / 2 / 2);
-  // After a timed-out stream kernel the job records may be stale: do nothing (the
-  // status word already reports the timeout).
-  if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return;
-  const long long total = (long long)A.B * R;
-  for (long long task = gw; task < total; task += nw) {
-    const int b = (int)(task / R), p = (int)(task - (long long)b * R);
-    const TermJob J = A.jobs[b];
-    if (J.kind == J_NONE) continue;
-    if (!((J.kind == J_RESID && J.j >= 0 && J.j < K) || (J.kind == J_BONUS && J.j >= 0 && J.j <= K)))
-      continue;
-    const bool resid = J.kind == J_RESID;
-    const TermW W{A.a, A.a_lo, J.MAt, J.invSt, J.MAd, J.invSd, resid};
+  while (tc < t1) {
+    const int b = (int)(tc / R), p = (int)(tc - (long long)b * R);
+    ++tc;
+    const int kind = __ldcg(&A.jobs[b].kind), j = __ldcg(&A.jobs[b].j);
+    if (!((kind == J_RESID && j >= 0 && j < K) || (kind == J_BONUS && j >= 0 && j <= K))) continue;
     const int e0 = p * A.E2;
     const int n = min(A.E2, A.V - e0);
-    const T* t = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + J.j) * A.V + e0;
-    const T* d = resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + J.j) * A.V + e0 : t;
-    const double acc = piece_weights<T>(t, d, n, W, nullptr, lane);
+    const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V + e0;
+    meta.kind = K_TERM;
+    meta.jkind = kind;
+    meta.b = b;
+    meta.r = j;
+    meta.p = p;
+    meta.e0 = e0;
+    meta.Mt = __ldcg(&A.jobs[b].MAt);
+    meta.iSt = __ldcg(&A.jobs[b].invSt);
+    meta.Md = __ldcg(&A.jobs[b].MAd);
+    meta.iSd = __ldcg(&A.jobs[b].invSd);
+    meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
+    bool whole = meta.s0.head == 0 && meta.s0.body == n;
+    if (kind == J_RESID) {
+      const T* dr = static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V + e0;
+      meta.s1 = make_seg(reinterpret_cast<const unsigned char*>(dr), n, eb);
+      whole = whole && meta.s1.head == 0 && meta.s1.body == n;
+    } else {
+      meta.s1 = meta.s0;
+    }
+    // A piece whose rows are not both 16-byte aligned and whole multiples of 16 bytes
+    // is read straight from global memory.
+    meta.direct = !whole;
+    if (whole) {
+      const uint32_t bytes = (uint32_t)(n * eb);
+      mbar_arrive_expect_tx(full, (kind == J_RESID ? 2u : 1u) * bytes);
+      bulk_g2s(slot, meta.s0.g, bytes, full);
+      if (kind == J_RESID) bulk_g2s(slot + SLOT_BYTES / 2, meta.s1.g, bytes, full);
+    } else {
+      mbar_arrive(full);
+    }
+    return true;
+  }
+  return false;
+}
+
+// Weight total of one terminal piece, from its slot (or from global memory in direct
+// mode): compensated fp32 per lane, reduced in float64.
+template <typename T>
+__device__ double term_piece_sum(const SlotMeta& M, const TermW& W, const unsigned char* slot,
+                                 int lane) {
+  constexpr int VEC = ET<T>::VEC;
+  const int n = M.s0.n;
+  if (M.direct)
+    return piece_weights<T>(reinterpret_cast<const T*>(M.s0.g),
+                            reinterpret_cast<const T*>(M.s1.g), n, W, nullptr, lane);
+  const uint4* t4 = reinterpret_cast<const uint4*>(slot);
+  const uint4* d4 = reinterpret_cast<const uint4*>(W.resid ? slot + SLOT_BYTES / 2 : slot);
+  float hs = 0.f, hc = 0.f;
+  const int nv = n / VEC;
+#pragma unroll 2
+  for (int i = lane; i < nv; i += 32) {
+    float w[VEC];
+    vec_weights<T>(t4[i], d4[i], W, w);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) two_sum(hs, hc, w[e]);
+  }
+  return warp_sum_d((double)hs + (double)hc, lane);
+}
+
+// One warp's range of terminal tasks. cons[] carries the slots' consumed-phase counts
+// from the stream phase.
+template <typename T>
+__device__ void term_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, int w, int lane,
+                          uint32_t* cons) {
+  const long long N2 = (long long)A.B * A.R;
+  const long long nw = (long long)gridDim.x * NCW;
+  const long long gw = (long long)blockIdx.x * NCW + w;
+  const long long t1 = N2 * (gw + 1) / nw;
+  long long tc = N2 * gw / nw;
+  int have[SLOTS_PER_WARP];
+#pragma unroll
+  for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+    int h = 0;
+    if (lane == 0) {
+      const int s = SLOTS_PER_WARP * w + q;
+      h = issue_term<T>(A, tc, t1, S.meta[s], &S.full[s], slots + (size_t)s * SLOT_BYTES);
+    }
+    have[q] = __shfl_sync(FULL, h, 0);
+  }
+  int k = 0;
+  bool aborted = false;
+  while (have[k]) {
+    const int s = SLOTS_PER_WARP * w + k;
+    const bool ok = wait_phase(&S.full[s], cons[k] & 1, S, A);
+    if (!__all_sync(FULL, ok)) {
+      aborted = true;
+      break;
+    }
+    const SlotMeta M = S.meta[s];
+    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
+    const TermW W{A.a, A.a_lo, M.Mt, M.iSt, M.Md, M.iSd, M.jkind == J_RESID};
+    const double acc = term_piece_sum<T>(M, W, slot, lane);
+    ++cons[k];
+    const int b = M.b;
     uint32_t old = 0;
     if (lane == 0) {
-      A.rpart[(size_t)b * A.Rmax + p] = acc;
+      A.rpart[(size_t)b * A.Rmax + M.p] = acc;
       old = atom_add_release(A.t_res + b, 1u);
     }
     old = __shfl_sync(FULL, old, 0);
     __syncwarp();
-    if (old != (uint32_t)(R - 1)) continue;
+    if (old == (uint32_t)(A.R - 1)) {  // last piece of this request: locate its token
+      __threadfence();
+      if (lane == 0) A.t_res[b] = 0;
+      TermJob J;
+      J.kind = M.jkind;
+      J.j = M.r;
+      // The slot's data has been consumed: it serves as the warp's weight buffer.
+      const int y = term_locate<T>(A, b, J, W, reinterpret_cast<float*>(slot), lane);
+      if (lane == 0) A.out_tok[(size_t)b * (A.K + 1) + M.r] = y;
+      __syncwarp();
+    }
+    int h = 0;
+    if (lane == 0) {
+      // Order this warp's generic reads and writes of the slot before the async-proxy
+      // write of the next copy.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      h = issue_term<T>(A, tc, t1, S.meta[s], &S.full[s], slot);
+    }
+    have[k] = __shfl_sync(FULL, h, 0);
+    k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
+  }
+  if (aborted) {
+    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+      if (!have[q]) continue;
+      const long long c0 = clock64();
+      while (!mbar_test(&S.full[SLOTS_PER_WARP * w + q], cons[q] & 1) &&
+             clock64() - c0 < WAIT_CYCLES) {
+      }
+    }
+  }
+}
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs A) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ Shared S;
+  unsigned char* slots = dsm;
+  int* prefix = reinterpret_cast<int*>(dsm + (size_t)NSLOT * SLOT_BYTES);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = A.B;
+
+  // Exclusive prefix of active rows per request (every CTA computes the same one).
+  const int per = (B + NTHREADS - 1) / NTHREADS;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += nrows_of(A, b, GREEDY);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) S.scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = (lane < NTHREADS / 32) ? S.scan[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < NTHREADS / 32) S.scan[lane] = v;
+  }
+  __syncthreads();
+  int run = incl - local + (warp ? S.scan[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    prefix[b] = run;
+    run += nrows_of(A, b, GREEDY);
+  }
+  if (tid == 0) {
+    S.total_rows = S.scan[NTHREADS / 32 - 1];
+    prefix[B] = S.scan[NTHREADS / 32 - 1];
+    S.abort_flag = 0;
+    S.last_cta = 0;
+    for (int s = 0; s < NSLOT; ++s) mbar_init(&S.full[s], 1);
+    fence_mbar_init();
+  }
+  // Requests whose verify length is out of range have no rows: CTA 0 marks them.
+  if (blockIdx.x == 0) {
+    for (int b = warp; b < B; b += NTHREADS / 32) {
+      const int L = A.vlen[b];
+      if (L < 0 || L > A.K) emit_invalid(A, b, lane);
+    }
+  }
+  __syncthreads();
+
+  uint32_t cons[SLOTS_PER_WARP];
+#pragma unroll
+  for (int q = 0; q < SLOTS_PER_WARP; ++q) cons[q] = 0;
+  warp_loop<T, GREEDY>(A, S, slots, prefix, warp, lane, cons);
+  __syncthreads();
+
+  if (!GREEDY) {
+    // Grid-wide barrier: every request has been decided (and its terminal job
+    // written) once all CTAs have arrived. The wait is bounded; after a timeout
+    // anywhere the terminal phase is skipped (the status word reports it).
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(&A.hdr->grid_sync, 1u);
+      const long long c0 = clock64();
+      int ok = 1;
+      while (ld_acquire(&A.hdr->grid_sync) < gridDim.x) {
+        if (clock64() - c0 > WAIT_CYCLES) {
+          raise_status(A, ST_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+      __threadfence();
+      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) ok = 0;
+      S.grid_ok = ok && !S.abort_flag;
+    }
+    __syncthreads();
+    if (S.grid_ok) term_loop<T>(A, S, slots, warp, lane, cons);
+    __syncthreads();
+  }
+
+  // The last CTA to finish resets the CTA counter (and, after an abort, every
+  // ticket) so the workspace is ready for the next call.
+  if (tid == 0) {
     __threadfence();
-    if (lane == 0) A.t_res[b] = 0;
-    const int y = term_locate<T>(A, b, J, W, wbuf, lane);
-    if (lane == 0) A.out_tok[(size_t)b * (K + 1) + J.j] = y;
-    __syncwarp();
+    const unsigned old = atomicAdd(&A.hdr->cta_done, 1u);
+    S.last_cta = (old == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (S.last_cta) {
+    __threadfence();
+    const bool dirty = (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) != 0;
+    if (dirty) {
+      for (size_t i = tid; i < TICKET_ROW_WORDS; i += NTHREADS) A.t_row[i] = 0;
+      for (int i = tid; i < SV_MAX_B; i += NTHREADS) {
+        A.t_req[i] = 0;
+        A.t_res[i] = 0;
+      }
+    }
+    if (tid == 0) {
+      A.hdr->grid_sync = 0;
+      A.hdr->cta_done = 0;
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Host launchers (called from the C-ABI layer).
+// Host launcher (called from the C-ABI layer).
 // ---------------------------------------------------------------------------
-// Terminal kernel shared memory: one piece of fp32 weights per warp (the largest
-// piece holds SLOT_BYTES / 2 / 2 bf16 elements).
-constexpr int TERM_SMEM = TERM_WARPS * (SLOT_BYTES / 2 / 2) * 4;
-
 template <typename T, bool GREEDY>
 static cudaError_t launch_t(const VerifyArgs& A, int grid, size_t dsmem, cudaStream_t st) {
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, GREEDY>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(NSLOT * SLOT_BYTES + 4 * (SV_MAX_B + 1) + 256));
+    const cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, GREEDY>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(NSLOT * SLOT_BYTES + 4 * (SV_MAX_B + 1) + 256));
     if (e != cudaSuccess) return e;
-    if (!GREEDY) {
-      e = cudaFuncSetAttribute(sv_terminal_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               TERM_SMEM);
-      if (e != cudaSuccess) return e;
-    }
     attr_set = true;
   }
-  sv_verify_kernel<T, GREEDY><<<grid, NTHREADS, dsmem, st>>>(A);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || GREEDY) return e;
-  // The terminal kernel is a programmatic dependent launch: it may be scheduled while
-  // the stream kernel drains, and waits for its completion on the device.
-  const long long tasks = (long long)A.B * A.R;
-  const long long want = (tasks + TERM_WARPS - 1) / TERM_WARPS;
+  // At T > 0 the kernel holds a grid-wide barrier between its two phases: a cooperative
+  // launch guarantees that all its CTAs (at most one per SM) are resident together.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(want < 4LL * grid ? want : 4LL * grid));
-  cfg.blockDim = dim3(32 * TERM_WARPS);
-  cfg.dynamicSmemBytes = TERM_SMEM;
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = dsmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = GREEDY ? 0 : 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sv_terminal_kernel<T>, A);
+  return cudaLaunchKernelEx(&cfg, sv_verify_kernel<T, GREEDY>, A);
 }
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st) {
