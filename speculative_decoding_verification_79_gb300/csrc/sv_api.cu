@@ -117,7 +117,7 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.t_res = reinterpret_cast<uint32_t*>(ws + L.t_res);
   A.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   A.part = reinterpret_cast<float2*>(ws + L.part);
-  A.rpart = reinterpret_cast<double*>(ws + L.rpart);
+  A.rpart = reinterpret_cast<float2*>(ws + L.rpart);
   A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);
 
   // One persistent CTA per SM, fewer when the batch cannot give every warp a piece.

@@ -68,7 +68,7 @@ struct WsLayout {
   size_t t_row, t_req, t_res;  // uint32 tickets: [B*RS], [B], [B]
   size_t rowstat;              // float2 [B*RS]
   size_t part;                 // float2 [B*RS*Pmax]
-  size_t rpart;                // double [B*Rmax]
+  size_t rpart;                // float2 [B*Rmax] (float-float piece sums)
   size_t jobs;                 // TermJob [B]
   size_t total;
   int RS, Pmax, Rmax;
@@ -139,7 +139,7 @@ struct VerifyArgs {
   uint32_t* t_res;
   float2* rowstat;
   float2* part;
-  double* rpart;
+  float2* rpart;
   TermJob* jobs;
 };
 

@@ -26,9 +26,9 @@
 //     cooperative, so all CTAs are resident): the (request, piece) tasks of the
 //     terminal rows (residual max(0, p_j - q_j), or p of the bonus row) are split
 //     over all warps and copied through the same slots; each sums its piece's weights
-//     with compensated fp32 arithmetic, reduced in float64; the last piece of a
-//     request locates the token by inverse CDF at u_{b,K} (float64 prefix over piece
-//     sums, one piece re-scanned in float64).
+//     with compensated fp32 arithmetic, reduced as float-float pairs; the last piece
+//     of a request locates the token by inverse CDF at u_{b,K} (float-float prefix
+//     over piece sums, one piece re-scanned).
 //  Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
 //  status word, lets its copies in flight land, and returns.
 #include <cfloat>
@@ -262,20 +262,64 @@ __device__ __forceinline__ void two_sum(float& s, float& c, float w) {
   s = t;
 }
 
-__device__ __forceinline__ double warp_sum_d(double x, int lane) {
+// ---------------------------------------------------------------------------
+// Float-float ("double-fp32") values: hi + lo with |lo| <= ulp(hi)/2, about 48
+// significant bits. The terminal-sample sums and prefixes use them instead of fp64,
+// whose throughput on this GPU is a small fraction of fp32's.
+// ---------------------------------------------------------------------------
+struct ff {
+  float hi, lo;
+};
+
+// Exact sum of two floats as a normalised pair (Knuth's TwoSum).
+__device__ __forceinline__ ff two_sum_ff(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+  return ff{s, e};
+}
+
+// Normalise s + e when |s| >= |e| (Dekker's FastTwoSum).
+__device__ __forceinline__ ff fast_two_sum_ff(float s, float e) {
+  const float h = __fadd_rn(s, e);
+  return ff{h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+
+// a + b. Commutative bit for bit, so both lanes of a butterfly step agree.
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const ff s = two_sum_ff(a.hi, b.hi);
+  return fast_two_sum_ff(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+
+// a * u for a float u (exact product of the high parts by fma).
+__device__ __forceinline__ ff ff_mul_f(ff a, float u) {
+  const float p = __fmul_rn(a.hi, u);
+  const float e = fmaf(a.hi, u, -p);
+  return fast_two_sum_ff(p, fmaf(a.lo, u, e));
+}
+
+// a < b for normalised pairs.
+__device__ __forceinline__ bool ff_lt(ff a, ff b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+__device__ __forceinline__ ff shfl_xor_ff(ff x, int o) {
+  return ff{__shfl_xor_sync(FULL, x.hi, o), __shfl_xor_sync(FULL, x.lo, o)};
+}
+
+__device__ __forceinline__ ff warp_sum_ff(ff x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const double y = __shfl_xor_sync(FULL, x, o);
-    x = (lane & o) ? (y + x) : (x + y);
-  }
+  for (int o = 16; o; o >>= 1) x = ff_add(x, shfl_xor_ff(x, o));
   return x;
 }
 
-__device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
+__device__ __forceinline__ ff warp_incl_scan_ff(ff x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(FULL, x, o);
-    if (lane >= o) x = y + x;
+    const ff y{__shfl_up_sync(FULL, x.hi, o), __shfl_up_sync(FULL, x.lo, o)};
+    if (lane >= o) x = ff_add(y, x);
   }
   return x;
 }
@@ -894,12 +938,12 @@ __device__ __forceinline__ void vec_weights(const uint4 vt, const uint4 vd, cons
   }
 }
 
-// Compensated total of the weights of elements [0, n) of rows t (and d), n <= E2;
-// with wbuf != nullptr the weights are also stored there (shared, per warp). Vector
-// loads are issued a half-piece at a time before use.
+// Compensated total of the weights of elements [0, n) of rows t (and d), n <= E2,
+// read from global memory; with wbuf != nullptr the weights are also stored there
+// (shared, per warp). Vector loads are issued a half-piece at a time before use.
 template <typename T>
-__device__ double piece_weights(const T* t, const T* d, int n, const TermW& W, float* wbuf,
-                                int lane) {
+__device__ ff piece_weights(const T* t, const T* d, int n, const TermW& W, float* wbuf,
+                            int lane) {
   constexpr int VEC = ET<T>::VEC;
   constexpr int HALF = SLOT_BYTES / 2 / 16 / 32 / 2;  // uint4 per lane per half-piece
   const bool vec = ((reinterpret_cast<uintptr_t>(t) | reinterpret_cast<uintptr_t>(d)) & 15) == 0;
@@ -943,13 +987,13 @@ __device__ double piece_weights(const T* t, const T* d, int n, const TermW& W, f
     two_sum(hs, hc, w);
   }
   __syncwarp();
-  return warp_sum_d((double)hs + (double)hc, lane);
+  return warp_sum_ff(two_sum_ff(hs, hc));
 }
 
 // Inverse-CDF step over weights wbuf[0, n): the smallest v with target < cum(v), cum
-// in float64. Lanes take contiguous ranges; falls back to the last positive weight
-// when rounding leaves target past the end.
-__device__ int locate_weights(const float* wbuf, int n, double target, int lane) {
+// a float-float prefix. Lanes take contiguous ranges; falls back to the last positive
+// weight when rounding leaves target past the end.
+__device__ int locate_weights(const float* wbuf, int n, ff target, int lane) {
   const int c = (n + 31) / 32;
   const int v0 = min(n, lane * c), v1 = min(n, v0 + c);
   float hs = 0.f, hc = 0.f;
@@ -959,17 +1003,18 @@ __device__ int locate_weights(const float* wbuf, int n, double target, int lane)
     two_sum(hs, hc, w);
     if (w > 0.f) lastpos = v;
   }
-  const double ls = (double)hs + (double)hc;
-  const double incl = warp_incl_scan_d(ls, lane);
-  const unsigned hit = __ballot_sync(FULL, target < incl);
+  const ff ls = two_sum_ff(hs, hc);
+  const ff incl = warp_incl_scan_ff(ls, lane);
+  const unsigned hit = __ballot_sync(FULL, ff_lt(target, incl));
   int y = -1;
   if (hit) {
     const int ln = __ffs(hit) - 1;
     if (lane == ln) {
-      double cum = incl - ls;
+      // Running prefix in float-float from the lane's exclusive prefix.
+      ff cum = ff_add(incl, ff_neg(ls));
       for (int v = v0; v < v1; ++v) {
-        cum += (double)wbuf[v];
-        if (target < cum) {
+        cum = ff_add(cum, ff{wbuf[v], 0.f});
+        if (ff_lt(target, cum)) {
           y = v;
           break;
         }
@@ -992,83 +1037,96 @@ __device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const T
   const int R = A.R, K = A.K, j = J.j;
   const T* trow = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V;
   const T* drow = W.resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V : trow;
-  const double uK = (double)__ldg(A.uni + (size_t)b * (K + 1) + K);
-  const double* rp = A.rpart + (size_t)b * A.Rmax;
+  const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
+  const float2* rp = A.rpart + (size_t)b * A.Rmax;
   const int c = (R + 31) / 32;
   const int p0 = min(R, lane * c), p1 = min(R, p0 + c);
-  double ls = 0.0;
+  ff ls{0.f, 0.f};
   int lastpos = -1;
   for (int p = p0; p < p1; ++p) {
-    const double w = __ldcg(rp + p);
-    ls += w;
-    if (w > 0.0) lastpos = p;
+    const float2 w = __ldcg(rp + p);
+    ls = ff_add(ls, ff{w.x, w.y});
+    if (w.x > 0.f) lastpos = p;
   }
-  const double incl = warp_incl_scan_d(ls, lane);
-  double Z = __shfl_sync(FULL, incl, 31);
+  const ff incl = warp_incl_scan_ff(ls, lane);
+  ff Z{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
   TermW Wl = W;
   bool whole_row = false;
-  if (W.resid && (!(Z > 0.0) || !(Z < 1e300))) {
+  if (W.resid && !(Z.hi > 0.f && Z.hi <= 3.402823466e38f)) {
     // No residual mass left (p == q up to rounding): sample p_j itself instead, piece
     // by piece over the whole row.
     Wl.resid = false;
     whole_row = true;
-    Z = 0.0;
+    Z = ff{0.f, 0.f};
     for (int p = 0; p < R; ++p) {
       const int e0 = p * A.E2;
-      Z += piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
+      Z = ff_add(Z, piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane));
       __syncwarp();
     }
   }
-  const double target = uK * Z;
+  const ff target = ff_mul_f(Z, uK);
   int pstar = -1;
-  double base = 0.0;
+  ff base{0.f, 0.f};
+  bool past_end = false;
   if (whole_row) {
     for (int p = 0; p < R && pstar < 0; ++p) {
       const int e0 = p * A.E2;
-      const double w =
-          piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
+      const ff w = piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
       __syncwarp();
-      if (target < base + w || p == R - 1) pstar = p;
-      else base += w;
+      const ff nb = ff_add(base, w);
+      if (ff_lt(target, nb)) pstar = p;
+      else if (p == R - 1) {
+        pstar = p;
+        past_end = true;
+      } else {
+        base = nb;
+      }
     }
   } else {
-    const unsigned hit = __ballot_sync(FULL, target < incl);
+    const unsigned hit = __ballot_sync(FULL, ff_lt(target, incl));
     if (hit) {
       const int ln = __ffs(hit) - 1;
       if (lane == ln) {
-        double cum = incl - ls;
+        ff cum = ff_add(incl, ff_neg(ls));
         for (int p = p0; p < p1; ++p) {
-          const double w = __ldcg(rp + p);
-          if (target < cum + w) {
+          const float2 w = __ldcg(rp + p);
+          const ff nc = ff_add(cum, ff{w.x, w.y});
+          if (ff_lt(target, nc)) {
             pstar = p;
             break;
           }
-          cum += w;
+          cum = nc;
         }
-        if (pstar < 0) pstar = lastpos;
+        if (pstar < 0) {
+          pstar = lastpos;
+          past_end = true;
+        }
         base = cum;
       }
       pstar = __shfl_sync(FULL, pstar, ln);
-      base = __shfl_sync(FULL, base, ln);
+      past_end = __shfl_sync(FULL, past_end, ln);
+      base = ff{__shfl_sync(FULL, base.hi, ln), __shfl_sync(FULL, base.lo, ln)};
     }
     if (pstar < 0) {  // rounding put the target past the last piece
       const unsigned has = __ballot_sync(FULL, lastpos >= 0);
       const int ln = has ? 31 - __clz(has) : 0;
       pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
-      base = target;
+      past_end = true;
     }
   }
   const int e0 = pstar * A.E2;
   const int ne = min(A.E2, A.V - e0);
   piece_weights<T>(trow + e0, drow + e0, ne, Wl, wbuf, lane);
-  return e0 + locate_weights(wbuf, ne, target - base, lane);
+  // Past the end: the last positive weight of the piece.
+  const ff t2 = past_end ? ff{INFINITY, 0.f} : ff_add(target, ff_neg(base));
+  return e0 + locate_weights(wbuf, ne, t2, lane);
 }
 
 // ---------------------------------------------------------------------------
 // Terminal phase (T > 0), after every CTA has finished its stream work: the terminal
 // piece tasks (request b, piece p) are split in equal contiguous ranges over all warps
 // and fed through the same slots. Each task sums the weights of its piece (compensated
-// fp32, reduced in float64); the task completing a request locates its token.
+// fp32, reduced as float-float); the task completing a request locates its token.
 // ---------------------------------------------------------------------------
 
 // Next terminal task of the warp's range that has a job, into a slot (lane 0 only).
@@ -1122,9 +1180,9 @@ __device__ bool issue_term(const VerifyArgs& A, long long& tc, long long t1, Slo
 }
 
 // Weight total of one terminal piece, from its slot (or from global memory in direct
-// mode): compensated fp32 per lane, reduced in float64.
+// mode): compensated fp32 per lane, reduced as float-float.
 template <typename T>
-__device__ double term_piece_sum(const SlotMeta& M, const TermW& W, const unsigned char* slot,
+__device__ ff term_piece_sum(const SlotMeta& M, const TermW& W, const unsigned char* slot,
                                  int lane) {
   constexpr int VEC = ET<T>::VEC;
   const int n = M.s0.n;
@@ -1142,7 +1200,7 @@ __device__ double term_piece_sum(const SlotMeta& M, const TermW& W, const unsign
 #pragma unroll
     for (int e = 0; e < VEC; ++e) two_sum(hs, hc, w[e]);
   }
-  return warp_sum_d((double)hs + (double)hc, lane);
+  return warp_sum_ff(two_sum_ff(hs, hc));
 }
 
 // One warp's range of terminal tasks. cons[] carries the slots' consumed-phase counts
@@ -1177,12 +1235,12 @@ __device__ void term_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
     const SlotMeta M = S.meta[s];
     unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
     const TermW W{A.a, A.a_lo, M.Mt, M.iSt, M.Md, M.iSd, M.jkind == J_RESID};
-    const double acc = term_piece_sum<T>(M, W, slot, lane);
+    const ff acc = term_piece_sum<T>(M, W, slot, lane);
     ++cons[k];
     const int b = M.b;
     uint32_t old = 0;
     if (lane == 0) {
-      A.rpart[(size_t)b * A.Rmax + M.p] = acc;
+      A.rpart[(size_t)b * A.Rmax + M.p] = make_float2(acc.hi, acc.lo);
       old = atom_add_release(A.t_res + b, 1u);
     }
     old = __shfl_sync(FULL, old, 0);
