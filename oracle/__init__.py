@@ -62,6 +62,11 @@ def _bind(path):
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_verify_u64.argtypes = common + [f64p] + tail + [ctypes.c_double] + outs
     lib.oracle_verify_u64.restype = ctypes.c_int
+    outs_m = [i32p, i32p, f64p, f64p, i32p, f64p, ctypes.c_int]
+    lib.oracle_verify_m.argtypes = common + [f32p] + tail + [ctypes.c_float] + outs_m
+    lib.oracle_verify_m.restype = ctypes.c_int
+    lib.oracle_verify_u64m.argtypes = common + [f64p] + tail + [ctypes.c_double] + outs_m
+    lib.oracle_verify_u64m.restype = ctypes.c_int
     return lib
 
 
@@ -127,7 +132,8 @@ def verify(target, draft, draft_tok, verify_len, uniforms, temperature: float,
     target [B,K+1,V] and draft [B,K,V]: float32, or bf16 given as uint16 bit patterns.
     draft_tok [B,K] int32, verify_len [B] int32, uniforms [B,K+1] float32 (float64 when
     ``u64``; only the brute-force tests use that). Returns dict(out_tok, out_accepted,
-    p, q, flags, status).
+    p, q, flags, margin, status); margin [B] is each request's smallest decision margin
+    (the quantity the near-tie flags threshold).
     """
     t, dt = _logits(target)
     d, dd = _logits(draft)
@@ -145,9 +151,11 @@ def verify(target, draft, draft_tok, verify_len, uniforms, temperature: float,
     p = np.zeros((B, K), np.float64) if diag else None
     q = np.zeros((B, K), np.float64) if diag else None
     flags = np.zeros(B, np.int32)
+    margin = np.zeros(B, np.float64)
     lib = lib or _load()
-    fn = lib.oracle_verify_u64 if u64 else lib.oracle_verify
+    fn = lib.oracle_verify_u64m if u64 else lib.oracle_verify_m
     rc = fn(_ptr(t), _ptr(d), dt, _ptr(tok), _ptr(vlen), _ptr(u), B, K, V, float(temperature),
-            _ptr(out_tok), _ptr(out_acc), _ptr(p), _ptr(q), _ptr(flags), int(nthreads))
+            _ptr(out_tok), _ptr(out_acc), _ptr(p), _ptr(q), _ptr(flags), _ptr(margin),
+            int(nthreads))
     return {"out_tok": out_tok, "out_accepted": out_acc, "p": p, "q": q, "flags": flags,
-            "status": rc}
+            "margin": margin, "status": rc}

@@ -223,8 +223,10 @@ int oracle_schedule(const float *conf, int B, int K, float tau, long long token_
 static int verify_one(const void *tgt, const void *drf, int dtype, const int32_t *tok,
                       const int32_t *vlen, const double *u, int b, int K, int V, double T,
                       int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
-                      int32_t *out_flags, double *p, double *q, double *r) {
+                      int32_t *out_flags, double *out_margin, double *p, double *q, double *r) {
     const int L = vlen[b];
+    double margin = INFINITY; /* smallest decision margin seen (diagnostic) */
+    if (out_margin) out_margin[b] = INFINITY;
     int32_t *ot = out_tok + (size_t)b * (K + 1);
     for (int k = 0; k <= K; k++) ot[k] = -1;
     for (int k = 0; k < K; k++) {
@@ -291,6 +293,7 @@ static int verify_one(const void *tgt, const void *drf, int dtype, const int32_t
         /* Near-tie bookkeeping (the decision itself is the line after). */
         double ratio = qx > 0.0 ? (px / qx < 1.0 ? px / qx : 1.0) : (px > 0.0 ? 1.0 : 0.0);
         if (fabs(uk - ratio) < NEAR_TIE) out_flags[b] |= ORC_FLAG_ACCEPT_TIE;
+        if (fabs(uk - ratio) < margin) margin = fabs(uk - ratio);
         if (px < 1e-30 && qx < 1e-30) out_flags[b] |= ORC_FLAG_TINY_PROB;
         if (uk * qx < px) {
             ot[k] = x;
@@ -313,6 +316,7 @@ static int verify_one(const void *tgt, const void *drf, int dtype, const int32_t
             y = inverse_cdf(p, V, uK, &Z, &gap);
         }
         if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;
+        if (out_margin) out_margin[b] = gap < margin ? gap : margin;
         ot[j] = y;
         out_acc[b] = j;
         return 0;
@@ -326,6 +330,7 @@ static int verify_one(const void *tgt, const void *drf, int dtype, const int32_t
         double Z, gap;
         int y = inverse_cdf(p, V, u[(size_t)b * (K + 1) + K], &Z, &gap);
         if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;
+        if (out_margin) out_margin[b] = gap < margin ? gap : margin;
         ot[L] = y;
         out_acc[b] = L;
     }
@@ -351,14 +356,18 @@ invalid:
  *  out_acc [B]: number of accepted drafts j (or -1 for an invalid request).
  *  out_p, out_q [B, K] or NULL: p_k(x_k), q_k(x_k) for k < L_b (T > 0).
  *  out_flags [B]: ORC_FLAG_* bits.
+ *  out_margin [B] or NULL (T > 0): the smallest decision margin of the request,
+ *  the quantity the near-tie flags threshold: min over tested positions of
+ *  |u_k - min(1, p/q)| and the terminal sample's distance to its nearest CDF edge
+ *  (normalised units). A diagnostic; no decision depends on it.
  *  nthreads: OpenMP threads over requests (requests are independent, so the
  *  result does not depend on it).
  * Returns ORC_OK, ORC_ERR_ARG, or ORC_ERR_INPUT if any request was invalid.
  */
-int oracle_verify_u64(const void *target, const void *draft, int dtype, const int32_t *tok,
-                      const int32_t *vlen, const double *u, int B, int K, int V, double T,
-                      int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
-                      int32_t *out_flags, int nthreads) {
+int oracle_verify_u64m(const void *target, const void *draft, int dtype, const int32_t *tok,
+                       const int32_t *vlen, const double *u, int B, int K, int V, double T,
+                       int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
+                       int32_t *out_flags, double *out_margin, int nthreads) {
     if (B < 0 || K < 1 || K > 32 || V < 1 || (dtype != 0 && dtype != 1) || !(T >= 0.0) ||
         !isfinite(T))
         return ORC_ERR_ARG;
@@ -379,7 +388,7 @@ int oracle_verify_u64(const void *target, const void *draft, int dtype, const in
 #endif
         for (int b = 0; b < B; b++)
             if (verify_one(target, draft, dtype, tok, vlen, u, b, K, V, T, out_tok, out_acc, out_p,
-                           out_q, out_flags, p, q, r))
+                           out_q, out_flags, out_margin, p, q, r))
                 n_invalid++;
         free(p);
         free(q);
@@ -388,19 +397,37 @@ int oracle_verify_u64(const void *target, const void *draft, int dtype, const in
     return n_invalid ? ORC_ERR_INPUT : ORC_OK;
 }
 
-/* Same as oracle_verify_u64 with the float32 uniforms of the C-ABI, widened
+/* oracle_verify_u64m without the margin output. */
+int oracle_verify_u64(const void *target, const void *draft, int dtype, const int32_t *tok,
+                      const int32_t *vlen, const double *u, int B, int K, int V, double T,
+                      int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
+                      int32_t *out_flags, int nthreads) {
+    return oracle_verify_u64m(target, draft, dtype, tok, vlen, u, B, K, V, T, out_tok, out_acc,
+                              out_p, out_q, out_flags, NULL, nthreads);
+}
+
+/* Same as oracle_verify_u64m with the float32 uniforms of the C-ABI, widened
  * exactly to float64. */
-int oracle_verify(const void *target, const void *draft, int dtype, const int32_t *tok,
-                  const int32_t *vlen, const float *u, int B, int K, int V, float T,
-                  int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
-                  int32_t *out_flags, int nthreads) {
+int oracle_verify_m(const void *target, const void *draft, int dtype, const int32_t *tok,
+                    const int32_t *vlen, const float *u, int B, int K, int V, float T,
+                    int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
+                    int32_t *out_flags, double *out_margin, int nthreads) {
     double *u64 = NULL;
     if (u && B > 0) {
         u64 = (double *)malloc(sizeof(double) * (size_t)B * (K + 1));
         for (size_t i = 0; i < (size_t)B * (K + 1); i++) u64[i] = (double)u[i];
     }
-    int rc = oracle_verify_u64(target, draft, dtype, tok, vlen, u64, B, K, V, (double)T, out_tok,
-                               out_acc, out_p, out_q, out_flags, nthreads);
+    int rc = oracle_verify_u64m(target, draft, dtype, tok, vlen, u64, B, K, V, (double)T,
+                                out_tok, out_acc, out_p, out_q, out_flags, out_margin, nthreads);
     free(u64);
     return rc;
+}
+
+/* oracle_verify_m without the margin output. */
+int oracle_verify(const void *target, const void *draft, int dtype, const int32_t *tok,
+                  const int32_t *vlen, const float *u, int B, int K, int V, float T,
+                  int32_t *out_tok, int32_t *out_acc, double *out_p, double *out_q,
+                  int32_t *out_flags, int nthreads) {
+    return oracle_verify_m(target, draft, dtype, tok, vlen, u, B, K, V, T, out_tok, out_acc,
+                           out_p, out_q, out_flags, NULL, nthreads);
 }

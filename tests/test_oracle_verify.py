@@ -225,6 +225,31 @@ def test_hand_cases(oracle_mod):
         assert j == 0 and ot[0] == y
 
 
+def test_decision_margin_hand_case(oracle_mod):
+    """The margin diagnostic is the smaller of |u_0 - min(1, p/q)| at the tested position
+    and the terminal sample's distance to the nearer edge of its CDF bucket (normalised),
+    derived by hand here for V=3, L=1 (accepted -> bonus from p_1; rejected -> residual)."""
+    def rows(ps):
+        return np.log(np.array(ps, np.float64)).astype(np.float32)
+
+    t = np.stack([rows([0.5, 0.3, 0.2]), rows([0.1, 0.6, 0.3])])
+    d = rows([0.2, 0.5, 0.3])[None]
+    p0, q0, p1 = softmax64(t[0], 1.0), softmax64(d[0], 1.0), softmax64(t[1], 1.0)
+    # (u0, uK): accept margin 0.01 / bonus gap 0.05; accept margin 0.05 / bonus gap 0.01;
+    # reject (margin 0.01) with residual [0.3, 0, 0] whose single bucket gives gap 0.5.
+    for u0, uK in [(0.59, 0.65), (0.55, 0.69), (0.61, 0.5)]:
+        u = np.array([u0, uK], np.float32)
+        r = oracle_mod.verify(t[None], d[None], np.array([[1]]), np.array([1]), u[None], 1.0,
+                              diag=False)
+        accept_margin = abs(float(u[0]) - min(1.0, p0[1] / q0[1]))
+        w = p1 if float(u[0]) * q0[1] < p0[1] else np.maximum(p0 - q0, 0.0)
+        cum = np.cumsum(w)
+        target = float(u[1]) * cum[-1]
+        y = int(np.searchsorted(cum, target, side="right"))
+        gap = min(target - (cum[y] - w[y]), cum[y] - target) / cum[-1]
+        assert abs(r["margin"][0] - min(accept_margin, gap)) < 1e-12, (u0, uK)
+
+
 def test_zero_length_block_is_plain_sampling(oracle_mod):
     """L = 0: nothing to verify; the call emits one token sampled from p_0 (greedy: argmax)."""
     t = np.log(np.array([[0.25, 0.25, 0.5], [1 / 3, 1 / 3, 1 / 3]])).astype(np.float32)
