@@ -119,6 +119,8 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.part = reinterpret_cast<float2*>(ws + L.part);
   A.rpart = reinterpret_cast<float2*>(ws + L.rpart);
   A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);
+  A.dec_flag = reinterpret_cast<uint32_t*>(ws + L.dec);
+  A.lsum = reinterpret_cast<float*>(ws + L.lsum);
 
   // One persistent CTA per SM, fewer when the batch cannot give every warp a piece.
   const long long max_pieces = (long long)B * (greedy ? K + 1 : 2 * K + 1) * A.P;

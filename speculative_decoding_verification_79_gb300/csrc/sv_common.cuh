@@ -46,13 +46,12 @@ struct WsHeader {
   uint32_t status;    // ST_* bits
   uint32_t reserved;
   uint32_t cta_done;  // verify: CTAs that have finished
-  uint32_t grid_sync; // verify: CTAs done with the stream phase (T > 0)
-  uint32_t pad[60];
+  uint32_t pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
-// Terminal-sample job of one request, written by the deciding warp in the stream
-// phase and read in the terminal phase: the residual max(0, p_j - q_j) over rows
+// Terminal-sample job of one request, written by the deciding warp and read by the
+// warps running its terminal tasks: the residual max(0, p_j - q_j) over rows
 // t_j and d_j, a plain sample of p over target row j (the bonus row L), or nothing
 // (an invalid request, or greedy verification).
 enum : int { J_NONE = -1, J_RESID = 0, J_BONUS = 1 };
@@ -66,10 +65,12 @@ struct __align__(32) TermJob {
 
 struct WsLayout {
   size_t t_row, t_req, t_res;  // uint32 tickets: [B*RS], [B], [B]
+  size_t dec;                  // uint32 decision flags [B]
   size_t rowstat;              // float2 [B*RS]
   size_t part;                 // float2 [B*RS*Pmax]
   size_t rpart;                // float2 [B*Rmax] (float-float piece sums)
   size_t jobs;                 // TermJob [B]
+  size_t lsum;                 // float [B*Rmax*32] lane-range totals of terminal pieces
   size_t total;
   int RS, Pmax, Rmax;
 };
@@ -87,11 +88,11 @@ __host__ __device__ inline int resid_pieces(int V, int eb) {
   return (V + E2 - 1) / E2;
 }
 
-// The ticket counters sit at fixed offsets sized for the library maxima, so that calls
-// of different shapes sharing one workspace never find another call's data where they
-// expect a counter. Every counter is back to zero when a call ends.
+// The ticket counters and decision flags sit at fixed offsets sized for the library
+// maxima, so that calls of different shapes sharing one workspace never find another
+// call's data where they expect a counter. Every one is back to zero when a call ends.
 constexpr size_t TICKET_ROW_WORDS = (size_t)SV_MAX_B * (2 * SV_MAX_K + 1);
-constexpr size_t TICKET_BYTES = 4 * (TICKET_ROW_WORDS + 2 * (size_t)SV_MAX_B);
+constexpr size_t TICKET_BYTES = 4 * (TICKET_ROW_WORDS + 3 * (size_t)SV_MAX_B);
 
 __host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
   WsLayout L;
@@ -102,11 +103,13 @@ __host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
   L.t_row = sizeof(WsHeader);
   L.t_req = L.t_row + 4 * TICKET_ROW_WORDS;
   L.t_res = L.t_req + 4 * (size_t)SV_MAX_B;
+  L.dec = L.t_res + 4 * (size_t)SV_MAX_B;
   size_t off = align_up(sizeof(WsHeader) + TICKET_BYTES, 256);
   L.rowstat = off; off = align_up(off + 8 * nb * L.RS, 256);
   L.part = off;    off = align_up(off + 8 * nb * L.RS * (size_t)L.Pmax, 256);
   L.rpart = off;   off = align_up(off + 8 * nb * (size_t)L.Rmax, 256);
   L.jobs = off;    off = align_up(off + sizeof(TermJob) * nb, 256);
+  L.lsum = off;    off = align_up(off + 4 * 32 * nb * (size_t)L.Rmax, 256);
   L.total = off;
   return L;
 }
@@ -137,10 +140,12 @@ struct VerifyArgs {
   uint32_t* t_row;
   uint32_t* t_req;
   uint32_t* t_res;
+  uint32_t* dec_flag;  // per request: 0 undecided, 1 terminal job published, 2 no job
   float2* rowstat;
   float2* part;
   float2* rpart;
   TermJob* jobs;
+  float* lsum;
 };
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st);
@@ -215,6 +220,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+
+// Relaxed load (GPU scope): a poll that orders nothing.
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Release-ordered store (GPU scope): earlier writes of this thread become visible to
+// whoever observes the value (after an acquire fence).
+__device__ __forceinline__ void st_release(uint32_t* addr, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// Acquire-release fence (GPU scope): after a relaxed load that saw a released value,
+// later reads see what was written before the release.
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // 2^x on the special-function unit (hardware approximation).
 __device__ __forceinline__ float ex2(float x) {

@@ -5,30 +5,31 @@
 // Mathematics of Suffix Decay"; perchy.ai Technology, "Verified by the target").
 //
 // One launch on the caller's stream, no CPU round trip: sv_verify_kernel, one
-// persistent CTA per SM, in two phases.
-//  1. Stream phase. Work list: every active logit row
-//     of the batch (request b: target rows 0..L_b, and at T > 0 draft rows
-//     0..L_b-1) cut into pieces of SLOT_BYTES, ordered request-major; every warp of
-//     the grid takes an equal contiguous range of it. Each warp owns SLOTS_PER_WARP
-//     shared-memory slots and is its own producer: lane 0 issues a 1-D bulk copy
-//     (cp.async.bulk, TMA) of the next piece into the slot the warp has just
-//     finished, guarded by an mbarrier, while the warp reduces the other slots.
-//     Pieces are reduced whole: online softmax (running max + sum of
-//     2^(z*log2e/T - max)) at T > 0, or (max, lowest argmax) at T == 0, and merged in
-//     registers while consecutive pieces belong to the same row. Each row segment is
-//     published with a release-ordered atomic ticket whose value the warp inspects
-//     only after its next wait, so the round trip stays off the critical path. The
-//     warp completing a row combines it; the warp completing a request decides it:
-//     p_k(x_k), q_k(x_k),
-//     the accept tests u*q < p, a ballot for the first rejection j, the outputs,
-//     and (T > 0) the terminal-sample job of the request.
-//  2. Terminal phase (T > 0 only), after a grid-wide barrier (the launch is
-//     cooperative, so all CTAs are resident): the (request, piece) tasks of the
-//     terminal rows (residual max(0, p_j - q_j), or p of the bonus row) are split
-//     over all warps and copied through the same slots; each sums its piece's weights
-//     with compensated fp32 arithmetic, reduced as float-float pairs; the last piece
-//     of a request locates the token by inverse CDF at u_{b,K} (float-float prefix
-//     over piece sums, one piece re-scanned).
+// persistent CTA per SM of NCW warps.
+//  - Stream work. Work list: every active logit row of the batch (request b: target
+//    rows 0..L_b, and at T > 0 draft rows 0..L_b-1) cut into pieces of SLOT_BYTES,
+//    ordered request-major and split into equal contiguous ranges, one per warp of
+//    the grid. Each warp owns SLOTS_PER_WARP shared-memory slots and is its own
+//    producer: lane 0 issues a 1-D bulk copy (cp.async.bulk, TMA) of the next piece
+//    into the slot the warp has just finished, guarded by an mbarrier, while the warp
+//    reduces the other slots. Pieces are reduced whole: online softmax (running max
+//    + sum of 2^(z*log2e/T - max)) at T > 0, or (max, lowest argmax) at T == 0,
+//    merged in registers while consecutive pieces belong to the same row. A warp's
+//    run of pieces of one row is published with one release-ordered atomic ticket
+//    whose value the warp inspects only after its next wait, so the round trip stays
+//    off the critical path. The warp completing a row combines its partials in piece
+//    order; the warp completing a request decides it: p_k(x_k),
+//    q_k(x_k), the accept tests u*q < p, a ballot for the first rejection j, the
+//    outputs, and (T > 0) the request's terminal-sample job, announced by a
+//    release-ordered decision flag.
+//  - Terminal tasks (T > 0). The terminal rows of a request (residual
+//    max(0, p_j - q_j), or p of the bonus row) are cut into R pieces; task (b, p)
+//    belongs to warp (b*R + p) mod (warps in the grid). Once its stream range is
+//    done, a warp feeds its terminal tasks through the same slots, each as soon as its
+//    request's flag is up (no grid-wide barrier). Each task sums its piece's weights
+//    (compensated fp32, float-float across lanes) and stores the 32 lane-range
+//    totals; the task completing a request finds the token by inverse CDF at u_{b,K}
+//    over piece totals, lane-range totals and at most one lane range of elements.
 //  Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
 //  status word, lets its copies in flight land, and returns.
 #include <cfloat>
@@ -53,7 +54,7 @@ struct __align__(16) SlotMeta {
   int e0;             // first element of the piece within its row
   int direct;         // terminal piece: 1 = rows read straight from global memory
   int jkind;          // terminal piece: J_RESID or J_BONUS
-  int pad;
+  int last;           // stream piece: the warp's row segment ends here
   Seg s0, s1;         // stream piece: s0; terminal piece: target (s0) and draft (s1)
   float Mt, iSt, Md, iSd;
 };
@@ -62,7 +63,6 @@ struct Shared {
   SlotMeta meta[NSLOT];
   uint64_t full[NSLOT];
   int abort_flag;
-  int grid_ok;
   int last_cta;
   int total_rows;
   int scan[32];
@@ -175,16 +175,6 @@ __device__ __forceinline__ float exp2_precise(float z, float a, float a_lo, floa
   const float yl = fmaf(z, a_lo, pl + el);
   const float e = ex2(yh);
   return fmaf(e, yl * 0.6931471805599453f, e);
-}
-
-// 2^((z - M)*(a + a_lo)) for a row maximum M: z - M is exact for bf16 logits (and
-// nearly so for fp32), the product is split as above; -inf logits give 0.
-__device__ __forceinline__ float exp2_diff(float z, float M, float a, float a_lo) {
-  const float d = __fsub_rn(z, M);
-  const float yh = __fmul_rn(d, a);
-  const float yl = fmaf(d, a_lo, fmaf(d, a, -yh));
-  const float e = ex2(yh);
-  return (d == -INFINITY) ? 0.f : fmaf(e, yl * 0.6931471805599453f, e);
 }
 
 // ---------------------------------------------------------------------------
@@ -373,13 +363,6 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const Veri
 }
 
 
-// Acquire-ordered load (GPU scope).
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* addr) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-  return v;
-}
-
 // Release-ordered atomic add (GPU scope): earlier stores of this thread become
 // visible to whoever observes the new count.
 __device__ __forceinline__ uint32_t atom_add_release(uint32_t* addr, uint32_t v) {
@@ -403,6 +386,7 @@ __device__ void emit_invalid(const VerifyArgs& A, int b, int lane) {
     A.out_acc[b] = -1;
     A.jobs[b].kind = J_NONE;
     raise_status(A, ST_DEVICE_INPUT);
+    st_release(A.dec_flag + b, 2u);  // decided, no terminal sample
   }
 }
 
@@ -452,21 +436,17 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = q;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
-  // Terminal-sample job. Weights are computed as 2^((z - M)*a) against the exact
-  // maximum, so each inverse row sum absorbs the frame offset 2^(M*a - fl(M*a)).
-  const float jM = (lane < L) ? __ldcg(A.rowstat + rb + lane).x : 0.f;
-  const float jMd = (lane < L) ? __ldcg(A.rowstat + rb + L + 1 + lane).x : 0.f;
-  const float cSt = iSt * ex2(fmaf(jM, A.a, -MAt));
-  const float cSd = iSd * ex2(fmaf(jMd, A.a, -MAd));
-  const float jMt = __shfl_sync(FULL, jM, j & 31), jSt = __shfl_sync(FULL, cSt, j & 31);
-  const float jMdd = __shfl_sync(FULL, jMd, j & 31), jSd = __shfl_sync(FULL, cSd, j & 31);
+  // Terminal-sample job: a row's weights are taken in the frame its sum was formed
+  // in, 2^(fl(z*a - fl(M*a))), so that weight * (1/S) is p (or q) directly.
+  const float jMt = __shfl_sync(FULL, MAt, j & 31), jSt = __shfl_sync(FULL, iSt, j & 31);
+  const float jMdd = __shfl_sync(FULL, MAd, j & 31), jSd = __shfl_sync(FULL, iSd, j & 31);
   if (lane == 0) {
     A.out_acc[b] = j;
     TermJob J;
     J.j = j;
     if (j == L) {  // every draft accepted: bonus sample from p_L
       J.kind = J_BONUS;
-      J.MAt = sL.x;
+      J.MAt = __fmul_rn(sL.x, A.a);
       J.invSt = J.MAd = J.invSd = 0.f;
     } else {  // first rejection at j: residual sample
       J.kind = J_RESID;
@@ -477,6 +457,7 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
     }
     J.pad[0] = J.pad[1] = 0;
     A.jobs[b] = J;
+    st_release(A.dec_flag + b, 1u);  // the job is published
   }
 }
 
@@ -734,186 +715,19 @@ __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix
 }
 
 // ---------------------------------------------------------------------------
-// Per-warp work: a contiguous range [i0, i1) of the work list (equal shares), walked
-// by a cursor in lane 0 that issues the bulk copy of each piece into the warp's
-// next free slot.
+// Terminal-sample weights.
 // ---------------------------------------------------------------------------
-struct Cursor {
-  unsigned long long cur, end;
-  int cb, cr, cp, cL, cn;  // request, row slot, piece, L, rows of the current item
-};
-
-template <bool GREEDY>
-__device__ void cursor_init(Cursor& c, const VerifyArgs& A, const int* prefix,
-                            unsigned long long i0, unsigned long long i1) {
-  c.cur = i0;
-  c.end = i1;
-  if (i0 >= i1) return;
-  const int P = A.P;
-  const unsigned long long g = i0 / P;
-  c.cp = static_cast<int>(i0 - g * P);
-  int lo = 0, hi = A.B - 1;
-  while (lo < hi) {  // last request whose prefix is <= g
-    const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<unsigned long long>(prefix[mid]) <= g)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  c.cb = lo;
-  c.cr = static_cast<int>(g - prefix[lo]);
-  c.cn = prefix[lo + 1] - prefix[lo];
-  c.cL = L_of_rows(c.cn, GREEDY);
-}
-
-// Next piece of the warp's range into a slot: fills the slot's metadata and starts
-// its bulk copy. Returns false at the end of the range. Lane 0 only.
-template <typename T, bool GREEDY>
-__device__ bool issue_next(const VerifyArgs& A, Cursor& c, const int* prefix, SlotMeta& meta,
-                           uint64_t* full, unsigned char* slot) {
-  constexpr int eb = sizeof(T);
-  const int P = A.P, B = A.B;
-  if (c.cur >= c.end) return false;
-  const T* row = row_ptr<T>(A, c.cb, c.cr, c.cL);
-  const int e0 = c.cp * A.E;
-  const int n = min(A.E, A.V - e0);
-  meta.kind = K_STREAM;
-  meta.b = c.cb;
-  meta.r = c.cr;
-  meta.p = c.cp;
-  meta.e0 = e0;
-  meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
-  ++c.cur;
-  if (++c.cp == P) {
-    c.cp = 0;
-    if (++c.cr == c.cn) {
-      c.cr = 0;
-      do {
-        ++c.cb;
-      } while (c.cb < B && prefix[c.cb + 1] == prefix[c.cb]);
-      if (c.cb < B) {
-        c.cn = prefix[c.cb + 1] - prefix[c.cb];
-        c.cL = L_of_rows(c.cn, GREEDY);
-      }
-    }
-  }
-  const uint32_t tx = meta.s0.body * eb;
-  if (tx) {
-    mbar_arrive_expect_tx(full, tx);
-    bulk_g2s(slot, meta.s0.g + meta.s0.head * eb, tx, full);
-  } else {
-    mbar_arrive(full);
-  }
-  return true;
-}
-
-// One warp: its range of pieces through SLOTS_PER_WARP slots; each slot is refilled
-// right after the warp has reduced it.
-template <typename T, bool GREEDY>
-__device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
-                          int w, int lane, uint32_t* cons) {
-  const unsigned long long total =
-      static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(A.P);
-  const unsigned long long nw = (unsigned long long)gridDim.x * NCW;
-  const unsigned long long gw = (unsigned long long)blockIdx.x * NCW + w;
-  const unsigned long long i0 = total * gw / nw, i1 = total * (gw + 1) / nw;
-  Cursor c;
-  int have[SLOTS_PER_WARP];
-#pragma unroll
-  for (int q = 0; q < SLOTS_PER_WARP; ++q) have[q] = 0;
-  if (lane == 0) {
-    cursor_init<GREEDY>(c, A, prefix, i0, i1);
-#pragma unroll
-    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
-      const int s = SLOTS_PER_WARP * w + q;
-      have[q] = issue_next<T, GREEDY>(A, c, prefix, S.meta[s], &S.full[s],
-                                      slots + (size_t)s * SLOT_BYTES);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < SLOTS_PER_WARP; ++q) have[q] = __shfl_sync(FULL, have[q], 0);
-  Pending pd;
-  pd.valid = 0;
-  Segment sg;
-  sg.valid = 0;
-  LaneState st;
-  lane_reset(st);
-  if (GREEDY) st.s = __int_as_float(INT_MAX);
-  unsigned long long item = i0;
-  int k = 0;
-  bool aborted = false;
-  while (have[k]) {
-    const int s = SLOTS_PER_WARP * w + k;
-    const bool ok = wait_phase(&S.full[s], cons[k] & 1, S, A);
-    if (!__all_sync(FULL, ok)) {
-      aborted = true;
-      break;
-    }
-    if (pd.valid) {  // the previous segment's ticket has had a whole wait to come back
-      settle<T, GREEDY>(A, pd, prefix, lane);
-      pd.valid = 0;
-    }
-    const SlotMeta M = S.meta[s];
-    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
-    if (!(sg.valid && sg.b == M.b && sg.r == M.r)) {  // a new row segment starts here
-      sg.valid = 1;
-      sg.b = M.b;
-      sg.r = M.r;
-      sg.p0 = M.p;
-      lane_reset(st);
-      if (GREEDY) st.s = __int_as_float(INT_MAX);
-    }
-    sg.p1 = M.p;
-    fold_piece<T, GREEDY>(st, A, M, slot, lane);
-    ++cons[k];
-    __syncwarp();
-    int h = 0;
-    if (lane == 0) {
-      // The slot's shared-memory reads are done; order them before the async-proxy
-      // write of the next copy into the same slot.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      h = issue_next<T, GREEDY>(A, c, prefix, S.meta[s], &S.full[s], slot);
-    }
-    have[k] = __shfl_sync(FULL, h, 0);
-    // Publish at the row's last piece or the range's last piece.
-    ++item;
-    if (M.p == A.P - 1 || item == i1) {
-      if (pd.valid) {
-        settle<T, GREEDY>(A, pd, prefix, lane);
-        pd.valid = 0;
-      }
-      pd = publish<GREEDY>(A, sg, st, lane);
-      sg.valid = 0;
-    }
-    k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
-  }
-  if (pd.valid) settle<T, GREEDY>(A, pd, prefix, lane);
-  if (aborted) {
-    // Let this warp's copies in flight land before the CTA may exit.
-    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
-      if (!have[q]) continue;
-      const long long t0 = clock64();
-      while (!mbar_test(&S.full[SLOTS_PER_WARP * w + q], cons[q] & 1) &&
-             clock64() - t0 < WAIT_CYCLES) {
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Terminal sample (T > 0): weights, piece sums, inverse-CDF location.
-// ---------------------------------------------------------------------------
-
 // Weight of one element: residual max(0, p - q), or the unnormalised target weight
-// 2^((z - M)*a) of a plain sample. Mt, Md are the raw row maxima; iSt, iSd the
-// inverse row sums in that frame.
+// 2^(z*a - MA) of a plain sample. MAt, MAd are the frames fl(M*a) the row sums were
+// formed in, iSt, iSd the inverse row sums, so 2^(z*a - MA) * iS is the probability.
+// A -inf logit (a masked token) gives 2^-inf = 0.
 struct TermW {
-  float a, a_lo, Mt, iSt, Md, iSd;
+  float a, MAt, iSt, MAd, iSd;
   bool resid;
   __device__ __forceinline__ float operator()(float zt, float zd) const {
-    const float et = exp2_diff(zt, Mt, a, a_lo);
+    const float et = ex2(fmaf(zt, a, -MAt));
     if (!resid) return et;
-    return fmaxf(et * iSt - exp2_diff(zd, Md, a, a_lo) * iSd, 0.f);
+    return fmaxf(fmaf(et, iSt, -(ex2(fmaf(zd, a, -MAd)) * iSd)), 0.f);
   }
 };
 
@@ -938,86 +752,168 @@ __device__ __forceinline__ void vec_weights(const uint4 vt, const uint4 vd, cons
   }
 }
 
-// Compensated total of the weights of elements [0, n) of rows t (and d), n <= E2,
-// read from global memory; with wbuf != nullptr the weights are also stored there
-// (shared, per warp). Vector loads are issued a half-piece at a time before use.
+
+// ---------------------------------------------------------------------------
+// Terminal sample (T > 0): residual max(0, p_j - q_j) at the first rejection j, or
+// p_L when every draft was accepted, sampled by inverse CDF at u_{b,K}.
+//
+// A request's terminal rows are cut into R pieces of E2 elements (one task each);
+// inside a piece, lane l covers one contiguous range of whole vectors. A task stores
+// the piece's total (float-float) and its 32 lane-range totals; the task completing
+// the request then finds the token in three levels (piece, lane range, element), so
+// only one lane range (at most 64 elements) is evaluated again.
+// ---------------------------------------------------------------------------
+
+// Length of each lane's contiguous range in a terminal piece of n elements: a whole
+// number of vectors, ceil(n / 32) rounded up to a vector.
 template <typename T>
-__device__ ff piece_weights(const T* t, const T* d, int n, const TermW& W, float* wbuf,
-                            int lane) {
+__device__ __forceinline__ int range_len(int n) {
   constexpr int VEC = ET<T>::VEC;
-  constexpr int HALF = SLOT_BYTES / 2 / 16 / 32 / 2;  // uint4 per lane per half-piece
-  const bool vec = ((reinterpret_cast<uintptr_t>(t) | reinterpret_cast<uintptr_t>(d)) & 15) == 0;
-  float hs = 0.f, hc = 0.f;
-  int done = 0;
-  if (vec) {
-    const int nv = n / VEC;
-    const uint4* t4 = reinterpret_cast<const uint4*>(t);
-    const uint4* d4 = reinterpret_cast<const uint4*>(d);
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      uint4 vt[HALF], vd[HALF];
-#pragma unroll
-      for (int u = 0; u < HALF; ++u) {
-        const int i = lane + 32 * (u + HALF * h);
-        if (i < nv) {
-          vt[u] = __ldg(t4 + i);
-          vd[u] = W.resid ? __ldg(d4 + i) : vt[u];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < HALF; ++u) {
-        const int i = lane + 32 * (u + HALF * h);
-        if (i < nv) {
-          float w[VEC];
-          vec_weights<T>(vt[u], vd[u], W, w);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) two_sum(hs, hc, w[e]);
-          if (wbuf) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) wbuf[i * VEC + e] = w[e];
-          }
-        }
-      }
-    }
-    done = nv * VEC;
-  }
-  for (int e = done + lane; e < n; e += 32) {
-    const float w = W(ld_logit(t + e), ld_logit(d + e));
-    if (wbuf) wbuf[e] = w;
-    two_sum(hs, hc, w);
-  }
-  __syncwarp();
-  return warp_sum_ff(two_sum_ff(hs, hc));
+  return VEC * ((n + 32 * VEC - 1) / (32 * VEC));
 }
 
-// Inverse-CDF step over weights wbuf[0, n): the smallest v with target < cum(v), cum
-// a float-float prefix. Lanes take contiguous ranges; falls back to the last positive
-// weight when rounding leaves target past the end.
-__device__ int locate_weights(const float* wbuf, int n, ff target, int lane) {
-  const int c = (n + 31) / 32;
-  const int v0 = min(n, lane * c), v1 = min(n, v0 + c);
+// Sum of the weights of one vector as a balanced fp32 tree.
+template <typename T>
+__device__ __forceinline__ float vec_wsum(const uint4 vt, const uint4 vd, const TermW& W) {
+  float w[ET<T>::VEC];
+  vec_weights<T>(vt, vd, W, w);
+  if constexpr (ET<T>::VEC == 8) {
+    return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+  } else {
+    return (w[0] + w[1]) + (w[2] + w[3]);
+  }
+}
+
+// Weight total of this lane's range of a terminal piece held in a slot (target row
+// in the first half, draft row in the second), or read from global memory in direct
+// mode. Compensated fp32.
+template <typename T>
+__device__ ff lane_range_sum(const SlotMeta& M, const TermW& W, const unsigned char* slot,
+                             int lane) {
+  constexpr int VEC = ET<T>::VEC;
+  const int n = M.s0.n;
+  const int ce = range_len<T>(n);
+  const int lo = min(n, lane * ce), hi = min(n, lo + ce);
+  float hs = 0.f, hc = 0.f;
+  if (M.direct) {
+    const T* t = reinterpret_cast<const T*>(M.s0.g);
+    const T* d = reinterpret_cast<const T*>(M.s1.g);
+    for (int e = lo; e < hi; ++e) two_sum(hs, hc, W(ld_logit(t + e), ld_logit(d + e)));
+  } else {
+    const uint4* t4 = reinterpret_cast<const uint4*>(slot);
+    const uint4* d4 = reinterpret_cast<const uint4*>(W.resid ? slot + SLOT_BYTES / 2 : slot);
+    const int v0 = lo / VEC, nvl = (hi - lo) / VEC;
+    // Each lane starts at a different vector of its range, so that the lanes of one
+    // shared-memory wavefront read distinct banks.
+    if (nvl == 8) {  // every full piece of 8 KB slots
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = v0 + ((lane + i) & 7);
+        two_sum(hs, hc, vec_wsum<T>(t4[q], d4[q], W));
+      }
+    } else {
+      int q = nvl ? lane % nvl : 0;
+      for (int i = 0; i < nvl; ++i) {
+        two_sum(hs, hc, vec_wsum<T>(t4[v0 + q], d4[v0 + q], W));
+        q = (q + 1 == nvl) ? 0 : q + 1;
+      }
+    }
+  }
+  return two_sum_ff(hs, hc);
+}
+
+// The same lane-range total read from global memory (whole-row fallback only).
+template <typename T>
+__device__ ff range_sum_global(const T* t, const T* d, int n, const TermW& W, int lane) {
+  const int ce = range_len<T>(n);
+  const int lo = min(n, lane * ce), hi = min(n, lo + ce);
+  float hs = 0.f, hc = 0.f;
+  for (int e = lo; e < hi; ++e) two_sum(hs, hc, W(ld_logit(t + e), ld_logit(d + e)));
+  return two_sum_ff(hs, hc);
+}
+
+// A terminal task whose ticket value has not been inspected yet.
+struct TermPend {
+  int valid, b, j, jkind;
+  float Mt, iSt, Md, iSd;
+  uint32_t old;  // ticket value returned to lane 0
+};
+
+// Sum one terminal piece: lane-range totals staged in the (consumed) slot and
+// written by lane 0 with the piece total. The ticket increment follows one slot later
+// (term_ticket), when these stores have long completed and the release costs little.
+template <typename T>
+__device__ TermPend term_consume(const VerifyArgs& A, const SlotMeta& M, unsigned char* slot,
+                                 int lane) {
+  const TermW W{A.a, M.Mt, M.iSt, M.Md, M.iSd, M.jkind == J_RESID};
+  const ff mine = lane_range_sum<T>(M, W, slot, lane);
+  const ff tot = warp_sum_ff(mine);
+  float* stage = reinterpret_cast<float*>(slot);
+  __syncwarp();  // every lane has finished reading the slot
+  stage[lane] = mine.hi;
+  // Order the staging write before the async-proxy write of the slot's next copy.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  TermPend pt;
+  pt.valid = 1;
+  pt.b = M.b;
+  pt.j = M.r;
+  pt.jkind = M.jkind;
+  pt.Mt = M.Mt;
+  pt.iSt = M.iSt;
+  pt.Md = M.Md;
+  pt.iSd = M.iSd;
+  pt.old = 0;
+  if (lane == 0) {
+    const size_t pid = (size_t)M.b * A.Rmax + M.p;
+    float4* dst = reinterpret_cast<float4*>(A.lsum + pid * 32);
+    const float4* src = reinterpret_cast<const float4*>(stage);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = src[i];
+    A.rpart[pid] = make_float2(tot.hi, tot.lo);
+  }
+  return pt;
+}
+
+// Release-ordered ticket increment for a summed terminal piece (lane 0); its value is
+// inspected by term_settle a slot later.
+__device__ __forceinline__ void term_ticket(const VerifyArgs& A, TermPend& pt, int lane) {
+  if (lane == 0) pt.old = atom_add_release(A.t_res + pt.b, 1u);
+}
+
+// Element level: the first element e in [r0, r1) of rows t, d with t3 < cumulative
+// weight from r0 (or the last positive element when `past`, or when rounding leaves
+// t3 beyond the range's total). Each lane takes up to EPL consecutive elements and
+// keeps their weights in registers.
+template <typename T>
+__device__ int locate_elems(const T* t, const T* d, int r0, int r1, ff t3, bool past,
+                            const TermW& W, int lane) {
+  constexpr int VEC = ET<T>::VEC;
+  constexpr int E2 = SLOT_BYTES / 2 / (int)sizeof(T);
+  constexpr int EPL = (VEC * ((E2 + 32 * VEC - 1) / (32 * VEC)) + 31) / 32;
+  static_assert(EPL >= 1 && EPL <= 4, "lane ranges of at most 128 elements");
+  const int e0 = min(r1, r0 + lane * EPL);
+  float w[EPL];
   float hs = 0.f, hc = 0.f;
   int lastpos = -1;
-  for (int v = v0; v < v1; ++v) {
-    const float w = wbuf[v];
-    two_sum(hs, hc, w);
-    if (w > 0.f) lastpos = v;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    w[i] = (e0 + i < r1) ? W(ld_logit(t + e0 + i), ld_logit(d + e0 + i)) : 0.f;
+    two_sum(hs, hc, w[i]);
+    if (w[i] > 0.f) lastpos = e0 + i;
   }
   const ff ls = two_sum_ff(hs, hc);
   const ff incl = warp_incl_scan_ff(ls, lane);
-  const unsigned hit = __ballot_sync(FULL, ff_lt(target, incl));
   int y = -1;
+  const unsigned hit = past ? 0u : __ballot_sync(FULL, ff_lt(t3, incl));
   if (hit) {
     const int ln = __ffs(hit) - 1;
     if (lane == ln) {
-      // Running prefix in float-float from the lane's exclusive prefix.
       ff cum = ff_add(incl, ff_neg(ls));
-      for (int v = v0; v < v1; ++v) {
-        cum = ff_add(cum, ff{wbuf[v], 0.f});
-        if (ff_lt(target, cum)) {
-          y = v;
-          break;
-        }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        cum = ff_add(cum, ff{w[i], 0.f});
+        if (y < 0 && e0 + i < r1 && ff_lt(t3, cum)) y = e0 + i;
       }
       if (y < 0) y = lastpos;
     }
@@ -1025,69 +921,126 @@ __device__ int locate_weights(const float* wbuf, int n, ff target, int lane) {
   }
   if (y < 0) {
     const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-    y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : 0;
+    y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : r0;
   }
   return y;
 }
 
-// Locate the terminal token of request b from its R piece sums.
+// Lane-range and element levels inside piece `pstar` of rows trow, drow, given each
+// lane's range total `lsv` and the target t2 relative to the piece start.
 template <typename T>
-__device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const TermW& W,
-                           float* wbuf, int lane) {
-  const int R = A.R, K = A.K, j = J.j;
+__device__ int locate_in_piece(const VerifyArgs& A, const T* trow, const T* drow, int pstar,
+                               float lsv, ff t2, bool past, const TermW& W, int lane) {
+  const ff mine{lsv, 0.f};
+  const ff incl = warp_incl_scan_ff(mine, lane);
+  int lstar;
+  ff t3{0.f, 0.f};
+  const unsigned hit = past ? 0u : __ballot_sync(FULL, ff_lt(t2, incl));
+  if (hit) {
+    lstar = __ffs(hit) - 1;
+    const ff ex = ff_add(incl, ff_neg(mine));
+    const ff base2{__shfl_sync(FULL, ex.hi, lstar), __shfl_sync(FULL, ex.lo, lstar)};
+    t3 = ff_add(t2, ff_neg(base2));
+  } else {
+    const unsigned has = __ballot_sync(FULL, lsv > 0.f);
+    lstar = has ? 31 - __clz(has) : 0;
+    past = true;
+  }
+  const int e0 = pstar * A.E2;
+  const int n = min(A.E2, A.V - e0);
+  const int ce = range_len<T>(n);
+  const int r0 = min(n, lstar * ce), r1 = min(n, r0 + ce);
+  return e0 + locate_elems<T>(trow + e0, drow + e0, r0, r1, t3, past, W, lane);
+}
+
+// No residual mass left (p == q up to rounding): sample p_j itself instead, its piece
+// totals computed here, piece by piece.
+template <typename T>
+__device__ int locate_whole_row(const VerifyArgs& A, const T* trow, float uK, TermW W, int lane) {
+  W.resid = false;
+  const int R = A.R;
+  ff Z{0.f, 0.f};
+  for (int p = 0; p < R; ++p) {
+    const int e0 = p * A.E2;
+    Z = ff_add(Z, warp_sum_ff(range_sum_global<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), W,
+                                                  lane)));
+  }
+  const ff target = ff_mul_f(Z, uK);
+  ff base{0.f, 0.f};
+  int pstar = R - 1;
+  bool past = true;
+  float lsv = 0.f;
+  for (int p = 0; p < R; ++p) {
+    const int e0 = p * A.E2;
+    const ff mine = range_sum_global<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), W, lane);
+    const ff nb = ff_add(base, warp_sum_ff(mine));
+    lsv = mine.hi;
+    if (ff_lt(target, nb)) {
+      pstar = p;
+      past = false;
+      break;
+    }
+    base = nb;
+  }
+  return locate_in_piece<T>(A, trow, trow, pstar, lsv, ff_add(target, ff_neg(base)), past, W,
+                            lane);
+}
+
+// Locate the terminal token of request b (row j) from its piece and lane-range totals.
+template <typename T>
+__device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, int lane) {
+  const int R = A.R, K = A.K;
   const T* trow = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V;
   const T* drow = W.resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V : trow;
   const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
   const float2* rp = A.rpart + (size_t)b * A.Rmax;
   const int c = (R + 31) / 32;
   const int p0 = min(R, lane * c), p1 = min(R, p0 + c);
+  constexpr int CREG = 4;  // piece totals a lane keeps in registers (R <= 128)
+  float2 wr[CREG];
   ff ls{0.f, 0.f};
   int lastpos = -1;
-  for (int p = p0; p < p1; ++p) {
-    const float2 w = __ldcg(rp + p);
-    ls = ff_add(ls, ff{w.x, w.y});
-    if (w.x > 0.f) lastpos = p;
-  }
-  const ff incl = warp_incl_scan_ff(ls, lane);
-  ff Z{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
-  TermW Wl = W;
-  bool whole_row = false;
-  if (W.resid && !(Z.hi > 0.f && Z.hi <= 3.402823466e38f)) {
-    // No residual mass left (p == q up to rounding): sample p_j itself instead, piece
-    // by piece over the whole row.
-    Wl.resid = false;
-    whole_row = true;
-    Z = ff{0.f, 0.f};
-    for (int p = 0; p < R; ++p) {
-      const int e0 = p * A.E2;
-      Z = ff_add(Z, piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane));
-      __syncwarp();
-    }
-  }
-  const ff target = ff_mul_f(Z, uK);
-  int pstar = -1;
-  ff base{0.f, 0.f};
-  bool past_end = false;
-  if (whole_row) {
-    for (int p = 0; p < R && pstar < 0; ++p) {
-      const int e0 = p * A.E2;
-      const ff w = piece_weights<T>(trow + e0, trow + e0, min(A.E2, A.V - e0), Wl, nullptr, lane);
-      __syncwarp();
-      const ff nb = ff_add(base, w);
-      if (ff_lt(target, nb)) pstar = p;
-      else if (p == R - 1) {
-        pstar = p;
-        past_end = true;
-      } else {
-        base = nb;
-      }
+  if (c <= CREG) {
+#pragma unroll
+    for (int i = 0; i < CREG; ++i) wr[i] = (p0 + i < p1) ? __ldcg(rp + p0 + i) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < CREG; ++i) {
+      ls = ff_add(ls, ff{wr[i].x, wr[i].y});
+      if (wr[i].x > 0.f) lastpos = p0 + i;
     }
   } else {
-    const unsigned hit = __ballot_sync(FULL, ff_lt(target, incl));
-    if (hit) {
-      const int ln = __ffs(hit) - 1;
-      if (lane == ln) {
-        ff cum = ff_add(incl, ff_neg(ls));
+    for (int p = p0; p < p1; ++p) {
+      const float2 w = __ldcg(rp + p);
+      ls = ff_add(ls, ff{w.x, w.y});
+      if (w.x > 0.f) lastpos = p;
+    }
+  }
+  const ff incl = warp_incl_scan_ff(ls, lane);
+  const ff Z{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
+  if (W.resid && !(Z.hi > 0.f && Z.hi <= 3.402823466e38f))
+    return locate_whole_row<T>(A, trow, uK, W, lane);
+  const ff target = ff_mul_f(Z, uK);
+  // Piece level.
+  int pstar = -1;
+  bool past = false;
+  ff base{0.f, 0.f};
+  const unsigned hit = __ballot_sync(FULL, ff_lt(target, incl));
+  if (hit) {
+    const int ln = __ffs(hit) - 1;
+    if (lane == ln) {
+      ff cum = ff_add(incl, ff_neg(ls));
+      if (c <= CREG) {
+#pragma unroll
+        for (int i = 0; i < CREG; ++i) {
+          if (pstar < 0 && p0 + i < p1) {
+            const ff nc = ff_add(cum, ff{wr[i].x, wr[i].y});
+            if (ff_lt(target, nc))
+              pstar = p0 + i;
+            else
+              cum = nc;
+          }
+        }
+      } else {
         for (int p = p0; p < p1; ++p) {
           const float2 w = __ldcg(rp + p);
           const ff nc = ff_add(cum, ff{w.x, w.y});
@@ -1097,181 +1050,385 @@ __device__ int term_locate(const VerifyArgs& A, int b, const TermJob& J, const T
           }
           cum = nc;
         }
-        if (pstar < 0) {
-          pstar = lastpos;
-          past_end = true;
-        }
-        base = cum;
       }
-      pstar = __shfl_sync(FULL, pstar, ln);
-      past_end = __shfl_sync(FULL, past_end, ln);
-      base = ff{__shfl_sync(FULL, base.hi, ln), __shfl_sync(FULL, base.lo, ln)};
+      if (pstar < 0) {
+        pstar = lastpos;
+        past = true;
+      }
+      base = cum;
     }
-    if (pstar < 0) {  // rounding put the target past the last piece
-      const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-      const int ln = has ? 31 - __clz(has) : 0;
-      pstar = has ? __shfl_sync(FULL, lastpos, ln) : 0;
-      past_end = true;
-    }
+    pstar = __shfl_sync(FULL, pstar, ln);
+    past = __shfl_sync(FULL, (int)past, ln) != 0;
+    base = ff{__shfl_sync(FULL, base.hi, ln), __shfl_sync(FULL, base.lo, ln)};
   }
-  const int e0 = pstar * A.E2;
-  const int ne = min(A.E2, A.V - e0);
-  piece_weights<T>(trow + e0, drow + e0, ne, Wl, wbuf, lane);
-  // Past the end: the last positive weight of the piece.
-  const ff t2 = past_end ? ff{INFINITY, 0.f} : ff_add(target, ff_neg(base));
-  return e0 + locate_weights(wbuf, ne, t2, lane);
+  if (pstar < 0) {  // rounding put the target past the last piece
+    const unsigned has = __ballot_sync(FULL, lastpos >= 0);
+    pstar = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : 0;
+    past = true;
+  }
+  const float lsv = __ldcg(A.lsum + ((size_t)b * A.Rmax + pstar) * 32 + lane);
+  const ff t2 = past ? ff{0.f, 0.f} : ff_add(target, ff_neg(base));
+  return locate_in_piece<T>(A, trow, drow, pstar, lsv, t2, past, W, lane);
+}
+
+// Inspect a terminal ticket: the task completing its request locates the token.
+template <typename T>
+__device__ void term_settle(const VerifyArgs& A, const TermPend& pt, int lane) {
+  const uint32_t old = __shfl_sync(FULL, pt.old, 0);
+  if (old != (uint32_t)(A.R - 1)) return;
+  fence_acq_rel();
+  if (lane == 0) A.t_res[pt.b] = 0;
+  const TermW W{A.a, pt.Mt, pt.iSt, pt.Md, pt.iSd, pt.jkind == J_RESID};
+  const int y = term_locate<T>(A, pt.b, pt.j, W, lane);
+  if (lane == 0) A.out_tok[(size_t)pt.b * (A.K + 1) + pt.j] = y;
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// Terminal phase (T > 0), after every CTA has finished its stream work: the terminal
-// piece tasks (request b, piece p) are split in equal contiguous ranges over all warps
-// and fed through the same slots. Each task sums the weights of its piece (compensated
-// fp32, reduced as float-float); the task completing a request locates its token.
+// Per-warp work. Stream: the work list (every active row of the batch, request-major,
+// cut into pieces) is split into equal contiguous ranges, one per warp of the grid.
+// Terminal tasks (T > 0): task (b, p) belongs to warp (b*R + p) mod (warps in the
+// grid); a warp takes them up once its stream range is done, each as soon as its
+// request is decided.
 // ---------------------------------------------------------------------------
+struct Cursor {
+  unsigned long long cur, end;
+  int cb, cr, cp, cL, cn;  // request, row slot, piece, L, rows of the current item
+};
 
-// Next terminal task of the warp's range that has a job, into a slot (lane 0 only).
-// Returns false at the end of the range.
-template <typename T>
-__device__ bool issue_term(const VerifyArgs& A, long long& tc, long long t1, SlotMeta& meta,
-                           uint64_t* full, unsigned char* slot) {
+template <bool GREEDY>
+__device__ void cursor_init(Cursor& c, const VerifyArgs& A, const int* prefix,
+                            unsigned long long i0, unsigned long long i1) {
+  c.cur = i0;
+  c.end = i1;
+  if (i0 >= i1) return;
+  const int P = A.P;
+  const unsigned long long g = i0 / P;
+  c.cp = static_cast<int>(i0 - g * P);
+  int lo = 0, hi = A.B - 1;
+  while (lo < hi) {  // last request whose first row is <= g
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<unsigned long long>(prefix[mid]) <= g)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  c.cb = lo;
+  c.cr = static_cast<int>(g - prefix[lo]);
+  c.cn = prefix[lo + 1] - prefix[lo];
+  c.cL = L_of_rows(c.cn, GREEDY);
+}
+
+// Next stream piece of the warp's range into a slot (lane 0 only); false at the end.
+template <typename T, bool GREEDY>
+__device__ bool issue_stream(const VerifyArgs& A, Cursor& c, const int* prefix, SlotMeta& meta,
+                             uint64_t* full, unsigned char* slot) {
   constexpr int eb = sizeof(T);
-  const int R = A.R, K = A.K;
-  while (tc < t1) {
-    const int b = (int)(tc / R), p = (int)(tc - (long long)b * R);
-    ++tc;
-    const int kind = __ldcg(&A.jobs[b].kind), j = __ldcg(&A.jobs[b].j);
-    if (!((kind == J_RESID && j >= 0 && j < K) || (kind == J_BONUS && j >= 0 && j <= K))) continue;
-    const int e0 = p * A.E2;
-    const int n = min(A.E2, A.V - e0);
-    const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V + e0;
-    meta.kind = K_TERM;
-    meta.jkind = kind;
-    meta.b = b;
-    meta.r = j;
-    meta.p = p;
-    meta.e0 = e0;
-    meta.Mt = __ldcg(&A.jobs[b].MAt);
-    meta.iSt = __ldcg(&A.jobs[b].invSt);
-    meta.Md = __ldcg(&A.jobs[b].MAd);
-    meta.iSd = __ldcg(&A.jobs[b].invSd);
-    meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
-    bool whole = meta.s0.head == 0 && meta.s0.body == n;
-    if (kind == J_RESID) {
-      const T* dr = static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V + e0;
-      meta.s1 = make_seg(reinterpret_cast<const unsigned char*>(dr), n, eb);
-      whole = whole && meta.s1.head == 0 && meta.s1.body == n;
-    } else {
-      meta.s1 = meta.s0;
+  const int P = A.P, B = A.B;
+  if (c.cur >= c.end) return false;
+  const T* row = row_ptr<T>(A, c.cb, c.cr, c.cL);
+  const int e0 = c.cp * A.E;
+  const int n = min(A.E, A.V - e0);
+  meta.kind = K_STREAM;
+  meta.b = c.cb;
+  meta.r = c.cr;
+  meta.p = c.cp;
+  meta.e0 = e0;
+  meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
+  ++c.cur;
+  // The warp's segment of this row ends at the row's last piece or the range's end.
+  meta.last = (c.cp == P - 1 || c.cur == c.end) ? 1 : 0;
+  if (++c.cp == P) {
+    c.cp = 0;
+    if (++c.cr == c.cn) {
+      c.cr = 0;
+      do {
+        ++c.cb;
+      } while (c.cb < B && prefix[c.cb + 1] == prefix[c.cb]);
+      if (c.cb < B) {
+        c.cn = prefix[c.cb + 1] - prefix[c.cb];
+        c.cL = L_of_rows(c.cn, GREEDY);
+      }
     }
-    // A piece whose rows are not both 16-byte aligned and whole multiples of 16 bytes
-    // is read straight from global memory.
-    meta.direct = !whole;
-    if (whole) {
-      const uint32_t bytes = (uint32_t)(n * eb);
-      mbar_arrive_expect_tx(full, (kind == J_RESID ? 2u : 1u) * bytes);
-      bulk_g2s(slot, meta.s0.g, bytes, full);
-      if (kind == J_RESID) bulk_g2s(slot + SLOT_BYTES / 2, meta.s1.g, bytes, full);
-    } else {
-      mbar_arrive(full);
-    }
-    return true;
   }
-  return false;
+  const uint32_t tx = meta.s0.body * eb;
+  if (tx) {
+    mbar_arrive_expect_tx(full, tx);
+    bulk_g2s(slot, meta.s0.g + meta.s0.head * eb, tx, full);
+  } else {
+    mbar_arrive(full);
+  }
+  return true;
 }
 
-// Weight total of one terminal piece, from its slot (or from global memory in direct
-// mode): compensated fp32 per lane, reduced as float-float.
+// Terminal task (request b, piece p) into a slot (lane 0 only; the request's job is
+// published).
 template <typename T>
-__device__ ff term_piece_sum(const SlotMeta& M, const TermW& W, const unsigned char* slot,
-                                 int lane) {
-  constexpr int VEC = ET<T>::VEC;
-  const int n = M.s0.n;
-  if (M.direct)
-    return piece_weights<T>(reinterpret_cast<const T*>(M.s0.g),
-                            reinterpret_cast<const T*>(M.s1.g), n, W, nullptr, lane);
-  const uint4* t4 = reinterpret_cast<const uint4*>(slot);
-  const uint4* d4 = reinterpret_cast<const uint4*>(W.resid ? slot + SLOT_BYTES / 2 : slot);
-  float hs = 0.f, hc = 0.f;
-  const int nv = n / VEC;
-#pragma unroll 2
-  for (int i = lane; i < nv; i += 32) {
-    float w[VEC];
-    vec_weights<T>(t4[i], d4[i], W, w);
+__device__ void issue_term(const VerifyArgs& A, int b, int p, SlotMeta& meta, uint64_t* full,
+                           unsigned char* slot) {
+  constexpr int eb = sizeof(T);
+  const int K = A.K;
+  const int kind = __ldcg(&A.jobs[b].kind), j = __ldcg(&A.jobs[b].j);
+  const int e0 = p * A.E2;
+  const int n = min(A.E2, A.V - e0);
+  const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V + e0;
+  meta.kind = K_TERM;
+  meta.jkind = kind;
+  meta.b = b;
+  meta.r = j;
+  meta.p = p;
+  meta.e0 = e0;
+  meta.Mt = __ldcg(&A.jobs[b].MAt);
+  meta.iSt = __ldcg(&A.jobs[b].invSt);
+  meta.Md = __ldcg(&A.jobs[b].MAd);
+  meta.iSd = __ldcg(&A.jobs[b].invSd);
+  meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
+  bool whole = meta.s0.head == 0 && meta.s0.body == n;
+  if (kind == J_RESID) {
+    const T* dr = static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V + e0;
+    meta.s1 = make_seg(reinterpret_cast<const unsigned char*>(dr), n, eb);
+    whole = whole && meta.s1.head == 0 && meta.s1.body == n;
+  } else {
+    meta.s1 = meta.s0;
+  }
+  // Rows that are not 16-byte aligned whole multiples of 16 bytes are read straight
+  // from global memory.
+  meta.direct = !whole;
+  if (whole) {
+    const uint32_t bytes = (uint32_t)(n * eb);
+    mbar_arrive_expect_tx(full, (kind == J_RESID ? 2u : 1u) * bytes);
+    bulk_g2s(slot, meta.s0.g, bytes, full);
+    if (kind == J_RESID) bulk_g2s(slot + SLOT_BYTES / 2, meta.s1.g, bytes, full);
+  } else {
+    mbar_arrive(full);
+  }
+}
+
+enum : int { SLOT_EMPTY = 0, SLOT_FULL = 1, SLOT_DEFERRED = 2 };
+
+// Per-warp issue state (meaningful in lane 0).
+struct Issuer {
+  Cursor c;
+  long long nw;     // warps in the grid
+  long long tt, NT; // next terminal task of this warp (gw + m*nw); tasks in the batch
+  uint32_t pf;      // decision flag of task tt's request, loaded earlier
+};
+
+// Refill a slot (lane 0): the next stream piece while the warp's range lasts, then
+// its terminal tasks, each once its request is decided. Returns SLOT_FULL, SLOT_EMPTY
+// (nothing left at all), or SLOT_DEFERRED (only terminal tasks of undecided requests
+// are left). `fresh`: read the decision flag now instead of using the prefetched one.
+template <typename T, bool GREEDY>
+__device__ int refill(const VerifyArgs& A, Issuer& I, const int* prefix, bool fresh,
+                      SlotMeta& meta, uint64_t* full, unsigned char* slot) {
+  if (issue_stream<T, GREEDY>(A, I.c, prefix, meta, full, slot)) return SLOT_FULL;
+  if (!GREEDY) {
+    while (I.tt < I.NT) {
+      const int b = static_cast<int>(I.tt / A.R);
+      const uint32_t f = fresh ? ld_relaxed(A.dec_flag + b) : I.pf;
+      if (f == 0) break;
+      fresh = true;  // a later task's flag has not been read yet
+      if (f == 1) {
+        fence_acq_rel();  // the job record was published before the flag
+        issue_term<T>(A, b, static_cast<int>(I.tt - (long long)b * A.R), meta, full, slot);
+        I.tt += I.nw;
+        I.pf = 0;
+        return SLOT_FULL;
+      }
+      I.tt += I.nw;  // the request has no terminal sample
+    }
+  }
+  return (!GREEDY && I.tt < I.NT) ? SLOT_DEFERRED : SLOT_EMPTY;
+}
+
+// A refill that found nothing at all left: slots waiting for a terminal task have
+// nothing to wait for either.
+__device__ __forceinline__ void drop_deferred(int* st, int h) {
+  if (h != SLOT_EMPTY) return;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) two_sum(hs, hc, w[e]);
-  }
-  return warp_sum_ff(two_sum_ff(hs, hc));
+  for (int q = 0; q < SLOTS_PER_WARP; ++q)
+    if (st[q] == SLOT_DEFERRED) st[q] = SLOT_EMPTY;
 }
 
-// One warp's range of terminal tasks. cons[] carries the slots' consumed-phase counts
-// from the stream phase.
-template <typename T>
-__device__ void term_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, int w, int lane,
-                          uint32_t* cons) {
-  const long long N2 = (long long)A.B * A.R;
-  const long long nw = (long long)gridDim.x * NCW;
+// Bounded wait until the request of terminal task tt is decided (lane 0).
+__device__ bool wait_decided(const VerifyArgs& A, Shared& S, long long tt, long long NT) {
+  if (tt >= NT) return true;
+  const int b = static_cast<int>(tt / A.R);
+  const long long t0 = clock64();
+  while (ld_relaxed(A.dec_flag + b) == 0) {
+    if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
+    if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) {
+      S.abort_flag = 1;
+      return false;
+    }
+    if (clock64() - t0 > WAIT_CYCLES) {
+      S.abort_flag = 1;
+      raise_status(A, ST_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// One warp: its chunks of the stream and its terminal tasks through SLOTS_PER_WARP
+// slots; each slot is refilled right after the warp has consumed it.
+template <typename T, bool GREEDY>
+__device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
+                          int w, int lane) {
+  Issuer I;
+  I.nw = (long long)gridDim.x * NCW;
   const long long gw = (long long)blockIdx.x * NCW + w;
-  const long long t1 = N2 * (gw + 1) / nw;
-  long long tc = N2 * gw / nw;
-  int have[SLOTS_PER_WARP];
+  I.tt = gw;
+  I.NT = GREEDY ? 0 : (long long)A.B * A.R;
+  I.pf = 0;
+  {
+    const unsigned long long total =
+        static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(A.P);
+    const unsigned long long nw = I.nw, g = gw;
+    if (lane == 0) cursor_init<GREEDY>(I.c, A, prefix, total * g / nw, total * (g + 1) / nw);
+  }
+  int st[SLOTS_PER_WARP];
+  uint32_t cons[SLOTS_PER_WARP];
 #pragma unroll
   for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+    const int s = SLOTS_PER_WARP * w + q;
     int h = 0;
-    if (lane == 0) {
-      const int s = SLOTS_PER_WARP * w + q;
-      h = issue_term<T>(A, tc, t1, S.meta[s], &S.full[s], slots + (size_t)s * SLOT_BYTES);
-    }
-    have[q] = __shfl_sync(FULL, h, 0);
+    if (lane == 0)
+      h = refill<T, GREEDY>(A, I, prefix, true, S.meta[s], &S.full[s],
+                            slots + (size_t)s * SLOT_BYTES);
+    st[q] = __shfl_sync(FULL, h, 0);
+    cons[q] = 0;
   }
+  Pending pd;
+  pd.valid = 0;
+  TermPend pti, pts;  // terminal pieces summed (ticket not taken yet) / ticket taken
+  pti.valid = 0;
+  pts.valid = 0;
+  Segment sg;
+  sg.valid = 0;
+  LaneState ls;
+  lane_reset(ls);
+  if (GREEDY) ls.s = __int_as_float(INT_MAX);
   int k = 0;
   bool aborted = false;
-  while (have[k]) {
+  while (true) {
     const int s = SLOTS_PER_WARP * w + k;
-    const bool ok = wait_phase(&S.full[s], cons[k] & 1, S, A);
-    if (!__all_sync(FULL, ok)) {
+    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
+    if (!GREEDY && st[k] == SLOT_DEFERRED) {  // retry a refill that had to wait
+      int h = 0;
+      if (lane == 0) h = refill<T, GREEDY>(A, I, prefix, true, S.meta[s], &S.full[s], slot);
+      st[k] = __shfl_sync(FULL, h, 0);
+      drop_deferred(st, st[k]);
+    }
+    if (st[k] == SLOT_FULL) {
+      const bool ok = wait_phase(&S.full[s], cons[k] & 1, S, A);
+      if (!__all_sync(FULL, ok)) {
+        aborted = true;
+        break;
+      }
+      ++cons[k];
+      st[k] = SLOT_EMPTY;
+      if (pd.valid) {  // the previous segment's ticket has had a whole wait to come back
+        settle<T, GREEDY>(A, pd, prefix, lane);
+        pd.valid = 0;
+      }
+      if (!GREEDY && pts.valid) {
+        term_settle<T>(A, pts, lane);
+        pts.valid = 0;
+      }
+      if (!GREEDY && pti.valid) {
+        pts = pti;
+        term_ticket(A, pts, lane);
+        pti.valid = 0;
+      }
+      // Once the stream range is done, prefetch the decision flag the next refill
+      // will look at.
+      if (!GREEDY && lane == 0 && I.c.cur >= I.c.end && I.tt < I.NT)
+        I.pf = ld_relaxed(A.dec_flag + I.tt / A.R);
+      const SlotMeta M = S.meta[s];
+      if (GREEDY || M.kind == K_STREAM) {
+        if (!(sg.valid && sg.b == M.b && sg.r == M.r)) {  // a new row segment starts here
+          sg.valid = 1;
+          sg.b = M.b;
+          sg.r = M.r;
+          sg.p0 = M.p;
+          lane_reset(ls);
+          if (GREEDY) ls.s = __int_as_float(INT_MAX);
+        }
+        sg.p1 = M.p;
+        fold_piece<T, GREEDY>(ls, A, M, slot, lane);
+      } else {
+        pti = term_consume<T>(A, M, slot, lane);
+      }
+      __syncwarp();
+      int h = 0;
+      if (lane == 0) {
+        // The slot's shared-memory accesses are done; order them before the
+        // async-proxy write of the next copy into the same slot.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        h = refill<T, GREEDY>(A, I, prefix, false, S.meta[s], &S.full[s], slot);
+      }
+      st[k] = __shfl_sync(FULL, h, 0);
+      drop_deferred(st, st[k]);
+      if ((GREEDY || M.kind == K_STREAM) && M.last) {
+        if (pd.valid) {
+          settle<T, GREEDY>(A, pd, prefix, lane);
+          pd.valid = 0;
+        }
+        pd = publish<GREEDY>(A, sg, ls, lane);
+        sg.valid = 0;
+      }
+      k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
+      continue;
+    }
+    // Slot k has nothing to consume: move on to a slot that has.
+    bool any_full = false, any_def = false;
+#pragma unroll
+    for (int q = 0; q < SLOTS_PER_WARP; ++q) {
+      any_full |= st[q] == SLOT_FULL;
+      any_def |= st[q] == SLOT_DEFERRED;
+    }
+    if (any_full) {
+      k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
+      continue;
+    }
+    if (GREEDY || !any_def) break;
+    // Only terminal tasks of undecided requests are left. Settle the pending tickets
+    // first (the awaited decision may be one this warp owes), then wait for it.
+    if (pd.valid) {
+      settle<T, GREEDY>(A, pd, prefix, lane);
+      pd.valid = 0;
+    }
+    if (pts.valid) {
+      term_settle<T>(A, pts, lane);
+      pts.valid = 0;
+    }
+    if (pti.valid) {
+      term_ticket(A, pti, lane);
+      term_settle<T>(A, pti, lane);
+      pti.valid = 0;
+    }
+    int ok = 1;
+    if (lane == 0) ok = wait_decided(A, S, I.tt, I.NT);
+    if (!__shfl_sync(FULL, ok, 0)) {
       aborted = true;
       break;
     }
-    const SlotMeta M = S.meta[s];
-    unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
-    const TermW W{A.a, A.a_lo, M.Mt, M.iSt, M.Md, M.iSd, M.jkind == J_RESID};
-    const ff acc = term_piece_sum<T>(M, W, slot, lane);
-    ++cons[k];
-    const int b = M.b;
-    uint32_t old = 0;
-    if (lane == 0) {
-      A.rpart[(size_t)b * A.Rmax + M.p] = make_float2(acc.hi, acc.lo);
-      old = atom_add_release(A.t_res + b, 1u);
-    }
-    old = __shfl_sync(FULL, old, 0);
-    __syncwarp();
-    if (old == (uint32_t)(A.R - 1)) {  // last piece of this request: locate its token
-      __threadfence();
-      if (lane == 0) A.t_res[b] = 0;
-      TermJob J;
-      J.kind = M.jkind;
-      J.j = M.r;
-      // The slot's data has been consumed: it serves as the warp's weight buffer.
-      const int y = term_locate<T>(A, b, J, W, reinterpret_cast<float*>(slot), lane);
-      if (lane == 0) A.out_tok[(size_t)b * (A.K + 1) + M.r] = y;
-      __syncwarp();
-    }
-    int h = 0;
-    if (lane == 0) {
-      // Order this warp's generic reads and writes of the slot before the async-proxy
-      // write of the next copy.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      h = issue_term<T>(A, tc, t1, S.meta[s], &S.full[s], slot);
-    }
-    have[k] = __shfl_sync(FULL, h, 0);
-    k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
+    while (st[k] != SLOT_DEFERRED) k = (k + 1 == SLOTS_PER_WARP) ? 0 : k + 1;
+  }
+  if (pd.valid) settle<T, GREEDY>(A, pd, prefix, lane);
+  if (!GREEDY && pts.valid) term_settle<T>(A, pts, lane);
+  if (!GREEDY && pti.valid) {
+    term_ticket(A, pti, lane);
+    term_settle<T>(A, pti, lane);
   }
   if (aborted) {
+    // Let this warp's copies in flight land before the CTA may exit.
     for (int q = 0; q < SLOTS_PER_WARP; ++q) {
-      if (!have[q]) continue;
-      const long long c0 = clock64();
+      if (st[q] != SLOT_FULL) continue;
+      const long long t0 = clock64();
       while (!mbar_test(&S.full[SLOTS_PER_WARP * w + q], cons[q] & 1) &&
-             clock64() - c0 < WAIT_CYCLES) {
+             clock64() - t0 < WAIT_CYCLES) {
       }
     }
   }
@@ -1331,39 +1488,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
   }
   __syncthreads();
 
-  uint32_t cons[SLOTS_PER_WARP];
-#pragma unroll
-  for (int q = 0; q < SLOTS_PER_WARP; ++q) cons[q] = 0;
-  warp_loop<T, GREEDY>(A, S, slots, prefix, warp, lane, cons);
+  warp_loop<T, GREEDY>(A, S, slots, prefix, warp, lane);
   __syncthreads();
 
-  if (!GREEDY) {
-    // Grid-wide barrier: every request has been decided (and its terminal job
-    // written) once all CTAs have arrived. The wait is bounded; after a timeout
-    // anywhere the terminal phase is skipped (the status word reports it).
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(&A.hdr->grid_sync, 1u);
-      const long long c0 = clock64();
-      int ok = 1;
-      while (ld_acquire(&A.hdr->grid_sync) < gridDim.x) {
-        if (clock64() - c0 > WAIT_CYCLES) {
-          raise_status(A, ST_TIMEOUT);
-          ok = 0;
-          break;
-        }
-      }
-      __threadfence();
-      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) ok = 0;
-      S.grid_ok = ok && !S.abort_flag;
-    }
-    __syncthreads();
-    if (S.grid_ok) term_loop<T>(A, S, slots, warp, lane, cons);
-    __syncthreads();
-  }
-
-  // The last CTA to finish resets the CTA counter (and, after an abort, every
-  // ticket) so the workspace is ready for the next call.
+  // The last CTA to finish resets the CTA counter and the decision flags (and, after
+  // an abort, every ticket) so the workspace is ready for the next call.
   if (tid == 0) {
     __threadfence();
     const unsigned old = atomicAdd(&A.hdr->cta_done, 1u);
@@ -1380,10 +1509,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
         A.t_res[i] = 0;
       }
     }
-    if (tid == 0) {
-      A.hdr->grid_sync = 0;
-      A.hdr->cta_done = 0;
-    }
+    for (int i = tid; i < B; i += NTHREADS) A.dec_flag[i] = 0;
+    if (tid == 0) A.hdr->cta_done = 0;
   }
 }
 
@@ -1400,8 +1527,8 @@ static cudaError_t launch_t(const VerifyArgs& A, int grid, size_t dsmem, cudaStr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // At T > 0 the kernel holds a grid-wide barrier between its two phases: a cooperative
-  // launch guarantees that all its CTAs (at most one per SM) are resident together.
+  // At T > 0 warps wait for decisions made in other CTAs: a cooperative launch
+  // guarantees that all the CTAs (at most one per SM) are resident together.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(NTHREADS);

@@ -15,10 +15,17 @@ NTHREADS = max(1, min(32, os.cpu_count() or 1))
 # the bound stated for fp32 inputs (bf16's stated bound, 2e-3, is looser).
 P_RTOL = 1e-5
 
+# Resolution of the GPU's decisions: its probabilities carry fp32 rounding (p, q within
+# ~5e-7 relative, CDF positions within ~1e-7), so a decision whose oracle margin (the
+# distance |u - min(1, p/q)|, or the terminal sample's distance to a CDF edge) is below
+# this may come out differently. Differing decisions with a larger margin fail.
+MARGIN_RESOLUTION = 2e-6
+
 # Running totals over the full-size parity tests: verified positions, requests flagged
 # as near-ties by the oracle (windows of 1e-5 on the accept ratio and on the inverse-CDF
-# position), and flagged requests on which the GPU actually decided differently.
-TOTALS = {"positions": 0, "flagged": 0, "mismatch": 0}
+# position), flagged requests on which the GPU actually decided differently, and the
+# largest oracle margin among those.
+TOTALS = {"positions": 0, "flagged": 0, "mismatch": 0, "max_margin": 0.0}
 
 
 def to_dev(inp, device="cuda"):
@@ -84,16 +91,20 @@ def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
                     f"{int(badm.sum())} elements over")
     positions = int((np.clip(L, 0, None) + 1).sum())
     differ = flagged & ((acc != ref["out_accepted"]) | (tok != ref["out_tok"]).any(axis=1))
+    margins = ref["margin"][differ] if "margin" in ref else np.zeros(0)
     for b in np.nonzero(differ)[0][:5]:
-        print(f"[near-ties] differs: request {b} flags {ref['flags'][b]} gpu acc {acc[b]} "
-              f"tok {tok[b].tolist()} ref acc {ref['out_accepted'][b]} "
-              f"tok {ref['out_tok'][b].tolist()}")
-    return int(flagged.sum()), positions, int(differ.sum())
+        print(f"[near-ties] differs: request {b} flags {ref['flags'][b]} margin "
+              f"{ref['margin'][b]:.2e} gpu acc {acc[b]} tok {tok[b].tolist()} ref acc "
+              f"{ref['out_accepted'][b]} tok {ref['out_tok'][b].tolist()}")
+    assert (margins < MARGIN_RESOLUTION).all(), (
+        f"decisions differ at oracle margins {margins.tolist()}, above the GPU's resolution")
+    return int(flagged.sum()), positions, int(differ.sum()), float(margins.max(initial=0.0))
 
 
-def account(name, nf, npos, nmis):
+def account(name, nf, npos, nmis, max_margin=0.0):
     TOTALS["positions"] += npos
     TOTALS["flagged"] += nf
     TOTALS["mismatch"] += nmis
+    TOTALS["max_margin"] = max(TOTALS["max_margin"], max_margin)
     print(f"[near-ties] {name}: {nf} flagged requests, {nmis} of them decided differently, "
           f"{npos} positions")

@@ -277,15 +277,18 @@ def test_cuda_graph_replay(sv):
 
 @needs_cuda
 def test_near_tie_summary():
-    """Reading of the near-tie rule: outside flagged near-ties every decision above was
-    bit-exact. At V = 151,936 the mean inverse-CDF bucket (6.6e-6) is narrower than
-    the 1e-5 window, so a sizeable share of terminal samples is flagged whatever the
-    arithmetic; the bar is therefore held on the decisions that actually differ from
-    the oracle: fewer than 1e-4 of verified positions."""
+    """Reading of the near-tie rule. Outside the oracle's 1e-5 near-tie windows every
+    decision above was bit-exact. At V = 151,936 the mean inverse-CDF bucket (6.6e-6) is
+    narrower than that window, so a few percent of terminal samples are flagged whatever
+    the arithmetic; inside the window a decision may differ from the oracle only where
+    the oracle's own margin is below the GPU's fp32 resolution (MARGIN_RESOLUTION), which
+    every comparison above asserted. Reported here: flagged requests, differing
+    decisions, and the largest margin among those."""
     t = gpu_util.TOTALS
     if t["positions"] == 0:
         pytest.skip("no full-size parity test ran")
     print(f"[near-ties] total: {t['flagged']} flagged requests "
           f"({t['flagged'] / t['positions']:.2e} of {t['positions']} positions), "
-          f"{t['mismatch']} decided differently ({t['mismatch'] / t['positions']:.2e})")
-    assert t["mismatch"] <= 1e-4 * t["positions"]
+          f"{t['mismatch']} decided differently ({t['mismatch'] / t['positions']:.2e}), "
+          f"largest oracle margin among them {t['max_margin']:.2e}")
+    assert t["max_margin"] < gpu_util.MARGIN_RESOLUTION
