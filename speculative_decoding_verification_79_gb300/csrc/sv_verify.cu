@@ -23,10 +23,11 @@
 //    outputs, and (T > 0) the request's terminal-sample job, announced by a
 //    release-ordered decision flag.
 //  - Terminal tasks (T > 0). The terminal rows of a request (residual
-//    max(0, p_j - q_j), or p of the bonus row) are cut into R pieces; task (b, p)
-//    belongs to warp (b*R + p) mod (warps in the grid). Once its stream range is
-//    done, a warp feeds its terminal tasks through the same slots, each as soon as its
-//    request's flag is up (no grid-wide barrier). Each task sums its piece's weights
+//    max(0, p_j - q_j), or p of the bonus row) are cut into R pieces; the tasks
+//    (b, p), request-major, are split into equal contiguous shares, one per warp.
+//    Once its stream range is done, a warp feeds its terminal tasks through the same
+//    slots, each as soon as its request's flag is up (no grid-wide barrier); the
+//    deciding warp has already asked L2 to prefetch the request's terminal rows. Each task sums its piece's weights
 //    (compensated fp32, float-float across lanes) and stores the 32 lane-range
 //    totals; the task completing a request finds the token by inverse CDF at u_{b,K}
 //    over piece totals, lane-range totals and at most one lane range of elements.
@@ -55,6 +56,7 @@ struct __align__(16) SlotMeta {
   int direct;         // terminal piece: 1 = rows read straight from global memory
   int jkind;          // terminal piece: J_RESID or J_BONUS
   int last;           // stream piece: the warp's row segment ends here
+  int xk;             // stream piece (T > 0): the drafted token of its row, or -1
   Seg s0, s1;         // stream piece: s0; terminal piece: target (s0) and draft (s1)
   float Mt, iSt, Md, iSd;
 };
@@ -80,6 +82,10 @@ struct ET<uint16_t> {
 };
 
 __device__ __forceinline__ float ld_logit(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float sm_logit(const float* p) { return *p; }
+__device__ __forceinline__ float sm_logit(const uint16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(*p) << 16);
+}
 __device__ __forceinline__ float ld_logit(const uint16_t* p) {
   return __uint_as_float(static_cast<uint32_t>(__ldg(p)) << 16);
 }
@@ -390,6 +396,20 @@ __device__ void emit_invalid(const VerifyArgs& A, int b, int lane) {
   }
 }
 
+// Ask L2 to fetch [p, p + bytes) ahead of its use: the 16-byte aligned interior, in
+// pieces of up to 64 KB spread over the warp's lanes.
+__device__ void prefetch_l2(const void* p, size_t bytes, int lane) {
+  constexpr size_t CH = 65536;
+  const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
+  if (a1 <= a0) return;
+  const size_t n = a1 - a0;
+  for (size_t off = (size_t)lane * CH; off < n; off += 32 * CH) {
+    const uint32_t sz = static_cast<uint32_t>(n - off < CH ? n - off : CH);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0 + off), "r"(sz) : "memory");
+  }
+}
+
 // Decision for one request at T > 0 (one warp).
 template <typename T>
 __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
@@ -398,20 +418,28 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   float p = __int_as_float(0x7fc00000), q = p, MAt = 0.f, MAd = 0.f, iSt = 0.f, iSd = 0.f;
   int x = -1;
   bool ok = true, acc = false;
+  // Every load of the decision is issued up front. The drafted tokens' logits were
+  // picked up while their rows streamed past.
+  const float2 sL = __ldcg(A.rowstat + rb + L);
+  const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
+  float2 st = make_float2(0.f, 0.f), sd = st;
+  float u = 0.f, zt = 0.f, zd = 0.f;
   if (lane < L) {
-    const float2 st = __ldcg(A.rowstat + rb + lane);
-    const float2 sd = __ldcg(A.rowstat + rb + L + 1 + lane);
+    st = __ldcg(A.rowstat + rb + lane);
+    sd = __ldcg(A.rowstat + rb + L + 1 + lane);
     x = __ldg(A.tok + (size_t)b * K + lane);
-    const float u = __ldg(A.uni + (size_t)b * (K + 1) + lane);
+    u = __ldg(A.uni + (size_t)b * (K + 1) + lane);
+    zt = __ldcg(A.xz + rb + lane);
+    zd = __ldcg(A.xz + rb + L + 1 + lane);
+  }
+  if (lane < L) {
     ok = x >= 0 && x < V && finitef(st.x) && finitef(sd.x) && st.y > 0.f && finitef(st.y) &&
          sd.y > 0.f && finitef(sd.y) && u >= 0.f && u < 1.f;
     if (ok) {
       MAt = __fmul_rn(st.x, A.a);
       MAd = __fmul_rn(sd.x, A.a);
-      const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + lane) * V;
-      const T* dr = static_cast<const T*>(A.drf) + ((size_t)b * K + lane) * V;
-      const float et = exp2_precise(ld_logit(tr + x), A.a, A.a_lo, MAt);
-      const float ed = exp2_precise(ld_logit(dr + x), A.a, A.a_lo, MAd);
+      const float et = exp2_precise(zt, A.a, A.a_lo, MAt);
+      const float ed = exp2_precise(zd, A.a, A.a_lo, MAd);
       p = __fdiv_rn(et, st.y);
       q = __fdiv_rn(ed, sd.y);
       iSt = __fdiv_rn(1.f, st.y);
@@ -419,8 +447,6 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
       acc = u * q < p;
     }
   }
-  const float2 sL = __ldcg(A.rowstat + rb + L);
-  const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
   const bool okL = finitef(sL.x) && sL.y > 0.f && finitef(sL.y) && uK >= 0.f && uK < 1.f;
   if (__any_sync(FULL, !ok) || !okL) {
     emit_invalid(A, b, lane);
@@ -459,6 +485,12 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
     A.jobs[b] = J;
     st_release(A.dec_flag + b, 1u);  // the job is published
   }
+  // The terminal rows are read again shortly by the terminal tasks: start fetching
+  // them into L2 now.
+  prefetch_l2(static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * V, (size_t)V * sizeof(T),
+              lane);
+  if (j < L)
+    prefetch_l2(static_cast<const T*>(A.drf) + ((size_t)b * K + j) * V, (size_t)V * sizeof(T), lane);
 }
 
 // Decision for one request at T == 0 (one warp): argmax matching.
@@ -1087,9 +1119,8 @@ __device__ void term_settle(const VerifyArgs& A, const TermPend& pt, int lane) {
 // ---------------------------------------------------------------------------
 // Per-warp work. Stream: the work list (every active row of the batch, request-major,
 // cut into pieces) is split into equal contiguous ranges, one per warp of the grid.
-// Terminal tasks (T > 0): task (b, p) belongs to warp (b*R + p) mod (warps in the
-// grid); a warp takes them up once its stream range is done, each as soon as its
-// request is decided.
+// Terminal tasks (T > 0), request-major, likewise; a warp takes them up once its
+// stream range is done, each as soon as its request is decided.
 // ---------------------------------------------------------------------------
 struct Cursor {
   unsigned long long cur, end;
@@ -1135,6 +1166,11 @@ __device__ bool issue_stream(const VerifyArgs& A, Cursor& c, const int* prefix, 
   meta.p = c.cp;
   meta.e0 = e0;
   meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
+  meta.xk = -1;
+  if (!GREEDY) {
+    const int k = (c.cr <= c.cL) ? c.cr : c.cr - c.cL - 1;  // target row k or draft row k
+    if (k < c.cL) meta.xk = __ldg(A.tok + (size_t)c.cb * A.K + k);
+  }
   ++c.cur;
   // The warp's segment of this row ends at the row's last piece or the range's end.
   meta.last = (c.cp == P - 1 || c.cur == c.end) ? 1 : 0;
@@ -1164,11 +1200,11 @@ __device__ bool issue_stream(const VerifyArgs& A, Cursor& c, const int* prefix, 
 // Terminal task (request b, piece p) into a slot (lane 0 only; the request's job is
 // published).
 template <typename T>
-__device__ void issue_term(const VerifyArgs& A, int b, int p, SlotMeta& meta, uint64_t* full,
-                           unsigned char* slot) {
+__device__ void issue_term(const VerifyArgs& A, int b, int p, const TermJob& J, SlotMeta& meta,
+                           uint64_t* full, unsigned char* slot) {
   constexpr int eb = sizeof(T);
   const int K = A.K;
-  const int kind = __ldcg(&A.jobs[b].kind), j = __ldcg(&A.jobs[b].j);
+  const int kind = J.kind, j = J.j;
   const int e0 = p * A.E2;
   const int n = min(A.E2, A.V - e0);
   const T* tr = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V + e0;
@@ -1178,10 +1214,10 @@ __device__ void issue_term(const VerifyArgs& A, int b, int p, SlotMeta& meta, ui
   meta.r = j;
   meta.p = p;
   meta.e0 = e0;
-  meta.Mt = __ldcg(&A.jobs[b].MAt);
-  meta.iSt = __ldcg(&A.jobs[b].invSt);
-  meta.Md = __ldcg(&A.jobs[b].MAd);
-  meta.iSd = __ldcg(&A.jobs[b].invSd);
+  meta.Mt = J.MAt;
+  meta.iSt = J.invSt;
+  meta.Md = J.MAd;
+  meta.iSd = J.invSd;
   meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
   bool whole = meta.s0.head == 0 && meta.s0.body == n;
   if (kind == J_RESID) {
@@ -1209,9 +1245,12 @@ enum : int { SLOT_EMPTY = 0, SLOT_FULL = 1, SLOT_DEFERRED = 2 };
 // Per-warp issue state (meaningful in lane 0).
 struct Issuer {
   Cursor c;
-  long long nw;     // warps in the grid
-  long long tt, NT; // next terminal task of this warp (gw + m*nw); tasks in the batch
-  uint32_t pf;      // decision flag of task tt's request, loaded earlier
+  long long nw;      // warps in the grid
+  long long tt, te;  // this warp's terminal tasks still to issue: [tt, te)
+  uint32_t pf;       // decision flag of task tt's request, loaded earlier
+  int pacq;          // pf came from an acquire load (no fence needed before the job)
+  int jb;            // request whose job record J holds (-1: none)
+  TermJob J;
 };
 
 // Refill a slot (lane 0): the next stream piece while the warp's range lasts, then
@@ -1223,22 +1262,41 @@ __device__ int refill(const VerifyArgs& A, Issuer& I, const int* prefix, bool fr
                       SlotMeta& meta, uint64_t* full, unsigned char* slot) {
   if (issue_stream<T, GREEDY>(A, I.c, prefix, meta, full, slot)) return SLOT_FULL;
   if (!GREEDY) {
-    while (I.tt < I.NT) {
+    bool acq = I.pacq;  // I.pf was read with acquire semantics
+    I.pacq = 0;
+    while (I.tt < I.te) {
       const int b = static_cast<int>(I.tt / A.R);
-      const uint32_t f = fresh ? ld_relaxed(A.dec_flag + b) : I.pf;
-      if (f == 0) break;
-      fresh = true;  // a later task's flag has not been read yet
-      if (f == 1) {
-        fence_acq_rel();  // the job record was published before the flag
-        issue_term<T>(A, b, static_cast<int>(I.tt - (long long)b * A.R), meta, full, slot);
-        I.tt += I.nw;
-        I.pf = 0;
-        return SLOT_FULL;
+      if (b != I.jb) {  // first task of this request: its flag, then its job record
+        uint32_t f = I.pf;
+        if (fresh) {
+          f = ld_relaxed(A.dec_flag + b);
+          acq = false;
+        }
+        if (f == 0) break;
+        fresh = true;  // a later request's flag has not been read yet
+        if (f != 1) {  // the request has no terminal sample: skip its tasks
+          I.tt = min(I.te, (long long)(b + 1) * A.R);
+          continue;
+        }
+        if (!acq) fence_acq_rel();  // the job record was published before the flag
+        acq = false;
+        const int4 j0 = __ldcg(reinterpret_cast<const int4*>(A.jobs + b));
+        const int4 j1 = __ldcg(reinterpret_cast<const int4*>(A.jobs + b) + 1);
+        I.J.kind = j0.x;
+        I.J.j = j0.y;
+        I.J.MAt = __int_as_float(j0.z);
+        I.J.invSt = __int_as_float(j0.w);
+        I.J.MAd = __int_as_float(j1.x);
+        I.J.invSd = __int_as_float(j1.y);
+        I.jb = b;
       }
-      I.tt += I.nw;  // the request has no terminal sample
+      issue_term<T>(A, b, static_cast<int>(I.tt - (long long)b * A.R), I.J, meta, full, slot);
+      ++I.tt;
+      I.pf = 0;
+      return SLOT_FULL;
     }
   }
-  return (!GREEDY && I.tt < I.NT) ? SLOT_DEFERRED : SLOT_EMPTY;
+  return (!GREEDY && I.tt < I.te) ? SLOT_DEFERRED : SLOT_EMPTY;
 }
 
 // A refill that found nothing at all left: slots waiting for a terminal task have
@@ -1251,11 +1309,17 @@ __device__ __forceinline__ void drop_deferred(int* st, int h) {
 }
 
 // Bounded wait until the request of terminal task tt is decided (lane 0).
-__device__ bool wait_decided(const VerifyArgs& A, Shared& S, long long tt, long long NT) {
-  if (tt >= NT) return true;
-  const int b = static_cast<int>(tt / A.R);
+// On success I.pf holds the flag, read with acquire semantics.
+__device__ bool wait_decided(const VerifyArgs& A, Shared& S, Issuer& I) {
+  if (I.tt >= I.te) return true;
+  const int b = static_cast<int>(I.tt / A.R);
   const long long t0 = clock64();
-  while (ld_relaxed(A.dec_flag + b) == 0) {
+  // Every idle warp of the grid may be polling: back off between polls so that the
+  // flags' and the status word's cache lines stay free for the warps still working.
+  uint32_t f;
+  for (unsigned it = 1; (f = ld_acquire(A.dec_flag + b)) == 0; ++it) {
+    __nanosleep(256);
+    if ((it & 15) != 0) continue;
     if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
     if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) {
       S.abort_flag = 1;
@@ -1267,10 +1331,12 @@ __device__ bool wait_decided(const VerifyArgs& A, Shared& S, long long tt, long 
       return false;
     }
   }
+  I.pf = f;
+  I.pacq = 1;
   return true;
 }
 
-// One warp: its chunks of the stream and its terminal tasks through SLOTS_PER_WARP
+// One warp: its stream range and then its terminal tasks through SLOTS_PER_WARP
 // slots; each slot is refilled right after the warp has consumed it.
 template <typename T, bool GREEDY>
 __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, const int* prefix,
@@ -1278,9 +1344,16 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
   Issuer I;
   I.nw = (long long)gridDim.x * NCW;
   const long long gw = (long long)blockIdx.x * NCW + w;
-  I.tt = gw;
-  I.NT = GREEDY ? 0 : (long long)A.B * A.R;
+  {
+    // Terminal tasks (b, p) in request-major order, an equal contiguous share per
+    // warp: a warp's tasks mostly belong to one request, whose job it reads once.
+    const long long NT = GREEDY ? 0 : (long long)A.B * A.R;
+    I.tt = NT * gw / I.nw;
+    I.te = NT * (gw + 1) / I.nw;
+  }
   I.pf = 0;
+  I.pacq = 0;
+  I.jb = -1;
   {
     const unsigned long long total =
         static_cast<unsigned long long>(S.total_rows) * static_cast<unsigned long long>(A.P);
@@ -1316,7 +1389,8 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
     unsigned char* slot = slots + (size_t)s * SLOT_BYTES;
     if (!GREEDY && st[k] == SLOT_DEFERRED) {  // retry a refill that had to wait
       int h = 0;
-      if (lane == 0) h = refill<T, GREEDY>(A, I, prefix, true, S.meta[s], &S.full[s], slot);
+      if (lane == 0)
+        h = refill<T, GREEDY>(A, I, prefix, !I.pacq, S.meta[s], &S.full[s], slot);
       st[k] = __shfl_sync(FULL, h, 0);
       drop_deferred(st, st[k]);
     }
@@ -1343,8 +1417,11 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
       }
       // Once the stream range is done, prefetch the decision flag the next refill
       // will look at.
-      if (!GREEDY && lane == 0 && I.c.cur >= I.c.end && I.tt < I.NT)
+      if (!GREEDY && lane == 0 && I.c.cur >= I.c.end && I.tt < I.te &&
+          I.tt / A.R != I.jb) {
         I.pf = ld_relaxed(A.dec_flag + I.tt / A.R);
+        I.pacq = 0;
+      }
       const SlotMeta M = S.meta[s];
       if (GREEDY || M.kind == K_STREAM) {
         if (!(sg.valid && sg.b == M.b && sg.r == M.r)) {  // a new row segment starts here
@@ -1357,6 +1434,15 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
         }
         sg.p1 = M.p;
         fold_piece<T, GREEDY>(ls, A, M, slot, lane);
+        if (!GREEDY && lane == 0 && M.xk >= M.e0 && M.xk < M.e0 + M.s0.n) {
+          // This piece holds the row's drafted token: keep its logit for the decision.
+          const int off = M.xk - M.e0;
+          const T* g = reinterpret_cast<const T*>(M.s0.g);
+          const float z = (off >= M.s0.head && off < M.s0.head + M.s0.body)
+                              ? sm_logit(reinterpret_cast<const T*>(slot) + (off - M.s0.head))
+                              : ld_logit(g + off);
+          A.xz[(size_t)M.b * A.RS + M.r] = z;
+        }
       } else {
         pti = term_consume<T>(A, M, slot, lane);
       }
@@ -1409,7 +1495,7 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
       pti.valid = 0;
     }
     int ok = 1;
-    if (lane == 0) ok = wait_decided(A, S, I.tt, I.NT);
+    if (lane == 0) ok = wait_decided(A, S, I);
     if (!__shfl_sync(FULL, ok, 0)) {
       aborted = true;
       break;
