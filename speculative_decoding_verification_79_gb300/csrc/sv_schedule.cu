@@ -47,18 +47,27 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   __shared__ unsigned long long s_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 1-2. survival products and tau-lengths, one thread per request.
+  // 1-2. survival products and tau-lengths, one thread per request. The row of
+  // confidences is loaded up front (independent loads), and S >= 0 compares with tau
+  // as 64-bit patterns, keeping the slow fp64 pipe to the products alone.
   bool bad = false;
+  const unsigned long long tau_key = surv_key(static_cast<double>(A.tau));
   unsigned long long my_total = 0;
   for (int b = tid; b < B; b += SCHED_THREADS) {
+    float cv[SV_MAX_K];
+#pragma unroll
+    for (int k = 0; k < SV_MAX_K; ++k) cv[k] = (k < K) ? __ldg(A.conf + (size_t)b * K + k) : 0.f;
     double run = 1.0;
     int n = 0;
-    for (int k = 0; k < K; ++k) {
-      const float c = A.conf[(size_t)b * K + k];
-      if (!(c >= 0.f && c <= 1.f)) bad = true;
-      run = run * static_cast<double>(c);
-      S[(size_t)b * K + k] = run;
-      if (run >= static_cast<double>(A.tau)) n = k + 1;
+#pragma unroll
+    for (int k = 0; k < SV_MAX_K; ++k) {
+      if (k < K) {
+        const float c = cv[k];
+        if (!(c >= 0.f && c <= 1.f)) bad = true;
+        run = run * static_cast<double>(c);
+        S[(size_t)b * K + k] = run;
+        if (surv_key(run) >= tau_key) n = k + 1;
+      }
     }
     if (n < 1) n = 1;
     L0[b] = n;
@@ -71,7 +80,10 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
     if (tid == 0) atomicOr(&A.hdr->status, ST_DEVICE_INPUT);
     return;
   }
-  atomicAdd(&s_total, my_total);
+  // Sum of the tau-lengths: a warp reduction, then one shared atomic per warp.
+#pragma unroll
+  for (int o = 16; o; o >>= 1) my_total += __shfl_xor_sync(0xffffffffu, my_total, o);
+  if (lane == 0 && my_total) atomicAdd(&s_total, my_total);
   __syncthreads();
   const long long total = static_cast<long long>(s_total);
   if (total <= A.budget) {
@@ -105,15 +117,31 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
       atomicAdd(&hist[(key >> shift) & 255ull], 1u);
     }
     __syncthreads();
-    if (tid == 0) {
-      unsigned int acc = 0, rem = s_rem;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (acc + hist[d] >= rem) break;
-        acc += hist[d];
+    if (warp == 0) {
+      // The digit d holding the rem-th largest key: lane l owns digits
+      // 255-8l .. 248-8l; counts above each lane's block come from a suffix scan.
+      const unsigned int rem = s_rem;
+      unsigned int own = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) own += hist[255 - 8 * lane - q];
+      unsigned int above = own;  // inclusive prefix from the top digit down
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, above, o);
+        if (lane >= o) above += y;
       }
-      s_rem = rem - acc;
-      s_prefix = pre | (static_cast<unsigned long long>(d) << shift);
+      const unsigned int hit = __ballot_sync(0xffffffffu, above >= rem);
+      const int ln = hit ? __ffs(hit) - 1 : 31;
+      if (lane == ln) {
+        unsigned int acc = above - own;
+        int d = 255 - 8 * lane;
+        for (int q = 0; q < 7; ++q, --d) {
+          if (acc + hist[d] >= rem) break;
+          acc += hist[d];
+        }
+        s_rem = rem - acc;
+        s_prefix = pre | (static_cast<unsigned long long>(d) << shift);
+      }
     }
     mask |= 255ull << shift;
     __syncthreads();
