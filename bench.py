@@ -446,6 +446,26 @@ def run_sweep(args):
                 del g, ws
 
 
+def run_once(args):
+    """N untimed steps on one input set of the configured workload (for ncu captures)."""
+    import torch
+    import speculative_decoding_verification_79_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    g = _inputs(args.B, args.K, args.V, args.T, 0, dev)
+    ws = sv.Workspace(args.B, args.K, args.V)
+    out_len = torch.empty(args.B, dtype=torch.int32, device=dev)
+    for _ in range(args.once):
+        sv.sv_schedule(g["conf"], 0.0, args.B * args.K, ws, out_len=out_len)
+        sv.sv_verify(g["target"], g["draft"] if args.T > 0 else None, g["draft_tok"], out_len,
+                     g["uniforms"] if args.T > 0 else None, args.T, ws)
+    torch.cuda.synchronize()
+    status = ws.status()
+    print(json.dumps({"once": args.once, "status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -462,9 +482,14 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-T", default=None)
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--once", type=int, default=0,
+                    help="no timing: build one input set and run N schedule+verify steps "
+                         "(a short, self-contained program for profilers)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.once > 0:
+        run_once(args)
     elif args.sweep:
         run_sweep(args)
     else:
