@@ -409,41 +409,74 @@ def run_reference(args):
 
 
 def run_sweep(args):
-    """One JSON line per roofline sweep point (verify kernel only, CUDA events, L2
-    flushed between launches by a 256 MB memset)."""
+    """One JSON line per roofline sweep point: the verify kernel alone, timed inside a CUDA
+    graph (launch gaps excluded by event-record nodes around each launch), with enough
+    alternating input sets that their total exceeds L2, so no launch reads the previous
+    launch's data from L2."""
     import speculative_decoding_verification_79_gb300 as sv
     import synth
 
     dev = torch.device("cuda", 0)
     peak, _ = _peaks()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    temps = [args.T] if args.sweep_T is None else [float(x) for x in args.sweep_T.split(",")]
+    temps = [float(t) for t in args.sweep_T.split(",")] if args.sweep_T else [args.T]
+    st = torch.cuda.Stream(device=dev)
     for T in temps:
         for K in synth.SWEEP_K:
             for B in synth.SWEEP_B:
-                g = synth.sweep_point(B, K, seed=0, device=dev)
+                nbytes1 = synth.logit_bytes([K] * B, synth.QWEN3_VOCAB, 2, greedy=(T == 0.0))
+                nsets = max(2, -(-2 * (129 << 20) // max(1, nbytes1)))  # > 2x L2 in total
+                sets = [synth.sweep_point(B, K, seed=s, device=dev) for s in range(nsets)]
                 ws = sv.Workspace(B, K, synth.QWEN3_VOCAB, device=dev)
-                for _ in range(3):
-                    sv.sv_verify(g["target"], g["draft"], g["draft_tok"], g["verify_len"],
-                                 g["uniforms"], T, ws)
-                times = []
-                for _ in range(args.sweep_reps):
-                    flush.zero_()
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                    sv.sv_verify(g["target"], g["draft"], g["draft_tok"], g["verify_len"],
-                                 g["uniforms"], T, ws)
-                    e1.record()
-                    e1.synchronize()
-                    times.append(e0.elapsed_time(e1))
-                t = statistics.median(times) / 1e3
-                nbytes = synth.logit_bytes(g["verify_len"].cpu(), synth.QWEN3_VOCAB, 2,
-                                           greedy=(T == 0.0))
-                print(json.dumps({"sweep": True, "T": T, "B": B, "K": K, "us": t * 1e6,
-                                  "tokens_per_s": B * K / t, "gbs": nbytes / t / 1e9,
-                                  "frac": nbytes / t / 1e9 / peak, "bytes": nbytes}), flush=True)
-                del g, ws
+                outs = [(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                         torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(2)]
+
+                def launch(i):
+                    g = sets[i % nsets]
+                    o = outs[i & 1]
+                    sv.sv_verify(g["target"], g["draft"] if T > 0 else None, g["draft_tok"],
+                                 g["verify_len"], g["uniforms"] if T > 0 else None, T, ws,
+                                 out_tok=o[0], out_accepted=o[1], stream=st)
+
+                st.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(st):
+                    for i in range(3):
+                        launch(i)
+                st.synchronize()
+                n = max(args.sweep_reps, nsets)
+                try:
+                    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                           for _ in range(n)]
+                except TypeError:
+                    evs = None
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=st):
+                    for i in range(n):
+                        if evs:
+                            evs[i][0].record(st)
+                        launch(i)
+                        if evs:
+                            evs[i][1].record(st)
+                graph.replay()
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(st)
+                graph.replay()
+                t1.record(st)
+                st.synchronize()
+                if ws.status(stream=st) != sv.SV_OK:
+                    raise RuntimeError("device status not OK in the sweep")
+                try:
+                    us = sorted(e[0].elapsed_time(e[1]) * 1e3 for e in evs)[n // 2]
+                    src = "median of in-graph launch events"
+                except (TypeError, RuntimeError):
+                    us = t0.elapsed_time(t1) * 1e3 / n
+                    src = "graph replay time / launches"
+                tok = B * K
+                print(json.dumps({"sweep": True, "T": T, "B": B, "K": K, "us": us,
+                                  "tokens_per_s": tok / (us / 1e6),
+                                  "gbs": nbytes1 / (us / 1e6) / 1e9,
+                                  "frac": nbytes1 / (us / 1e6) / 1e9 / peak, "bytes": nbytes1,
+                                  "input_sets": nsets, "timing": src}), flush=True)
+                del sets, ws, graph
 
 
 def run_once(args):

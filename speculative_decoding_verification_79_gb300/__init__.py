@@ -96,7 +96,8 @@ def _dev(t, name, dtype=None):
 
 
 class Workspace:
-    """Device workspace for shapes up to (B, K, V); zeroed once at creation."""
+    """Device workspace for shapes up to (B, K, V); zeroed once at creation (the
+    constructor waits for the zeroing, so the workspace can be used on any stream)."""
 
     def __init__(self, B, K, V, device=None, stream=None):
         self.nbytes = int(load().sv_workspace_bytes(int(B), int(K), int(V)))
@@ -107,6 +108,8 @@ class Workspace:
         self.t = self.buf[off: off + self.nbytes]
         _check("sv_workspace_init",
                load().sv_workspace_init(_ptr(self.t), self.nbytes, _stream(stream)))
+        # The zeroing must be complete before a call on any other stream uses it.
+        torch.cuda.synchronize(self.t.device)
 
     def status(self, stream=None, clear=False) -> int:
         out = ctypes.c_int32(0)
