@@ -556,14 +556,39 @@ __device__ __forceinline__ uint32_t vmax_raw(uint32_t a, uint32_t b, uint16_t) {
   return bmax2_nan(a, b);
 }
 
-// Sum of 2^(z*a - ma) over one uint4 of elements.
-__device__ __forceinline__ float vec_expsum(uint4 v, float a, float nma, uint16_t) {
-  const float e0 = ex2(fmaf(bf_lo(v.x), a, nma)), e1 = ex2(fmaf(bf_hi(v.x), a, nma));
-  const float e2 = ex2(fmaf(bf_lo(v.y), a, nma)), e3 = ex2(fmaf(bf_hi(v.y), a, nma));
-  const float e4 = ex2(fmaf(bf_lo(v.z), a, nma)), e5 = ex2(fmaf(bf_hi(v.z), a, nma));
-  const float e6 = ex2(fmaf(bf_lo(v.w), a, nma)), e7 = ex2(fmaf(bf_hi(v.w), a, nma));
-  return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
+// Packed fp32x2 arithmetic: one instruction for a pair of values.
+__device__ __forceinline__ float2 ffma2(float2 x, float2 y, float2 z) {
+  float2 d;
+  asm("{\n\t.reg .b64 rx, ry, rz, rd;\n\t"
+      "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\tmov.b64 rz, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, rx, ry, rz;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y), "f"(z.x), "f"(z.y));
+  return d;
 }
+__device__ __forceinline__ float2 fadd2(float2 x, float2 y) {
+  float2 d;
+  asm("{\n\t.reg .b64 rx, ry, rd;\n\t"
+      "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, rx, ry;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return d;
+}
+
+// Sum of 2^(z*a - ma) over one uint4 of elements (8 bf16 / 4 fp32).
+__device__ __forceinline__ float vec_expsum(uint4 v, float a, float nma, uint16_t) {
+  const float2 aa = make_float2(a, a), cc = make_float2(nma, nma);
+  const float2 y0 = ffma2(make_float2(bf_lo(v.x), bf_hi(v.x)), aa, cc);
+  const float2 y1 = ffma2(make_float2(bf_lo(v.y), bf_hi(v.y)), aa, cc);
+  const float2 y2 = ffma2(make_float2(bf_lo(v.z), bf_hi(v.z)), aa, cc);
+  const float2 y3 = ffma2(make_float2(bf_lo(v.w), bf_hi(v.w)), aa, cc);
+  const float2 e0 = make_float2(ex2(y0.x), ex2(y0.y)), e1 = make_float2(ex2(y1.x), ex2(y1.y));
+  const float2 e2 = make_float2(ex2(y2.x), ex2(y2.y)), e3 = make_float2(ex2(y3.x), ex2(y3.y));
+  const float2 s = fadd2(fadd2(e0, e1), fadd2(e2, e3));
+  return s.x + s.y;
+}
+
 __device__ __forceinline__ float vec_expsum(uint4 v, float a, float nma, float) {
   const float e0 = ex2(fmaf(__uint_as_float(v.x), a, nma));
   const float e1 = ex2(fmaf(__uint_as_float(v.y), a, nma));
@@ -1166,6 +1191,7 @@ __device__ bool issue_stream(const VerifyArgs& A, Cursor& c, const int* prefix, 
   meta.p = c.cp;
   meta.e0 = e0;
   meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(row + e0), n, eb);
+  const int kpos0 = (c.cr <= c.cL) ? c.cr : c.cr - c.cL - 1;
   meta.xk = -1;
   if (!GREEDY) {
     const int k = (c.cr <= c.cL) ? c.cr : c.cr - c.cL - 1;  // target row k or draft row k
@@ -1190,7 +1216,10 @@ __device__ bool issue_stream(const VerifyArgs& A, Cursor& c, const int* prefix, 
   const uint32_t tx = meta.s0.body * eb;
   if (tx) {
     mbar_arrive_expect_tx(full, tx);
-    bulk_g2s(slot, meta.s0.g + meta.s0.head * eb, tx, full);
+    // Rows of the first two positions of a request are the likeliest terminal rows
+    // (read again after the decision): ask L2 to keep them; the rest is read once.
+    const uint64_t pol = (!GREEDY && kpos0 <= 1) ? policy_evict_last() : policy_evict_first();
+    bulk_g2s_hint(slot, meta.s0.g + meta.s0.head * eb, tx, full, pol);
   } else {
     mbar_arrive(full);
   }
@@ -1233,8 +1262,9 @@ __device__ void issue_term(const VerifyArgs& A, int b, int p, const TermJob& J, 
   if (whole) {
     const uint32_t bytes = (uint32_t)(n * eb);
     mbar_arrive_expect_tx(full, (kind == J_RESID ? 2u : 1u) * bytes);
-    bulk_g2s(slot, meta.s0.g, bytes, full);
-    if (kind == J_RESID) bulk_g2s(slot + SLOT_BYTES / 2, meta.s1.g, bytes, full);
+    const uint64_t pol = policy_evict_first();
+    bulk_g2s_hint(slot, meta.s0.g, bytes, full, pol);
+    if (kind == J_RESID) bulk_g2s_hint(slot + SLOT_BYTES / 2, meta.s1.g, bytes, full, pol);
   } else {
     mbar_arrive(full);
   }
