@@ -116,7 +116,7 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.t_req = reinterpret_cast<uint32_t*>(ws + L.t_req);
   A.t_res = reinterpret_cast<uint32_t*>(ws + L.t_res);
   A.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
-  A.xz = reinterpret_cast<float*>(ws + L.xz);
+  A.xz = reinterpret_cast<unsigned long long*>(ws + L.xz);
   A.part = reinterpret_cast<float2*>(ws + L.part);
   A.rpart = reinterpret_cast<float2*>(ws + L.rpart);
   A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);

@@ -67,7 +67,7 @@ struct WsLayout {
   size_t t_row, t_req, t_res;  // uint32 tickets: [B*RS], [B], [B]
   size_t dec;                  // uint32 decision flags [B]
   size_t rowstat;              // float2 [B*RS]
-  size_t xz;                   // float [B*RS]: logit of the drafted token in each row
+  size_t xz;                   // u64 [B*RS]: logit of the drafted token in each row
   size_t part;                 // float2 [B*RS*Pmax]
   size_t rpart;                // float2 [B*Rmax] (float-float piece sums)
   size_t jobs;                 // TermJob [B]
@@ -107,7 +107,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
   L.dec = L.t_res + 4 * (size_t)SV_MAX_B;
   size_t off = align_up(sizeof(WsHeader) + TICKET_BYTES, 256);
   L.rowstat = off; off = align_up(off + 8 * nb * L.RS, 256);
-  L.xz = off;      off = align_up(off + 4 * nb * L.RS, 256);
+  L.xz = off;      off = align_up(off + 8 * nb * L.RS, 256);
   L.part = off;    off = align_up(off + 8 * nb * L.RS * (size_t)L.Pmax, 256);
   L.rpart = off;   off = align_up(off + 8 * nb * (size_t)L.Rmax, 256);
   L.jobs = off;    off = align_up(off + sizeof(TermJob) * nb, 256);
@@ -144,7 +144,7 @@ struct VerifyArgs {
   uint32_t* t_res;
   uint32_t* dec_flag;  // per request: 0 undecided, 1 terminal job published, 2 no job
   float2* rowstat;
-  float* xz;
+  unsigned long long* xz;
   float2* part;
   float2* rpart;
   TermJob* jobs;

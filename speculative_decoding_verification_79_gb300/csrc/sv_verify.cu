@@ -354,6 +354,51 @@ __device__ __forceinline__ int L_of_rows(int nrows, bool greedy) {
 
 __device__ void raise_status(const VerifyArgs& A, uint32_t bits) { atomicOr(&A.hdr->status, bits); }
 
+// ---------------------------------------------------------------------------
+// Fence-free publication. Results passed between warps (row partials, row
+// statistics, drafted-token logits) are single 64-bit words written and read with
+// relaxed GPU-scope accesses (single-copy atomic); a word is never 0 once written
+// (its high half is stored bit-inverted and is the bits of a value >= 0 or of an
+// index), so 0 means "not visible yet". The reader waits (bounded) for a non-zero
+// word and resets it to 0 once consumed. Tickets are relaxed atomics. Nothing on the
+// stream path then waits for a memory fence, which under full HBM load can take
+// microseconds.
+// ---------------------------------------------------------------------------
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 enc_pair(float x, uint32_t y_bits) {
+  return (static_cast<u64>(~y_bits) << 32) | __float_as_uint(x);
+}
+__device__ __forceinline__ float dec_x(u64 w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+__device__ __forceinline__ uint32_t dec_y(u64 w) { return ~static_cast<uint32_t>(w >> 32); }
+
+__device__ __forceinline__ void st_word(u64* p, u64 v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ u64 ld_word(const u64* p) {
+  u64 v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A published word: waits (bounded) until it is visible, then resets the slot.
+__device__ u64 take_word(const VerifyArgs& A, u64* p) {
+  u64 w = ld_word(p);
+  if (w == 0) {
+    const long long t0 = clock64();
+    while ((w = ld_word(p)) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return 0;
+      if (clock64() - t0 > WAIT_CYCLES) {
+        raise_status(A, ST_TIMEOUT);
+        return 0;
+      }
+      __nanosleep(32);
+    }
+  }
+  st_word(p, 0ull);
+  return w;
+}
+
 // Bounded wait on an mbarrier phase; false on abort or timeout.
 __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const VerifyArgs& A) {
   const long long t0 = clock64();
@@ -420,17 +465,26 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   bool ok = true, acc = false;
   // Every load of the decision is issued up front. The drafted tokens' logits were
   // picked up while their rows streamed past.
-  const float2 sL = __ldcg(A.rowstat + rb + L);
   const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
-  float2 st = make_float2(0.f, 0.f), sd = st;
-  float u = 0.f, zt = 0.f, zd = 0.f;
+  float u = 0.f;
   if (lane < L) {
-    st = __ldcg(A.rowstat + rb + lane);
-    sd = __ldcg(A.rowstat + rb + L + 1 + lane);
     x = __ldg(A.tok + (size_t)b * K + lane);
     u = __ldg(A.uni + (size_t)b * (K + 1) + lane);
-    zt = __ldcg(A.xz + rb + lane);
-    zd = __ldcg(A.xz + rb + L + 1 + lane);
+  }
+  u64* rsw = reinterpret_cast<u64*>(A.rowstat) + rb;
+  u64* xzw = A.xz + rb;
+  const u64 wL = take_word(A, rsw + L);
+  const float2 sL = make_float2(dec_x(wL), __uint_as_float(dec_y(wL)));
+  float2 st = make_float2(0.f, 0.f), sd = st;
+  float zt = 0.f, zd = 0.f;
+  if (lane < L) {
+    const u64 w1 = take_word(A, rsw + lane), w2 = take_word(A, rsw + L + 1 + lane);
+    st = make_float2(dec_x(w1), __uint_as_float(dec_y(w1)));
+    sd = make_float2(dec_x(w2), __uint_as_float(dec_y(w2)));
+    if (x >= 0 && x < V) {  // the stream stored these logits exactly when x is in range
+      zt = dec_x(take_word(A, xzw + lane));
+      zd = dec_x(take_word(A, xzw + L + 1 + lane));
+    }
   }
   if (lane < L) {
     ok = x >= 0 && x < V && finitef(st.x) && finitef(sd.x) && st.y > 0.f && finitef(st.y) &&
@@ -499,13 +553,15 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   const size_t rb = (size_t)b * A.RS;
   int x = -1, am = -1;
   bool ok = true;
+  u64* rsw = reinterpret_cast<u64*>(A.rowstat) + rb;
   if (lane < L) {
-    const float2 st = __ldcg(A.rowstat + rb + lane);
+    const u64 w = take_word(A, rsw + lane);
     x = __ldg(A.tok + (size_t)b * K + lane);
-    am = __float_as_int(st.y);
-    ok = finitef(st.x) && x >= 0 && x < V;
+    am = static_cast<int>(dec_y(w));
+    ok = finitef(dec_x(w)) && x >= 0 && x < V;
   }
-  const float2 sL = __ldcg(A.rowstat + rb + L);
+  const u64 wL = take_word(A, rsw + L);
+  const float2 sL = make_float2(dec_x(wL), __int_as_float(static_cast<int>(dec_y(wL))));
   const bool okL = finitef(sL.x);
   if (__any_sync(FULL, !ok) || !okL) {
     emit_invalid(A, b, lane);
@@ -683,8 +739,8 @@ struct Pending {
 };
 
 // Publish a segment: reduce the lane states, store the partial at slot p0 and
-// neutral partials at p0+1..p1, then a release-ordered ticket increment by the number
-// of pieces. Lane 0 writes everything.
+// neutral partials at p0+1..p1, then a ticket increment by the number of pieces.
+// Lane 0 writes everything (fence-free: see take_word).
 template <bool GREEDY>
 __device__ Pending publish(const VerifyArgs& A, const Segment& sg, LaneState st, int lane) {
   float2 v;
@@ -706,12 +762,12 @@ __device__ Pending publish(const VerifyArgs& A, const Segment& sg, LaneState st,
   pd.old = 0;
   if (lane == 0) {
     const size_t rowid = (size_t)sg.b * A.RS + sg.r;
-    float2* pr = A.part + rowid * A.P;
-    pr[sg.p0] = v;
-    const float2 neutral = GREEDY ? make_float2(-INFINITY, __int_as_float(INT_MAX))
-                                  : make_float2(-INFINITY, 0.f);
-    for (int q = sg.p0 + 1; q <= sg.p1; ++q) pr[q] = neutral;
-    pd.old = atom_add_release(A.t_row + rowid, (uint32_t)pd.count);
+    u64* pr = reinterpret_cast<u64*>(A.part) + rowid * A.P;
+    st_word(pr + sg.p0, enc_pair(v.x, __float_as_uint(v.y)));
+    const u64 neutral = GREEDY ? enc_pair(-INFINITY, static_cast<uint32_t>(INT_MAX))
+                               : enc_pair(-INFINITY, 0u);
+    for (int q = sg.p0 + 1; q <= sg.p1; ++q) st_word(pr + q, neutral);
+    pd.old = atomicAdd(A.t_row + rowid, (uint32_t)pd.count);
   }
   return pd;
 }
@@ -723,18 +779,18 @@ __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix
   const uint32_t old = __shfl_sync(FULL, pd.old, 0);
   const int P = A.P;
   if (old + (uint32_t)pd.count != (uint32_t)P) return;
-  __threadfence();
   const int b = pd.b;
   const size_t rowid = (size_t)b * A.RS + pd.r;
-  const float2* pr = A.part + rowid * P;
+  u64* pr = reinterpret_cast<u64*>(A.part) + rowid * P;
   float2 rs;
   if (GREEDY) {
     float best = -INFINITY;
     int idx = INT_MAX;
     bool bad = false;
     for (int p = lane; p < P; p += 32) {
-      const float2 v = __ldcg(pr + p);
-      const int vi = __float_as_int(v.y);
+      const u64 w = take_word(A, pr + p);
+      const float2 v = make_float2(dec_x(w), 0.f);
+      const int vi = static_cast<int>(dec_y(w));
       if (v.x != v.x) {
         bad = true;
       } else if (v.x > best || (v.x == best && vi < idx)) {
@@ -747,8 +803,8 @@ __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix
   } else {
     float m = -INFINITY, s = 0.f;
     for (int p = lane; p < P; p += 32) {
-      const float2 v = __ldcg(pr + p);
-      soft_merge(m, s, v.x, v.y, A.a);
+      const u64 w = take_word(A, pr + p);
+      soft_merge(m, s, dec_x(w), __uint_as_float(dec_y(w)), A.a);
     }
     soft_warp(m, s, A.a, lane);
     rs = make_float2(m, s);
@@ -756,13 +812,12 @@ __device__ void settle(const VerifyArgs& A, const Pending& pd, const int* prefix
   const int nrows = prefix[b + 1] - prefix[b];
   uint32_t o2 = 0;
   if (lane == 0) {
-    A.rowstat[rowid] = rs;
+    st_word(reinterpret_cast<u64*>(A.rowstat) + rowid, enc_pair(rs.x, __float_as_uint(rs.y)));
     A.t_row[rowid] = 0;
-    o2 = atom_add_release(A.t_req + b, 1u);
+    o2 = atomicAdd(A.t_req + b, 1u);
   }
   o2 = __shfl_sync(FULL, o2, 0);
   if (o2 != (uint32_t)(nrows - 1)) return;
-  __threadfence();
   if (lane == 0) A.t_req[b] = 0;
   const int L = L_of_rows(nrows, GREEDY);
   if (GREEDY)
@@ -1471,7 +1526,7 @@ __device__ void warp_loop(const VerifyArgs& A, Shared& S, unsigned char* slots, 
           const float z = (off >= M.s0.head && off < M.s0.head + M.s0.body)
                               ? sm_logit(reinterpret_cast<const T*>(slot) + (off - M.s0.head))
                               : ld_logit(g + off);
-          A.xz[(size_t)M.b * A.RS + M.r] = z;
+          st_word(A.xz + (size_t)M.b * A.RS + M.r, enc_pair(z, 0u));
         }
       } else {
         pti = term_consume<T>(A, M, slot, lane);
@@ -1619,6 +1674,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
     __threadfence();
     const bool dirty = (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) != 0;
     if (dirty) {
+      // An aborted call can leave published words behind: clear them all.
+      const size_t nrow = (size_t)B * A.RS;
+      u64* pw = reinterpret_cast<u64*>(A.part);
+      for (size_t i = tid; i < nrow * A.P; i += NTHREADS) pw[i] = 0ull;
+      for (size_t i = tid; i < nrow; i += NTHREADS) {
+        reinterpret_cast<u64*>(A.rowstat)[i] = 0ull;
+        A.xz[i] = 0ull;
+      }
       for (size_t i = tid; i < TICKET_ROW_WORDS; i += NTHREADS) A.t_row[i] = 0;
       for (int i = tid; i < SV_MAX_B; i += NTHREADS) {
         A.t_req[i] = 0;
