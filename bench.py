@@ -190,8 +190,9 @@ def run_gpu(args):
         with torch.cuda.graph(graph_rem, stream=st):
             for i in range(rem):
                 step(i)
-    for _ in range(2):  # graph warm-up
-        graph.replay()
+    with torch.cuda.stream(st):  # replays go on the stream the events are recorded on
+        for _ in range(2):  # graph warm-up
+            graph.replay()
     st.synchronize()
     if ws.status(stream=st) != sv.SV_OK:
         raise RuntimeError("device status not OK after warm-up")
@@ -201,7 +202,7 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    with Clocks(dev.index if world == 1 else local) as clk:
+    with Clocks(dev.index if world == 1 else local) as clk, torch.cuda.stream(st):
         t0.record(st)
         for _ in range(reps):
             graph.replay()
@@ -456,11 +457,12 @@ def run_sweep(args):
                         launch(i)
                         if evs:
                             evs[i][1].record(st)
-                graph.replay()
                 t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                t0.record(st)
-                graph.replay()
-                t1.record(st)
+                with torch.cuda.stream(st):
+                    graph.replay()
+                    t0.record(st)
+                    graph.replay()
+                    t1.record(st)
                 st.synchronize()
                 if ws.status(stream=st) != sv.SV_OK:
                     raise RuntimeError("device status not OK in the sweep")
