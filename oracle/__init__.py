@@ -8,7 +8,9 @@ gcc and marshals numpy arrays through ctypes.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (brute-force output distribution at small V, greedy argmax, q == p, closed-form
-acceptance rate, hand-computed golden cases, schedule invariants and brute force).
+acceptance rate, hand-computed golden cases, schedule invariants and brute force;
+calibration by the power-form identity and its fixed points, the load-aware threshold
+by its end points, the window statistics by brute-force counting and hand cases).
 """
 from __future__ import annotations
 
@@ -67,6 +69,19 @@ def _bind(path):
     lib.oracle_verify_m.restype = ctypes.c_int
     lib.oracle_verify_u64m.argtypes = common + [f64p] + tail + [ctypes.c_double] + outs_m
     lib.oracle_verify_u64m.restype = ctypes.c_int
+    lib.oracle_calibrate.argtypes = [ctypes.c_double, ctypes.c_double]
+    lib.oracle_calibrate.restype = ctypes.c_double
+    lib.oracle_load_tau.argtypes = [f32p, ctypes.c_double, ctypes.c_double]
+    lib.oracle_load_tau.restype = ctypes.c_double
+    lib.oracle_schedule_ex.argtypes = [f32p, f32p, f32p, ctypes.c_float, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_longlong, i32p, f64p, i32p, f32p, f64p]
+    lib.oracle_schedule_ex.restype = ctypes.c_int
+    lib.oracle_calib_observe.argtypes = [f32p, i32p, i32p, ctypes.c_int, ctypes.c_int, f64p]
+    lib.oracle_calib_observe.restype = ctypes.c_int
+    lib.oracle_calib_update.argtypes = [f64p, f32p, ctypes.c_int, ctypes.c_double,
+                                        ctypes.c_double, f64p]
+    lib.oracle_calib_update.restype = ctypes.c_int
     return lib
 
 
@@ -111,6 +126,65 @@ def schedule(conf, tau: float, token_budget: int, lib=None):
     rc = (lib or _load()).oracle_schedule(_ptr(conf), B, K, float(tau), int(token_budget),
                                           _ptr(out_len), _ptr(surv), _ptr(l0))
     return {"out_len": out_len, "surv": surv, "l0": l0, "status": rc}
+
+
+CALIB_BINS = 10
+
+
+def calib_stats_len(K: int) -> int:
+    """Length (float64) of the calibration window statistics for K positions."""
+    return 3 * K + 3 * CALIB_BINS
+
+
+def calibrate(c: float, T: float, lib=None) -> float:
+    """One calibrated confidence sigmoid(logit(c) / T), float64."""
+    return (lib or _load()).oracle_calibrate(float(c), float(T))
+
+
+def load_tau(load, tau_min: float, tau_max: float, lib=None) -> float:
+    """Load-aware threshold from {Q, Q_max, M_gpu, M_max} (float32); -1 if invalid."""
+    ld = np.ascontiguousarray(load, dtype=np.float32)
+    return (lib or _load()).oracle_load_tau(_ptr(ld), float(tau_min), float(tau_max))
+
+
+def schedule_ex(conf, temps, load, tau: float, tau_min: float, tau_max: float,
+                token_budget: int, lib=None):
+    """Schedule on calibrated confidences (temps [K] or None) with an optional
+    load-aware threshold (load [4] or None). Returns dict(out_len, surv, l0, cal, tau,
+    status)."""
+    conf = np.ascontiguousarray(conf, dtype=np.float32)
+    B, K = conf.shape
+    t = None if temps is None else np.ascontiguousarray(temps, dtype=np.float32)
+    ld = None if load is None else np.ascontiguousarray(load, dtype=np.float32)
+    out_len = np.zeros(B, np.int32)
+    surv = np.zeros((B, K), np.float64)
+    l0 = np.zeros(B, np.int32)
+    cal = np.zeros((B, K), np.float32)
+    tau_used = np.zeros(1, np.float64)
+    rc = (lib or _load()).oracle_schedule_ex(
+        _ptr(conf), _ptr(t), _ptr(ld), float(tau), float(tau_min), float(tau_max), B, K,
+        int(token_budget), _ptr(out_len), _ptr(surv), _ptr(l0), _ptr(cal), _ptr(tau_used))
+    return {"out_len": out_len, "surv": surv, "l0": l0, "cal": cal, "tau": float(tau_used[0]),
+            "status": rc}
+
+
+def calib_observe(conf_cal, verify_len, accepted, stats, lib=None):
+    """Add one verification round to the window statistics (in place)."""
+    c = np.ascontiguousarray(conf_cal, dtype=np.float32)
+    B, K = c.shape
+    vl = np.ascontiguousarray(verify_len, dtype=np.int32)
+    ac = np.ascontiguousarray(accepted, dtype=np.int32)
+    assert stats.dtype == np.float64 and stats.size == calib_stats_len(K)
+    return (lib or _load()).oracle_calib_observe(_ptr(c), _ptr(vl), _ptr(ac), B, K, _ptr(stats))
+
+
+def calib_update(stats, temps, lr: float, temp_floor: float, lib=None):
+    """Window update of temps (float32 [K], in place); returns (status, ece)."""
+    assert stats.dtype == np.float64 and temps.dtype == np.float32
+    ece = np.zeros(1, np.float64)
+    rc = (lib or _load()).oracle_calib_update(_ptr(stats), _ptr(temps), temps.size, float(lr),
+                                              float(temp_floor), _ptr(ece))
+    return rc, float(ece[0])
 
 
 def _logits(a):

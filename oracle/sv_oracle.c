@@ -163,14 +163,10 @@ static int cand_order(const void *pa, const void *pb) {
  * out_l0: [B] or NULL (lengths after step 2). Returns ORC_ERR_INPUT (and all
  * out_len = 0) when any confidence is NaN or outside [0,1].
  */
-int oracle_schedule(const float *conf, int B, int K, float tau, long long token_budget,
-                    int32_t *out_len, double *out_surv, int32_t *out_l0) {
-    if (B < 0 || K < 1 || token_budget < 0 || !(tau >= 0.0f && tau <= 1.0f)) return ORC_ERR_ARG;
-    for (int b = 0; b < B; b++) out_len[b] = 0;
-    if (B == 0) return ORC_OK;
-    for (long long i = 0; i < (long long)B * K; i++)
-        if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) return ORC_ERR_INPUT;
-
+/* Steps 1-3 on confidences already widened (or calibrated) to float64, against
+ * the float64 threshold th. */
+static void schedule_core(const double *c, int B, int K, double th, long long token_budget,
+                          int32_t *out_len, double *out_surv, int32_t *out_l0) {
     double *S = (double *)malloc(sizeof(double) * (size_t)B * K);
     int *L0 = (int *)malloc(sizeof(int) * (size_t)B);
     long long total = 0;
@@ -178,9 +174,9 @@ int oracle_schedule(const float *conf, int B, int K, float tau, long long token_
         double run = 1.0;
         int n = 0;
         for (int k = 0; k < K; k++) {
-            run = run * (double)conf[(size_t)b * K + k];
+            run = run * c[(size_t)b * K + k];
             S[(size_t)b * K + k] = run;
-            if (run >= (double)tau) n = k + 1; /* S is non-increasing: count = last index */
+            if (run >= th) n = k + 1; /* S is non-increasing: count = last index */
         }
         if (n < 1) n = 1;
         L0[b] = n;
@@ -193,23 +189,36 @@ int oracle_schedule(const float *conf, int B, int K, float tau, long long token_
     if (total <= token_budget) {
         for (int b = 0; b < B; b++) out_len[b] = L0[b];
     } else {
-        orc_cand *c = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)total);
+        orc_cand *cd = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)total);
         int floor_first = token_budget >= B;
         size_t n = 0;
         for (int b = 0; b < B; b++)
             for (int k = 0; k < L0[b]; k++) {
-                c[n].s = S[(size_t)b * K + k];
-                c[n].k = k;
-                c[n].b = b;
-                c[n].floor = floor_first && k == 0;
+                cd[n].s = S[(size_t)b * K + k];
+                cd[n].k = k;
+                cd[n].b = b;
+                cd[n].floor = floor_first && k == 0;
                 n++;
             }
-        qsort(c, n, sizeof(orc_cand), cand_order);
-        for (long long i = 0; i < token_budget; i++) out_len[c[i].b]++;
-        free(c);
+        qsort(cd, n, sizeof(orc_cand), cand_order);
+        for (long long i = 0; i < token_budget; i++) out_len[cd[i].b]++;
+        free(cd);
     }
     free(S);
     free(L0);
+}
+
+int oracle_schedule(const float *conf, int B, int K, float tau, long long token_budget,
+                    int32_t *out_len, double *out_surv, int32_t *out_l0) {
+    if (B < 0 || K < 1 || token_budget < 0 || !(tau >= 0.0f && tau <= 1.0f)) return ORC_ERR_ARG;
+    for (int b = 0; b < B; b++) out_len[b] = 0;
+    if (B == 0) return ORC_OK;
+    for (long long i = 0; i < (long long)B * K; i++)
+        if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) return ORC_ERR_INPUT;
+    double *c = (double *)malloc(sizeof(double) * (size_t)B * K);
+    for (long long i = 0; i < (long long)B * K; i++) c[i] = (double)conf[i];
+    schedule_core(c, B, K, (double)tau, token_budget, out_len, out_surv, out_l0);
+    free(c);
     return ORC_OK;
 }
 
@@ -431,3 +440,177 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
     return oracle_verify_m(target, draft, dtype, tok, vlen, u, B, K, V, T, out_tok, out_acc,
                            out_p, out_q, out_flags, NULL, nthreads);
 }
+
+/* ======================================================================== */
+/* Calibration prologue, load-aware threshold, and the online calibration  */
+/* loop                                                                      */
+/* ======================================================================== */
+
+/*
+ * Sequential temperature scaling of one confidence [DD "Sequential Temperature
+ * Scaling"]: the raw score is mapped to a logit, divided by the temperature of
+ * its draft position, and mapped back through the sigmoid,
+ *     c' = sigmoid(logit(c) / T_k),  logit(c) = ln(c / (1 - c)).
+ * The end points are fixed (c = 0 -> 0, c = 1 -> 1) for every T > 0.
+ */
+static double calibrate_one(double c, double T) {
+    if (c <= 0.0) return 0.0;
+    if (c >= 1.0) return 1.0;
+    double z = (log(c) - log1p(-c)) / T;
+    return 1.0 / (1.0 + exp(-z));
+}
+
+/*
+ * Load-aware threshold [GD "Dynamic Verification Scheduling Algorithm", steps 1
+ * and 2]: load factor LF = 0.6 * Q / Q_max + 0.4 * M_gpu / M_max, then
+ * tau = tau_min + (tau_max - tau_min) * LF^2. Reading: the page states LF in
+ * [0, 1]; a load beyond its maximum is clamped to 1.
+ * load: {Q, Q_max, M_gpu, M_max} as float32 (widened exactly).
+ * Returns -1 when a load value is NaN/inf or negative, or a maximum is not > 0.
+ */
+static double load_tau(const float *load, double tau_min, double tau_max) {
+    double Q = load[0], Qmax = load[1], M = load[2], Mmax = load[3];
+    if (!(isfinite(Q) && isfinite(Qmax) && isfinite(M) && isfinite(Mmax))) return -1.0;
+    if (Q < 0.0 || M < 0.0 || !(Qmax > 0.0) || !(Mmax > 0.0)) return -1.0;
+    double lf = 0.6 * (Q / Qmax) + 0.4 * (M / Mmax);
+    if (lf > 1.0) lf = 1.0;
+    return tau_min + (tau_max - tau_min) * (lf * lf);
+}
+
+double oracle_load_tau(const float *load, double tau_min, double tau_max) {
+    return load_tau(load, tau_min, tau_max);
+}
+
+/*
+ * oracle_schedule_ex: the schedule of oracle_schedule run on calibrated
+ * confidences, optionally with the load-aware threshold [DD "The Full Scheduling
+ * Pipeline": raw scores -> online calibration -> scheduler with the GPU's load].
+ *
+ *  temps [K] float32 > 0, or NULL for no calibration (c' = c).
+ *  load [4] {Q, Q_max, M_gpu, M_max}, or NULL to use tau as given.
+ *  out_cal [B,K] float32 or NULL: c' rounded to float32.
+ *  out_tau: the threshold used (float64), or NULL.
+ * Steps 1-3 of oracle_schedule then run on c' in float64: S_{b,k} =
+ * c'_{b,0} * ... * c'_{b,k}, compared with the float64 threshold.
+ * Returns ORC_ERR_INPUT (and out_len = 0) for a confidence outside [0,1], a
+ * temperature that is not a positive finite number, or an invalid load.
+ */
+int oracle_schedule_ex(const float *conf, const float *temps, const float *load, float tau,
+                       float tau_min, float tau_max, int B, int K, long long token_budget,
+                       int32_t *out_len, double *out_surv, int32_t *out_l0, float *out_cal,
+                       double *out_tau) {
+    if (B < 0 || K < 1 || token_budget < 0) return ORC_ERR_ARG;
+    if (!(tau >= 0.0f && tau <= 1.0f) || !(tau_min >= 0.0f && tau_min <= 1.0f) ||
+        !(tau_max >= 0.0f && tau_max <= 1.0f))
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; b++) out_len[b] = 0;
+    double th = (double)tau;
+    int bad = 0;
+    if (load) {
+        th = load_tau(load, (double)tau_min, (double)tau_max);
+        if (th < 0.0) bad = 1;
+    }
+    if (out_tau) *out_tau = th;
+    if (temps)
+        for (int k = 0; k < K; k++)
+            if (!(isfinite(temps[k]) && temps[k] > 0.0f)) bad = 1;
+    for (long long i = 0; i < (long long)B * K; i++)
+        if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) bad = 1;
+    if (bad) return ORC_ERR_INPUT;
+    if (B == 0) return ORC_OK;
+
+    double *c = (double *)malloc(sizeof(double) * (size_t)B * K);
+    for (int b = 0; b < B; b++)
+        for (int k = 0; k < K; k++) {
+            size_t i = (size_t)b * K + k;
+            c[i] = temps ? calibrate_one((double)conf[i], (double)temps[k]) : (double)conf[i];
+            if (out_cal) out_cal[i] = (float)c[i];
+        }
+    schedule_core(c, B, K, th, token_budget, out_len, out_surv, out_l0);
+    free(c);
+    return ORC_OK;
+}
+
+/*
+ * Calibration window statistics [DD "The Calibration Loop in Practice"]. Over a
+ * window of verification rounds, per draft position i: the mean calibrated
+ * confidence and the fraction of tokens at position i that were accepted; and,
+ * for the expected calibration error [DD "The Raw Confidence Problem": the average
+ * gap between predicted confidence and observed acceptance], the same two
+ * quantities per confidence bin.
+ *
+ * Reading: a position counts when the verifier tested it, i.e. k < L_b and k <= j_b
+ * (j_b = accepted count; positions after the first rejection were never tested);
+ * it was accepted when k < j_b. Requests with j_b < 0 (invalid) do not count. The
+ * bins are ORC_CALIB_BINS equal-width bins of c' over [0, 1] (the last one closed).
+ *
+ * stats layout (float64): [3*K] per position (sum of c', tested, accepted), then
+ * [3*ORC_CALIB_BINS] per bin (tested, sum of c', accepted).
+ */
+#define ORC_CALIB_BINS 10
+
+static int calib_bin(float c) {
+    int bin = (int)floor((double)c * ORC_CALIB_BINS);
+    if (bin < 0) bin = 0;
+    if (bin > ORC_CALIB_BINS - 1) bin = ORC_CALIB_BINS - 1;
+    return bin;
+}
+
+int oracle_calib_observe(const float *conf_cal, const int32_t *vlen, const int32_t *acc, int B,
+                         int K, double *stats) {
+    if (B < 0 || K < 1) return ORC_ERR_ARG;
+    double *bins = stats + 3 * (size_t)K;
+    for (int b = 0; b < B; b++) {
+        int L = vlen[b], j = acc[b];
+        if (j < 0 || L < 0 || L > K) continue;
+        for (int k = 0; k < L && k <= j; k++) {
+            float c = conf_cal[(size_t)b * K + k];
+            int a = k < j;
+            stats[3 * k + 0] += (double)c;
+            stats[3 * k + 1] += 1.0;
+            stats[3 * k + 2] += (double)a;
+            int bin = calib_bin(c);
+            bins[3 * bin + 0] += 1.0;
+            bins[3 * bin + 1] += (double)c;
+            bins[3 * bin + 2] += (double)a;
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Window update [DD "The Calibration Loop in Practice"]: for each position with
+ * at least one tested token, error = mean c' - acceptance rate and
+ * T_k <- T_k + lr * error (an overconfident position gets a higher temperature,
+ * [DD "Online Adaptation"]). Reading: the temperature is kept at or above
+ * temp_floor > 0 so that the scaling stays defined. The new T_k is rounded to
+ * float32. ECE = sum over bins of (n_bin / N) * |acceptance_bin - mean c'_bin| =
+ * sum_bins |accepted_bin - sum c'_bin| / N (0 when N = 0). The statistics are then
+ * reset for the next window.
+ */
+int oracle_calib_update(double *stats, float *temps, int K, double lr, double temp_floor,
+                        double *ece_out) {
+    if (K < 1 || !(temp_floor > 0.0)) return ORC_ERR_ARG;
+    for (int k = 0; k < K; k++) {
+        double n = stats[3 * k + 1];
+        if (n > 0.0) {
+            double err = stats[3 * k + 0] / n - stats[3 * k + 2] / n;
+            double t = (double)temps[k] + lr * err;
+            float tf = (float)t;
+            if ((double)tf < temp_floor) tf = (float)temp_floor;
+            temps[k] = tf;
+        }
+    }
+    const double *bins = stats + 3 * (size_t)K;
+    double N = 0.0, gap = 0.0;
+    for (int i = 0; i < ORC_CALIB_BINS; i++) {
+        N += bins[3 * i + 0];
+        gap += fabs(bins[3 * i + 2] - bins[3 * i + 1]);
+    }
+    if (ece_out) *ece_out = N > 0.0 ? gap / N : 0.0;
+    for (size_t i = 0; i < 3 * (size_t)K + 3 * ORC_CALIB_BINS; i++) stats[i] = 0.0;
+    return ORC_OK;
+}
+
+/* Exposed for the pins: one calibrated value. */
+double oracle_calibrate(double c, double T) { return calibrate_one(c, T); }

@@ -36,7 +36,7 @@ def test_lossless_pin_catches(oracle_mod, tmp_path, name):
 
 
 SCHED_MUTANTS = {
-    "strict tau comparison": ("if (run >= (double)tau) n = k + 1;", "if (run > (double)tau) n = k + 1;"),
+    "strict tau comparison": ("if (run >= th) n = k + 1;", "if (run > th) n = k + 1;"),
     "no floor of one": ("if (n < 1) n = 1;", "if (n < 0) n = 1;"),
     "tie-break on k reversed": ("if (a->k != b->k) return a->k < b->k ? -1 : 1;",
                                 "if (a->k != b->k) return a->k > b->k ? -1 : 1;"),
@@ -72,6 +72,40 @@ def test_schedule_pins_catch(oracle_mod, tmp_path, name):
     for t in tests:
         try:
             t()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name
+
+
+CALIB_MUTANTS = {
+    "temperature multiplies the logit": ("double z = (log(c) - log1p(-c)) / T;",
+                                         "double z = (log(c) - log1p(-c)) * T;"),
+    "logit sign flipped": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    "load weights swapped": ("double lf = 0.6 * (Q / Qmax) + 0.4 * (M / Mmax);",
+                             "double lf = 0.4 * (Q / Qmax) + 0.6 * (M / Mmax);"),
+    "load factor not squared": ("return tau_min + (tau_max - tau_min) * (lf * lf);",
+                                "return tau_min + (tau_max - tau_min) * lf;"),
+    "rejected position not counted": ("for (int k = 0; k < L && k <= j; k++) {",
+                                      "for (int k = 0; k < L && k < j; k++) {"),
+    "update sign reversed": ("double t = (double)temps[k] + lr * err;",
+                             "double t = (double)temps[k] - lr * err;"),
+    "ECE without the bin weights": ("if (ece_out) *ece_out = N > 0.0 ? gap / N : 0.0;",
+                                    "if (ece_out) *ece_out = N > 0.0 ? gap / ORC_CALIB_BINS : 0.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CALIB_MUTANTS))
+def test_calibration_pins_catch(oracle_mod, tmp_path, name):
+    import test_oracle_calib as tc
+
+    old, new = CALIB_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    failed = 0
+    for t in tc.PINS:
+        try:
+            t(lib)
         except AssertionError:
             failed += 1
     assert failed > 0, name
