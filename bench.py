@@ -481,6 +481,64 @@ def run_sweep(args):
                 del sets, ws, graph
 
 
+def _graph_median_us(fn, st, n=50):
+    """Median per-call time of fn() captured n times in a CUDA graph, from event-record
+    nodes around each call (launch gaps excluded)."""
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            fn()
+    st.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+           for _ in range(n)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for i in range(n):
+            evs[i][0].record(st)
+            fn()
+            evs[i][1].record(st)
+    with torch.cuda.stream(st):
+        graph.replay()
+    st.synchronize()
+    return sorted(e[0].elapsed_time(e[1]) * 1e3 for e in evs)[n // 2]
+
+
+def run_calib(args):
+    """One JSON line per configuration: per-call time of the plain schedule, the
+    calibrated load-aware schedule, and the two calibration-loop kernels."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    for B, K in ((64, 8), (256, 16), (4096, 4)):
+        conf = synth.confidences(B, K, seed=1).to(dev)
+        temps = synth.temperatures(K, seed=1).to(dev)
+        load = synth.load_state(seed=1).to(dev)
+        c, vl, acc = (t.to(dev) for t in synth.calib_round(B, K, seed=1))
+        ws = sv.Workspace(B, K, 16, device=dev)
+        out_len = torch.empty(B, dtype=torch.int32, device=dev)
+        cal = torch.empty(B, K, dtype=torch.float32, device=dev)
+        tau = torch.empty(1, dtype=torch.float64, device=dev)
+        stats = torch.zeros(sv.sv_calib_stats_len(K), dtype=torch.float64, device=dev)
+        ece = torch.empty(1, dtype=torch.float64, device=dev)
+        t_cur = temps.clone()
+        budget = B * K // 2
+        res = {"calib": True, "B": B, "K": K, "budget": budget}
+        res["schedule_us"] = _graph_median_us(
+            lambda: sv.sv_schedule(conf, 0.3, budget, ws, out_len=out_len, stream=st), st)
+        res["schedule_cal_us"] = _graph_median_us(
+            lambda: sv.sv_schedule_cal(conf, temps, load, 0.3, 0.2, 0.75, budget, ws,
+                                       out_len=out_len, conf_cal=cal, tau_out=tau, stream=st), st)
+        res["observe_us"] = _graph_median_us(
+            lambda: sv.sv_calib_observe(c, vl, acc, stats, stream=st), st)
+        res["update_us"] = _graph_median_us(
+            lambda: sv.sv_calib_update(stats, t_cur, 0.01, 0.05, ece=ece, stream=st), st)
+        if ws.status(stream=st) != sv.SV_OK:
+            raise RuntimeError("device status not OK in the calibration timing")
+        res["timing"] = "median of 50 in-graph call events"
+        print(json.dumps(res), flush=True)
+
+
 def run_once(args):
     """N untimed steps on one input set of the configured workload (for ncu captures)."""
     import torch
@@ -517,6 +575,8 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-T", default=None)
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--calib", action="store_true",
+                    help="time the calibrated schedule and the calibration-loop kernels")
     ap.add_argument("--once", type=int, default=0,
                     help="no timing: build one input set and run N schedule+verify steps "
                          "(a short, self-contained program for profilers)")
@@ -527,6 +587,8 @@ def main():
         run_once(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.calib:
+        run_calib(args)
     else:
         run_gpu(args)
 

@@ -58,6 +58,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_V (1 << 24)    /* vocabulary entries */
 #define SV_MAX_SCHED_B 8192   /* requests per schedule call */
 #define SV_MAX_SCHED_BK 16384 /* B*K per schedule call */
+#define SV_CALIB_BINS 10      /* equal-width confidence bins of the calibration error */
 
 /*
  * sv_workspace_bytes: size of the device workspace needed by sv_schedule and
@@ -100,6 +101,73 @@ sv_status sv_workspace_init(void *ws_d, size_t ws_bytes, void *stream);
  */
 sv_status sv_schedule(const float *conf_d, int B, int K, float tau, int token_budget,
                       int32_t *out_len_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_schedule_cal: sv_schedule with its two device-resident inputs from the pages'
+ * scheduling pipeline [DD "The Full Scheduling Pipeline": raw confidence -> online
+ * calibration -> scheduler with the GPU's load state -> verify length].
+ *
+ *  temps_d    [K] float32 per-position temperatures T_k (> 0, finite), or NULL for
+ *             no calibration. Each confidence becomes c' = sigmoid(logit(c) / T_k)
+ *             [DD "Sequential Temperature Scaling"], computed in fp32 (c = 0 and
+ *             c = 1 stay fixed); the survival products then run on c' in float64.
+ *  load_d     [4] float32 {Q, Q_max, M_gpu, M_max}: queue depth and GPU memory use
+ *             with their maxima, or NULL to use `tau` as given. Otherwise
+ *             LF = 0.6 Q/Q_max + 0.4 M_gpu/M_max, clamped to 1, and
+ *             tau = tau_min + (tau_max - tau_min) LF^2, in float64
+ *             [GD "Dynamic Verification Scheduling Algorithm", steps 1-2].
+ *  tau_min, tau_max  in [0,1]; read only when load_d is given (the page's example
+ *             range is 0.20 to 0.75).
+ *  conf_cal_d [B,K] float32 out: c' (the input of sv_calib_observe), or NULL.
+ *  tau_out_d  [1] float64 out: the threshold used, or NULL.
+ *  Other arguments, steps 1-3, limits and the workspace: as sv_schedule. Device
+ *  errors (SV_ERR_DEVICE_INPUT, out_len = 0 everywhere): a confidence outside [0,1],
+ *  a temperature that is not a positive finite number, a load value that is not
+ *  finite, a negative Q or M_gpu, or a maximum that is not > 0. When B == 0 nothing
+ *  is enqueued and nothing is written.
+ */
+sv_status sv_schedule_cal(const float *conf_d, const float *temps_d, const float *load_d,
+                          float tau, float tau_min, float tau_max, int B, int K,
+                          int token_budget, int32_t *out_len_d, float *conf_cal_d,
+                          double *tau_out_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * Online calibration loop [DD "The Calibration Loop in Practice", "Online
+ * Adaptation"; ECE: "The Raw Confidence Problem"]. The caller owns a window buffer
+ * of sv_calib_stats_len(K) float64 values (zeroed once), calls sv_calib_observe after
+ * every verification round and sv_calib_update every N rounds (the page's example
+ * window is about 500 rounds).
+ *
+ * Window layout (float64): per position k (3K values): sum of c', tested tokens,
+ * accepted tokens; then per confidence bin i (3 SV_CALIB_BINS values; bin i holds
+ * c' in [i/10, (i+1)/10), the last bin also 1): tested, sum of c', accepted.
+ */
+size_t sv_calib_stats_len(int K); /* 0 for K outside [1, SV_MAX_K] */
+
+/*
+ * sv_calib_observe: add one verification round to the window.
+ *  conf_cal_d [B,K] float32 c' (sv_schedule_cal's conf_cal_d), verify_len_d [B] and
+ *  accepted_d [B] (sv_verify's input and out_accepted). Position k of request b
+ *  counts when it was tested, k < L_b and k <= j_b (j_b = accepted count; later
+ *  positions were never tested), and as accepted when k < j_b; requests with
+ *  j_b < 0 or L_b outside [0,K] are skipped. One small launch; the sums are formed
+ *  in a fixed order, so repeated runs give identical windows.
+ *  Limits: 0 <= B <= SV_MAX_B, 1 <= K <= SV_MAX_K. stats_d is read and written.
+ */
+sv_status sv_calib_observe(const float *conf_cal_d, const int32_t *verify_len_d,
+                           const int32_t *accepted_d, int B, int K, double *stats_d,
+                           void *stream);
+
+/*
+ * sv_calib_update: close the window. For each position k with a tested token,
+ * error_k = (sum c')/tested - accepted/tested and T_k <- T_k + lr * error_k (float64,
+ * rounded to float32), then T_k <- max(T_k, temp_floor) so the scaling stays defined
+ * (an overconfident position gets a higher temperature). ece_d [1] float64 out (or
+ * NULL): sum over bins of |accepted - sum c'| / total tested (0 for an empty window).
+ * The window is then zeroed. lr finite (the pages use 0.001 to 0.01); temp_floor > 0.
+ */
+sv_status sv_calib_update(double *stats_d, float *temps_d, int K, float lr, float temp_floor,
+                          double *ece_d, void *stream);
 
 /*
  * sv_verify: standard speculative rejection sampling over a batch of drafted blocks.

@@ -49,6 +49,15 @@ def load(build_if_missing: bool = True):
     lib.sv_workspace_init.restype = i32
     lib.sv_schedule.argtypes = [vp, i32, i32, f32, i32, vp, vp, sz, vp]
     lib.sv_schedule.restype = i32
+    lib.sv_schedule_cal.argtypes = [vp, vp, vp, f32, f32, f32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                    vp]
+    lib.sv_schedule_cal.restype = i32
+    lib.sv_calib_stats_len.argtypes = [i32]
+    lib.sv_calib_stats_len.restype = sz
+    lib.sv_calib_observe.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+    lib.sv_calib_observe.restype = i32
+    lib.sv_calib_update.argtypes = [vp, vp, i32, f32, f32, vp, vp]
+    lib.sv_calib_update.restype = i32
     lib.sv_verify.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
     lib.sv_verify.restype = i32
     lib.sv_verify_diag.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp,
@@ -62,6 +71,9 @@ def load(build_if_missing: bool = True):
     lib.sv_version.restype = i32
     _lib = lib
     return lib
+
+
+load_lib = load  # the library loader, for functions whose arguments shadow `load`
 
 
 def status_string(code: int) -> str:
@@ -129,6 +141,68 @@ def sv_schedule(conf, tau, token_budget, ws: Workspace, out_len=None, stream=Non
                                              _ptr(out_len), _ptr(ws.t), ws.nbytes,
                                              _stream(stream)))
     return out_len
+
+
+def sv_schedule_cal(conf, temps, load, tau, tau_min, tau_max, token_budget, ws: Workspace,
+                    out_len=None, conf_cal=None, tau_out=None, stream=None):
+    """sv_schedule on calibrated confidences, optionally with the load-aware threshold
+    (see specverify.h). temps [K] float32 or None; load [4] float32 or None. Returns
+    (out_len, conf_cal, tau_out); conf_cal [B,K] float32 and tau_out [1] float64 are
+    allocated when not given."""
+    conf = _dev(conf, "conf", torch.float32)
+    B, K = conf.shape
+    if temps is not None:
+        _dev(temps, "temps", torch.float32)
+    if load is not None:
+        _dev(load, "load", torch.float32)
+    if out_len is None:
+        out_len = torch.empty(B, dtype=torch.int32, device=conf.device)
+    if conf_cal is None:
+        conf_cal = torch.empty(B, K, dtype=torch.float32, device=conf.device)
+    if tau_out is None:
+        tau_out = torch.empty(1, dtype=torch.float64, device=conf.device)
+    _dev(out_len, "out_len", torch.int32)
+    _dev(conf_cal, "conf_cal", torch.float32)
+    _dev(tau_out, "tau_out", torch.float64)
+    _check("sv_schedule_cal", load_lib().sv_schedule_cal(
+        _ptr(conf), _ptr(temps), _ptr(load), float(tau), float(tau_min), float(tau_max), B, K,
+        int(token_budget), _ptr(out_len), _ptr(conf_cal), _ptr(tau_out), _ptr(ws.t), ws.nbytes,
+        _stream(stream)))
+    return out_len, conf_cal, tau_out
+
+
+def sv_calib_stats_len(K: int) -> int:
+    """Length (float64) of the calibration window buffer for K positions."""
+    return int(load_lib().sv_calib_stats_len(int(K)))
+
+
+def sv_calib_observe(conf_cal, verify_len, accepted, stats, stream=None):
+    """Add one verification round to the window stats (float64, in place)."""
+    conf_cal = _dev(conf_cal, "conf_cal", torch.float32)
+    B, K = conf_cal.shape
+    _dev(verify_len, "verify_len", torch.int32)
+    _dev(accepted, "accepted", torch.int32)
+    _dev(stats, "stats", torch.float64)
+    if stats.numel() != sv_calib_stats_len(K):
+        raise ValueError("stats has the wrong length")
+    _check("sv_calib_observe", load_lib().sv_calib_observe(
+        _ptr(conf_cal), _ptr(verify_len), _ptr(accepted), B, K, _ptr(stats), _stream(stream)))
+
+
+def sv_calib_update(stats, temps, lr, temp_floor, ece=None, stream=None):
+    """Close the window: update temps [K] float32 in place, write the ECE into ece [1]
+    float64 (allocated when not given) and zero stats. Returns ece."""
+    _dev(stats, "stats", torch.float64)
+    _dev(temps, "temps", torch.float32)
+    K = temps.numel()
+    if stats.numel() != sv_calib_stats_len(K):
+        raise ValueError("stats has the wrong length")
+    if ece is None:
+        ece = torch.empty(1, dtype=torch.float64, device=temps.device)
+    _dev(ece, "ece", torch.float64)
+    _check("sv_calib_update", load_lib().sv_calib_update(
+        _ptr(stats), _ptr(temps), K, float(lr), float(temp_floor), _ptr(ece), _stream(stream)))
+    return ece
 
 
 def _dtype_code(t):

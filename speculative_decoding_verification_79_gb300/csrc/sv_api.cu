@@ -41,17 +41,61 @@ sv_status sv_workspace_init(void* ws_d, size_t ws_bytes, void* stream) {
   return SV_OK;
 }
 
-sv_status sv_schedule(const float* conf_d, int B, int K, float tau, int token_budget,
-                      int32_t* out_len_d, void* ws_d, size_t ws_bytes, void* stream) {
+sv_status sv_schedule_cal(const float* conf_d, const float* temps_d, const float* load_d,
+                          float tau, float tau_min, float tau_max, int B, int K,
+                          int token_budget, int32_t* out_len_d, float* conf_cal_d,
+                          double* tau_out_d, void* ws_d, size_t ws_bytes, void* stream) {
   if (B < 0 || B > SV_MAX_SCHED_B || K < 1 || K > SV_MAX_K || (long long)B * K > SV_MAX_SCHED_BK)
     return SV_ERR_SHAPE;
   if (!(tau >= 0.f && tau <= 1.f) || token_budget < 0) return SV_ERR_ARG;
+  if (load_d && !(tau_min >= 0.f && tau_min <= 1.f && tau_max >= 0.f && tau_max <= 1.f))
+    return SV_ERR_ARG;
   if (!ws_d || ws_bytes < sizeof(WsHeader) || !aligned(ws_d, 256)) return SV_ERR_WORKSPACE;
   if (B == 0) return SV_OK;
   if (!conf_d || !out_len_d || !aligned(conf_d, 4) || !aligned(out_len_d, 4)) return SV_ERR_ARG;
-  const cudaError_t e =
-      launch_schedule(conf_d, B, K, tau, token_budget, out_len_d, static_cast<WsHeader*>(ws_d),
-                      static_cast<cudaStream_t>(stream));
+  if ((temps_d && !aligned(temps_d, 4)) || (load_d && !aligned(load_d, 4)) ||
+      (conf_cal_d && !aligned(conf_cal_d, 4)) || (tau_out_d && !aligned(tau_out_d, 8)))
+    return SV_ERR_ARG;
+  const cudaError_t e = launch_schedule(conf_d, temps_d, load_d, B, K, tau, tau_min, tau_max,
+                                        token_budget, out_len_d, conf_cal_d, tau_out_d,
+                                        static_cast<WsHeader*>(ws_d),
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_schedule(const float* conf_d, int B, int K, float tau, int token_budget,
+                      int32_t* out_len_d, void* ws_d, size_t ws_bytes, void* stream) {
+  return sv_schedule_cal(conf_d, nullptr, nullptr, tau, 0.f, 0.f, B, K, token_budget, out_len_d,
+                         nullptr, nullptr, ws_d, ws_bytes, stream);
+}
+
+size_t sv_calib_stats_len(int K) {
+  if (K < 1 || K > SV_MAX_K) return 0;
+  return 3 * (size_t)K + 3 * (size_t)SV_CALIB_BINS;
+}
+
+sv_status sv_calib_observe(const float* conf_cal_d, const int32_t* verify_len_d,
+                           const int32_t* accepted_d, int B, int K, double* stats_d,
+                           void* stream) {
+  if (B < 0 || B > SV_MAX_B || K < 1 || K > SV_MAX_K) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!conf_cal_d || !verify_len_d || !accepted_d || !stats_d || !aligned(conf_cal_d, 4) ||
+      !aligned(verify_len_d, 4) || !aligned(accepted_d, 4) || !aligned(stats_d, 8))
+    return SV_ERR_ARG;
+  const cudaError_t e = launch_calib_observe(conf_cal_d, verify_len_d, accepted_d, B, K, stats_d,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_calib_update(double* stats_d, float* temps_d, int K, float lr, float temp_floor,
+                          double* ece_d, void* stream) {
+  if (K < 1 || K > SV_MAX_K) return SV_ERR_SHAPE;
+  if (!std::isfinite(lr) || !std::isfinite(temp_floor) || !(temp_floor > 0.f)) return SV_ERR_ARG;
+  if (!stats_d || !temps_d || !aligned(stats_d, 8) || !aligned(temps_d, 4) ||
+      (ece_d && !aligned(ece_d, 8)))
+    return SV_ERR_ARG;
+  const cudaError_t e = launch_calib_update(stats_d, temps_d, K, lr, temp_floor, ece_d,
+                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -152,8 +152,14 @@ struct VerifyArgs {
 };
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st);
-cudaError_t launch_schedule(const float* conf, int B, int K, float tau, int budget,
-                            int32_t* out_len, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_schedule(const float* conf, const float* temps, const float* load, int B,
+                            int K, float tau, float tau_min, float tau_max, int budget,
+                            int32_t* out_len, float* conf_cal, double* tau_out, WsHeader* hdr,
+                            cudaStream_t st);
+cudaError_t launch_calib_observe(const float* conf_cal, const int32_t* vlen, const int32_t* acc,
+                                 int B, int K, double* stats, cudaStream_t st);
+cudaError_t launch_calib_update(double* stats, float* temps, int K, float lr, float temp_floor,
+                                double* ece, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // PTX wrappers.

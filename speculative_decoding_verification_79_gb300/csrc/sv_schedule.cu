@@ -14,6 +14,12 @@
 //     radix select on the 64-bit patterns of S (order-preserving for S >= 0) and a
 //     k-major prefix count that ranks positions tied with the threshold
 //     (DSpark Deep Dive, "The Optimization Logic").
+//  0. Optional prologue: sequential temperature scaling of each confidence,
+//     c' = sigmoid(logit(c) / T_k) with one temperature per draft position (DSpark
+//     Deep Dive, "Sequential Temperature Scaling"), in fp32; and the load-aware
+//     threshold tau = tau_min + (tau_max - tau_min) * LF^2, LF = 0.6 Q/Q_max +
+//     0.4 M/M_max clamped to 1 (DSpark Guide, "Dynamic Verification Scheduling
+//     Algorithm"), in fp64 from the device-resident load state.
 // One CTA of 1024 threads; everything lives in shared memory.
 #include "sv_common.cuh"
 
@@ -23,12 +29,38 @@ constexpr int SCHED_THREADS = 1024;
 
 struct ScheduleArgs {
   const float* conf;
+  const float* temps;  // [K] or nullptr: no calibration
+  const float* load;   // [4] {Q, Q_max, M_gpu, M_max} or nullptr: tau as given
   int B, K;
-  float tau;
+  float tau, tau_min, tau_max;
   int budget;
   int32_t* out_len;
+  float* conf_cal;     // [B,K] or nullptr
+  double* tau_out;     // [1] or nullptr
   WsHeader* hdr;
 };
+
+// sigmoid(logit(c) / T) in fp32; the end points stay fixed. logit(c) is taken as the
+// log of one rounded ratio c / (1 - c): near c = 1/2 this avoids the cancellation of
+// log(c) - log(1 - c), and elsewhere the error is that of logf itself (an absolute
+// error of a few ulps of |logit c|, scaled by (1 - c') / T in c').
+__device__ __forceinline__ float calibrate(float c, float T) {
+  if (c <= 0.f) return 0.f;
+  if (c >= 1.f) return 1.f;
+  const float z = __fdiv_rn(logf(__fdiv_rn(c, __fsub_rn(1.f, c))), T);
+  return __fdiv_rn(1.f, __fadd_rn(1.f, expf(-z)));
+}
+
+// Load-aware threshold in fp64 (no contraction: each step rounds once). Returns a
+// negative value for an invalid load state.
+__device__ double load_tau(const float* load, double tau_min, double tau_max) {
+  const double Q = load[0], Qm = load[1], M = load[2], Mm = load[3];
+  if (!(isfinite(Q) && isfinite(Qm) && isfinite(M) && isfinite(Mm))) return -1.0;
+  if (Q < 0.0 || M < 0.0 || !(Qm > 0.0) || !(Mm > 0.0)) return -1.0;
+  double lf = __dadd_rn(__dmul_rn(0.6, __ddiv_rn(Q, Qm)), __dmul_rn(0.4, __ddiv_rn(M, Mm)));
+  if (lf > 1.0) lf = 1.0;
+  return __dadd_rn(tau_min, __dmul_rn(__dsub_rn(tau_max, tau_min), __dmul_rn(lf, lf)));
+}
 
 __device__ __forceinline__ unsigned long long surv_key(double s) {
   return static_cast<unsigned long long>(__double_as_longlong(s == 0.0 ? 0.0 : s));
@@ -45,26 +77,57 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   __shared__ unsigned int s_rem;
   __shared__ int s_scan[32];
   __shared__ unsigned long long s_total;
+  __shared__ float s_temps[SV_MAX_K];
+  __shared__ double s_tau;
+  __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 1-2. survival products and tau-lengths, one thread per request. The row of
-  // confidences is loaded up front (independent loads), and S >= 0 compares with tau
-  // as 64-bit patterns, keeping the slow fp64 pipe to the products alone.
-  bool bad = false;
-  const unsigned long long tau_key = surv_key(static_cast<double>(A.tau));
+  // 0. Threshold (load-aware or as given) and the position temperatures.
+  if (tid == 0) {
+    double th = static_cast<double>(A.tau);
+    int bad = 0;
+    if (A.load) {
+      th = load_tau(A.load, static_cast<double>(A.tau_min), static_cast<double>(A.tau_max));
+      bad = th < 0.0;
+    }
+    if (A.tau_out) *A.tau_out = th;
+    s_tau = th;
+    s_bad = bad;
+  }
+  __syncthreads();
+  if (A.temps && tid < K) {
+    const float t = __ldg(A.temps + tid);
+    s_temps[tid] = t;
+    if (!(isfinite(t) && t > 0.f)) s_bad = 1;
+  }
+  __syncthreads();
+
+  // 0b. Each confidence (calibrated when temperatures are given) into S, one
+  // element per thread.
+  bool bad = s_bad != 0;
+  const bool cal = A.temps != nullptr;
+  for (int i = tid; i < N; i += SCHED_THREADS) {
+    float c = __ldg(A.conf + i);
+    if (!(c >= 0.f && c <= 1.f)) bad = true;
+    if (cal) c = calibrate(c, s_temps[i % K]);
+    if (A.conf_cal) A.conf_cal[i] = c;
+    S[i] = static_cast<double>(c);
+  }
+  __syncthreads();
+  // 1-2. survival products and tau-lengths, one thread per request; S >= 0 compares
+  // with tau as 64-bit patterns, keeping the slow fp64 pipe to the products alone.
+  const unsigned long long tau_key = surv_key(s_tau < 0.0 ? 0.0 : s_tau);
   unsigned long long my_total = 0;
   for (int b = tid; b < B; b += SCHED_THREADS) {
-    float cv[SV_MAX_K];
+    double cv[SV_MAX_K];
 #pragma unroll
-    for (int k = 0; k < SV_MAX_K; ++k) cv[k] = (k < K) ? __ldg(A.conf + (size_t)b * K + k) : 0.f;
+    for (int k = 0; k < SV_MAX_K; ++k) cv[k] = (k < K) ? S[(size_t)b * K + k] : 0.0;
     double run = 1.0;
     int n = 0;
 #pragma unroll
     for (int k = 0; k < SV_MAX_K; ++k) {
       if (k < K) {
-        const float c = cv[k];
-        if (!(c >= 0.f && c <= 1.f)) bad = true;
-        run = run * static_cast<double>(c);
+        run = run * cv[k];
         S[(size_t)b * K + k] = run;
         if (surv_key(run) >= tau_key) n = k + 1;
       }
@@ -198,8 +261,10 @@ static size_t schedule_smem_bytes(int B, int K) {
   return (size_t)B * K * sizeof(double) + 2 * (size_t)B * sizeof(int);
 }
 
-cudaError_t launch_schedule(const float* conf, int B, int K, float tau, int budget,
-                            int32_t* out_len, WsHeader* hdr, cudaStream_t st) {
+cudaError_t launch_schedule(const float* conf, const float* temps, const float* load, int B,
+                            int K, float tau, float tau_min, float tau_max, int budget,
+                            int32_t* out_len, float* conf_cal, double* tau_out, WsHeader* hdr,
+                            cudaStream_t st) {
   const size_t smem = schedule_smem_bytes(B, K);
   static bool attr_set = false;  // idempotent if two threads race here
   if (!attr_set) {
@@ -209,7 +274,8 @@ cudaError_t launch_schedule(const float* conf, int B, int K, float tau, int budg
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  ScheduleArgs A{conf, B, K, tau, budget, out_len, hdr};
+  ScheduleArgs A{conf, temps, load, B, K, tau, tau_min, tau_max, budget, out_len, conf_cal,
+                 tau_out, hdr};
   sv_schedule_kernel<<<1, SCHED_THREADS, smem, st>>>(A);
   return cudaGetLastError();
 }

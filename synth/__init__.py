@@ -164,3 +164,39 @@ def logit_bytes(verify_len, V, elem_bytes, greedy=False):
     rows = (L + 1) if greedy else (2 * L + 1)
     return int(rows.sum().item()) * V * elem_bytes
 
+
+
+# ----------------------------------------------------------------------------------
+# Calibration-loop inputs (random numbers only).
+# ----------------------------------------------------------------------------------
+
+def temperatures(K, *, lo=0.5, hi=2.5, seed=0):
+    """Per-position temperatures [K] float32, uniform in [lo, hi]."""
+    rng = np.random.default_rng(int(seed) + 1000)
+    return torch.from_numpy(rng.uniform(lo, hi, size=K).astype(np.float32))
+
+
+def load_state(*, seed=0, q_max=64.0, m_max=80.0):
+    """{Q, Q_max, M_gpu, M_max} float32: queue depth and memory use, each up to a bit
+    past its maximum (so the load factor's clamp is reached now and then)."""
+    rng = np.random.default_rng(int(seed) + 2000)
+    q = rng.uniform(0.0, 1.2 * q_max)
+    m = rng.uniform(0.0, 1.1 * m_max)
+    return torch.tensor([q, q_max, m, m_max], dtype=torch.float32)
+
+
+def calib_round(B, K, *, seed=0):
+    """One verification round as the calibration loop sees it: calibrated confidences
+    [B,K] float32 in [0,1] (some exactly 0, 1 or on a bin boundary of tenths), verify
+    lengths [B] in [0,K] and accepted counts [B] in [0, L_b], a few -1 (invalid)."""
+    rng = np.random.default_rng(int(seed) + 3000)
+    c = rng.uniform(0.0, 1.0, size=(B, K)).astype(np.float32)
+    pick = rng.random((B, K))
+    c[pick < 0.02] = 0.0
+    c[(pick >= 0.02) & (pick < 0.04)] = 1.0
+    edges = (rng.integers(1, 10, size=(B, K)) / 10.0).astype(np.float32)
+    c[(pick >= 0.04) & (pick < 0.08)] = edges[(pick >= 0.04) & (pick < 0.08)]
+    vlen = rng.integers(0, K + 1, size=B).astype(np.int32)
+    acc = np.array([rng.integers(0, v + 1) for v in vlen], np.int32)
+    acc[rng.random(B) < 0.05] = -1
+    return torch.from_numpy(c), torch.from_numpy(vlen), torch.from_numpy(acc)

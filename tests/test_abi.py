@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared()
     for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
-              "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version"):
+              "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version",
+              "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update"):
         assert n in names
 
 
@@ -98,3 +99,29 @@ def test_no_fallback_without_cuda():
         pytest.skip("a GPU is present")
     with pytest.raises(Exception):
         sv.Workspace(4, 4, 100)
+
+
+def test_calibration_host_checks(lib):
+    """The calibration entry points reject bad calls before any device work."""
+    import speculative_decoding_verification_79_gb300 as sv
+
+    fake = ctypes.c_void_p(256)
+    n = lib.sv_workspace_bytes(4, 4, 100)
+    assert lib.sv_calib_stats_len(8) == 3 * 8 + 3 * 10
+    assert lib.sv_calib_stats_len(0) == 0 and lib.sv_calib_stats_len(33) == 0
+    cal = lambda tau=0.3, tmin=0.2, tmax=0.75, load=None, B=4, K=4, ws=fake: (  # noqa: E731
+        fake, None, load, tau, tmin, tmax, B, K, 10, fake, None, None, ws, n, None)
+    assert lib.sv_schedule_cal(*cal(tau=1.5)) == sv.SV_ERR_ARG
+    assert lib.sv_schedule_cal(*cal(load=fake, tmax=1.5)) == sv.SV_ERR_ARG
+    assert lib.sv_schedule_cal(*cal(load=fake, tmin=float("nan"))) == sv.SV_ERR_ARG
+    assert lib.sv_schedule_cal(*cal(K=33)) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule_cal(*cal(ws=None)) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_schedule_cal(*cal(B=0)) == sv.SV_OK
+    assert lib.sv_calib_observe(fake, fake, fake, 4, 0, fake, None) == sv.SV_ERR_SHAPE
+    assert lib.sv_calib_observe(fake, fake, fake, 5000, 4, fake, None) == sv.SV_ERR_SHAPE
+    assert lib.sv_calib_observe(None, fake, fake, 4, 4, fake, None) == sv.SV_ERR_ARG
+    assert lib.sv_calib_observe(fake, fake, fake, 0, 4, fake, None) == sv.SV_OK
+    assert lib.sv_calib_update(fake, fake, 4, 0.01, 0.0, None, None) == sv.SV_ERR_ARG
+    assert lib.sv_calib_update(fake, fake, 4, float("inf"), 0.05, None, None) == sv.SV_ERR_ARG
+    assert lib.sv_calib_update(fake, None, 4, 0.01, 0.05, None, None) == sv.SV_ERR_ARG
+    assert lib.sv_calib_update(fake, fake, 40, 0.01, 0.05, None, None) == sv.SV_ERR_SHAPE
