@@ -15,13 +15,13 @@
 //    reduces the other slots. Pieces are reduced whole: online softmax (running max
 //    + sum of 2^(z*log2e/T - max)) at T > 0, or (max, lowest argmax) at T == 0,
 //    merged in registers while consecutive pieces belong to the same row. A warp's
-//    run of pieces of one row is published with one release-ordered atomic ticket
-//    whose value the warp inspects only after its next wait, so the round trip stays
-//    off the critical path. The warp completing a row combines its partials in piece
-//    order; the warp completing a request decides it: p_k(x_k),
-//    q_k(x_k), the accept tests u*q < p, a ballot for the first rejection j, the
-//    outputs, and (T > 0) the request's terminal-sample job, announced by a
-//    release-ordered decision flag.
+//    run of pieces of one row is published as one self-validating 64-bit word and a
+//    relaxed ticket increment, whose value the warp inspects only after its next
+//    wait, so the round trip stays off the critical path (no fences on the stream
+//    path). The warp completing a row combines its partials in piece order; the
+//    warp completing a request decides it: p_k(x_k), q_k(x_k), the accept tests
+//    u*q < p, a ballot for the first rejection j, the outputs, and (T > 0) the
+//    request's terminal-sample job, announced by a release-ordered decision flag.
 //  - Terminal tasks (T > 0). The terminal rows of a request (residual
 //    max(0, p_j - q_j), or p of the bonus row) are cut into R pieces; the tasks
 //    (b, p), request-major, are split into equal contiguous shares, one per warp.
