@@ -82,6 +82,9 @@ def _bind(path):
     lib.oracle_calib_update.argtypes = [f64p, f32p, ctypes.c_int, ctypes.c_double,
                                         ctypes.c_double, f64p]
     lib.oracle_calib_update.restype = ctypes.c_int
+    lib.oracle_markov_draft.argtypes = [vp, vp, vp, i32p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, vp, i32p, f64p, f64p]
+    lib.oracle_markov_draft.restype = ctypes.c_int
     return lib
 
 
@@ -185,6 +188,26 @@ def calib_update(stats, temps, lr: float, temp_floor: float, lib=None):
     rc = (lib or _load()).oracle_calib_update(_ptr(stats), _ptr(temps), temps.size, float(lr),
                                               float(temp_floor), _ptr(ece))
     return rc, float(ece[0])
+
+
+def markov_draft(logits, U, Vm, prev, lib=None):
+    """Markov logit-bias drafting loop. logits [B,K,V], U and Vm [V,r]: bf16 as uint16
+    bits; prev [B] int32. Returns dict(corrected [B,K,V] uint16 bits, tok [B,K] int32,
+    edge [B,K], gap [B,K], status)."""
+    L = np.ascontiguousarray(logits, dtype=np.uint16)
+    Um = np.ascontiguousarray(U, dtype=np.uint16)
+    Wm = np.ascontiguousarray(Vm, dtype=np.uint16)
+    pv = np.ascontiguousarray(prev, dtype=np.int32)
+    B, K, V = L.shape
+    r = Um.shape[1]
+    assert Um.shape == (V, r) and Wm.shape == (V, r) and pv.shape == (B,)
+    corr = np.zeros_like(L)
+    tok = np.zeros((B, K), np.int32)
+    edge = np.zeros((B, K), np.float64)
+    gap = np.zeros((B, K), np.float64)
+    rc = (lib or _load()).oracle_markov_draft(_ptr(L), _ptr(Um), _ptr(Wm), _ptr(pv), B, K, V, r,
+                                              _ptr(corr), _ptr(tok), _ptr(edge), _ptr(gap))
+    return {"corrected": corr, "tok": tok, "edge": edge, "gap": gap, "status": rc}
 
 
 def _logits(a):

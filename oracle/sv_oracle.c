@@ -614,3 +614,106 @@ int oracle_calib_update(double *stats, float *temps, int K, double lr, double te
 
 /* Exposed for the pins: one calibrated value. */
 double oracle_calibrate(double c, double T) { return calibrate_one(c, T); }
+
+/* ======================================================================== */
+/* Markov logit-bias head (drafting side)                                    */
+/* ======================================================================== */
+
+/* Round a float64 value to bf16 (round to nearest, ties to even) and return its
+ * bit pattern; |x| must be finite and within bf16 range. */
+static uint16_t to_bf16_rne(double x) {
+    if (x == 0.0) return signbit(x) ? 0x8000u : 0u;
+    int e;
+    double m = frexp(fabs(x), &e);           /* |x| = m * 2^e, m in [0.5, 1) */
+    double scaled = ldexp(m, 8);             /* 8 significant bits: bf16 keeps 8 (1 implicit + 7) */
+    double lo = floor(scaled), frac = scaled - lo;
+    double q;
+    if (frac > 0.5 || (frac == 0.5 && fmod(lo, 2.0) != 0.0)) q = lo + 1.0;
+    else q = lo;
+    double r = ldexp(q, e - 8);
+    float rf = (float)r;                      /* exact: r has 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &rf, sizeof bits);
+    if (x < 0) bits |= 0x80000000u;
+    return (uint16_t)(bits >> 16);
+}
+
+static double bf16_value(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * oracle_markov_draft: the semi-autoregressive sampling loop of [GD "1. The Markov
+ * Logit-Bias Head" and "Hands-On Implementation"]. For each request b and position
+ * k = 0..K-1, with y_{-1} = prev[b]:
+ *     L'_{b,k} = L_{b,k} + U (Vm[y_{k-1}, :])^T      (a [V] vector; U, Vm are [V, r])
+ *     y_k      = argmax_v L'_{b,k}[v]  (lowest index on ties)
+ * The correction is formed in float64 from the bf16 inputs (exact products, sums in
+ * index order), L + correction is rounded once to bf16 (to nearest, ties to even) and
+ * stored; the argmax is taken over the stored bf16 values. Reading: greedy drafting,
+ * as the sketch's argmax; the corrected logits keep the dtype of the raw ones because
+ * they are the draft logits the verifier reads.
+ *
+ * L: [B,K,V] bf16 bits; U, Vm: [V,r] bf16 bits; prev: [B] in [0,V).
+ * out_corr: [B,K,V] bf16 bits; out_tok: [B,K].
+ * out_edge (or NULL): [B,K] the smallest distance, in units of the bf16 spacing at the
+ *   value, between an exact L + correction and a bf16 rounding midpoint, over the row's
+ *   elements (a diagnostic for comparing against a kernel with fp32 sums).
+ * out_gap (or NULL): [B,K] the gap between the row's largest and second largest
+ *   exact L + correction values, relative to the largest magnitude (diagnostic).
+ * Returns ORC_ERR_INPUT if a prev token is out of range.
+ */
+int oracle_markov_draft(const uint16_t *L, const uint16_t *U, const uint16_t *Vm,
+                        const int32_t *prev, int B, int K, int V, int r, uint16_t *out_corr,
+                        int32_t *out_tok, double *out_edge, double *out_gap) {
+    if (B < 0 || K < 1 || V < 1 || r < 1) return ORC_ERR_ARG;
+    for (int b = 0; b < B; b++)
+        if (prev[b] < 0 || prev[b] >= V) return ORC_ERR_INPUT;
+    double *x = (double *)malloc(sizeof(double) * (size_t)r);
+    for (int b = 0; b < B; b++) {
+        int y = prev[b];
+        for (int k = 0; k < K; k++) {
+            for (int j = 0; j < r; j++) x[j] = bf16_value(Vm[(size_t)y * r + j]);
+            size_t row = ((size_t)b * K + k) * (size_t)V;
+            int best = -1;
+            double bestv = 0.0, edge = INFINITY, top1 = -INFINITY, top2 = -INFINITY, amax = 0.0;
+            for (int v = 0; v < V; v++) {
+                double c = 0.0;
+                for (int j = 0; j < r; j++) c += bf16_value(U[(size_t)v * r + j]) * x[j];
+                double z = bf16_value(L[row + v]) + c;
+                uint16_t h = to_bf16_rne(z);
+                out_corr[row + v] = h;
+                double stored = bf16_value(h);
+                if (best < 0 || stored > bestv) {
+                    best = v;
+                    bestv = stored;
+                }
+                /* diagnostics: distance of z to the nearest rounding midpoint */
+                if (z != 0.0) {
+                    int e;
+                    frexp(fabs(z), &e);
+                    double spacing = ldexp(1.0, e - 8);
+                    double t = fabs(z) / spacing;
+                    double d = fabs((t - floor(t)) - 0.5);
+                    if (d < edge) edge = d;
+                }
+                if (z > top1) {
+                    top2 = top1;
+                    top1 = z;
+                } else if (z > top2) {
+                    top2 = z;
+                }
+                if (fabs(z) > amax) amax = fabs(z);
+            }
+            out_tok[(size_t)b * K + k] = best;
+            if (out_edge) out_edge[(size_t)b * K + k] = edge;
+            if (out_gap) out_gap[(size_t)b * K + k] = amax > 0 ? (top1 - top2) / amax : 0.0;
+            y = best;
+        }
+    }
+    free(x);
+    return ORC_OK;
+}

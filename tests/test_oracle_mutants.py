@@ -109,3 +109,32 @@ def test_calibration_pins_catch(oracle_mod, tmp_path, name):
         except AssertionError:
             failed += 1
     assert failed > 0, name
+
+
+MARKOV_MUTANTS = {
+    "correction subtracted": ("double z = bf16_value(L[row + v]) + c;",
+                              "double z = bf16_value(L[row + v]) - c;"),
+    "U and Vm swapped": ("for (int j = 0; j < r; j++) c += bf16_value(U[(size_t)v * r + j]) * x[j];",
+                         "for (int j = 0; j < r; j++) c += bf16_value(Vm[(size_t)v * r + j]) * bf16_value(U[(size_t)y * r + j]);"),
+    "previous token never advances": ("            y = best;\n", "            (void)best;\n"),
+    "argmax keeps the last tie": ("if (best < 0 || stored > bestv) {", "if (best < 0 || stored >= bestv) {"),
+    "rounding truncates": ("if (frac > 0.5 || (frac == 0.5 && fmod(lo, 2.0) != 0.0)) q = lo + 1.0;",
+                           "if (0) q = lo + 1.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MARKOV_MUTANTS))
+def test_markov_pins_catch(oracle_mod, tmp_path, name):
+    import test_oracle_markov as tm
+
+    old, new = MARKOV_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    failed = 0
+    for t in tm.PINS:
+        try:
+            t(lib)
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name
