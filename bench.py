@@ -52,10 +52,11 @@ def _peaks():
 
 
 def kernel_sha():
-    """Hash of the CUDA sources; ties a committed ncu summary to the kernel it measured."""
+    """Hash of the verify kernel's sources (its file and the shared header); ties a
+    committed ncu summary to the kernel it measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_79_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("sv_common.cuh", "sv_verify.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -539,6 +540,39 @@ def run_calib(args):
         print(json.dumps(res), flush=True)
 
 
+def run_markov(args):
+    """One JSON line per rank r: the Markov logit-bias drafting loop (K positions) at the
+    bench batch, timed per call inside a CUDA graph."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    peak, _ = _peaks()
+    B, K, V = args.B, args.K, args.V
+    for r in (128, 256):
+        inp = {k: v.to(dev) for k, v in synth.markov_inputs(B, K, V, r, seed=3).items()}
+        ws = sv.Workspace(B, K, 16, device=dev)
+        corr = torch.empty_like(inp["logits"])
+        tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+        keys = torch.empty(B * K, dtype=torch.int64, device=dev)
+        us = _graph_median_us(lambda: sv.sv_markov_draft(inp["logits"], inp["U"], inp["Vm"],
+                                                         inp["prev"], ws, corrected=corr,
+                                                         draft_tok=tok, keys=keys, stream=st),
+                              st, n=20)
+        if ws.status(stream=st) != sv.SV_OK:
+            raise RuntimeError("device status not OK in the Markov timing")
+        nbytes = K * 2 * B * V * 2 + V * r * 2  # logits in and out per position, U once
+        flops = K * 2.0 * V * r * B
+        print(json.dumps({"markov": True, "B": B, "K": K, "V": V, "r": r, "us": us,
+                          "us_per_position": us / K, "algorithmic_bytes": nbytes,
+                          "gbs": nbytes / (us / 1e6) / 1e9,
+                          "frac_hbm": nbytes / (us / 1e6) / 1e9 / peak,
+                          "tflops": flops / (us / 1e6) / 1e12,
+                          "timing": "median of 20 in-graph call events (K+2 launches each)"}),
+              flush=True)
+
+
 def run_once(args):
     """N untimed steps on one input set of the configured workload (for ncu captures)."""
     import torch
@@ -577,6 +611,8 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=30)
     ap.add_argument("--calib", action="store_true",
                     help="time the calibrated schedule and the calibration-loop kernels")
+    ap.add_argument("--markov", action="store_true",
+                    help="time the Markov logit-bias drafting loop")
     ap.add_argument("--once", type=int, default=0,
                     help="no timing: build one input set and run N schedule+verify steps "
                          "(a short, self-contained program for profilers)")
@@ -589,6 +625,8 @@ def main():
         run_sweep(args)
     elif args.calib:
         run_calib(args)
+    elif args.markov:
+        run_markov(args)
     else:
         run_gpu(args)
 

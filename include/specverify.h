@@ -59,6 +59,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_SCHED_B 8192   /* requests per schedule call */
 #define SV_MAX_SCHED_BK 16384 /* B*K per schedule call */
 #define SV_CALIB_BINS 10      /* equal-width confidence bins of the calibration error */
+#define SV_MAX_MARKOV_R 256   /* rank of the Markov logit-bias head */
 
 /*
  * sv_workspace_bytes: size of the device workspace needed by sv_schedule and
@@ -168,6 +169,34 @@ sv_status sv_calib_observe(const float *conf_cal_d, const int32_t *verify_len_d,
  */
 sv_status sv_calib_update(double *stats_d, float *temps_d, int K, float lr, float temp_floor,
                           double *ece_d, void *stream);
+
+/*
+ * sv_markov_draft: the drafter's Markov logit-bias head and greedy drafting loop
+ * [GD "1. The Markov Logit-Bias Head"; GD "Hands-On Implementation"]. For k = 0..K-1
+ * and every request b, with y_{-1} = prev_tok[b]:
+ *     L'_{b,k} = L_{b,k} + U (Vm[y_{k-1}, :])^T       (U, Vm: [V, r] low-rank factors)
+ *     y_k      = the lowest index of the largest value of L'_{b,k} (as stored)
+ *
+ *  logits_d    [B, K, V] bf16 raw logits of the parallel backbone.
+ *  U_d, Vm_d   [V, r] bf16, r a multiple of 16 in [16, SV_MAX_MARKOV_R].
+ *  prev_tok_d  [B] int32, the last token before the block (in [0, V)).
+ *  corrected_d [B, K, V] bf16 out: L' (the correction in fp32 on the tensor cores,
+ *              added to L in fp32 and rounded once to bf16); these are the draft
+ *              logits that sv_verify reads.
+ *  draft_tok_d [B, K] int32 out: y_k (-1 for a request whose prev_tok is invalid; its
+ *              corrected rows are then unspecified and SV_ERR_DEVICE_INPUT is set).
+ *  keys_d      [K * B] uint64 scratch (sv_markov_keys_len), overwritten.
+ *  ws_d        a workspace (its status word only; any size from sv_workspace_bytes).
+ *  K + 1 launches (one per position, then one that writes the tokens) after zeroing
+ *  keys_d; capturable in a CUDA graph. logits_d and corrected_d must be 16-byte
+ *  aligned, U_d and Vm_d too. Limits: 0 <= B <= SV_MAX_B, 1 <= K <= SV_MAX_K,
+ *  1 <= V <= SV_MAX_V.
+ */
+size_t sv_markov_keys_len(int B, int K); /* uint64 elements of keys_d; 0 if out of range */
+sv_status sv_markov_draft(const void *logits_d, const void *U_d, const void *Vm_d,
+                          const int32_t *prev_tok_d, int B, int K, int V, int r,
+                          void *corrected_d, int32_t *draft_tok_d, unsigned long long *keys_d,
+                          void *ws_d, size_t ws_bytes, void *stream);
 
 /*
  * sv_verify: standard speculative rejection sampling over a batch of drafted blocks.

@@ -58,6 +58,10 @@ def load(build_if_missing: bool = True):
     lib.sv_calib_observe.restype = i32
     lib.sv_calib_update.argtypes = [vp, vp, i32, f32, f32, vp, vp]
     lib.sv_calib_update.restype = i32
+    lib.sv_markov_keys_len.argtypes = [i32, i32]
+    lib.sv_markov_keys_len.restype = sz
+    lib.sv_markov_draft.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.sv_markov_draft.restype = i32
     lib.sv_verify.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
     lib.sv_verify.restype = i32
     lib.sv_verify_diag.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp,
@@ -203,6 +207,35 @@ def sv_calib_update(stats, temps, lr, temp_floor, ece=None, stream=None):
     _check("sv_calib_update", load_lib().sv_calib_update(
         _ptr(stats), _ptr(temps), K, float(lr), float(temp_floor), _ptr(ece), _stream(stream)))
     return ece
+
+
+def sv_markov_draft(logits, U, Vm, prev_tok, ws: Workspace, corrected=None, draft_tok=None,
+                    keys=None, stream=None):
+    """Markov logit-bias head + greedy drafting loop (see specverify.h). logits [B,K,V]
+    bf16, U and Vm [V,r] bf16, prev_tok [B] int32. Returns (corrected [B,K,V] bf16,
+    draft_tok [B,K] int32)."""
+    logits = _dev(logits, "logits", torch.bfloat16)
+    U = _dev(U, "U", torch.bfloat16)
+    Vm = _dev(Vm, "Vm", torch.bfloat16)
+    prev_tok = _dev(prev_tok, "prev_tok", torch.int32)
+    B, K, V = logits.shape
+    r = U.shape[1]
+    if tuple(U.shape) != (V, r) or tuple(Vm.shape) != (V, r):
+        raise ValueError("U and Vm must be [V, r]")
+    dev = logits.device
+    if corrected is None:
+        corrected = torch.empty_like(logits)
+    if draft_tok is None:
+        draft_tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if keys is None:
+        keys = torch.empty(max(1, B * K), dtype=torch.int64, device=dev)
+    _dev(corrected, "corrected", torch.bfloat16)
+    _dev(draft_tok, "draft_tok", torch.int32)
+    _dev(keys, "keys", torch.int64)
+    _check("sv_markov_draft", load_lib().sv_markov_draft(
+        _ptr(logits), _ptr(U), _ptr(Vm), _ptr(prev_tok), B, K, V, r, _ptr(corrected),
+        _ptr(draft_tok), _ptr(keys), _ptr(ws.t), ws.nbytes, _stream(stream)))
+    return corrected, draft_tok
 
 
 def _dtype_code(t):

@@ -69,6 +69,33 @@ sv_status sv_schedule(const float* conf_d, int B, int K, float tau, int token_bu
                          nullptr, nullptr, ws_d, ws_bytes, stream);
 }
 
+size_t sv_markov_keys_len(int B, int K) {
+  if (B < 0 || B > SV_MAX_B || K < 1 || K > SV_MAX_K) return 0;
+  return (size_t)B * K;
+}
+
+sv_status sv_markov_draft(const void* logits_d, const void* U_d, const void* Vm_d,
+                          const int32_t* prev_tok_d, int B, int K, int V, int r,
+                          void* corrected_d, int32_t* draft_tok_d, unsigned long long* keys_d,
+                          void* ws_d, size_t ws_bytes, void* stream) {
+  if (B < 0 || B > SV_MAX_B || K < 1 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_SHAPE;
+  if (r < 16 || r > SV_MAX_MARKOV_R || r % 16 != 0) return SV_ERR_SHAPE;
+  if (!ws_d || ws_bytes < sizeof(WsHeader) || !aligned(ws_d, 256)) return SV_ERR_WORKSPACE;
+  if (B == 0) return SV_OK;
+  if (!logits_d || !U_d || !Vm_d || !prev_tok_d || !corrected_d || !draft_tok_d || !keys_d)
+    return SV_ERR_ARG;
+  if (!aligned(logits_d, 16) || !aligned(U_d, 16) || !aligned(Vm_d, 16) ||
+      !aligned(corrected_d, 16) || !aligned(prev_tok_d, 4) || !aligned(draft_tok_d, 4) ||
+      !aligned(keys_d, 8))
+    return SV_ERR_ARG;
+  const cudaError_t e = launch_markov(
+      static_cast<const uint16_t*>(logits_d), static_cast<const uint16_t*>(U_d),
+      static_cast<const uint16_t*>(Vm_d), prev_tok_d, B, K, V, r,
+      static_cast<uint16_t*>(corrected_d), draft_tok_d, keys_d, static_cast<WsHeader*>(ws_d),
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 size_t sv_calib_stats_len(int K) {
   if (K < 1 || K > SV_MAX_K) return 0;
   return 3 * (size_t)K + 3 * (size_t)SV_CALIB_BINS;

@@ -200,3 +200,17 @@ def calib_round(B, K, *, seed=0):
     acc = np.array([rng.integers(0, v + 1) for v in vlen], np.int32)
     acc[rng.random(B) < 0.05] = -1
     return torch.from_numpy(c), torch.from_numpy(vlen), torch.from_numpy(acc)
+
+
+
+def markov_inputs(B, K, V, r, *, seed=0, logit_sigma=3.0):
+    """Drafting-side inputs: raw logits [B,K,V] ~ N(0, logit_sigma^2) and low-rank factors
+    U, Vm [V,r] ~ N(0, r^-1/2) (so a correction U Vm[y]^T is of order 1), all bf16, and
+    previous tokens [B] ~ U{0..V-1}."""
+    g = torch.Generator().manual_seed(int(seed))
+    L = (torch.randn((B, K, V), generator=g) * logit_sigma).to(torch.bfloat16)
+    s = float(r) ** -0.25
+    U = (torch.randn((V, r), generator=g) * s).to(torch.bfloat16)
+    Vm = (torch.randn((V, r), generator=g) * s).to(torch.bfloat16)
+    prev = torch.randint(0, V, (B,), generator=g, dtype=torch.int32)
+    return {"logits": L, "U": U, "Vm": Vm, "prev": prev}

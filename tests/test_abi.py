@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     names = _declared()
     for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
               "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version",
-              "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update"):
+              "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update",
+              "sv_markov_keys_len", "sv_markov_draft"):
         assert n in names
 
 
@@ -125,3 +126,20 @@ def test_calibration_host_checks(lib):
     assert lib.sv_calib_update(fake, fake, 4, float("inf"), 0.05, None, None) == sv.SV_ERR_ARG
     assert lib.sv_calib_update(fake, None, 4, 0.01, 0.05, None, None) == sv.SV_ERR_ARG
     assert lib.sv_calib_update(fake, fake, 40, 0.01, 0.05, None, None) == sv.SV_ERR_SHAPE
+
+
+def test_markov_host_checks(lib):
+    import speculative_decoding_verification_79_gb300 as sv
+
+    fake = ctypes.c_void_p(256)
+    n = lib.sv_workspace_bytes(4, 4, 100)
+    args = lambda B=4, K=4, V=100, r=64, lg=fake, ws=fake: (  # noqa: E731
+        lg, fake, fake, fake, B, K, V, r, fake, fake, fake, ws, n, None)
+    assert lib.sv_markov_keys_len(64, 8) == 512 and lib.sv_markov_keys_len(64, 0) == 0
+    assert lib.sv_markov_draft(*args(r=24)) == sv.SV_ERR_SHAPE
+    assert lib.sv_markov_draft(*args(r=512)) == sv.SV_ERR_SHAPE
+    assert lib.sv_markov_draft(*args(K=0)) == sv.SV_ERR_SHAPE
+    assert lib.sv_markov_draft(*args(ws=None)) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_markov_draft(*args(lg=None)) == sv.SV_ERR_ARG
+    assert lib.sv_markov_draft(*args(lg=ctypes.c_void_p(264))) == sv.SV_ERR_ARG
+    assert lib.sv_markov_draft(*args(B=0)) == sv.SV_OK
