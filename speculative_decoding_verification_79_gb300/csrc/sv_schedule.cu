@@ -79,57 +79,73 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   __shared__ unsigned long long s_total;
   __shared__ float s_temps[SV_MAX_K];
   __shared__ double s_tau;
-  __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // 0. Threshold (load-aware or as given) and the position temperatures.
-  if (tid == 0) {
-    double th = static_cast<double>(A.tau);
-    int bad = 0;
-    if (A.load) {
-      th = load_tau(A.load, static_cast<double>(A.tau_min), static_cast<double>(A.tau_max));
-      bad = th < 0.0;
-    }
-    if (A.tau_out) *A.tau_out = th;
-    s_tau = th;
-    s_bad = bad;
-  }
-  __syncthreads();
-  if (A.temps && tid < K) {
-    const float t = __ldg(A.temps + tid);
-    s_temps[tid] = t;
-    if (!(isfinite(t) && t > 0.f)) s_bad = 1;
-  }
-  __syncthreads();
-
-  // 0b. Each confidence (calibrated when temperatures are given) into S, one
-  // element per thread.
-  bool bad = s_bad != 0;
+  // 0. Threshold (as given, or from the load state by thread 0) and the position
+  // temperatures; barriers only when either is in use.
   const bool cal = A.temps != nullptr;
-  for (int i = tid; i < N; i += SCHED_THREADS) {
-    float c = __ldg(A.conf + i);
-    if (!(c >= 0.f && c <= 1.f)) bad = true;
-    if (cal) c = calibrate(c, s_temps[i % K]);
-    if (A.conf_cal) A.conf_cal[i] = c;
-    S[i] = static_cast<double>(c);
+  double th = static_cast<double>(A.tau);
+  bool bad = false;
+  if (A.load || cal) {
+    int mine = 0;
+    if (A.load && tid == 0) {
+      const double t = load_tau(A.load, static_cast<double>(A.tau_min),
+                                static_cast<double>(A.tau_max));
+      s_tau = t;
+      mine = t < 0.0;
+    }
+    if (cal && tid < K) {
+      const float t = __ldg(A.temps + tid);
+      s_temps[tid] = t;
+      mine |= !(isfinite(t) && t > 0.f);
+    }
+    bad = __syncthreads_or(mine) != 0;
+    if (A.load) th = s_tau;
+    if (cal) {
+      // 0b. Calibrated confidences into S, one element per thread.
+      for (int i = tid; i < N; i += SCHED_THREADS) {
+        const float c0 = __ldg(A.conf + i);
+        if (!(c0 >= 0.f && c0 <= 1.f)) bad = true;
+        const float c = calibrate(c0, s_temps[i % K]);
+        if (A.conf_cal) A.conf_cal[i] = c;
+        S[i] = static_cast<double>(c);
+      }
+      __syncthreads();
+    }
   }
-  __syncthreads();
-  // 1-2. survival products and tau-lengths, one thread per request; S >= 0 compares
-  // with tau as 64-bit patterns, keeping the slow fp64 pipe to the products alone.
-  const unsigned long long tau_key = surv_key(s_tau < 0.0 ? 0.0 : s_tau);
+  if (tid == 0 && A.tau_out) *A.tau_out = th;
+
+  // 1-2. survival products and tau-lengths, one thread per request; the row of
+  // confidences is loaded up front (independent loads), and S >= 0 compares with tau
+  // as 64-bit patterns, keeping the slow fp64 pipe to the products alone.
+  const unsigned long long tau_key = surv_key(th < 0.0 ? 0.0 : th);
   unsigned long long my_total = 0;
   for (int b = tid; b < B; b += SCHED_THREADS) {
-    double cv[SV_MAX_K];
-#pragma unroll
-    for (int k = 0; k < SV_MAX_K; ++k) cv[k] = (k < K) ? S[(size_t)b * K + k] : 0.0;
     double run = 1.0;
     int n = 0;
+    if (cal) {  // calibrated confidences are in S already
 #pragma unroll
-    for (int k = 0; k < SV_MAX_K; ++k) {
-      if (k < K) {
-        run = run * cv[k];
-        S[(size_t)b * K + k] = run;
-        if (surv_key(run) >= tau_key) n = k + 1;
+      for (int k = 0; k < SV_MAX_K; ++k) {
+        if (k < K) {
+          run = run * S[(size_t)b * K + k];
+          S[(size_t)b * K + k] = run;
+          if (surv_key(run) >= tau_key) n = k + 1;
+        }
+      }
+    } else {
+      float cv[SV_MAX_K];
+#pragma unroll
+      for (int k = 0; k < SV_MAX_K; ++k) cv[k] = (k < K) ? __ldg(A.conf + (size_t)b * K + k) : 0.f;
+#pragma unroll
+      for (int k = 0; k < SV_MAX_K; ++k) {
+        if (k < K) {
+          const float c = cv[k];
+          if (!(c >= 0.f && c <= 1.f)) bad = true;
+          if (A.conf_cal) A.conf_cal[(size_t)b * K + k] = c;
+          run = run * static_cast<double>(c);
+          S[(size_t)b * K + k] = run;
+          if (surv_key(run) >= tau_key) n = k + 1;
+        }
       }
     }
     if (n < 1) n = 1;
