@@ -573,6 +573,23 @@ def run_markov(args):
               flush=True)
 
 
+def run_markov_once(args):
+    """N untimed calls of the Markov drafting loop at rank 256 (for ncu captures)."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    inp = {k: v.to(dev) for k, v in synth.markov_inputs(args.B, args.K, args.V, 256, seed=3).items()}
+    ws = sv.Workspace(args.B, args.K, 16, device=dev)
+    for _ in range(args.once):
+        sv.sv_markov_draft(inp["logits"], inp["U"], inp["Vm"], inp["prev"], ws)
+    torch.cuda.synchronize()
+    status = ws.status()
+    print(json.dumps({"markov_once": args.once, "status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def run_once(args):
     """N untimed steps on one input set of the configured workload (for ncu captures)."""
     import torch
@@ -619,6 +636,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.once > 0 and args.markov:
+        run_markov_once(args)
     elif args.once > 0:
         run_once(args)
     elif args.sweep:
