@@ -12,8 +12,9 @@
 // contraction, done on the tensor cores (bf16 inputs, fp32 accumulation) by
 // mma.sync.m16n8k16. A CTA owns 128 vocabulary rows and up to 64 requests: it copies
 // its U tile (kept in L2 across positions: evict_last) and the 64 gathered rows of Vm
-// into shared memory with cp.async, multiplies (8 warps x 16 rows x 64 columns), adds
-// the raw logits, rounds once to bf16, writes the corrected tile, and folds the tile's
+// into shared memory with cp.async while each thread loads the raw logits of its own
+// accumulator elements into registers, multiplies (8 warps x 16 rows x 64 columns),
+// adds, rounds once to bf16 and stores from the registers, and folds the tile's
 // argmax of each request into a 64-bit key per (position, request) with atomicMax:
 // key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v), so the
 // largest value wins and, among equal values, the lowest index; max is order-free,
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(MK_THREADS, 2) sv_markov_step_kernel(const Mar
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int v0 = blockIdx.x * MK_ROWS, b0 = blockIdx.y * MK_COLS;
   const int nrows = min(MK_ROWS, A.V - v0), ncols = min(MK_COLS, A.B - b0);
-  const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+  const uint64_t keep = policy_evict_last();
   const int cpr = r / 8;  // 16-byte chunks per row of U / Vm
 
   // Copies: the U tile and the gathered rows of Vm (zero rows past the ends).
@@ -120,6 +121,22 @@ __global__ void __launch_bounds__(MK_THREADS, 2) sv_markov_step_kernel(const Mar
     else
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
+  // The raw logits of this thread's accumulator elements, straight into registers
+  // (their latency overlaps the copies above and the product below): element (n, e)
+  // is row 16w + g (+8 for e >= 2), column 8n + 2t (+1 for odd e).
+  const int g = lane >> 2, tq = lane & 3;
+  const size_t KV = (size_t)A.K * A.V;
+  uint16_t lraw[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = 16 * w + g + ((e & 2) ? 8 : 0), col = 8 * n + 2 * tq + (e & 1);
+      lraw[n][e] = (row < nrows && col < ncols)
+                       ? __ldcs(A.L + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + row)
+                       : static_cast<uint16_t>(0);
+    }
+  }
   cp_async_wait_all();
   __syncthreads();
 
@@ -139,69 +156,41 @@ __global__ void __launch_bounds__(MK_THREADS, 2) sv_markov_step_kernel(const Mar
       mma_bf16(acc[n], a0, a1, a2, a3, b0r, b1r);
     }
   }
-  __syncthreads();  // Us is free: it becomes the output tile
 
-  // Output tile O[col][row] (bf16) in the space of Us: raw logits in, corrected out.
-  constexpr int OS = MK_ROWS + MK_PAD;
-  uint16_t* O = Us;
-  const size_t KV = (size_t)A.K * A.V;
-  const bool vec = (A.V % 8) == 0;  // rows start on 16-byte boundaries
-  for (int i = tid; i < MK_COLS * (MK_ROWS / 8); i += MK_THREADS) {
-    const int col = i / (MK_ROWS / 8), c = i - col * (MK_ROWS / 8);
-    uint16_t* dst = O + (size_t)col * OS + c * 8;
-    if (col >= ncols) continue;
-    const uint16_t* src = A.L + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + c * 8;
-    if (vec && c * 8 + 8 <= nrows) {
-      cp_async16(dst, src, once);
-    } else {
-      for (int e = 0; e < 8; ++e) dst[e] = (c * 8 + e < nrows) ? src[e] : 0;
-    }
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  {
-    const int g = lane >> 2, t = lane & 3;
+  // Raw logits + correction, rounded once to bf16, stored from the registers; each
+  // column's best key over the warp's 16 rows, then over the 8 warps in shared memory.
+  __shared__ unsigned long long red[MK_WARPS][MK_COLS];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < 8; ++n) {
+    unsigned long long kb[2] = {0ull, 0ull};  // columns 8n + 2t and 8n + 2t + 1
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = 16 * w + g + ((q & 2) ? 8 : 0);
-        const int col = 8 * n + 2 * t + (q & 1);
-        uint16_t* p = O + (size_t)col * OS + row;
-        const float z = __fadd_rn(bf2f(*p), acc[n][q]);
-        *p = __bfloat16_as_ushort(__float2bfloat16_rn(z));
-      }
-    }
-  }
-  __syncthreads();
-  // Corrected tile out, and each column's argmax over the tile's rows.
-  for (int i = tid; i < MK_COLS * (MK_ROWS / 8); i += MK_THREADS) {
-    const int col = i / (MK_ROWS / 8), c = i - col * (MK_ROWS / 8);
-    if (col >= ncols) continue;
-    const uint16_t* src = O + (size_t)col * OS + c * 8;
-    uint16_t* dst = A.out + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + c * 8;
-    if (vec && c * 8 + 8 <= nrows) {
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-    } else {
-      for (int e = 0; e < 8 && c * 8 + e < nrows; ++e) dst[e] = src[e];
-    }
-  }
-  for (int col = w; col < MK_COLS; col += MK_WARPS) {
-    unsigned long long best = 0ull;
-    if (col < ncols) {
-      for (int row = lane; row < nrows; row += 32) {
-        const uint16_t h = O[(size_t)col * OS + row];
+    for (int e = 0; e < 4; ++e) {
+      const int row = 16 * w + g + ((e & 2) ? 8 : 0), col = 8 * n + 2 * tq + (e & 1);
+      const uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf2f(lraw[n][e]), acc[n][e])));
+      if (row < nrows && col < ncols) {
+        __stcs(A.out + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + row, h);
         const unsigned long long key = (static_cast<unsigned long long>(bf_order(h)) << 32) |
                                        static_cast<unsigned long long>(0xffffffffu - (uint32_t)(v0 + row));
-        best = key > best ? key : best;
+        kb[e & 1] = key > kb[e & 1] ? key : kb[e & 1];
       }
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-      best = y > best ? y : best;
+    for (int c = 0; c < 2; ++c) {
+      unsigned long long m = kb[c];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {  // over g: lanes with the same t hold the same column
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, m, o);
+        m = y > m ? y : m;
+      }
+      if (g == 0) red[w][8 * n + 2 * tq + c] = m;
     }
-    if (lane == 0 && col < ncols && best) atomicMax(A.keys + (size_t)A.k * A.B + b0 + col, best);
+  }
+  __syncthreads();
+  if (tid < MK_COLS && tid < ncols) {
+    unsigned long long m = 0ull;
+#pragma unroll
+    for (int q = 0; q < MK_WARPS; ++q) m = red[q][tid] > m ? red[q][tid] : m;
+    if (m) atomicMax(A.keys + (size_t)A.k * A.B + b0 + tid, m);
   }
 }
 
@@ -219,13 +208,8 @@ __global__ void sv_markov_finish_kernel(const MarkovArgs A) {
   }
 }
 
-// The U and Vm tiles, or the output tile that reuses their space after the product,
-// whichever is larger (for small ranks the output tile is).
-size_t markov_smem_bytes(int r) {
-  const size_t tiles = (size_t)(MK_ROWS + MK_COLS) * (r + MK_PAD) * 2;
-  const size_t out = (size_t)MK_COLS * (MK_ROWS + MK_PAD) * 2;
-  return tiles > out ? tiles : out;
-}
+// The U tile and the gathered Vm rows.
+size_t markov_smem_bytes(int r) { return (size_t)(MK_ROWS + MK_COLS) * (r + MK_PAD) * 2; }
 
 cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* Vm,
                           const int32_t* prev, int B, int K, int V, int r, uint16_t* out,
