@@ -399,6 +399,24 @@ __device__ u64 take_word(const VerifyArgs& A, u64* p) {
   return w;
 }
 
+// A published word that stays in place for several readers (job words): waits
+// (bounded) until it is visible.
+__device__ u64 wait_word(const VerifyArgs& A, const u64* p) {
+  u64 w = ld_word(p);
+  if (w == 0) {
+    const long long t0 = clock64();
+    while ((w = ld_word(p)) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return 0;
+      if (clock64() - t0 > WAIT_CYCLES) {
+        raise_status(A, ST_TIMEOUT);
+        return 0;
+      }
+      __nanosleep(32);
+    }
+  }
+  return w;
+}
+
 // Bounded wait on an mbarrier phase; false on abort or timeout.
 __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const VerifyArgs& A) {
   const long long t0 = clock64();
@@ -435,7 +453,6 @@ __device__ void emit_invalid(const VerifyArgs& A, int b, int lane) {
     for (int k = lane; k < A.K; k += 32) A.out_q[(size_t)b * A.K + k] = nan;
   if (lane == 0) {
     A.out_acc[b] = -1;
-    A.jobs[b].kind = J_NONE;
     raise_status(A, ST_DEVICE_INPUT);
     st_release(A.dec_flag + b, 2u);  // decided, no terminal sample
   }
@@ -535,9 +552,14 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
       J.MAd = jMdd;
       J.invSd = jSd;
     }
-    J.pad[0] = J.pad[1] = 0;
-    A.jobs[b] = J;
-    st_release(A.dec_flag + b, 1u);  // the job is published
+    // The job's frames travel as two published words and its kind and row in the flag
+    // itself (1 | bonus << 2 | (row + 1) << 8), so neither side needs a fence.
+    u64* jw = reinterpret_cast<u64*>(A.jobs + b);
+    st_word(jw, enc_pair(J.MAt, __float_as_uint(J.invSt)));
+    st_word(jw + 1, enc_pair(J.MAd, __float_as_uint(J.invSd)));
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(A.dec_flag + b),
+                 "r"(1u | (J.kind == J_BONUS ? 4u : 0u) | (static_cast<uint32_t>(j + 1) << 8))
+                 : "memory");
   }
   // The terminal rows are read again shortly by the terminal tasks: start fetching
   // them into L2 now.
@@ -579,10 +601,7 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = nan;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
-  if (lane == 0) {
-    A.out_acc[b] = j;
-    A.jobs[b].kind = J_NONE;
-  }
+  if (lane == 0) A.out_acc[b] = j;
 }
 
 // Per-lane running state of a row segment: (m, ma = fl(m*a), s) at T > 0, or
@@ -1359,20 +1378,19 @@ __device__ int refill(const VerifyArgs& A, Issuer& I, const int* prefix, bool fr
         }
         if (f == 0) break;
         fresh = true;  // a later request's flag has not been read yet
-        if (f != 1) {  // the request has no terminal sample: skip its tasks
+        if ((f & 3u) != 1u) {  // the request has no terminal sample: skip its tasks
           I.tt = min(I.te, (long long)(b + 1) * A.R);
           continue;
         }
-        if (!acq) fence_acq_rel();  // the job record was published before the flag
-        acq = false;
-        const int4 j0 = __ldcg(reinterpret_cast<const int4*>(A.jobs + b));
-        const int4 j1 = __ldcg(reinterpret_cast<const int4*>(A.jobs + b) + 1);
-        I.J.kind = j0.x;
-        I.J.j = j0.y;
-        I.J.MAt = __int_as_float(j0.z);
-        I.J.invSt = __int_as_float(j0.w);
-        I.J.MAd = __int_as_float(j1.x);
-        I.J.invSd = __int_as_float(j1.y);
+        (void)acq;
+        const u64* jw = reinterpret_cast<const u64*>(A.jobs + b);
+        const u64 w1 = wait_word(A, jw), w2 = wait_word(A, jw + 1);
+        I.J.kind = (f & 4u) ? J_BONUS : J_RESID;
+        I.J.j = static_cast<int>(f >> 8) - 1;
+        I.J.MAt = dec_x(w1);
+        I.J.invSt = __uint_as_float(dec_y(w1));
+        I.J.MAd = dec_x(w2);
+        I.J.invSd = __uint_as_float(dec_y(w2));
         I.jb = b;
       }
       issue_term<T>(A, b, static_cast<int>(I.tt - (long long)b * A.R), I.J, meta, full, slot);
@@ -1402,7 +1420,7 @@ __device__ bool wait_decided(const VerifyArgs& A, Shared& S, Issuer& I) {
   // Every idle warp of the grid may be polling: back off between polls so that the
   // flags' and the status word's cache lines stay free for the warps still working.
   uint32_t f;
-  for (unsigned it = 1; (f = ld_acquire(A.dec_flag + b)) == 0; ++it) {
+  for (unsigned it = 1; (f = ld_relaxed(A.dec_flag + b)) == 0; ++it) {
     __nanosleep(256);
     if ((it & 15) != 0) continue;
     if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
@@ -1688,7 +1706,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
         A.t_res[i] = 0;
       }
     }
-    for (int i = tid; i < B; i += NTHREADS) A.dec_flag[i] = 0;
+    for (int i = tid; i < B; i += NTHREADS) {
+      A.dec_flag[i] = 0;
+      reinterpret_cast<u64*>(A.jobs + i)[0] = 0ull;
+      reinterpret_cast<u64*>(A.jobs + i)[1] = 0ull;
+    }
     if (tid == 0) A.hdr->cta_done = 0;
   }
 }
