@@ -42,6 +42,21 @@ def _rank():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over the ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the max-over-ranks time
+    (each rank is a replica that processes its own batch: weak scaling)."""
+    return units_per_step * steps * world / (elapsed_ms / 1e3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -213,11 +228,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     clocks = clk.summary()
     try:
         ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -238,7 +249,7 @@ def run_gpu(args):
     L = out_len.cpu()
     tokens_per_step = int(L.sum().item())
     bytes_per_launch = synth.logit_bytes(L, V, 2, greedy=(T == 0.0))
-    value = tokens_per_step * args.steps * world / (elapsed_ms / 1e3)
+    value = job_rate(tokens_per_step, args.steps, world, elapsed_ms)
     ver_avg = sum(ver_ms) / len(ver_ms)
     peak, peak_kind = _peaks()
     achieved = bytes_per_launch / (ver_avg / 1e3) / 1e9
@@ -257,7 +268,7 @@ def run_gpu(args):
                    "l2": "inputs larger than L2: two alternating input sets of "
                          f"{bytes_per_launch / 1e6:.0f} MB each (L2 129 MB)",
                    "timing": f"CUDA graph of {n_graph} steps replayed; CUDA events"},
-        "logit_gbs": bytes_per_launch * args.steps * world / (elapsed_ms / 1e3) / 1e9,
+        "logit_gbs": job_rate(bytes_per_launch, args.steps, world, elapsed_ms) / 1e9,
         "verify_us_avg": ver_avg * 1e3, "schedule_us_avg": sum(sch_ms) / len(sch_ms) * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
