@@ -85,6 +85,10 @@ def _bind(path):
     lib.oracle_markov_draft.argtypes = [vp, vp, vp, i32p, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, vp, i32p, f64p, f64p]
     lib.oracle_markov_draft.restype = ctypes.c_int
+    lib.oracle_schedule_curve.argtypes = [f32p, f32p, f32p, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float, f32p, f32p, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_longlong, i32p, i32p, f64p]
+    lib.oracle_schedule_curve.restype = ctypes.c_int
     return lib
 
 
@@ -188,6 +192,25 @@ def calib_update(stats, temps, lr: float, temp_floor: float, lib=None):
     rc = (lib or _load()).oracle_calib_update(_ptr(stats), _ptr(temps), temps.size, float(lr),
                                               float(temp_floor), _ptr(ece))
     return rc, float(ece[0])
+
+
+def schedule_curve(conf, temps, load, tau, tau_min, tau_max, curve_x, curve_y, token_budget,
+                   lib=None):
+    """Schedule whose budget is chosen from a throughput curve (curve_x ascending tokens,
+    curve_y tokens/s). Returns dict(out_len, n, g, status)."""
+    conf = np.ascontiguousarray(conf, dtype=np.float32)
+    B, K = conf.shape
+    t = None if temps is None else np.ascontiguousarray(temps, dtype=np.float32)
+    ld = None if load is None else np.ascontiguousarray(load, dtype=np.float32)
+    cx = np.ascontiguousarray(curve_x, dtype=np.float32)
+    cy = np.ascontiguousarray(curve_y, dtype=np.float32)
+    out_len = np.zeros(B, np.int32)
+    n = np.zeros(1, np.int32)
+    g = np.zeros(1, np.float64)
+    rc = (lib or _load()).oracle_schedule_curve(
+        _ptr(conf), _ptr(t), _ptr(ld), float(tau), float(tau_min), float(tau_max), _ptr(cx),
+        _ptr(cy), cx.size, B, K, int(token_budget), _ptr(out_len), _ptr(n), _ptr(g))
+    return {"out_len": out_len, "n": int(n[0]), "g": float(g[0]), "status": rc}
 
 
 def markov_draft(logits, U, Vm, prev, lib=None):

@@ -717,3 +717,101 @@ int oracle_markov_draft(const uint16_t *L, const uint16_t *U, const uint16_t *Vm
     free(x);
     return ORC_OK;
 }
+
+/* ======================================================================== */
+/* Throughput-curve scheduling                                               */
+/* ======================================================================== */
+
+/* The throughput curve at x tokens: linear between its points (x ascending), flat
+ * beyond its first and last points. */
+static double curve_at(const float *cx, const float *cy, int n, double x) {
+    if (x <= (double)cx[0]) return (double)cy[0];
+    for (int i = 1; i < n; i++) {
+        if (x <= (double)cx[i]) {
+            double x0 = cx[i - 1], x1 = cx[i], y0 = cy[i - 1], y1 = cy[i];
+            return y0 + (y1 - y0) * ((x - x0) / (x1 - x0));
+        }
+    }
+    return (double)cy[n - 1];
+}
+
+static int desc_double(const void *pa, const void *pb) {
+    double a = *(const double *)pa, b = *(const double *)pb;
+    return (a < b) - (a > b);
+}
+
+/*
+ * oracle_schedule_curve: the verify budget chosen from a throughput curve
+ * [DD "The Throughput Curve", "The Optimization Logic"]. Reading: a verified token of
+ * survival S adds S expected accepted tokens; a step of B requests verifying N drafted
+ * tokens runs B + N tokens through the target at T(B + N) tokens/s (the curve) and
+ * emits B + A(N) tokens on average, A(N) the sum of the survivals of the N positions
+ * kept (the best N in the budget-trim order). The budget is the smallest N maximising
+ * the goodput G(N) = (B + A(N)) * T(B + N) / (B + N) over N_lo <= N <= N_hi, with
+ * N_hi = min(sum L0, token_budget) and N_lo = B when token_budget >= B (each request
+ * keeps its floor position), else 0; then the trim of oracle_schedule runs with it.
+ * At small batches, where T grows with the batch, adding a token raises G and every
+ * tau-survivor is verified; where T is flat, low-survival tokens lower it.
+ *
+ * conf/temps/load/tau...: as oracle_schedule_ex. curve_x [n_pts] ascending (tokens),
+ * curve_y [n_pts] > 0 (tokens/s), float32. out_n: the chosen N; out_g: G(N).
+ * Returns ORC_ERR_INPUT for an invalid curve (n_pts < 1, x not strictly ascending,
+ * y <= 0 or not finite) as for the other device inputs.
+ */
+int oracle_schedule_curve(const float *conf, const float *temps, const float *load, float tau,
+                          float tau_min, float tau_max, const float *curve_x,
+                          const float *curve_y, int n_pts, int B, int K, long long token_budget,
+                          int32_t *out_len, int32_t *out_n, double *out_g) {
+    if (B < 0 || K < 1 || token_budget < 0 || n_pts < 1) return ORC_ERR_ARG;
+    int bad = 0;
+    for (int i = 0; i < n_pts; i++) {
+        if (!(isfinite(curve_x[i]) && isfinite(curve_y[i]) && curve_y[i] > 0.0f)) bad = 1;
+        if (i > 0 && !(curve_x[i] > curve_x[i - 1])) bad = 1;
+    }
+    for (int b = 0; b < B; b++) out_len[b] = 0;
+    if (bad) return ORC_ERR_INPUT;
+    double *S = (double *)malloc(sizeof(double) * ((size_t)B * K + 1));
+    int32_t *L0 = (int32_t *)malloc(sizeof(int32_t) * ((size_t)B + 1));
+    int rc = oracle_schedule_ex(conf, temps, load, tau, tau_min, tau_max, B, K, (long long)B * K,
+                                out_len, S, L0, NULL, NULL);
+    if (rc != ORC_OK || B == 0) {
+        free(S);
+        free(L0);
+        return rc;
+    }
+    long long total = 0;
+    for (int b = 0; b < B; b++) total += L0[b];
+    long long n_hi = total < token_budget ? total : token_budget;
+    int floors = token_budget >= B;
+    long long n_lo = floors ? B : 0;
+    /* competing survivals, descending (ties in any order: only their sum matters) */
+    double *c = (double *)malloc(sizeof(double) * ((size_t)B * K + 1));
+    size_t nc = 0;
+    double a_floor = 0.0;
+    for (int b = 0; b < B; b++)
+        for (int k = 0; k < L0[b]; k++) {
+            double s = S[(size_t)b * K + k];
+            if (floors && k == 0) a_floor += s;
+            else c[nc++] = s;
+        }
+    qsort(c, nc, sizeof(double), desc_double);
+    double best_g = -1.0, a = a_floor;
+    long long best_n = n_lo;
+    for (long long n = n_lo; n <= n_hi; n++) {
+        if (n > n_lo) a += c[n - n_lo - 1];
+        double x = (double)B + (double)n;
+        double g = ((double)B + a) * curve_at(curve_x, curve_y, n_pts, x) / x;
+        if (g > best_g) {
+            best_g = g;
+            best_n = n;
+        }
+    }
+    if (out_n) *out_n = (int32_t)best_n;
+    if (out_g) *out_g = best_g;
+    rc = oracle_schedule_ex(conf, temps, load, tau, tau_min, tau_max, B, K, best_n, out_len, NULL,
+                            NULL, NULL, NULL);
+    free(c);
+    free(S);
+    free(L0);
+    return rc;
+}

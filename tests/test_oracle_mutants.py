@@ -138,3 +138,32 @@ def test_markov_pins_catch(oracle_mod, tmp_path, name):
         except AssertionError:
             failed += 1
     assert failed > 0, name
+
+
+CURVE_MUTANTS = {
+    "step time ignores the batch size": (
+        "double g = ((double)B + a) * curve_at(curve_x, curve_y, n_pts, x) / x;",
+        "double g = ((double)B + a) * curve_at(curve_x, curve_y, n_pts, x);"),
+    "floor survivals left out": ("if (floors && k == 0) a_floor += s;",
+                                 "if (floors && k == 0) a_floor += 0.0;"),
+    "interpolation from the wrong end": ("return y0 + (y1 - y0) * ((x - x0) / (x1 - x0));",
+                                         "return y1 + (y0 - y1) * ((x - x0) / (x1 - x0));"),
+    "competing survivals ascending": ("return (a < b) - (a > b);", "return (a > b) - (a < b);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CURVE_MUTANTS))
+def test_curve_pins_catch(oracle_mod, tmp_path, name):
+    import test_oracle_curve as tc
+
+    old, new = CURVE_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    failed = 0
+    for t in tc.PINS:
+        try:
+            t(lib)
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name
