@@ -541,6 +541,11 @@ def run_calib(args):
         res["schedule_cal_us"] = _graph_median_us(
             lambda: sv.sv_schedule_cal(conf, temps, load, 0.3, 0.2, 0.75, budget, ws,
                                        out_len=out_len, conf_cal=cal, tau_out=tau, stream=st), st)
+        if B * K <= 8192:
+            curve = synth.throughput_curve(8, seed=1).to(dev)
+            res["schedule_curve_us"] = _graph_median_us(
+                lambda: sv.sv_schedule_curve(conf, temps, load, 0.3, 0.2, 0.75, curve, budget, ws,
+                                             out_len=out_len, stream=st), st)
         res["observe_us"] = _graph_median_us(
             lambda: sv.sv_calib_observe(c, vl, acc, stats, stream=st), st)
         res["update_us"] = _graph_median_us(

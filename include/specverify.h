@@ -60,6 +60,8 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_SCHED_BK 16384 /* B*K per schedule call */
 #define SV_CALIB_BINS 10      /* equal-width confidence bins of the calibration error */
 #define SV_MAX_MARKOV_R 256   /* rank of the Markov logit-bias head */
+#define SV_MAX_CURVE 64       /* points of a throughput curve */
+#define SV_MAX_CURVE_BK 8192  /* B*K of a throughput-curve schedule */
 
 /*
  * sv_workspace_bytes: size of the device workspace needed by sv_schedule and
@@ -131,6 +133,30 @@ sv_status sv_schedule_cal(const float *conf_d, const float *temps_d, const float
                           float tau, float tau_min, float tau_max, int B, int K,
                           int token_budget, int32_t *out_len_d, float *conf_cal_d,
                           double *tau_out_d, void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_schedule_curve: sv_schedule_cal whose budget is chosen from the target's
+ * throughput curve [DD "The Throughput Curve", "The Optimization Logic"].
+ *
+ *  curve_d  [2 * n_pts] float32: batch sizes in tokens (strictly ascending), then the
+ *           tokens/s at each (> 0); linear between points, flat beyond the ends.
+ *  n_pts    1 <= n_pts <= SV_MAX_CURVE.
+ *  n_out_d  [1] int32 out (or NULL): the chosen budget N; g_out_d [1] float64 out (or
+ *           NULL): its goodput.
+ *  A verified token of survival S adds S expected accepted tokens; a step verifying N
+ *  drafted tokens of B requests runs B + N tokens at T(B + N) tokens/s and emits
+ *  B + A(N) on average, A(N) the sum of the survivals kept (the best N in the trim
+ *  order). N is the smallest value maximising (B + A(N)) T(B + N) / (B + N) between
+ *  N_lo = B (0 when token_budget < B) and min(sum L0, token_budget), all in float64;
+ *  the trim of sv_schedule then runs with budget N. Limits: as sv_schedule, and
+ *  B * K <= SV_MAX_CURVE_BK. An invalid curve is a device error (SV_ERR_DEVICE_INPUT,
+ *  out_len = 0).
+ */
+sv_status sv_schedule_curve(const float *conf_d, const float *temps_d, const float *load_d,
+                            float tau, float tau_min, float tau_max, const float *curve_d,
+                            int n_pts, int B, int K, int token_budget, int32_t *out_len_d,
+                            float *conf_cal_d, double *tau_out_d, int32_t *n_out_d,
+                            double *g_out_d, void *ws_d, size_t ws_bytes, void *stream);
 
 /*
  * Online calibration loop [DD "The Calibration Loop in Practice", "Online

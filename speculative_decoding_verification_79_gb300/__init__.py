@@ -52,6 +52,9 @@ def load(build_if_missing: bool = True):
     lib.sv_schedule_cal.argtypes = [vp, vp, vp, f32, f32, f32, i32, i32, i32, vp, vp, vp, vp, sz,
                                     vp]
     lib.sv_schedule_cal.restype = i32
+    lib.sv_schedule_curve.argtypes = [vp, vp, vp, f32, f32, f32, vp, i32, i32, i32, i32, vp, vp,
+                                      vp, vp, vp, vp, sz, vp]
+    lib.sv_schedule_curve.restype = i32
     lib.sv_calib_stats_len.argtypes = [i32]
     lib.sv_calib_stats_len.restype = sz
     lib.sv_calib_observe.argtypes = [vp, vp, vp, i32, i32, vp, vp]
@@ -173,6 +176,32 @@ def sv_schedule_cal(conf, temps, load, tau, tau_min, tau_max, token_budget, ws: 
         int(token_budget), _ptr(out_len), _ptr(conf_cal), _ptr(tau_out), _ptr(ws.t), ws.nbytes,
         _stream(stream)))
     return out_len, conf_cal, tau_out
+
+
+def sv_schedule_curve(conf, temps, load, tau, tau_min, tau_max, curve, token_budget,
+                      ws: Workspace, out_len=None, stream=None):
+    """Schedule whose budget is chosen from a throughput curve (see specverify.h).
+    curve: [2, n_pts] float32 (tokens, tokens/s). Returns (out_len, n [1] int32,
+    goodput [1] float64)."""
+    conf = _dev(conf, "conf", torch.float32)
+    B, K = conf.shape
+    curve = _dev(curve, "curve", torch.float32)
+    if curve.dim() != 2 or curve.shape[0] != 2:
+        raise ValueError("curve must be [2, n_pts]")
+    if temps is not None:
+        _dev(temps, "temps", torch.float32)
+    if load is not None:
+        _dev(load, "load", torch.float32)
+    dev = conf.device
+    if out_len is None:
+        out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    n_out = torch.empty(1, dtype=torch.int32, device=dev)
+    g_out = torch.empty(1, dtype=torch.float64, device=dev)
+    _check("sv_schedule_curve", load_lib().sv_schedule_curve(
+        _ptr(conf), _ptr(temps), _ptr(load), float(tau), float(tau_min), float(tau_max),
+        _ptr(curve), curve.shape[1], B, K, int(token_budget), _ptr(out_len), None, None,
+        _ptr(n_out), _ptr(g_out), _ptr(ws.t), ws.nbytes, _stream(stream)))
+    return out_len, n_out, g_out
 
 
 def sv_calib_stats_len(K: int) -> int:

@@ -41,11 +41,14 @@ sv_status sv_workspace_init(void* ws_d, size_t ws_bytes, void* stream) {
   return SV_OK;
 }
 
-sv_status sv_schedule_cal(const float* conf_d, const float* temps_d, const float* load_d,
-                          float tau, float tau_min, float tau_max, int B, int K,
-                          int token_budget, int32_t* out_len_d, float* conf_cal_d,
-                          double* tau_out_d, void* ws_d, size_t ws_bytes, void* stream) {
+static sv_status schedule_any(const float* conf_d, const float* temps_d, const float* load_d,
+                              float tau, float tau_min, float tau_max, const float* curve_d,
+                              int n_pts, int B, int K, int token_budget, int32_t* out_len_d,
+                              float* conf_cal_d, double* tau_out_d, int32_t* n_out_d,
+                              double* g_out_d, void* ws_d, size_t ws_bytes, void* stream) {
   if (B < 0 || B > SV_MAX_SCHED_B || K < 1 || K > SV_MAX_K || (long long)B * K > SV_MAX_SCHED_BK)
+    return SV_ERR_SHAPE;
+  if (curve_d && (n_pts < 1 || n_pts > SV_MAX_CURVE || (long long)B * K > SV_MAX_CURVE_BK))
     return SV_ERR_SHAPE;
   if (!(tau >= 0.f && tau <= 1.f) || token_budget < 0) return SV_ERR_ARG;
   if (load_d && !(tau_min >= 0.f && tau_min <= 1.f && tau_max >= 0.f && tau_max <= 1.f))
@@ -54,13 +57,36 @@ sv_status sv_schedule_cal(const float* conf_d, const float* temps_d, const float
   if (B == 0) return SV_OK;
   if (!conf_d || !out_len_d || !aligned(conf_d, 4) || !aligned(out_len_d, 4)) return SV_ERR_ARG;
   if ((temps_d && !aligned(temps_d, 4)) || (load_d && !aligned(load_d, 4)) ||
-      (conf_cal_d && !aligned(conf_cal_d, 4)) || (tau_out_d && !aligned(tau_out_d, 8)))
+      (conf_cal_d && !aligned(conf_cal_d, 4)) || (tau_out_d && !aligned(tau_out_d, 8)) ||
+      (curve_d && !aligned(curve_d, 4)) || (n_out_d && !aligned(n_out_d, 4)) ||
+      (g_out_d && !aligned(g_out_d, 8)))
     return SV_ERR_ARG;
-  const cudaError_t e = launch_schedule(conf_d, temps_d, load_d, B, K, tau, tau_min, tau_max,
-                                        token_budget, out_len_d, conf_cal_d, tau_out_d,
+  const cudaError_t e = launch_schedule(conf_d, temps_d, load_d, curve_d, n_pts, B, K, tau,
+                                        tau_min, tau_max, token_budget, out_len_d, conf_cal_d,
+                                        tau_out_d, n_out_d, g_out_d,
                                         static_cast<WsHeader*>(ws_d),
                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_schedule_cal(const float* conf_d, const float* temps_d, const float* load_d,
+                          float tau, float tau_min, float tau_max, int B, int K,
+                          int token_budget, int32_t* out_len_d, float* conf_cal_d,
+                          double* tau_out_d, void* ws_d, size_t ws_bytes, void* stream) {
+  return schedule_any(conf_d, temps_d, load_d, tau, tau_min, tau_max, nullptr, 0, B, K,
+                      token_budget, out_len_d, conf_cal_d, tau_out_d, nullptr, nullptr, ws_d,
+                      ws_bytes, stream);
+}
+
+sv_status sv_schedule_curve(const float* conf_d, const float* temps_d, const float* load_d,
+                            float tau, float tau_min, float tau_max, const float* curve_d,
+                            int n_pts, int B, int K, int token_budget, int32_t* out_len_d,
+                            float* conf_cal_d, double* tau_out_d, int32_t* n_out_d,
+                            double* g_out_d, void* ws_d, size_t ws_bytes, void* stream) {
+  if (!curve_d) return SV_ERR_ARG;
+  return schedule_any(conf_d, temps_d, load_d, tau, tau_min, tau_max, curve_d, n_pts, B, K,
+                      token_budget, out_len_d, conf_cal_d, tau_out_d, n_out_d, g_out_d, ws_d,
+                      ws_bytes, stream);
 }
 
 sv_status sv_schedule(const float* conf_d, int B, int K, float tau, int token_budget,

@@ -31,6 +31,10 @@ struct ScheduleArgs {
   const float* conf;
   const float* temps;  // [K] or nullptr: no calibration
   const float* load;   // [4] {Q, Q_max, M_gpu, M_max} or nullptr: tau as given
+  const float* curve;  // [2 * n_pts] tokens then tokens/s, or nullptr: budget as given
+  int n_pts;
+  int32_t* n_out;      // [1] or nullptr: the budget the curve chose
+  double* g_out;       // [1] or nullptr: its goodput
   int B, K;
   float tau, tau_min, tau_max;
   int budget;
@@ -51,6 +55,19 @@ __device__ __forceinline__ float calibrate(float c, float T) {
   return __fdiv_rn(1.f, __fadd_rn(1.f, expf(-z)));
 }
 
+// The throughput curve at x tokens (fp64, each step rounded once): linear between its
+// points, flat beyond the first and the last.
+__device__ double curve_at(const float* cx, const float* cy, int n, double x) {
+  if (x <= static_cast<double>(cx[0])) return cy[0];
+  for (int i = 1; i < n; ++i) {
+    if (x <= static_cast<double>(cx[i])) {
+      const double x0 = cx[i - 1], x1 = cx[i], y0 = cy[i - 1], y1 = cy[i];
+      return __dadd_rn(y0, __dmul_rn(__dsub_rn(y1, y0), __ddiv_rn(__dsub_rn(x, x0), __dsub_rn(x1, x0))));
+    }
+  }
+  return cy[n - 1];
+}
+
 // Load-aware threshold in fp64 (no contraction: each step rounds once). Returns a
 // negative value for an invalid load state.
 __device__ double load_tau(const float* load, double tau_min, double tau_max) {
@@ -66,6 +83,130 @@ __device__ __forceinline__ unsigned long long surv_key(double s) {
   return static_cast<unsigned long long>(__double_as_longlong(s == 0.0 ? 0.0 : s));
 }
 
+// Throughput-curve budget (DSpark Deep Dive, "The Throughput Curve", "The Optimization
+// Logic"): the smallest N in [N_lo, N_hi] maximising the goodput
+// G(N) = (B + A(N)) T(B + N) / (B + N), A(N) the sum of the N best survivals in the trim
+// order (the floor positions first when the budget allows one per request), T the curve.
+// The competing survivals are sorted (bitonic, descending) in C, prefix-summed in
+// float64, and every N is evaluated by some thread; the block keeps the best (G, N).
+__device__ long long curve_budget(const ScheduleArgs& A, const double* S, const int* L0,
+                                  double* C, long long total, const float* cx, const float* cy) {
+  __shared__ unsigned int s_nc;
+  __shared__ double s_red[SCHED_THREADS / 32];
+  __shared__ unsigned long long s_bestn[SCHED_THREADS / 32];
+  __shared__ double s_bestg[SCHED_THREADS / 32];
+  const int B = A.B, K = A.K, N = B * K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool floors = A.budget >= B;
+  const long long n_hi = total < A.budget ? total : A.budget;
+  const long long n_lo = floors ? B : 0;
+  // Competing survivals into C (any order: they are sorted next), the floors' sum.
+  if (tid == 0) s_nc = 0;
+  __syncthreads();
+  double fsum = 0.0;
+  for (int i = tid; i < N; i += SCHED_THREADS) {
+    const int b = i / K, k = i - b * K;
+    if (k >= L0[b]) continue;
+    if (floors && k == 0)
+      fsum += S[i];
+    else
+      C[atomicAdd(&s_nc, 1u)] = S[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
+  if (lane == 0) s_red[warp] = fsum;
+  __syncthreads();
+  const int nc = static_cast<int>(s_nc);
+  int P = 1;
+  while (P < nc) P <<= 1;
+  for (int i = nc + tid; i < P; i += SCHED_THREADS) C[i] = 0.0;  // padding sorts last
+  double a_floor = 0.0;
+  for (int w = 0; w < SCHED_THREADS / 32; ++w) a_floor += s_red[w];
+  __syncthreads();
+  // Bitonic sort, descending, on the bit patterns (S >= 0 orders like its bits).
+  unsigned long long* Ck = reinterpret_cast<unsigned long long*>(C);
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P; i += SCHED_THREADS) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long x = Ck[i], y = Ck[l];
+          const bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            Ck[i] = y;
+            Ck[l] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // Inclusive prefix sums of the first nc values: a chunk per thread, then the chunks.
+  const int per = (nc + SCHED_THREADS - 1) / SCHED_THREADS;
+  const int i0 = min(nc, tid * per), i1 = min(nc, i0 + per);
+  double run = 0.0;
+  for (int i = i0; i < i1; ++i) {
+    run += C[i];
+    C[i] = run;
+  }
+  double incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  double off = incl - run;
+  for (int w = 0; w < warp; ++w) off += s_red[w];
+  for (int i = i0; i < i1; ++i) C[i] += off;
+  __syncthreads();
+  // Goodput of every N; the best (largest G, then smallest N) over the block.
+  double bg = -1.0;
+  long long bn = n_lo;
+  for (long long n = n_lo + tid; n <= n_hi; n += SCHED_THREADS) {
+    const double a = (n > n_lo) ? __dadd_rn(a_floor, C[n - n_lo - 1]) : a_floor;
+    const double x = static_cast<double>(B) + static_cast<double>(n);
+    const double g = __ddiv_rn(__dmul_rn(__dadd_rn(static_cast<double>(B), a),
+                                         curve_at(cx, cy, A.n_pts, x)), x);
+    if (g > bg) {
+      bg = g;
+      bn = n;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const double g2 = __shfl_xor_sync(0xffffffffu, bg, o);
+    const long long n2 = __shfl_xor_sync(0xffffffffu, bn, o);
+    if (g2 > bg || (g2 == bg && n2 < bn)) {
+      bg = g2;
+      bn = n2;
+    }
+  }
+  if (lane == 0) {
+    s_bestg[warp] = bg;
+    s_bestn[warp] = static_cast<unsigned long long>(bn);
+  }
+  __syncthreads();
+  double g = s_bestg[0];
+  long long n = static_cast<long long>(s_bestn[0]);
+  for (int w = 1; w < SCHED_THREADS / 32; ++w) {
+    const double g2 = s_bestg[w];
+    const long long n2 = static_cast<long long>(s_bestn[w]);
+    if (g2 > g || (g2 == g && n2 < n)) {
+      g = g2;
+      n = n2;
+    }
+  }
+  if (tid == 0) {
+    if (A.n_out) *A.n_out = static_cast<int32_t>(n);
+    if (A.g_out) *A.g_out = g;
+  }
+  __syncthreads();
+  return n;
+}
+
 __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const ScheduleArgs A) {
   extern __shared__ __align__(16) unsigned char dsm[];
   const int B = A.B, K = A.K, N = B * K;
@@ -79,6 +220,7 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   __shared__ unsigned long long s_total;
   __shared__ float s_temps[SV_MAX_K];
   __shared__ double s_tau;
+  __shared__ float s_cx[SV_MAX_CURVE], s_cy[SV_MAX_CURVE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // 0. Threshold (as given, or from the load state by thread 0) and the position
@@ -86,8 +228,16 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   const bool cal = A.temps != nullptr;
   double th = static_cast<double>(A.tau);
   bool bad = false;
-  if (A.load || cal) {
+  if (A.load || cal || A.curve) {
     int mine = 0;
+    if (A.curve && tid == 0) {  // the curve: finite, tokens/s > 0, tokens ascending
+      for (int i = 0; i < A.n_pts; ++i) {
+        const float x = __ldg(A.curve + i), y = __ldg(A.curve + A.n_pts + i);
+        s_cx[i] = x;
+        s_cy[i] = y;
+        if (!(isfinite(x) && isfinite(y) && y > 0.f) || (i > 0 && !(x > s_cx[i - 1]))) mine = 1;
+      }
+    }
     if (A.load && tid == 0) {
       const double t = load_tau(A.load, static_cast<double>(A.tau_min),
                                 static_cast<double>(A.tau_max));
@@ -165,13 +315,15 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   if (lane == 0 && my_total) atomicAdd(&s_total, my_total);
   __syncthreads();
   const long long total = static_cast<long long>(s_total);
-  if (total <= A.budget) {
+  long long budget = A.budget;
+  if (A.curve) budget = curve_budget(A, S, L0, reinterpret_cast<double*>(cnt + B), total, s_cx, s_cy);
+  if (total <= budget) {
     for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = L0[b];
     return;
   }
-  const bool floor_first = A.budget >= B;
+  const bool floor_first = budget >= B;
   const int lo = floor_first ? 1 : 0;
-  const unsigned int bud = static_cast<unsigned int>(floor_first ? A.budget - B : A.budget);
+  const unsigned int bud = static_cast<unsigned int>(floor_first ? budget - B : budget);
   if (bud == 0) {
     for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = lo;
     return;
@@ -273,25 +425,32 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const Sch
   for (int b = tid; b < B; b += SCHED_THREADS) A.out_len[b] = lo + cnt[b];
 }
 
-static size_t schedule_smem_bytes(int B, int K) {
-  return (size_t)B * K * sizeof(double) + 2 * (size_t)B * sizeof(int);
+static size_t schedule_smem_bytes(int B, int K, bool curve) {
+  size_t sort = 0;
+  if (curve) {
+    size_t p = 1;
+    while (p < (size_t)B * K) p <<= 1;
+    sort = p * sizeof(double);
+  }
+  return (size_t)B * K * sizeof(double) + 2 * (size_t)B * sizeof(int) + sort;
 }
 
-cudaError_t launch_schedule(const float* conf, const float* temps, const float* load, int B,
-                            int K, float tau, float tau_min, float tau_max, int budget,
-                            int32_t* out_len, float* conf_cal, double* tau_out, WsHeader* hdr,
+cudaError_t launch_schedule(const float* conf, const float* temps, const float* load,
+                            const float* curve, int n_pts, int B, int K, float tau, float tau_min,
+                            float tau_max, int budget, int32_t* out_len, float* conf_cal,
+                            double* tau_out, int32_t* n_out, double* g_out, WsHeader* hdr,
                             cudaStream_t st) {
-  const size_t smem = schedule_smem_bytes(B, K);
+  const size_t smem = schedule_smem_bytes(B, K, curve != nullptr);
   static bool attr_set = false;  // idempotent if two threads race here
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(
         sv_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)schedule_smem_bytes(SV_MAX_SCHED_B, SV_MAX_SCHED_BK / SV_MAX_SCHED_B));
+        (int)schedule_smem_bytes(SV_MAX_SCHED_B, SV_MAX_SCHED_BK / SV_MAX_SCHED_B, false));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  ScheduleArgs A{conf, temps, load, B, K, tau, tau_min, tau_max, budget, out_len, conf_cal,
-                 tau_out, hdr};
+  ScheduleArgs A{conf, temps, load, curve, n_pts, n_out, g_out, B, K, tau, tau_min, tau_max,
+                 budget, out_len, conf_cal, tau_out, hdr};
   sv_schedule_kernel<<<1, SCHED_THREADS, smem, st>>>(A);
   return cudaGetLastError();
 }

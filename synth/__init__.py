@@ -214,3 +214,15 @@ def markov_inputs(B, K, V, r, *, seed=0, logit_sigma=3.0):
     Vm = (torch.randn((V, r), generator=g) * s).to(torch.bfloat16)
     prev = torch.randint(0, V, (B,), generator=g, dtype=torch.int32)
     return {"logits": L, "U": U, "Vm": Vm, "prev": prev}
+
+
+def throughput_curve(n, *, seed=0, x_max=4096.0):
+    """A throughput curve [2, n] float32: batch sizes in tokens (ascending, from 1 to
+    about x_max) and tokens/s rising with a falling slope (memory-bound, then flat)."""
+    rng = np.random.default_rng(int(seed) + 4000)
+    x = np.unique(np.round(np.geomspace(1.0, x_max, n) * rng.uniform(0.9, 1.1, n)).astype(np.float64))
+    x = np.maximum.accumulate(x)
+    x = np.unique(x)
+    knee = rng.uniform(16.0, 512.0)
+    y = 30.0 * x / (1.0 + x / knee) + rng.uniform(0.0, 5.0)
+    return torch.tensor(np.stack([x, y]), dtype=torch.float32)

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
               "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version",
               "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update",
-              "sv_markov_keys_len", "sv_markov_draft"):
+              "sv_markov_keys_len", "sv_markov_draft", "sv_schedule_curve"):
         assert n in names
 
 
@@ -143,3 +143,18 @@ def test_markov_host_checks(lib):
     assert lib.sv_markov_draft(*args(lg=None)) == sv.SV_ERR_ARG
     assert lib.sv_markov_draft(*args(lg=ctypes.c_void_p(264))) == sv.SV_ERR_ARG
     assert lib.sv_markov_draft(*args(B=0)) == sv.SV_OK
+
+
+def test_curve_host_checks(lib):
+    import speculative_decoding_verification_79_gb300 as sv
+
+    fake = ctypes.c_void_p(256)
+    n = lib.sv_workspace_bytes(4, 4, 100)
+    args = lambda curve=fake, npts=4, B=4, K=4: (  # noqa: E731
+        fake, None, None, 0.3, 0.2, 0.75, curve, npts, B, K, 10, fake, None, None, None, None,
+        fake, n, None)
+    assert lib.sv_schedule_curve(*args(curve=None)) == sv.SV_ERR_ARG
+    assert lib.sv_schedule_curve(*args(npts=0)) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule_curve(*args(npts=65)) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule_curve(*args(B=4096, K=4)) == sv.SV_ERR_SHAPE
+    assert lib.sv_schedule_curve(*args(B=0)) == sv.SV_OK
