@@ -25,7 +25,13 @@ MARGIN_RESOLUTION = 2e-6
 # as near-ties by the oracle (windows of 1e-5 on the accept ratio and on the inverse-CDF
 # position), flagged requests on which the GPU actually decided differently, and the
 # largest oracle margin among those.
-TOTALS = {"positions": 0, "flagged": 0, "mismatch": 0, "max_margin": 0.0}
+TOTALS = {"positions": 0, "flagged": 0, "mismatch": 0, "max_margin": 0.0,
+          "requests": 0, "accept_tie": 0, "cdf_edge": 0, "degenerate": 0}
+# The flag kinds of the last comparison (added to TOTALS by account()): requests with
+# an accept test within 1e-5 of its ratio, a terminal sample within 1e-5 of a CDF
+# bucket edge, and degenerate cases (both probabilities below 1e-30, or a residual
+# with less than 1e-5 of mass).
+LAST = {"requests": 0, "accept_tie": 0, "cdf_edge": 0, "degenerate": 0}
 
 
 def to_dev(inp, device="cuda"):
@@ -90,6 +96,10 @@ def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
                     f"q {gq[bb, kk]:.6e}; ref p {ref['p'][bb, kk]:.6e} q {ref['q'][bb, kk]:.6e}); "
                     f"{int(badm.sum())} elements over")
     positions = int((np.clip(L, 0, None) + 1).sum())
+    fl = ref["flags"]
+    LAST.update(requests=int(fl.size), accept_tie=int(((fl & oracle.FLAG_ACCEPT_TIE) != 0).sum()),
+                cdf_edge=int(((fl & oracle.FLAG_CDF_EDGE) != 0).sum()),
+                degenerate=int(((fl & (oracle.FLAG_TINY_PROB | oracle.FLAG_SMALL_RESIDUAL)) != 0).sum()))
     differ = flagged & ((acc != ref["out_accepted"]) | (tok != ref["out_tok"]).any(axis=1))
     margins = ref["margin"][differ] if "margin" in ref else np.zeros(0)
     for b in np.nonzero(differ)[0][:5]:
@@ -106,5 +116,7 @@ def account(name, nf, npos, nmis, max_margin=0.0):
     TOTALS["flagged"] += nf
     TOTALS["mismatch"] += nmis
     TOTALS["max_margin"] = max(TOTALS["max_margin"], max_margin)
+    for k in ("requests", "accept_tie", "cdf_edge", "degenerate"):
+        TOTALS[k] += LAST[k]
     print(f"[near-ties] {name}: {nf} flagged requests, {nmis} of them decided differently, "
           f"{npos} positions")

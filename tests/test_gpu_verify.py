@@ -291,4 +291,8 @@ def test_near_tie_summary():
           f"({t['flagged'] / t['positions']:.2e} of {t['positions']} positions), "
           f"{t['mismatch']} decided differently ({t['mismatch'] / t['positions']:.2e}), "
           f"largest oracle margin among them {t['max_margin']:.2e}")
+    print(f"[near-ties] by kind: accept test within 1e-5 of its ratio in {t['accept_tie']} "
+          f"requests ({t['accept_tie'] / t['positions']:.2e} of positions); terminal sample "
+          f"within 1e-5 of a CDF edge in {t['cdf_edge']} of {t['requests']} requests; "
+          f"degenerate (tiny probabilities, empty residual) in {t['degenerate']}")
     assert t["max_margin"] < gpu_util.MARGIN_RESOLUTION
