@@ -589,6 +589,24 @@ def run_markov(args):
               flush=True)
 
 
+def run_curve_once(args):
+    """N untimed calls of the throughput-curve schedule at B=64, K=8 (for ncu captures)."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    conf = synth.confidences(64, 8, seed=1).to(dev)
+    curve = synth.throughput_curve(8, seed=1).to(dev)
+    ws = sv.Workspace(64, 8, 16, device=dev)
+    for _ in range(args.once):
+        sv.sv_schedule_curve(conf, None, None, 0.3, 0.2, 0.75, curve, 256, ws)
+    torch.cuda.synchronize()
+    status = ws.status()
+    print(json.dumps({"curve_once": args.once, "status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def run_markov_once(args):
     """N untimed calls of the Markov drafting loop at rank 256 (for ncu captures)."""
     import speculative_decoding_verification_79_gb300 as sv
@@ -654,6 +672,8 @@ def main():
         run_reference(args)
     elif args.once > 0 and args.markov:
         run_markov_once(args)
+    elif args.once > 0 and args.calib:
+        run_curve_once(args)
     elif args.once > 0:
         run_once(args)
     elif args.sweep:

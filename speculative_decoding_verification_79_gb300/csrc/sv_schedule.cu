@@ -57,10 +57,13 @@ __device__ __forceinline__ float calibrate(float c, float T) {
 
 // The throughput curve at x tokens (fp64, each step rounded once): linear between its
 // points, flat beyond the first and the last.
+// x is a whole number of tokens below 2^24, exact in fp32, so the segment is found
+// with fp32 compares; only the interpolation runs on the (slow) fp64 pipe.
 __device__ double curve_at(const float* cx, const float* cy, int n, double x) {
-  if (x <= static_cast<double>(cx[0])) return cy[0];
+  const float xf = static_cast<float>(x);
+  if (xf <= cx[0]) return cy[0];
   for (int i = 1; i < n; ++i) {
-    if (x <= static_cast<double>(cx[i])) {
+    if (xf <= cx[i]) {
       const double x0 = cx[i - 1], x1 = cx[i], y0 = cy[i - 1], y1 = cy[i];
       return __dadd_rn(y0, __dmul_rn(__dsub_rn(y1, y0), __ddiv_rn(__dsub_rn(x, x0), __dsub_rn(x1, x0))));
     }
@@ -93,6 +96,8 @@ __device__ long long curve_budget(const ScheduleArgs& A, const double* S, const 
                                   double* C, long long total, const float* cx, const float* cy) {
   __shared__ unsigned int s_nc;
   __shared__ double s_red[SCHED_THREADS / 32];
+  __shared__ double s_floor;
+  __shared__ long long s_n;
   __shared__ unsigned long long s_bestn[SCHED_THREADS / 32];
   __shared__ double s_bestg[SCHED_THREADS / 32];
   const int B = A.B, K = A.K, N = B * K;
@@ -120,9 +125,13 @@ __device__ long long curve_budget(const ScheduleArgs& A, const double* S, const 
   int P = 1;
   while (P < nc) P <<= 1;
   for (int i = nc + tid; i < P; i += SCHED_THREADS) C[i] = 0.0;  // padding sorts last
-  double a_floor = 0.0;
-  for (int w = 0; w < SCHED_THREADS / 32; ++w) a_floor += s_red[w];
+  if (tid == 0) {  // the floors' sum, once (fp64 work is scarce on this GPU)
+    double a = 0.0;
+    for (int w = 0; w < SCHED_THREADS / 32; ++w) a += s_red[w];
+    s_floor = a;
+  }
   __syncthreads();
+  const double a_floor = s_floor;
   // Bitonic sort, descending, on the bit patterns (S >= 0 orders like its bits).
   unsigned long long* Ck = reinterpret_cast<unsigned long long*>(C);
   for (int k = 2; k <= P; k <<= 1) {
@@ -158,8 +167,19 @@ __device__ long long curve_budget(const ScheduleArgs& A, const double* S, const 
   __syncthreads();
   if (lane == 31) s_red[warp] = incl;
   __syncthreads();
-  double off = incl - run;
-  for (int w = 0; w < warp; ++w) off += s_red[w];
+  if (warp == 0) {  // exclusive scan of the warps' totals, once
+    const double v = s_red[lane];
+    double e = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, e, o);
+      if (lane >= o) e += y;
+    }
+    __syncwarp();
+    s_red[lane] = e - v;
+  }
+  __syncthreads();
+  const double off = (incl - run) + s_red[warp];
   for (int i = i0; i < i1; ++i) C[i] += off;
   __syncthreads();
   // Goodput of every N; the best (largest G, then smallest N) over the block.
@@ -189,22 +209,26 @@ __device__ long long curve_budget(const ScheduleArgs& A, const double* S, const 
     s_bestn[warp] = static_cast<unsigned long long>(bn);
   }
   __syncthreads();
-  double g = s_bestg[0];
-  long long n = static_cast<long long>(s_bestn[0]);
-  for (int w = 1; w < SCHED_THREADS / 32; ++w) {
-    const double g2 = s_bestg[w];
-    const long long n2 = static_cast<long long>(s_bestn[w]);
-    if (g2 > g || (g2 == g && n2 < n)) {
-      g = g2;
-      n = n2;
+  if (warp == 0) {  // the best over the warps, once
+    double g = s_bestg[lane];
+    long long n = static_cast<long long>(s_bestn[lane]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const double g2 = __shfl_xor_sync(0xffffffffu, g, o);
+      const long long n2 = __shfl_xor_sync(0xffffffffu, n, o);
+      if (g2 > g || (g2 == g && n2 < n)) {
+        g = g2;
+        n = n2;
+      }
+    }
+    if (lane == 0) {
+      s_n = n;
+      if (A.n_out) *A.n_out = static_cast<int32_t>(n);
+      if (A.g_out) *A.g_out = g;
     }
   }
-  if (tid == 0) {
-    if (A.n_out) *A.n_out = static_cast<int32_t>(n);
-    if (A.g_out) *A.g_out = g;
-  }
   __syncthreads();
-  return n;
+  return s_n;
 }
 
 __global__ void __launch_bounds__(SCHED_THREADS, 1) sv_schedule_kernel(const ScheduleArgs A) {
