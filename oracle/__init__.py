@@ -89,6 +89,12 @@ def _bind(path):
                                           ctypes.c_float, f32p, f32p, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_longlong, i32p, i32p, f64p]
     lib.oracle_schedule_curve.restype = ctypes.c_int
+    tree = [vp, vp, ctypes.c_int, i32p, i32p, i32p]
+    tree_outs = [i32p, i32p, i32p, i32p, f64p, ctypes.c_int]
+    lib.oracle_verify_tree.argtypes = tree + [f32p] + tail + [ctypes.c_float] + tree_outs
+    lib.oracle_verify_tree.restype = ctypes.c_int
+    lib.oracle_verify_tree_u64.argtypes = tree + [f64p] + tail + [ctypes.c_double] + tree_outs
+    lib.oracle_verify_tree_u64.restype = ctypes.c_int
     return lib
 
 
@@ -279,3 +285,37 @@ def verify(target, draft, draft_tok, verify_len, uniforms, temperature: float,
             int(nthreads))
     return {"out_tok": out_tok, "out_accepted": out_acc, "p": p, "q": q, "flags": flags,
             "margin": margin, "status": rc}
+
+
+def verify_tree(target, draft, parent, draft_tok, n_nodes, uniforms, temperature: float,
+                nthreads: int = 1, u64: bool = False, lib=None):
+    """Batched tree verification (multi-candidate rejection sampling).
+
+    target, draft [B,N,V]: float32, or bf16 as uint16 bit patterns (draft may be None
+    at T == 0). parent, draft_tok [B,N] int32; n_nodes [B] int32; uniforms [B,N]
+    float32 (float64 when ``u64``). Returns dict(out_tok [B,N], out_accepted [B],
+    out_path [B,N], flags [B], margin [B], status).
+    """
+    t, dt = _logits(target)
+    d, dd = _logits(draft)
+    if d is not None and dd != dt:
+        raise TypeError("target and draft logits must share a dtype")
+    B, N, V = t.shape
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    tok = np.ascontiguousarray(draft_tok, dtype=np.int32)
+    nn = np.ascontiguousarray(n_nodes, dtype=np.int32)
+    u = None
+    if uniforms is not None:
+        u = np.ascontiguousarray(uniforms, dtype=np.float64 if u64 else np.float32)
+    out_tok = np.zeros((B, N), np.int32)
+    out_acc = np.zeros(B, np.int32)
+    out_path = np.zeros((B, N), np.int32)
+    flags = np.zeros(B, np.int32)
+    margin = np.zeros(B, np.float64)
+    lib = lib or _load()
+    fn = lib.oracle_verify_tree_u64 if u64 else lib.oracle_verify_tree
+    rc = fn(_ptr(t), _ptr(d), dt, _ptr(par), _ptr(tok), _ptr(nn), _ptr(u), B, N, V,
+            float(temperature), _ptr(out_tok), _ptr(out_acc), _ptr(out_path), _ptr(flags),
+            _ptr(margin), int(nthreads))
+    return {"out_tok": out_tok, "out_accepted": out_acc, "out_path": out_path,
+            "flags": flags, "margin": margin, "status": rc}

@@ -815,3 +815,252 @@ int oracle_schedule_curve(const float *conf, const float *temps, const float *lo
     free(L0);
     return rc;
 }
+
+/* ======================================================================== */
+/* Tree (multi-candidate) verification                                      */
+/* ======================================================================== */
+
+/*
+ * The pages name tree verification without defining it: the DSpark Guide's
+ * pipeline ("Deep Dive into the DSpark Architecture", step 4) forwards the
+ * verified prefix "with tree / sequence mask", and its feature matrix ("3.
+ * Comprehensive Technical Feature Matrix") lists "Static / Tree" verification
+ * for EAGLE-3. Reading taken here, the plainest lossless one that reduces to the
+ * chain of [DD "The Speculative Decoding Solution"] when every node has at most
+ * one child:
+ *
+ *  - Request b holds a token tree of n_nodes[b] nodes. Node 0 is the committed
+ *    context; node n >= 1 carries the drafted token tok[n] and has parent
+ *    par[n] < n. Target row n is the target's logits after the path 0 -> n;
+ *    draft row n is the drafter's logits the children of n were drawn from,
+ *    each child independently (with replacement).
+ *  - The walk starts at node 0. At node c the children are tested in index
+ *    order against a residual distribution r that starts as p_c: child n with
+ *    token x is accepted when u_n * q_c(x) < r(x) (probability
+ *    min(1, r(x)/q_c(x))); the walk then moves to n. After a rejection r
+ *    becomes normalize(max(0, r - q_c)), so the next child is tested against
+ *    the target mass the rejected draws left uncovered.
+ *  - When every child of c is rejected, the token is sampled from r by inverse
+ *    CDF at u_{b,0} (for one child this is the chain's residual sample); at a
+ *    leaf, from p_c (the chain's bonus token).
+ *  - At T == 0: accept the first child (index order) whose token is the lowest
+ *    index argmax of target row c; otherwise emit that argmax.
+ *  - Rows the walk never reaches are not read, so their contents (even NaN)
+ *    do not matter. A reached row that is not a valid logit row makes the
+ *    request invalid, as do bad tree links, tokens or uniforms.
+ *  - Reading for a residual with no mass left (p == q up to rounding): r starts
+ *    again from p_c, as the chain falls back to sampling p.
+ */
+
+/* Near-tie bookkeeping of one decision at residual state (lam, W), where
+ * r = max(0, p - lam*q) / W in closed form (lam = 0, W = 1 for r = p). A kernel
+ * forming r from fp32 p and q carries an error in r/q of about eps*(1 + 2 lam)/W,
+ * and in a CDF position of about eps*(1 + lam)/W, so the margins are divided by
+ * those factors before they are compared with the window. */
+static double tree_scale_test(double lam, double W) { return (1.0 + 2.0 * lam) / W; }
+static double tree_scale_cdf(double lam, double W) { return (1.0 + lam) / W; }
+
+static int tree_one(const void *tgt, const void *drf, int dtype, const int32_t *par,
+                    const int32_t *tok, const int32_t *nnod, const double *u, int b, int N,
+                    int V, double T, int32_t *out_tok, int32_t *out_acc, int32_t *out_path,
+                    int32_t *out_flags, double *out_margin, double *p, double *q, double *r,
+                    double *w) {
+    const size_t base = (size_t)b * N;
+    int32_t *ot = out_tok + base;
+    int32_t *op = out_path ? out_path + base : NULL;
+    for (int i = 0; i < N; i++) {
+        ot[i] = -1;
+        if (op) op[i] = -1;
+    }
+    out_acc[b] = -1;
+    out_flags[b] = 0;
+    double margin = INFINITY;
+    if (out_margin) out_margin[b] = INFINITY;
+
+    const int nn = nnod[b];
+    if (nn < 1 || nn > N) goto invalid;
+    for (int n = 1; n < nn; n++) {
+        if (par[base + n] < 0 || par[base + n] >= n) goto invalid;
+        if (tok[base + n] < 0 || tok[base + n] >= V) goto invalid;
+    }
+    if (T > 0.0)
+        for (int n = 0; n < nn; n++)
+            if (!(u[base + n] >= 0.0 && u[base + n] < 1.0)) goto invalid;
+
+    int c = 0, depth = 0;
+    for (;;) {
+        double Mt, Md;
+        int At, Ad;
+        if (row_scan(tgt, dtype, (base + c) * (size_t)V, V, &Mt, &At)) goto invalid;
+        int first_child = -1;
+        for (int n = c + 1; n < nn; n++)
+            if (par[base + n] == c) {
+                first_child = n;
+                break;
+            }
+
+        if (T == 0.0) {
+            int next = -1;
+            for (int n = c + 1; n < nn && next < 0; n++)
+                if (par[base + n] == c && tok[base + n] == At) next = n;
+            if (next < 0) {
+                ot[depth] = At;
+                out_acc[b] = depth;
+                return 0;
+            }
+            ot[depth] = tok[base + next];
+            if (op) op[depth] = next;
+            depth++;
+            c = next;
+            continue;
+        }
+
+        row_softmax(tgt, dtype, (base + c) * (size_t)V, V, T, Mt, p);
+        if (first_child < 0) {
+            /* A leaf: the bonus token from p_c. */
+            double Z, gap;
+            int y = inverse_cdf(p, V, u[base], &Z, &gap);
+            if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;
+            if (gap < margin) margin = gap;
+            if (out_margin) out_margin[b] = margin;
+            ot[depth] = y;
+            out_acc[b] = depth;
+            return 0;
+        }
+        if (row_scan(drf, dtype, (base + c) * (size_t)V, V, &Md, &Ad)) goto invalid;
+        row_softmax(drf, dtype, (base + c) * (size_t)V, V, T, Md, q);
+
+        for (int v = 0; v < V; v++) r[v] = p[v];
+        const double *wlast = p; /* weights of the terminal sample if all are rejected */
+        double lam = 0.0, W = 1.0; /* r = max(0, p - lam*q) / W (diagnostics only) */
+        int next = -1;
+        for (int n = first_child; n < nn; n++) {
+            if (par[base + n] != c) continue;
+            const int x = tok[base + n];
+            const double un = u[base + n];
+            const double rx = r[x], qx = q[x];
+            double ratio = qx > 0.0 ? (rx / qx < 1.0 ? rx / qx : 1.0) : (rx > 0.0 ? 1.0 : 0.0);
+            double mg = fabs(un - ratio) / tree_scale_test(lam, W);
+            if (mg < NEAR_TIE) out_flags[b] |= ORC_FLAG_ACCEPT_TIE;
+            if (mg < margin) margin = mg;
+            if (rx < 1e-30 && qx < 1e-30) out_flags[b] |= ORC_FLAG_TINY_PROB;
+            if (un * qx < rx) {
+                next = n;
+                break;
+            }
+            /* Rejected: r <- normalize(max(0, r - q)). */
+            double Z = 0.0;
+            for (int v = 0; v < V; v++) {
+                w[v] = r[v] - q[v] > 0.0 ? r[v] - q[v] : 0.0;
+                Z += w[v];
+            }
+            lam += W;
+            W *= Z;
+            if (W < NEAR_TIE) out_flags[b] |= ORC_FLAG_SMALL_RESIDUAL;
+            if (Z > 0.0) {
+                for (int v = 0; v < V; v++) r[v] = w[v] / Z;
+                wlast = w;
+            } else {
+                for (int v = 0; v < V; v++) r[v] = p[v];
+                wlast = p;
+                lam = 0.0;
+                W = 1.0;
+            }
+        }
+        if (next >= 0) {
+            ot[depth] = tok[base + next];
+            if (op) op[depth] = next;
+            depth++;
+            c = next;
+            continue;
+        }
+        /* Every child rejected: sample the residual at u_{b,0}. */
+        double Z, gap;
+        int y = inverse_cdf(wlast, V, u[base], &Z, &gap);
+        if (y < 0) y = inverse_cdf(p, V, u[base], &Z, &gap);
+        gap /= tree_scale_cdf(lam, W);
+        if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;
+        if (gap < margin) margin = gap;
+        if (out_margin) out_margin[b] = margin;
+        ot[depth] = y;
+        out_acc[b] = depth;
+        return 0;
+    }
+
+invalid:
+    for (int i = 0; i < N; i++) {
+        ot[i] = -1;
+        if (op) op[i] = -1;
+    }
+    out_acc[b] = -1;
+    out_flags[b] = ORC_FLAG_INVALID;
+    return -1;
+}
+
+/*
+ * oracle_verify_tree_u64: batched tree verification with float64 uniforms.
+ *
+ *  target, draft: [B, N, V] logits (dtype 0 = fp32, 1 = bf16 bits); draft may be
+ *    NULL at T == 0.
+ *  par, tok: [B, N] parent links and drafted tokens (entry 0 of each unused).
+ *  nnod: [B] nodes in use, 1..N.
+ *  u: [B, N]: u[b,n] (n >= 1) drives the test of node n; u[b,0] the terminal
+ *    sample. Unused at T == 0.
+ *  out_tok [B, N]: tokens of the accepted path, then the terminal token, then -1.
+ *  out_acc [B]: accepted drafted tokens (the path's depth), or -1 if invalid.
+ *  out_path [B, N] or NULL: node index of each accepted token, then -1.
+ *  out_flags [B], out_margin [B] or NULL: as oracle_verify (scaled margins).
+ * Returns ORC_OK, ORC_ERR_ARG, or ORC_ERR_INPUT if any request was invalid.
+ */
+int oracle_verify_tree_u64(const void *target, const void *draft, int dtype,
+                           const int32_t *par, const int32_t *tok, const int32_t *nnod,
+                           const double *u, int B, int N, int V, double T, int32_t *out_tok,
+                           int32_t *out_acc, int32_t *out_path, int32_t *out_flags,
+                           double *out_margin, int nthreads) {
+    if (B < 0 || N < 1 || V < 1 || (dtype != 0 && dtype != 1) || !(T >= 0.0) || !isfinite(T))
+        return ORC_ERR_ARG;
+    if (B == 0) return ORC_OK;
+    if (!target || !par || !tok || !nnod || !out_tok || !out_acc || !out_flags)
+        return ORC_ERR_ARG;
+    if (T > 0.0 && (!draft || !u)) return ORC_ERR_ARG;
+    int n_invalid = 0;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads) reduction(+ : n_invalid)
+#endif
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int b = 0; b < B; b++)
+            if (tree_one(target, draft, dtype, par, tok, nnod, u, b, N, V, T, out_tok, out_acc,
+                         out_path, out_flags, out_margin, p, q, r, w))
+                n_invalid++;
+        free(p);
+        free(q);
+        free(r);
+        free(w);
+    }
+    return n_invalid ? ORC_ERR_INPUT : ORC_OK;
+}
+
+/* oracle_verify_tree_u64 with the float32 uniforms of the C-ABI, widened exactly. */
+int oracle_verify_tree(const void *target, const void *draft, int dtype, const int32_t *par,
+                       const int32_t *tok, const int32_t *nnod, const float *u, int B, int N,
+                       int V, float T, int32_t *out_tok, int32_t *out_acc, int32_t *out_path,
+                       int32_t *out_flags, double *out_margin, int nthreads) {
+    double *u64 = NULL;
+    if (u && B > 0) {
+        u64 = (double *)malloc(sizeof(double) * (size_t)B * N);
+        for (size_t i = 0; i < (size_t)B * N; i++) u64[i] = (double)u[i];
+    }
+    int rc = oracle_verify_tree_u64(target, draft, dtype, par, tok, nnod, u64, B, N, V,
+                                    (double)T, out_tok, out_acc, out_path, out_flags, out_margin,
+                                    nthreads);
+    free(u64);
+    return rc;
+}

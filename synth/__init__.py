@@ -226,3 +226,122 @@ def throughput_curve(n, *, seed=0, x_max=4096.0):
     knee = rng.uniform(16.0, 512.0)
     y = 30.0 * x / (1.0 + x / knee) + rng.uniform(0.0, 5.0)
     return torch.tensor(np.stack([x, y]), dtype=torch.float32)
+
+
+# ----------------------------------------------------------------------------------
+# Tree verification inputs.
+# ----------------------------------------------------------------------------------
+
+# A 16-node draft tree of the kind tree drafters expand (several candidates for the
+# first token, fewer deeper down): node 0 is the committed context, parent links below.
+# Depths: nodes 1-4 at 1, 5-10 at 2, 11-13 at 3, 14-15 at 4.
+TREE16_PARENTS = (-1, 0, 0, 0, 0, 1, 1, 1, 2, 2, 3, 5, 5, 8, 11, 13)
+
+
+def tree_parents(B, N, shape="tree16", *, seed=0):
+    """Parent links [B, N] int32 (entry 0 is -1; 0 <= parent[n] < n).
+
+    shape: "tree16" (TREE16_PARENTS, N == 16), "chain" (parent n-1), "star" (every node
+    a child of the root), "random" (per request: parent n-1 with probability 1/2, else
+    uniform over 0..n-1), or an explicit sequence of N links shared by every request.
+    """
+    if isinstance(shape, str):
+        if shape == "tree16":
+            assert N == len(TREE16_PARENTS)
+            par = np.tile(np.array(TREE16_PARENTS, np.int32), (B, 1))
+        elif shape == "chain":
+            par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+        elif shape == "star":
+            par = np.zeros((B, N), np.int32)
+            par[:, 0] = -1
+        elif shape == "random":
+            rng = np.random.default_rng(int(seed) + 5000)
+            par = np.zeros((B, N), np.int32)
+            par[:, 0] = -1
+            for n in range(1, N):
+                deep = rng.random(B) < 0.5
+                par[:, n] = np.where(deep, n - 1, rng.integers(0, n, size=B))
+        else:
+            raise ValueError(shape)
+    else:
+        par = np.tile(np.asarray(shape, np.int32).reshape(1, N), (B, 1))
+    return torch.from_numpy(np.ascontiguousarray(par))
+
+
+def tree_inputs(B, N, V, *, dtype=torch.bfloat16, temperature=1.0, target_sigma=3.0,
+                draft_sigma=1.0, peak_prob=0.0, peak_height=12.0, shape="tree16",
+                n_nodes="full", seed=0, device="cpu"):
+    """Inputs of one tree verification call.
+
+    target [B,N,V] ~ N(0, target_sigma^2), each row peaked (+peak_height at one uniform
+    index) with probability peak_prob; draft [B,N,V] = target + N(0, draft_sigma^2),
+    both rounded to ``dtype``. parent [B,N] from ``tree_parents``. The token of node n
+    is an independent sample of softmax(draft[b, parent[n]] / T') from the rounded
+    draft logits (Gumbel-max), T' = temperature, or 1 at T == 0 so that siblings differ.
+    n_nodes: "full" (= N), "uniform" (U{1..N}), or an int sequence of length B.
+    uniforms [B,N] ~ U[0,1) float32.
+    """
+    g = _gen(device, seed)
+    par = tree_parents(B, N, shape, seed=seed).to(device)
+    target = torch.empty((B, N, V), dtype=dtype, device=device)
+    draft = torch.empty((B, N, V), dtype=dtype, device=device)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=device)
+    t_draw = temperature if temperature > 0.0 else 1.0
+    rb = max(1, _CHUNK_ELEMS // (N * V))
+    for b0 in range(0, B, rb):
+        b1 = min(B, b0 + rb)
+        n = b1 - b0
+        t32 = torch.randn((n, N, V), generator=g, device=device) * target_sigma
+        if peak_prob > 0.0:
+            hit = torch.rand((n, N), generator=g, device=device) < peak_prob
+            where = torch.randint(0, V, (n, N), generator=g, device=device)
+            t32.scatter_add_(2, where.unsqueeze(-1), (hit.float() * peak_height).unsqueeze(-1))
+        d32 = t32 + torch.randn((n, N, V), generator=g, device=device) * draft_sigma
+        target[b0:b1] = t32.to(dtype)
+        draft[b0:b1] = d32.to(dtype)
+        del t32, d32
+        # Row of the parent of every node (node 0 reads its own row; its token is unused).
+        src = par[b0:b1].clamp_min(0).long()
+        d = torch.gather(draft[b0:b1].float(), 1, src.unsqueeze(-1).expand(n, N, V))
+        e = torch.rand((n, N, V), generator=g, device=device).clamp_min_(1e-30)
+        d = d / t_draw - torch.log(-torch.log(e))
+        del e
+        tok[b0:b1] = torch.argmax(d, dim=-1).to(torch.int32)
+        del d
+    tok[:, 0] = 0
+    if isinstance(n_nodes, str) and n_nodes == "full":
+        nn = torch.full((B,), N, dtype=torch.int32, device=device)
+    elif isinstance(n_nodes, str) and n_nodes == "uniform":
+        nn = torch.randint(1, N + 1, (B,), generator=g, device=device).to(torch.int32)
+    else:
+        nn = torch.as_tensor(list(n_nodes), dtype=torch.int32).to(device)
+        assert nn.numel() == B
+    uniforms = torch.rand((B, N), generator=g, device=device, dtype=torch.float32)
+    return {"target": target, "draft": draft, "parent": par, "draft_tok": tok,
+            "n_nodes": nn, "uniforms": uniforms}
+
+
+def tree_qwen3(temperature, seed=0, device="cpu", B=64):
+    """B=64 trees of 16 nodes (TREE16_PARENTS), V=151,936 bf16; target N(0,3^2) with
+    rows peaked (+12) w.p. 0.2; draft noise N(0,1)."""
+    return tree_inputs(B, 16, QWEN3_VOCAB, dtype=torch.bfloat16, temperature=temperature,
+                       target_sigma=3.0, draft_sigma=1.0, peak_prob=0.2, peak_height=12.0,
+                       shape="tree16", seed=seed, device=device)
+
+
+def tree_path_bytes(out_path, out_accepted, parent, V, elem_bytes, greedy=False):
+    """Logit bytes a tree walk must read: the target row of every node on the accepted
+    path plus the stop node, and (unless greedy) the draft row of each of those nodes
+    that has children."""
+    par = torch.as_tensor(parent).cpu().numpy()
+    path = torch.as_tensor(out_path).cpu().numpy()
+    acc = torch.as_tensor(out_accepted).cpu().numpy()
+    rows = 0
+    for b in range(par.shape[0]):
+        if acc[b] < 0:
+            continue
+        nodes = [0] + [int(x) for x in path[b, :acc[b]]]
+        rows += len(nodes)
+        if not greedy:
+            rows += sum(1 for c in nodes if (par[b, c + 1:] == c).any())
+    return rows * V * elem_bytes

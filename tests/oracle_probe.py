@@ -45,3 +45,35 @@ def softmax64(z, T):
     z = np.asarray(z, dtype=np.float64) / T
     e = np.exp(z - z.max())
     return e / e.sum()
+
+
+def intervals_batch(fb, grid=GRID, tol=TOL):
+    """intervals() for a function evaluated on many uniforms at once: fb maps a float64
+    array of uniforms to an integer array of values. Returns {value: total length}."""
+    us = np.linspace(0.0, 1.0, grid + 1)
+    us[-1] = 1.0 - 1e-16
+    vals = np.asarray(fb(us))
+    step = np.nonzero(vals[:-1] != vals[1:])[0]
+    active = [(us[i], us[i + 1], vals[i], vals[i + 1]) for i in step]
+    cuts = []  # (position, value to the right)
+    while active:
+        mids = np.array([0.5 * (lo + hi) for lo, hi, _, _ in active])
+        fm = np.asarray(fb(mids))
+        nxt = []
+        for (lo, hi, flo, fhi), mid, v in zip(active, mids, fm):
+            for a, b, fa, fb_ in ((lo, mid, flo, v), (mid, hi, v, fhi)):
+                if fa == fb_:
+                    continue
+                if b - a < tol:
+                    cuts.append((0.5 * (a + b), fb_))
+                else:
+                    nxt.append((a, b, fa, fb_))
+        active = nxt
+    cuts.sort()
+    mass = {}
+    pos, cur = 0.0, vals[0]
+    for c, v in cuts:
+        mass[cur] = mass.get(cur, 0.0) + (c - pos)
+        pos, cur = c, v
+    mass[cur] = mass.get(cur, 0.0) + (1.0 - pos)
+    return {int(k): v for k, v in mass.items()}

@@ -167,3 +167,42 @@ def test_curve_pins_catch(oracle_mod, tmp_path, name):
         except AssertionError:
             failed += 1
     assert failed > 0, name
+
+
+TREE_MUTANTS = {
+    "tree: residual never updated": ("for (int v = 0; v < V; v++) r[v] = w[v] / Z;",
+                                     "for (int v = 0; v < V; v++) r[v] = r[v];"),
+    "tree: residual ignores q": ("w[v] = r[v] - q[v] > 0.0 ? r[v] - q[v] : 0.0;",
+                                 "w[v] = r[v] > 0.0 ? r[v] : 0.0;"),
+    "tree: terminal sample from p": ("int y = inverse_cdf(wlast, V, u[base], &Z, &gap);",
+                                     "int y = inverse_cdf(p, V, u[base], &Z, &gap);"),
+    "tree: non-children tested": ("if (par[base + n] != c) continue;",
+                                  "if (par[base + n] < 0) continue;"),
+    "tree: test uses the parent's uniform": ("const double un = u[base + n];",
+                                             "const double un = u[base + c];"),
+    "tree: greedy takes the last matching child": (
+        "for (int n = c + 1; n < nn && next < 0; n++)",
+        "for (int n = c + 1; n < nn; n++)"),
+    "tree: leaf bonus uses a test uniform": (
+        "int y = inverse_cdf(p, V, u[base], &Z, &gap);\n            if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;\n            if (gap < margin) margin = gap;\n            if (out_margin)",
+        "int y = inverse_cdf(p, V, u[base + c], &Z, &gap);\n            if (gap < NEAR_TIE) out_flags[b] |= ORC_FLAG_CDF_EDGE;\n            if (gap < margin) margin = gap;\n            if (out_margin)"),
+    "tree: accept test against q": ("if (un * qx < rx) {\n                next = n;",
+                                    "if (un * rx < qx) {\n                next = n;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TREE_MUTANTS))
+def test_tree_pins_catch(oracle_mod, tmp_path, name):
+    import test_oracle_tree as tt
+
+    old, new = TREE_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    failed = 0
+    for t in tt.PINS:
+        try:
+            t(lib)
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name
