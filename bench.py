@@ -589,6 +589,84 @@ def run_markov(args):
               flush=True)
 
 
+def run_tree(args):
+    """One JSON line per temperature: tree verification of B=64 trees of 16 nodes
+    (V=151,936 bf16), timed per call inside a CUDA graph with an L2 flush before each
+    call. Algorithmic bytes are the rows the walk must read (the target row of every node
+    on the accepted path and of the stop node, and the draft row of each of those with
+    children), from the call's own outputs."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    peak, _ = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ws = sv.Workspace(1, 1, 1, device=dev)
+    for T in (1.0, 0.0):
+        inp = synth.tree_qwen3(T, seed=1, device=dev)
+        B, N, V = inp["target"].shape
+        outs = [torch.empty((B, N), dtype=torch.int32, device=dev),
+                torch.empty(B, dtype=torch.int32, device=dev),
+                torch.empty((B, N), dtype=torch.int32, device=dev)]
+
+        def call():
+            sv.sv_verify_tree(inp["target"], inp["draft"] if T > 0 else None, inp["parent"],
+                              inp["draft_tok"], inp["n_nodes"],
+                              inp["uniforms"] if T > 0 else None, T, ws, *outs, stream=st)
+
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                call()
+        st.synchronize()
+        n = 30
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(n)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            for i in range(n):
+                flush.zero_()
+                evs[i][0].record(st)
+                call()
+                evs[i][1].record(st)
+        with torch.cuda.stream(st):
+            graph.replay()
+        st.synchronize()
+        us = sorted(e[0].elapsed_time(e[1]) * 1e3 for e in evs)[n // 2]
+        if ws.status(stream=st) != sv.SV_OK:
+            raise RuntimeError("device status not OK in the tree timing")
+        acc = outs[1].cpu()
+        nbytes = synth.tree_path_bytes(outs[2], acc, inp["parent"], V, 2, greedy=T == 0)
+        all_rows = B * N * V * 2 * (1 if T == 0 else 2)
+        emitted = int((acc + 1).sum())
+        print(json.dumps({"tree": True, "B": B, "N": N, "V": V, "T": T, "dtype": "bf16",
+                          "shape": "tree16", "us": us, "mean_accepted": float(acc.float().mean()),
+                          "tokens_per_s": emitted / (us / 1e6),
+                          "algorithmic_bytes": nbytes, "all_rows_bytes": all_rows,
+                          "gbs": nbytes / (us / 1e6) / 1e9,
+                          "frac_hbm": nbytes / (us / 1e6) / 1e9 / peak,
+                          "timing": "median of 30 in-graph call events, L2 flushed before "
+                                    "each call"}), flush=True)
+
+
+def run_tree_once(args):
+    """N untimed tree verification calls on the bench's tree workload (for ncu)."""
+    import speculative_decoding_verification_79_gb300 as sv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    inp = synth.tree_qwen3(1.0, seed=1, device=dev)
+    ws = sv.Workspace(1, 1, 1, device=dev)
+    for _ in range(args.once):
+        sv.sv_verify_tree(inp["target"], inp["draft"], inp["parent"], inp["draft_tok"],
+                          inp["n_nodes"], inp["uniforms"], 1.0, ws)
+    torch.cuda.synchronize()
+    status = ws.status()
+    print(json.dumps({"tree_once": args.once, "status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def run_curve_once(args):
     """N untimed calls of the throughput-curve schedule at B=64, K=8 (for ncu captures)."""
     import speculative_decoding_verification_79_gb300 as sv
@@ -664,12 +742,16 @@ def main():
                     help="time the calibrated schedule and the calibration-loop kernels")
     ap.add_argument("--markov", action="store_true",
                     help="time the Markov logit-bias drafting loop")
+    ap.add_argument("--tree", action="store_true",
+                    help="time tree (multi-candidate) verification")
     ap.add_argument("--once", type=int, default=0,
                     help="no timing: build one input set and run N schedule+verify steps "
                          "(a short, self-contained program for profilers)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.once > 0 and args.tree:
+        run_tree_once(args)
     elif args.once > 0 and args.markov:
         run_markov_once(args)
     elif args.once > 0 and args.calib:
@@ -682,6 +764,8 @@ def main():
         run_calib(args)
     elif args.markov:
         run_markov(args)
+    elif args.tree:
+        run_tree(args)
     else:
         run_gpu(args)
 

@@ -62,6 +62,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_MARKOV_R 256   /* rank of the Markov logit-bias head */
 #define SV_MAX_CURVE 64       /* points of a throughput curve */
 #define SV_MAX_CURVE_BK 8192  /* B*K of a throughput-curve schedule */
+#define SV_MAX_TREE 64        /* nodes of a draft tree */
 
 /*
  * sv_workspace_bytes: size of the device workspace needed by sv_schedule and
@@ -279,6 +280,54 @@ sv_status sv_verify_diag(const void *target_d, const void *draft_d, sv_dtype dty
                          int32_t *out_tok_d, int32_t *out_accepted_d, float *out_p_d,
                          float *out_q_d, uint32_t *accept_count_d, uint32_t *tested_count_d,
                          void *ws_d, size_t ws_bytes, void *stream);
+
+/*
+ * sv_verify_tree: verification of drafted token trees (multi-candidate rejection
+ * sampling). The DSpark Guide names tree verification without defining it ("Deep
+ * Dive into the DSpark Architecture", step 4, "tree / sequence mask"; "3.
+ * Comprehensive Technical Feature Matrix", "Static / Tree"); this call takes the
+ * lossless reading that reduces to sv_verify when every node has at most one child.
+ *
+ *  target_d   [B, N, V] target logits (dtype): row n = the target's prediction after
+ *             the path from node 0 to node n (node 0 = the committed context).
+ *  draft_d    [B, N, V] draft logits (dtype): row n = the distribution the children
+ *             of node n were drawn from, independently. Read only for nodes with
+ *             children that the walk reaches; not read at T == 0 (may be NULL then).
+ *  parent_d   [B, N] int32: parent of node n (0 <= parent < n for 1 <= n < n_nodes);
+ *             entry 0 is ignored.
+ *  draft_tok_d [B, N] int32: the drafted token of node n >= 1; entry 0 is ignored.
+ *  n_nodes_d  [B] int32 in [1, N]: nodes in use (nodes at or past it are ignored).
+ *  uniforms_d [B, N] float32 in [0,1): u_{b,n} (n >= 1) drives the test of node n,
+ *             u_{b,0} the terminal sample. Not read at T == 0 (may be NULL then).
+ *  temperature  as sv_verify.
+ *  out_tok_d  [B, N] int32: tokens of the accepted path, then the terminal token,
+ *             then -1.
+ *  out_accepted_d [B] int32: accepted drafted tokens (the depth of the path), or -1.
+ *  out_path_d [B, N] int32 or NULL: node index of each accepted token, then -1 (the
+ *             nodes whose KV entries the caller keeps).
+ *  ws_d       any workspace of at least 256 bytes (only its status word is used).
+ *
+ *  Per request: the walk starts at node 0. At node c the children are tested in
+ *  index order against a residual r that starts as p_c: child n with token x is
+ *  accepted iff u_{b,n} * q_c(x) < r(x) and the walk moves to n; after a rejection
+ *  r <- normalize(max(0, r - q_c)) (if no mass is left, r restarts from p_c). When
+ *  every child is rejected the terminal token is the inverse-CDF sample of r at
+ *  u_{b,0}; at a leaf it is sampled from p_c. At T == 0 the first child drafting the
+ *  lowest-index argmax of target row c is accepted, else that argmax is emitted. The
+ *  emitted tokens follow the target distribution exactly when siblings are
+ *  independent draws from the parent's draft distribution.
+ *  Only rows the walk reaches are read; a reached row with NaN or +inf (or all -inf),
+ *  a bad parent link or token, n_nodes outside [1, N] or a uniform outside [0,1) make
+ *  the request invalid: its outputs are -1 and SV_ERR_DEVICE_INPUT is set.
+ *  Arithmetic: fp32 softmax statistics and weights, float-float sums and prefixes.
+ *  Limits: 0 <= B <= SV_MAX_B, 1 <= N <= SV_MAX_TREE, 1 <= V <= SV_MAX_V.
+ */
+sv_status sv_verify_tree(const void *target_d, const void *draft_d, sv_dtype dtype,
+                         const int32_t *parent_d, const int32_t *draft_tok_d,
+                         const int32_t *n_nodes_d, const float *uniforms_d, int B, int N,
+                         int V, float temperature, int32_t *out_tok_d,
+                         int32_t *out_accepted_d, int32_t *out_path_d, void *ws_d,
+                         size_t ws_bytes, void *stream);
 
 /*
  * sv_get_status: wait for `stream`, then read the sticky status word of the

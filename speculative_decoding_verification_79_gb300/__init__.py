@@ -70,6 +70,9 @@ def load(build_if_missing: bool = True):
     lib.sv_verify_diag.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp,
                                    vp, vp, vp, sz, vp]
     lib.sv_verify_diag.restype = i32
+    lib.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp,
+                                   vp, sz, vp]
+    lib.sv_verify_tree.restype = i32
     lib.sv_get_status.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.sv_get_status.restype = i32
     lib.sv_status_string.argtypes = [i32]
@@ -312,3 +315,35 @@ def sv_verify(target, draft, draft_tok, verify_len, uniforms, temperature, ws: W
                        _ptr(out_tok), _ptr(out_accepted), _ptr(ws.t), ws.nbytes, _stream(stream))
     _check("sv_verify", rc)
     return out_tok, out_accepted
+
+
+def sv_verify_tree(target, draft, parent, draft_tok, n_nodes, uniforms, temperature,
+                   ws: Workspace, out_tok=None, out_accepted=None, out_path=None,
+                   want_path=True, stream=None):
+    """Tree (multi-candidate) verification (see specverify.h).
+
+    target, draft [B,N,V] (bf16 or fp32; draft/uniforms may be None at T=0), parent and
+    draft_tok [B,N] int32, n_nodes [B] int32, uniforms [B,N] float32. Any workspace works
+    (only its status word is used). Returns (out_tok [B,N], out_accepted [B], out_path
+    [B,N] or None).
+    """
+    target = _dev(target, "target")
+    B, N, V = target.shape
+    draft = _dev(draft, "draft", target.dtype)
+    parent = _dev(parent, "parent", torch.int32)
+    draft_tok = _dev(draft_tok, "draft_tok", torch.int32)
+    n_nodes = _dev(n_nodes, "n_nodes", torch.int32)
+    uniforms = _dev(uniforms, "uniforms", torch.float32)
+    dev = target.device
+    if out_tok is None:
+        out_tok = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_accepted is None:
+        out_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_path is None and want_path:
+        out_path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    rc = load().sv_verify_tree(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(parent),
+                               _ptr(draft_tok), _ptr(n_nodes), _ptr(uniforms), B, N, V,
+                               float(temperature), _ptr(out_tok), _ptr(out_accepted),
+                               _ptr(out_path), _ptr(ws.t), ws.nbytes, _stream(stream))
+    _check("sv_verify_tree", rc)
+    return out_tok, out_accepted, out_path

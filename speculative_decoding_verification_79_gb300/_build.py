@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
-SOURCES = ["sv_api.cu", "sv_verify.cu", "sv_schedule.cu", "sv_static.cu", "sv_calib.cu", "sv_markov.cu"]
+SOURCES = ["sv_api.cu", "sv_verify.cu", "sv_schedule.cu", "sv_static.cu", "sv_calib.cu", "sv_markov.cu",
+           "sv_tree.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

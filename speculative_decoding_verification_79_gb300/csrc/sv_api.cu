@@ -4,6 +4,7 @@
 #include <cmath>
 
 #include "sv_common.cuh"
+#include "sv_tree.cuh"
 
 namespace sv {
 
@@ -237,6 +238,53 @@ sv_status sv_verify(const void* target_d, const void* draft_d, sv_dtype dtype,
   return sv_verify_diag(target_d, draft_d, dtype, draft_tok_d, verify_len_d, uniforms_d, B, K, V,
                         temperature, out_tok_d, out_accepted_d, nullptr, nullptr, nullptr,
                         nullptr, ws_d, ws_bytes, stream);
+}
+
+sv_status sv_verify_tree(const void* target_d, const void* draft_d, sv_dtype dtype,
+                         const int32_t* parent_d, const int32_t* draft_tok_d,
+                         const int32_t* n_nodes_d, const float* uniforms_d, int B, int N, int V,
+                         float temperature, int32_t* out_tok_d, int32_t* out_accepted_d,
+                         int32_t* out_path_d, void* ws_d, size_t ws_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B > SV_MAX_B || N < 1 || N > SV_MAX_TREE || V < 1 || V > SV_MAX_V)
+    return SV_ERR_SHAPE;
+  const bool greedy = temperature == 0.f;
+  if (!std::isfinite(temperature) || temperature < 0.f ||
+      (!greedy && (temperature < 1e-6f || temperature > 1e6f)))
+    return SV_ERR_ARG;
+  if (!ws_d || !aligned(ws_d, 256) || ws_bytes < sizeof(WsHeader)) return SV_ERR_WORKSPACE;
+  if (B == 0) return SV_OK;
+  const size_t eb = dtype == SV_BF16 ? 2 : 4;
+  if (!target_d || !parent_d || !draft_tok_d || !n_nodes_d || !out_tok_d || !out_accepted_d)
+    return SV_ERR_ARG;
+  if (!greedy && (!draft_d || !uniforms_d)) return SV_ERR_ARG;
+  if (!aligned(target_d, eb) || (draft_d && !aligned(draft_d, eb)) || !aligned(parent_d, 4) ||
+      !aligned(draft_tok_d, 4) || !aligned(n_nodes_d, 4) ||
+      (uniforms_d && !aligned(uniforms_d, 4)) || !aligned(out_tok_d, 4) ||
+      !aligned(out_accepted_d, 4) || (out_path_d && !aligned(out_path_d, 4)))
+    return SV_ERR_ARG;
+  TreeArgs A;
+  A.tgt = target_d;
+  A.drf = greedy ? nullptr : draft_d;
+  A.par = parent_d;
+  A.tok = draft_tok_d;
+  A.nn = n_nodes_d;
+  A.uni = greedy ? nullptr : uniforms_d;
+  A.B = B;
+  A.N = N;
+  A.V = V;
+  {
+    const double ad = greedy ? 0.0 : 1.4426950408889634 / (double)temperature;
+    A.a = (float)ad;
+    A.a_lo = (float)(ad - (double)A.a);
+  }
+  A.out_tok = out_tok_d;
+  A.out_acc = out_accepted_d;
+  A.out_path = out_path_d;
+  A.hdr = static_cast<WsHeader*>(ws_d);
+  const cudaError_t e = launch_tree(A, dtype == SV_BF16, greedy,
+                                    static_cast<cudaStream_t>(stream), nullptr);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status sv_get_status(void* ws_d, void* stream, int clear, int32_t* status_out) {

@@ -1,0 +1,848 @@
+// sv_tree.cu -- verification of drafted token trees (multi-candidate rejection
+// sampling), sm_103a.
+//
+// Method. The DSpark Guide names tree verification ("Deep Dive into the DSpark
+// Architecture", step 4: the verified prefix goes to the target "with tree / sequence
+// mask"; "3. Comprehensive Technical Feature Matrix": "Static / Tree" verification) and
+// the DSpark Deep Dive ("The Speculative Decoding Solution") gives the chain rule it
+// extends. Reading implemented here: the walk starts at node 0; at node c the children
+// are tested in index order against a residual distribution r that starts as p_c; child
+// n with token x is accepted when u_n * q_c(x) < r(x), and the walk moves to n; after a
+// rejection r <- normalize(max(0, r - q_c)). When every child is rejected the token is
+// sampled from r by inverse CDF at u_{b,0}; at a leaf, from p_c. At T == 0 the first
+// child drafting the lowest-index argmax of p_c is accepted, else that argmax is emitted.
+//
+// Closed form. After i rejections r = max(0, p - lam_i q) / W_i, with lam_0 = 0,
+// W_0 = 1, lam_{i+1} = lam_i + W_i and W_{i+1} = sum_v max(0, p_v - lam_{i+1} q_v)
+// (because max(0, max(0, a) - b) = max(0, a - b) for b >= 0). A rejection therefore
+// costs one pass over the node's two rows, and no residual is ever stored.
+//
+// Layout. One cluster of C CTAs per request (C = 1..8, picked by the host so the batch
+// is resident at once). Each row is cut into 16-byte vectors on a grid anchored at the
+// row's own alignment, 32 vectors make a tile, and each CTA owns a contiguous range of
+// tiles, each warp a contiguous sub-range (lanes read consecutive vectors: coalesced).
+// Per visited node the cluster makes one pass for the softmax statistics of both rows
+// (argmax of the target row at T == 0), one pass per rejection for W, and samples from
+// the last pass's totals in three levels (CTA, warp group of tiles, element). Partial
+// results meet in distributed shared memory behind hardware cluster barriers; every CTA
+// merges the C partials in rank order, so all CTAs reach bit-identical values, take the
+// same branches and arrive at the same barriers. Only rows the walk reaches are read.
+#include <cfloat>
+#include <atomic>
+#include <cooperative_groups.h>
+
+#include "sv_tree.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+namespace {
+
+constexpr int TW = 16;          // warps per CTA
+constexpr int TT = 32 * TW;     // threads per CTA
+constexpr int UNR = 4;          // tiles a lane has in flight
+constexpr int NGRP = 32;        // group totals kept per warp for the inverse CDF
+constexpr int MAXC = 8;         // largest cluster
+constexpr unsigned FULLM = 0xffffffffu;
+
+template <typename T>
+struct EV;
+template <>
+struct EV<uint16_t> {
+  static constexpr int VEC = 8;
+};
+template <>
+struct EV<float> {
+  static constexpr int VEC = 4;
+};
+
+__device__ __forceinline__ float logit_at(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float logit_at(const uint16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(p)) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 v, float* z) {
+  if constexpr (EV<T>::VEC == 8) {
+    z[0] = bf_lo(v.x); z[1] = bf_hi(v.x); z[2] = bf_lo(v.y); z[3] = bf_hi(v.y);
+    z[4] = bf_lo(v.z); z[5] = bf_hi(v.z); z[6] = bf_lo(v.w); z[7] = bf_hi(v.w);
+  } else {
+    z[0] = __uint_as_float(v.x); z[1] = __uint_as_float(v.y);
+    z[2] = __uint_as_float(v.z); z[3] = __uint_as_float(v.w);
+  }
+}
+
+// Vector j of a row on the grid anchored at element offset `off`: elements
+// [j*VEC - off, j*VEC - off + VEC), -inf outside [0, V). `fast`: this row's own
+// 16-byte boundaries fall on the grid, so whole in-range vectors are one 16-byte load.
+template <typename T>
+__device__ __forceinline__ uint4 fetch(const T* p, bool fast, int V, int off, int j) {
+  constexpr int VEC = EV<T>::VEC;
+  const int e0 = j * VEC - off;
+  if (fast && e0 >= 0 && e0 + VEC <= V) return __ldg(reinterpret_cast<const uint4*>(p + e0));
+  uint32_t w[4];
+  if constexpr (VEC == 8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + 2 * i;
+      const uint32_t lo = (e >= 0 && e < V) ? static_cast<uint32_t>(__ldg(p + e)) : 0xff80u;
+      const uint32_t hi = (e + 1 >= 0 && e + 1 < V) ? static_cast<uint32_t>(__ldg(p + e + 1))
+                                                    : 0xff80u;
+      w[i] = lo | (hi << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i;
+      w[i] = (e >= 0 && e < V) ? __float_as_uint(__ldg(p + e)) : 0xff800000u;
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ int row_off(const T* p) {
+  return static_cast<int>((reinterpret_cast<uintptr_t>(p) & 15u) / sizeof(T));
+}
+
+// ---------------------------------------------------------------------------
+// Float-float values (hi + lo, about 48 significant bits) for sums and prefixes.
+// ---------------------------------------------------------------------------
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  return ff{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp))};
+}
+__device__ __forceinline__ ff ff_norm(float s, float e) {
+  const float h = __fadd_rn(s, e);
+  return ff{h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+// Commutative bit for bit (the TwoSum error is exact whatever the order).
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const ff s = ff_two_sum(a.hi, b.hi);
+  return ff_norm(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_mul_f(ff a, float u) {
+  const float p = __fmul_rn(a.hi, u);
+  return ff_norm(p, fmaf(a.lo, u, fmaf(a.hi, u, -p)));
+}
+__device__ __forceinline__ bool ff_lt(ff a, ff b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+__device__ __forceinline__ ff ff_shfl_xor(ff x, int o) {
+  return ff{__shfl_xor_sync(FULLM, x.hi, o), __shfl_xor_sync(FULLM, x.lo, o)};
+}
+__device__ __forceinline__ ff ff_warp_sum(ff x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
+  return x;
+}
+__device__ __forceinline__ ff ff_warp_incl_scan(ff x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff y{__shfl_up_sync(FULLM, x.hi, o), __shfl_up_sync(FULLM, x.lo, o)};
+    if (lane >= o) x = ff_add(y, x);
+  }
+  return x;
+}
+// Compensated accumulation of a float into (s, c).
+__device__ __forceinline__ void acc2(float& s, float& c, float w) {
+  const float t = __fadd_rn(s, w);
+  const float bp = __fsub_rn(t, s);
+  c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(w, bp)));
+  s = t;
+}
+
+// ---------------------------------------------------------------------------
+// Softmax statistics: m = running max of the raw logits, F = fl(m*a) the frame,
+// S = sum of 2^(z*(a + a_lo) - F) (float-float).
+// ---------------------------------------------------------------------------
+struct Soft {
+  float m, F;
+  ff S;
+};
+
+__device__ __forceinline__ Soft soft_empty() { return Soft{-INFINITY, 0.f, ff{0.f, 0.f}}; }
+
+// Unnormalised weight 2^(z*(a + a_lo) - F) of one logit in frame F; 0 for -inf (the clamp
+// keeps -inf * a_lo from meeting +inf).
+__device__ __forceinline__ float term(float z, float a, float alo, float F) {
+  const float zc = fmaxf(z, -FLT_MAX);
+  return ex2(fmaf(zc, alo, fmaf(zc, a, -F)));
+}
+
+// The same with the exponent carried in two floats (exact product error by fma, TwoSum
+// error of the subtraction), for the probabilities the accept tests use.
+__device__ __forceinline__ float term_precise(float z, float a, float alo, float F) {
+  if (!(z > -INFINITY)) return 0.f;
+  const float ph = __fmul_rn(z, a);
+  const float pl = fmaf(z, a, -ph);
+  const float yh = __fsub_rn(ph, F);
+  const float bp = __fsub_rn(yh, ph);
+  const float el = __fadd_rn(__fsub_rn(ph, __fsub_rn(yh, bp)), __fsub_rn(-F, bp));
+  const float yl = fmaf(z, alo, __fadd_rn(pl, el));
+  const float e = ex2(yh);
+  return fmaf(e, __fmul_rn(yl, 0.6931471805599453f), e);
+}
+
+template <int VEC>
+__device__ __forceinline__ void soft_add(Soft& s, const float* z, float a, float alo,
+                                         bool& bad) {
+  float vm = z[0];
+#pragma unroll
+  for (int i = 1; i < VEC; ++i) vm = fmaxf(vm, z[i]);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) bad |= (z[i] != z[i]) || (z[i] == INFINITY);
+  if (vm > s.m) {
+    const float Fn = __fmul_rn(vm, a);
+    const float f = (s.m == -INFINITY) ? 0.f : ex2(__fsub_rn(s.F, Fn));
+    s.S = ff_mul_f(s.S, f);
+    s.m = vm;
+    s.F = Fn;
+  }
+  if (s.m == -INFINITY) return;
+  float t[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) t[i] = term(z[i], a, alo, s.F);
+  float sum;
+  if constexpr (VEC == 8) {
+    sum = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+  } else {
+    sum = (t[0] + t[1]) + (t[2] + t[3]);
+  }
+  const ff r = ff_two_sum(s.S.hi, sum);
+  s.S = ff_norm(r.hi, __fadd_rn(r.lo, s.S.lo));
+}
+
+// Merge of two statistics; symmetric bit for bit.
+__device__ __forceinline__ Soft soft_merge(const Soft& x, const Soft& y, float a) {
+  if (y.m == -INFINITY) return x;
+  if (x.m == -INFINITY) return y;
+  const float mn = fmaxf(x.m, y.m);
+  const float Fn = __fmul_rn(mn, a);
+  const float fx = (x.m == mn) ? 1.f : ex2(__fsub_rn(x.F, Fn));
+  const float fy = (y.m == mn) ? 1.f : ex2(__fsub_rn(y.F, Fn));
+  return Soft{mn, Fn, ff_add(ff_mul_f(x.S, fx), ff_mul_f(y.S, fy))};
+}
+
+__device__ __forceinline__ Soft soft_shfl_xor(const Soft& s, int o) {
+  return Soft{__shfl_xor_sync(FULLM, s.m, o), __shfl_xor_sync(FULLM, s.F, o),
+              ff_shfl_xor(s.S, o)};
+}
+
+__device__ __forceinline__ Soft soft_warp(Soft s, float a) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s = soft_merge(s, soft_shfl_xor(s, o), a);
+  return s;
+}
+
+// Argmax with ties to the lowest index.
+__device__ __forceinline__ void arg_merge(float& best, int& idx, float b2, int i2) {
+  if (b2 > best || (b2 == best && i2 < idx)) {
+    best = b2;
+    idx = i2;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Residual and sample weights: w = max(0, p - lam*q), or p when use_d is false.
+// p = 2^(zt*(a + a_lo) - Ft) * iSt, q likewise; lq = lam * iSd.
+// ---------------------------------------------------------------------------
+struct WPar {
+  float a, alo, Ft, iSt, Fd, lq;
+  bool use_d;
+};
+
+__device__ __forceinline__ float weight(const WPar& P, float zt, float zd) {
+  const float pt = __fmul_rn(term(zt, P.a, P.alo, P.Ft), P.iSt);
+  if (!P.use_d) return pt;
+  return fmaxf(fmaf(-P.lq, term(zd, P.a, P.alo, P.Fd), pt), 0.f);
+}
+
+template <typename T>
+__device__ __forceinline__ float vec_weights(const WPar& P, uint4 vt, uint4 vd, float* w) {
+  constexpr int VEC = EV<T>::VEC;
+  float zt[VEC], zd[VEC];
+  unpack<T>(vt, zt);
+  if (P.use_d) unpack<T>(vd, zd);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) w[i] = weight(P, zt[i], P.use_d ? zd[i] : 0.f);
+  if constexpr (VEC == 8) {
+    return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+  } else {
+    return (w[0] + w[1]) + (w[2] + w[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared state of one CTA.
+// ---------------------------------------------------------------------------
+struct Xch {  // one CTA's partial result, read by the cluster
+  Soft st, sd;
+  float best;
+  int idx;
+  int bad;
+  ff tot;
+};
+
+struct Smem {
+  int par[SV_MAX_TREE];
+  int tok[SV_MAX_TREE];
+  float u[SV_MAX_TREE];
+  int nn;
+  int ok;
+  int dec;
+  int sel_w, sel_g;
+  ff sel_cum;
+  Soft wst[TW], wsd[TW];
+  float wbest[TW];
+  int widx[TW];
+  int wbad[TW];
+  ff wtot[TW];
+  ff gtot[TW][NGRP];
+  ff ctot[MAXC];
+  Xch xch[2];
+  Xch res;
+};
+
+// Tiles [t0, t1) of warp w in CTA `rank` of C, for a row of `ntiles` tiles.
+__device__ __forceinline__ void warp_tiles(int ntiles, int C, int rank, int w, int& t0,
+                                           int& t1) {
+  const int tpc = (ntiles + C - 1) / C;
+  const int c0 = min(ntiles, rank * tpc), c1 = min(ntiles, c0 + tpc);
+  const int tpw = (c1 - c0 + TW - 1) / TW;
+  t0 = min(c1, c0 + w * tpw);
+  t1 = min(c1, t0 + tpw);
+}
+
+__device__ __forceinline__ int group_size(int nt) { return max(1, (nt + NGRP - 1) / NGRP); }
+
+// First item whose running total passes `target` (items of zero total never qualify);
+// `cum` enters as the total before item 0 and leaves as the total before the chosen one.
+// If rounding lets no item pass, the last item with a positive total; -1 if none.
+__device__ int select_item(const ff* tot, int n, ff target, ff& cum) {
+  ff c = cum, c_last = cum;
+  int last = -1;
+  for (int i = 0; i < n; ++i) {
+    const ff nx = ff_add(c, tot[i]);
+    if (tot[i].hi > 0.f) {
+      last = i;
+      c_last = c;
+      if (ff_lt(target, nx)) {
+        cum = c;
+        return i;
+      }
+    }
+    c = nx;
+  }
+  cum = c_last;
+  return last;
+}
+
+// ---------------------------------------------------------------------------
+// Passes over one node's rows. Each ends with the cluster-wide result in sm.res and
+// every thread past a CTA barrier.
+// ---------------------------------------------------------------------------
+struct Geo {
+  int V, off, nvec, ntiles, t0, t1;
+};
+
+template <typename T>
+__device__ __forceinline__ Geo make_geo(const T* tr, int V, int C, int rank, int w) {
+  constexpr int VEC = EV<T>::VEC;
+  Geo g;
+  g.V = V;
+  g.off = row_off(tr);
+  g.nvec = (V + g.off + VEC - 1) / VEC;
+  g.ntiles = (g.nvec + 31) / 32;
+  warp_tiles(g.ntiles, C, rank, w, g.t0, g.t1);
+  return g;
+}
+
+// Publishes this CTA's partial (already in sm.xch[buf] by thread 0), waits for the
+// cluster, and merges the C partials in rank order into sm.res (thread 0).
+template <int KIND>
+__device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C, int buf,
+                                         float a) {
+  cl.sync();
+  if (threadIdx.x == 0) {
+    Xch r;
+    r.st = soft_empty();
+    r.sd = soft_empty();
+    r.best = -INFINITY;
+    r.idx = INT_MAX;
+    r.bad = 0;
+    r.tot = ff{0.f, 0.f};
+    for (int k = 0; k < C; ++k) {
+      const Xch* x = cl.map_shared_rank(&sm.xch[buf], k);
+      r.bad |= x->bad;
+      if (KIND == 0) {
+        r.st = soft_merge(r.st, x->st, a);
+        r.sd = soft_merge(r.sd, x->sd, a);
+      } else if (KIND == 1) {
+        arg_merge(r.best, r.idx, x->best, x->idx);
+      } else {
+        const ff t = x->tot;
+        sm.ctot[k] = t;
+        r.tot = ff_add(r.tot, t);
+      }
+    }
+    sm.res = r;
+  }
+  __syncthreads();
+}
+
+// Softmax statistics of the target row (and the draft row when use_d).
+template <typename T>
+__device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, const Geo& g,
+                           const T* tr, const T* dr, bool dfast, bool use_d, float a,
+                           float alo) {
+  constexpr int VEC = EV<T>::VEC;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  Soft st = soft_empty(), sd = soft_empty();
+  bool bad = false;
+  for (int tb = g.t0; tb < g.t1; tb += UNR) {
+    uint4 vt[UNR], vd[UNR];
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      if (tb + k < g.t1) {
+        const int j = (tb + k) * 32 + lane;
+        vt[k] = fetch<T>(tr, true, g.V, g.off, j);
+        if (use_d) vd[k] = fetch<T>(dr, dfast, g.V, g.off, j);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      if (tb + k < g.t1) {
+        float z[VEC];
+        unpack<T>(vt[k], z);
+        soft_add<VEC>(st, z, a, alo, bad);
+        if (use_d) {
+          unpack<T>(vd[k], z);
+          soft_add<VEC>(sd, z, a, alo, bad);
+        }
+      }
+    }
+  }
+  st = soft_warp(st, a);
+  if (use_d) sd = soft_warp(sd, a);
+  const bool wb = __any_sync(FULLM, bad);
+  if (lane == 0) {
+    sm.wst[w] = st;
+    sm.wsd[w] = sd;
+    sm.wbad[w] = wb;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Xch& x = sm.xch[buf];
+    x.st = soft_empty();
+    x.sd = soft_empty();
+    x.bad = 0;
+    for (int k = 0; k < TW; ++k) {
+      x.st = soft_merge(x.st, sm.wst[k], a);
+      if (use_d) x.sd = soft_merge(x.sd, sm.wsd[k], a);
+      x.bad |= sm.wbad[k];
+    }
+  }
+  exchange<0>(sm, cl, C, buf, a);
+  buf ^= 1;
+}
+
+// Maximum and lowest-index argmax of the target row (greedy verification).
+template <typename T>
+__device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, const Geo& g,
+                            const T* tr) {
+  constexpr int VEC = EV<T>::VEC;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float best = -INFINITY;
+  int idx = INT_MAX;
+  bool bad = false;
+  for (int tb = g.t0; tb < g.t1; tb += UNR) {
+    uint4 vt[UNR];
+#pragma unroll
+    for (int k = 0; k < UNR; ++k)
+      if (tb + k < g.t1) vt[k] = fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane);
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      if (tb + k < g.t1) {
+        float z[VEC];
+        unpack<T>(vt[k], z);
+        const int e0 = ((tb + k) * 32 + lane) * VEC - g.off;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+          bad |= (z[i] != z[i]) || (z[i] == INFINITY);
+          if (z[i] > best) {  // elements arrive in increasing index order per lane
+            best = z[i];
+            idx = e0 + i;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float b2 = __shfl_xor_sync(FULLM, best, o);
+    const int i2 = __shfl_xor_sync(FULLM, idx, o);
+    arg_merge(best, idx, b2, i2);
+  }
+  const bool wb = __any_sync(FULLM, bad);
+  if (lane == 0) {
+    sm.wbest[w] = best;
+    sm.widx[w] = idx;
+    sm.wbad[w] = wb;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Xch& x = sm.xch[buf];
+    x.best = -INFINITY;
+    x.idx = INT_MAX;
+    x.bad = 0;
+    for (int k = 0; k < TW; ++k) {
+      arg_merge(x.best, x.idx, sm.wbest[k], sm.widx[k]);
+      x.bad |= sm.wbad[k];
+    }
+  }
+  exchange<1>(sm, cl, C, buf, 0.f);
+  buf ^= 1;
+}
+
+// Sum of the weights over the row (cluster total in sm.res.tot, CTA totals in sm.ctot),
+// keeping per-warp group totals (sm.gtot) and warp totals (sm.wtot) for the sample.
+template <typename T>
+__device__ void wsum_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, const Geo& g,
+                          const T* tr, const T* dr, bool dfast, const WPar& P) {
+  constexpr int VEC = EV<T>::VEC;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nt = g.t1 - g.t0;
+  const int gsz = group_size(nt);
+  ff wt{0.f, 0.f};
+  float ls = 0.f, lc = 0.f;
+  for (int tb = 0; tb < nt; tb += UNR) {
+    uint4 vt[UNR], vd[UNR];
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      if (tb + k < nt) {
+        const int j = (g.t0 + tb + k) * 32 + lane;
+        vt[k] = fetch<T>(tr, true, g.V, g.off, j);
+        if (P.use_d) vd[k] = fetch<T>(dr, dfast, g.V, g.off, j);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      const int lt = tb + k;
+      if (lt < nt) {
+        float wv[VEC];
+        acc2(ls, lc, vec_weights<T>(P, vt[k], P.use_d ? vd[k] : vt[k], wv));
+        if ((lt + 1) % gsz == 0 || lt + 1 == nt) {  // the group ends (warp-uniform)
+          const ff gt = ff_warp_sum(ff_two_sum(ls, lc));
+          if (lane == 0) sm.gtot[w][lt / gsz] = gt;
+          wt = ff_add(wt, gt);
+          ls = 0.f;
+          lc = 0.f;
+        }
+      }
+    }
+  }
+  if (lane == 0) sm.wtot[w] = wt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ff t{0.f, 0.f};
+    for (int k = 0; k < TW; ++k) t = ff_add(t, sm.wtot[k]);
+    sm.xch[buf].tot = t;
+    sm.xch[buf].bad = 0;
+  }
+  exchange<2>(sm, cl, C, buf, 0.f);
+  buf ^= 1;
+}
+
+// Inverse CDF over the weights of the last wsum_pass at target = u * total: CTA, then
+// warp and group (thread 0 of that CTA), then element (that warp). Returns the element
+// in the lane that found it and -1 elsewhere; only the owning CTA finds one.
+template <typename T>
+__device__ int locate(Smem& sm, int C, int rank, const Geo& g, const T* tr, const T* dr,
+                      bool dfast, const WPar& P, float u) {
+  constexpr int VEC = EV<T>::VEC;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const ff target = ff_mul_f(sm.res.tot, u);
+  ff cum{0.f, 0.f};
+  int cs = select_item(sm.ctot, C, target, cum);
+  if (cs < 0) cs = 0;  // no mass at all cannot happen (the largest p weight is ~1)
+  if (cs != rank) return -1;
+  if (threadIdx.x == 0) {
+    int ws = select_item(sm.wtot, TW, target, cum);
+    if (ws < 0) ws = 0;
+    int t0, t1;
+    warp_tiles(g.ntiles, C, rank, ws, t0, t1);
+    const int nt = t1 - t0;
+    const int gsz = group_size(nt);
+    int gs = select_item(sm.gtot[ws], (nt + gsz - 1) / gsz, target, cum);
+    if (gs < 0) gs = 0;
+    sm.sel_w = ws;
+    sm.sel_g = gs;
+    sm.sel_cum = cum;
+  }
+  __syncthreads();
+  if (w != sm.sel_w) return -1;
+  int t0, t1;
+  warp_tiles(g.ntiles, C, rank, w, t0, t1);
+  const int gsz = group_size(t1 - t0);
+  const int ga = t0 + sm.sel_g * gsz, gb = min(t1, ga + gsz);
+  cum = sm.sel_cum;
+  int found = -1, last_pos = -1;
+  for (int t = ga; t < gb; ++t) {
+    const int j = t * 32 + lane;
+    const uint4 vt = fetch<T>(tr, true, g.V, g.off, j);
+    const uint4 vd = P.use_d ? fetch<T>(dr, dfast, g.V, g.off, j) : vt;
+    float wv[VEC];
+    const float s = vec_weights<T>(P, vt, vd, wv);
+    const ff incl = ff_warp_incl_scan(ff{s, 0.f}, lane);
+    const ff excl{__shfl_up_sync(FULLM, incl.hi, 1), __shfl_up_sync(FULLM, incl.lo, 1)};
+    const unsigned hit = __ballot_sync(FULLM, ff_lt(target, ff_add(cum, incl)) && s > 0.f);
+    int lp = -1;  // this lane's last element of positive weight
+#pragma unroll
+    for (int i = 0; i < VEC; ++i)
+      if (wv[i] > 0.f) lp = j * VEC - g.off + i;
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      int e = -1;
+      if (lane == L) {
+        ff c = lane ? ff_add(cum, excl) : cum;
+        for (int i = 0; i < VEC && e < 0; ++i) {
+          if (wv[i] > 0.f) {
+            const ff s2 = ff_two_sum(c.hi, wv[i]);
+            c = ff_norm(s2.hi, __fadd_rn(s2.lo, c.lo));
+            if (ff_lt(target, c)) e = j * VEC - g.off + i;
+          }
+        }
+        if (e < 0) e = lp;  // rounding: the lane's last positive element
+      }
+      found = __shfl_sync(FULLM, e, L);
+      break;
+    }
+    // the last positive element so far (elements grow with lane, then tile)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lp = max(lp, __shfl_xor_sync(FULLM, lp, o));
+    if (lp >= 0) last_pos = lp;
+    cum = ff_add(cum, ff{__shfl_sync(FULLM, incl.hi, 31), __shfl_sync(FULLM, incl.lo, 31)});
+  }
+  if (found < 0) found = last_pos;
+  return lane == 0 ? found : -1;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel: one cluster per request.
+// ---------------------------------------------------------------------------
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
+  __shared__ Smem sm;
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / C;
+  const int tid = threadIdx.x, w = tid >> 5;
+  const int N = A.N, V = A.V;
+  const size_t base = (size_t)b * N;
+  const T* tgt = static_cast<const T*>(A.tgt);
+  const T* drf = static_cast<const T*>(A.drf);
+
+  if (tid < N) {
+    sm.par[tid] = A.par[base + tid];
+    sm.tok[tid] = A.tok[base + tid];
+    sm.u[tid] = GREEDY ? 0.f : A.uni[base + tid];
+  }
+  if (tid == 0) sm.nn = A.nn[b];
+  __syncthreads();
+  if (tid == 0) {
+    const int nn = sm.nn;
+    bool ok = nn >= 1 && nn <= N;
+    for (int n = 1; ok && n < nn; ++n)
+      ok = sm.par[n] >= 0 && sm.par[n] < n && sm.tok[n] >= 0 && sm.tok[n] < V;
+    if (!GREEDY)
+      for (int n = 0; ok && n < nn; ++n) ok = sm.u[n] >= 0.f && sm.u[n] < 1.f;
+    sm.ok = ok;
+  }
+  __syncthreads();
+  const int nn = sm.nn;
+  bool valid = sm.ok != 0;
+  int depth = 0, c = 0, buf = 0;
+  int32_t* otok = A.out_tok + base;
+  int32_t* opath = A.out_path ? A.out_path + base : nullptr;
+  const bool writer = rank == 0 && tid == 0;
+
+  while (valid) {
+    const T* tr = tgt + (base + c) * (size_t)V;
+    const Geo g = make_geo(tr, V, C, rank, w);
+    int first_child = -1;
+    for (int n = c + 1; n < nn; ++n)
+      if (sm.par[n] == c) {
+        first_child = n;
+        break;
+      }
+
+    if (GREEDY) {
+      argmax_pass<T>(sm, cl, C, buf, g, tr);
+      if (sm.res.bad || !(sm.res.best > -INFINITY)) {
+        valid = false;
+        break;
+      }
+      const int am = sm.res.idx;
+      int next = -1;
+      for (int n = c + 1; n < nn && next < 0; ++n)
+        if (sm.par[n] == c && sm.tok[n] == am) next = n;
+      if (next < 0) {
+        if (writer) otok[depth] = am;
+        break;
+      }
+      if (writer) {
+        otok[depth] = sm.tok[next];
+        if (opath) opath[depth] = next;
+      }
+      ++depth;
+      c = next;
+      continue;
+    }
+
+    const bool kids = first_child >= 0;
+    const T* dr = drf + (base + c) * (size_t)V;
+    const bool dfast = kids && row_off(dr) == g.off;
+    stats_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, kids, A.a, A.a_lo);
+    if (sm.res.bad || !(sm.res.st.m > -INFINITY) || (kids && !(sm.res.sd.m > -INFINITY))) {
+      valid = false;
+      break;
+    }
+    // Frames and inverse sums (1/(hi + lo) to float precision).
+    const Soft st = sm.res.st, sd = sm.res.sd;
+    const float iSt = fmaf(-__fdiv_rn(1.f, st.S.hi), __fdiv_rn(st.S.lo, st.S.hi),
+                           __fdiv_rn(1.f, st.S.hi));
+    const float iSd = kids ? fmaf(-__fdiv_rn(1.f, sd.S.hi), __fdiv_rn(sd.S.lo, sd.S.hi),
+                                  __fdiv_rn(1.f, sd.S.hi))
+                           : 0.f;
+    WPar P{A.a, A.a_lo, st.F, iSt, sd.F, 0.f, false};
+    bool totals = false;  // sm.gtot/wtot/ctot hold the weights of P
+    int next = -1;
+    if (kids) {
+      ff lam{0.f, 0.f}, W{1.f, 0.f};
+      for (int n = first_child; n < nn; ++n) {
+        if (sm.par[n] != c) continue;
+        if (tid == 0) {
+          const int x = sm.tok[n];
+          const float px = __fmul_rn(term_precise(logit_at(tr + x), A.a, A.a_lo, st.F), iSt);
+          const float qx = __fmul_rn(term_precise(logit_at(dr + x), A.a, A.a_lo, sd.F), iSd);
+          // u * q(x) < r(x) with r = max(0, p - lam q) / W, division-free.
+          sm.dec = __fmul_rn(__fmul_rn(sm.u[n], qx), W.hi) < fmaxf(fmaf(-lam.hi, qx, px), 0.f);
+        }
+        __syncthreads();
+        if (sm.dec) {
+          next = n;
+          break;
+        }
+        lam = ff_add(lam, W);
+        P = WPar{A.a, A.a_lo, st.F, iSt, sd.F, __fmul_rn(lam.hi, iSd), true};
+        wsum_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, P);
+        if (sm.res.tot.hi > 0.f) {
+          W = sm.res.tot;
+          totals = true;
+        } else {  // no residual mass left: start again from p
+          lam = ff{0.f, 0.f};
+          W = ff{1.f, 0.f};
+          totals = false;
+        }
+      }
+    }
+    if (next >= 0) {
+      if (writer) {
+        otok[depth] = sm.tok[next];
+        if (opath) opath[depth] = next;
+      }
+      ++depth;
+      c = next;
+      continue;
+    }
+    // Terminal sample: the residual after the last rejection, or p (leaf, or restart).
+    if (!totals) {
+      P = WPar{A.a, A.a_lo, st.F, iSt, sd.F, 0.f, false};
+      wsum_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, P);
+    }
+    const int y = locate<T>(sm, C, rank, g, tr, dr, dfast, P, sm.u[0]);
+    if (y >= 0) otok[depth] = y;
+    break;
+  }
+
+  if (writer) {
+    if (!valid) {
+      for (int i = 0; i < N; ++i) {
+        otok[i] = -1;
+        if (opath) opath[i] = -1;
+      }
+      A.out_acc[b] = -1;
+      atomicOr(&A.hdr->status, ST_DEVICE_INPUT);
+    } else {
+      for (int i = depth + 1; i < N; ++i) otok[i] = -1;
+      if (opath)
+        for (int i = depth; i < N; ++i) opath[i] = -1;
+      A.out_acc[b] = depth;
+    }
+  }
+  // No CTA leaves while another may still read its shared memory.
+  cl.sync();
+}
+
+template <typename T, bool G>
+cudaError_t launch_variant(const TreeArgs& A, cudaStream_t st, int* cluster_out) {
+  // Largest cluster (8, 4, 2) for which every request's cluster is resident at once.
+  static std::atomic<int> max_clusters[MAXC + 1];
+  int C = 1;
+  for (int cand = MAXC; cand >= 2; cand >>= 1) {
+    int n = max_clusters[cand].load(std::memory_order_relaxed);
+    if (n == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = cand;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(cand);
+      cfg.blockDim = dim3(TT);
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, tree_kernel<T, G>, &cfg) != cudaSuccess || n < 1)
+        n = -1;
+      (void)cudaGetLastError();
+      max_clusters[cand].store(n, std::memory_order_relaxed);
+    }
+    if (n >= A.B) {
+      C = cand;
+      break;
+    }
+  }
+  if (cluster_out) *cluster_out = C;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(A.B * C);
+  cfg.blockDim = dim3(TT);
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tree_kernel<T, G>, A);
+}
+
+}  // namespace
+
+cudaError_t launch_tree(const TreeArgs& A, bool bf16, bool greedy, cudaStream_t st,
+                        int* cluster_out) {
+  if (bf16)
+    return greedy ? launch_variant<uint16_t, true>(A, st, cluster_out)
+                  : launch_variant<uint16_t, false>(A, st, cluster_out);
+  return greedy ? launch_variant<float, true>(A, st, cluster_out)
+                : launch_variant<float, false>(A, st, cluster_out);
+}
+
+}  // namespace sv

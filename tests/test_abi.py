@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
               "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version",
               "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update",
-              "sv_markov_keys_len", "sv_markov_draft", "sv_schedule_curve"):
+              "sv_markov_keys_len", "sv_markov_draft", "sv_schedule_curve", "sv_verify_tree"):
         assert n in names
 
 
@@ -158,3 +158,27 @@ def test_curve_host_checks(lib):
     assert lib.sv_schedule_curve(*args(npts=65)) == sv.SV_ERR_SHAPE
     assert lib.sv_schedule_curve(*args(B=4096, K=4)) == sv.SV_ERR_SHAPE
     assert lib.sv_schedule_curve(*args(B=0)) == sv.SV_OK
+
+
+def test_tree_host_checks(lib):
+    import speculative_decoding_verification_79_gb300 as sv
+
+    fake = ctypes.c_void_p(256)
+    args = lambda dt=1, B=4, N=16, V=100, T=1.0, tgt=fake, drf=fake, uni=fake, ws=fake, nb=256, \
+        path=fake: (tgt, drf, dt, fake, fake, fake, uni, B, N, V, T, fake, fake, path, ws, nb,
+                    None)  # noqa: E731
+    assert lib.sv_verify_tree(*args(dt=5)) == sv.SV_ERR_DTYPE
+    assert lib.sv_verify_tree(*args(N=0)) == sv.SV_ERR_SHAPE
+    assert lib.sv_verify_tree(*args(N=65)) == sv.SV_ERR_SHAPE
+    assert lib.sv_verify_tree(*args(V=0)) == sv.SV_ERR_SHAPE
+    assert lib.sv_verify_tree(*args(B=5000)) == sv.SV_ERR_SHAPE
+    for T in (-1.0, float("nan"), float("inf"), 1e-9):
+        assert lib.sv_verify_tree(*args(T=T)) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(nb=255)) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_verify_tree(*args(ws=ctypes.c_void_p(264))) == sv.SV_ERR_WORKSPACE
+    assert lib.sv_verify_tree(*args(tgt=None)) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(drf=None)) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(uni=None)) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(dt=0, tgt=ctypes.c_void_p(258))) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(path=ctypes.c_void_p(258))) == sv.SV_ERR_ARG
+    assert lib.sv_verify_tree(*args(B=0)) == sv.SV_OK
