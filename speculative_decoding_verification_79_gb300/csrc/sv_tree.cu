@@ -40,7 +40,8 @@ namespace {
 
 constexpr int TW = 16;          // warps per CTA
 constexpr int TT = 32 * TW;     // threads per CTA
-constexpr int UNR = 4;          // tiles a lane has in flight
+constexpr int UNR = 4;          // tiles a lane has in flight per row (two-row passes)
+constexpr int UNR_G = 8;        // the same for the one-row greedy pass
 constexpr int NGRP = 32;        // group totals kept per warp for the inverse CDF
 constexpr int MAXC = 8;         // largest cluster
 constexpr unsigned FULLM = 0xffffffffu;
@@ -168,15 +169,8 @@ struct Soft {
 
 __device__ __forceinline__ Soft soft_empty() { return Soft{-INFINITY, 0.f, ff{0.f, 0.f}}; }
 
-// Unnormalised weight 2^(z*(a + a_lo) - F) of one logit in frame F; 0 for -inf (the clamp
-// keeps -inf * a_lo from meeting +inf).
-__device__ __forceinline__ float term(float z, float a, float alo, float F) {
-  const float zc = fmaxf(z, -FLT_MAX);
-  return ex2(fmaf(zc, alo, fmaf(zc, a, -F)));
-}
-
-// The same with the exponent carried in two floats (exact product error by fma, TwoSum
-// error of the subtraction), for the probabilities the accept tests use.
+// 2^(z*(a + a_lo) - F) with the exponent carried in two floats (exact product error by
+// fma, TwoSum error of the subtraction), for the probabilities the accept tests use.
 __device__ __forceinline__ float term_precise(float z, float a, float alo, float F) {
   if (!(z > -INFINITY)) return 0.f;
   const float ph = __fmul_rn(z, a);
@@ -189,14 +183,73 @@ __device__ __forceinline__ float term_precise(float z, float a, float alo, float
   return fmaf(e, __fmul_rn(yl, 0.6931471805599453f), e);
 }
 
-template <int VEC>
-__device__ __forceinline__ void soft_add(Soft& s, const float* z, float a, float alo,
-                                         bool& bad) {
-  float vm = z[0];
+// Packed fp32x2 fused multiply-add (one instruction for two lanes of values).
+__device__ __forceinline__ float2 fma2(float2 x, float2 y, float2 z) {
+  float2 d;
+  asm("{\n\t.reg .b64 rx, ry, rz, rd;\n\t"
+      "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\tmov.b64 rz, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, rx, ry, rz;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y), "f"(z.x), "f"(z.y));
+  return d;
+}
+
+// The VEC logits of a raw vector as VEC/2 pairs.
+template <typename T>
+__device__ __forceinline__ float2 pair_of(const uint4 v, int i) {
+  const uint32_t w = i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+  if constexpr (EV<T>::VEC == 8) {
+    return make_float2(bf_lo(w), bf_hi(w));
+  } else {
+    const uint32_t w2 = i == 0 ? v.y : v.w;
+    return make_float2(__uint_as_float(i == 0 ? v.x : v.z), __uint_as_float(w2));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+  if constexpr (EV<T>::VEC == 8) return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+}
+
+// Maximum of a vector; NaN if any element is NaN.
+template <typename T>
+__device__ __forceinline__ float vmax(const uint4 v) {
+  if constexpr (EV<T>::VEC == 8) {
+    const uint32_t m = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+    return fmax_nan(bf_lo(m), bf_hi(m));
+  } else {
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+// Sum of 2^(z*a - F) over a vector (nF = -F): each element's unnormalised weight in
+// frame F (0 for -inf). The rounding of a = log2(e)/T moves every exponent by
+// (z - M)*a_lo plus a constant that the normalisation cancels: below 1e-6 relative for
+// the terms that carry the mass.
+template <typename T>
+__device__ __forceinline__ float vexpsum(const uint4 v, float a, float nF) {
+  constexpr int NP = EV<T>::VEC / 2;
+  const float2 aa = make_float2(a, a), cc = make_float2(nF, nF);
+  float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 1; i < VEC; ++i) vm = fmaxf(vm, z[i]);
+  for (int i = 0; i < NP; ++i) {
+    const float2 y = fma2(pair_of<T>(v, i), aa, cc);
+    acc.x += ex2(y.x);
+    acc.y += ex2(y.y);
+  }
+  return acc.x + acc.y;
+}
+
+// One round of UNR vectors into a softmax state: one max, at most one rescale, then
+// the exponentials. `bad` collects NaN and +inf.
+template <typename T>
+__device__ __forceinline__ void soft_round(Soft& s, const uint4* v, float a, bool& bad) {
+  float vm = vmax<T>(v[0]);
 #pragma unroll
-  for (int i = 0; i < VEC; ++i) bad |= (z[i] != z[i]) || (z[i] == INFINITY);
+  for (int k = 1; k < UNR; ++k) vm = fmax_nan(vm, vmax<T>(v[k]));
+  bad |= (vm != vm) || (vm == INFINITY);
   if (vm > s.m) {
     const float Fn = __fmul_rn(vm, a);
     const float f = (s.m == -INFINITY) ? 0.f : ex2(__fsub_rn(s.F, Fn));
@@ -205,15 +258,9 @@ __device__ __forceinline__ void soft_add(Soft& s, const float* z, float a, float
     s.F = Fn;
   }
   if (s.m == -INFINITY) return;
-  float t[VEC];
+  float sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < VEC; ++i) t[i] = term(z[i], a, alo, s.F);
-  float sum;
-  if constexpr (VEC == 8) {
-    sum = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
-  } else {
-    sum = (t[0] + t[1]) + (t[2] + t[3]);
-  }
+  for (int k = 0; k < UNR; ++k) sum += vexpsum<T>(v[k], a, -s.F);
   const ff r = ff_two_sum(s.S.hi, sum);
   s.S = ff_norm(r.hi, __fadd_rn(r.lo, s.S.lo));
 }
@@ -253,29 +300,33 @@ __device__ __forceinline__ void arg_merge(float& best, int& idx, float b2, int i
 // p = 2^(zt*(a + a_lo) - Ft) * iSt, q likewise; lq = lam * iSd.
 // ---------------------------------------------------------------------------
 struct WPar {
-  float a, alo, Ft, iSt, Fd, lq;
+  float a, Ft, iSt, Fd, lq;
   bool use_d;
 };
 
-__device__ __forceinline__ float weight(const WPar& P, float zt, float zd) {
-  const float pt = __fmul_rn(term(zt, P.a, P.alo, P.Ft), P.iSt);
-  if (!P.use_d) return pt;
-  return fmaxf(fmaf(-P.lq, term(zd, P.a, P.alo, P.Fd), pt), 0.f);
-}
-
+// Weights of the VEC elements of one vector of t (and d); returns their sum.
 template <typename T>
 __device__ __forceinline__ float vec_weights(const WPar& P, uint4 vt, uint4 vd, float* w) {
-  constexpr int VEC = EV<T>::VEC;
-  float zt[VEC], zd[VEC];
-  unpack<T>(vt, zt);
-  if (P.use_d) unpack<T>(vd, zd);
+  constexpr int NP = EV<T>::VEC / 2;
+  const float2 aa = make_float2(P.a, P.a), ct = make_float2(-P.Ft, -P.Ft);
+  const float2 st = make_float2(P.iSt, P.iSt), z0 = make_float2(0.f, 0.f);
+  const float2 cd = make_float2(-P.Fd, -P.Fd), nl = make_float2(-P.lq, -P.lq);
+  float sum = 0.f;
 #pragma unroll
-  for (int i = 0; i < VEC; ++i) w[i] = weight(P, zt[i], P.use_d ? zd[i] : 0.f);
-  if constexpr (VEC == 8) {
-    return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-  } else {
-    return (w[0] + w[1]) + (w[2] + w[3]);
+  for (int i = 0; i < NP; ++i) {
+    const float2 yt = fma2(pair_of<T>(vt, i), aa, ct);
+    float2 pt = fma2(make_float2(ex2(yt.x), ex2(yt.y)), st, z0);
+    if (P.use_d) {
+      const float2 yd = fma2(pair_of<T>(vd, i), aa, cd);
+      pt = fma2(nl, make_float2(ex2(yd.x), ex2(yd.y)), pt);
+      pt.x = fmaxf(pt.x, 0.f);
+      pt.y = fmaxf(pt.y, 0.f);
+    }
+    w[2 * i] = pt.x;
+    w[2 * i + 1] = pt.y;
+    sum += pt.x + pt.y;
   }
+  return sum;
 }
 
 // ---------------------------------------------------------------------------
@@ -293,6 +344,7 @@ struct Smem {
   int par[SV_MAX_TREE];
   int tok[SV_MAX_TREE];
   float u[SV_MAX_TREE];
+  float czt[SV_MAX_TREE], czd[SV_MAX_TREE];  // logits of each child's token (T > 0)
   int nn;
   int ok;
   int dec;
@@ -319,7 +371,9 @@ __device__ __forceinline__ void warp_tiles(int ntiles, int C, int rank, int w, i
   t1 = min(c1, t0 + tpw);
 }
 
-__device__ __forceinline__ int group_size(int nt) { return max(1, (nt + NGRP - 1) / NGRP); }
+// Tiles per group: at least a round of UNR (one warp reduction per round), and few
+// enough groups to fit NGRP.
+__device__ __forceinline__ int group_size(int nt) { return max(UNR, (nt + NGRP - 1) / NGRP); }
 
 // First item whose running total passes `target` (items of zero total never qualify);
 // `cum` enters as the total before item 0 and leaves as the total before the chosen one.
@@ -369,7 +423,9 @@ template <int KIND>
 __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C, int buf,
                                          float a) {
   cl.sync();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    // Lane k < C reads CTA k's partial; the merge is the same fixed tree in every CTA.
+    const int lane = threadIdx.x;
     Xch r;
     r.st = soft_empty();
     r.sd = soft_empty();
@@ -377,21 +433,41 @@ __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C,
     r.idx = INT_MAX;
     r.bad = 0;
     r.tot = ff{0.f, 0.f};
-    for (int k = 0; k < C; ++k) {
-      const Xch* x = cl.map_shared_rank(&sm.xch[buf], k);
-      r.bad |= x->bad;
+    if (lane < C) {
+      const Xch* x = cl.map_shared_rank(&sm.xch[buf], lane);
+      r.bad = x->bad;
       if (KIND == 0) {
-        r.st = soft_merge(r.st, x->st, a);
-        r.sd = soft_merge(r.sd, x->sd, a);
+        r.st = x->st;
+        r.sd = x->sd;
       } else if (KIND == 1) {
-        arg_merge(r.best, r.idx, x->best, x->idx);
+        r.best = x->best;
+        r.idx = x->idx;
       } else {
-        const ff t = x->tot;
-        sm.ctot[k] = t;
-        r.tot = ff_add(r.tot, t);
+        r.tot = x->tot;
       }
     }
-    sm.res = r;
+    r.bad = __any_sync(FULLM, r.bad);
+    if (KIND == 0) {
+      r.st = soft_warp(r.st, a);
+      r.sd = soft_warp(r.sd, a);
+    } else if (KIND == 1) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float b2 = __shfl_xor_sync(FULLM, r.best, o);
+        const int i2 = __shfl_xor_sync(FULLM, r.idx, o);
+        arg_merge(r.best, r.idx, b2, i2);
+      }
+    } else {
+      // Totals add up in rank order, the order the sample's search walks them.
+      ff t{0.f, 0.f};
+      for (int k = 0; k < C; ++k) {
+        const ff tk{__shfl_sync(FULLM, r.tot.hi, k), __shfl_sync(FULLM, r.tot.lo, k)};
+        if (lane == 0) sm.ctot[k] = tk;
+        t = ff_add(t, tk);
+      }
+      r.tot = t;
+    }
+    if (lane == 0) sm.res = r;
   }
   __syncthreads();
 }
@@ -399,9 +475,7 @@ __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C,
 // Softmax statistics of the target row (and the draft row when use_d).
 template <typename T>
 __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, const Geo& g,
-                           const T* tr, const T* dr, bool dfast, bool use_d, float a,
-                           float alo) {
-  constexpr int VEC = EV<T>::VEC;
+                           const T* tr, const T* dr, bool dfast, bool use_d, float a) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   Soft st = soft_empty(), sd = soft_empty();
   bool bad = false;
@@ -409,24 +483,12 @@ __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, con
     uint4 vt[UNR], vd[UNR];
 #pragma unroll
     for (int k = 0; k < UNR; ++k) {
-      if (tb + k < g.t1) {
-        const int j = (tb + k) * 32 + lane;
-        vt[k] = fetch<T>(tr, true, g.V, g.off, j);
-        if (use_d) vd[k] = fetch<T>(dr, dfast, g.V, g.off, j);
-      }
+      const int j = (tb + k) * 32 + lane;
+      vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, j) : neg_inf_vec<T>();
+      if (use_d) vd[k] = tb + k < g.t1 ? fetch<T>(dr, dfast, g.V, g.off, j) : neg_inf_vec<T>();
     }
-#pragma unroll
-    for (int k = 0; k < UNR; ++k) {
-      if (tb + k < g.t1) {
-        float z[VEC];
-        unpack<T>(vt[k], z);
-        soft_add<VEC>(st, z, a, alo, bad);
-        if (use_d) {
-          unpack<T>(vd[k], z);
-          soft_add<VEC>(sd, z, a, alo, bad);
-        }
-      }
-    }
+    soft_round<T>(st, vt, a, bad);
+    if (use_d) soft_round<T>(sd, vd, a, bad);
   }
   st = soft_warp(st, a);
   if (use_d) sd = soft_warp(sd, a);
@@ -437,15 +499,17 @@ __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, con
     sm.wbad[w] = wb;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    Xch& x = sm.xch[buf];
-    x.st = soft_empty();
-    x.sd = soft_empty();
-    x.bad = 0;
-    for (int k = 0; k < TW; ++k) {
-      x.st = soft_merge(x.st, sm.wst[k], a);
-      if (use_d) x.sd = soft_merge(x.sd, sm.wsd[k], a);
-      x.bad |= sm.wbad[k];
+  if (w == 0) {
+    Soft xs = lane < TW ? sm.wst[lane] : soft_empty();
+    Soft xd = (use_d && lane < TW) ? sm.wsd[lane] : soft_empty();
+    const bool xb = __any_sync(FULLM, lane < TW && sm.wbad[lane]);
+    xs = soft_warp(xs, a);
+    if (use_d) xd = soft_warp(xd, a);
+    if (lane == 0) {
+      Xch& x = sm.xch[buf];
+      x.st = xs;
+      x.sd = xd;
+      x.bad = xb;
     }
   }
   exchange<0>(sm, cl, C, buf, a);
@@ -461,26 +525,28 @@ __device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, co
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
-  for (int tb = g.t0; tb < g.t1; tb += UNR) {
-    uint4 vt[UNR];
+  for (int tb = g.t0; tb < g.t1; tb += UNR_G) {
+    uint4 vt[UNR_G];
 #pragma unroll
-    for (int k = 0; k < UNR; ++k)
-      if (tb + k < g.t1) vt[k] = fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane);
+    for (int k = 0; k < UNR_G; ++k)
+      vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane)
+                            : neg_inf_vec<T>();
+    float vm = vmax<T>(vt[0]);
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) {
-      if (tb + k < g.t1) {
+    for (int k = 1; k < UNR_G; ++k) vm = fmax_nan(vm, vmax<T>(vt[k]));
+    bad |= (vm != vm) || (vm == INFINITY);
+    if (vm > best) {  // rare: find the round's first element equal to its maximum
+      best = vm;
+      int e = -1;
+#pragma unroll
+      for (int k = 0; k < UNR_G; ++k) {
         float z[VEC];
         unpack<T>(vt[k], z);
-        const int e0 = ((tb + k) * 32 + lane) * VEC - g.off;
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          bad |= (z[i] != z[i]) || (z[i] == INFINITY);
-          if (z[i] > best) {  // elements arrive in increasing index order per lane
-            best = z[i];
-            idx = e0 + i;
-          }
-        }
+        for (int i = 0; i < VEC; ++i)
+          if (e < 0 && z[i] == vm) e = ((tb + k) * 32 + lane) * VEC - g.off + i;
       }
+      idx = e;
     }
   }
 #pragma unroll
@@ -496,14 +562,21 @@ __device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, co
     sm.wbad[w] = wb;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    Xch& x = sm.xch[buf];
-    x.best = -INFINITY;
-    x.idx = INT_MAX;
-    x.bad = 0;
-    for (int k = 0; k < TW; ++k) {
-      arg_merge(x.best, x.idx, sm.wbest[k], sm.widx[k]);
-      x.bad |= sm.wbad[k];
+  if (w == 0) {
+    float xb = lane < TW ? sm.wbest[lane] : -INFINITY;
+    int xi = lane < TW ? sm.widx[lane] : INT_MAX;
+    const bool bd = __any_sync(FULLM, lane < TW && sm.wbad[lane]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float b2 = __shfl_xor_sync(FULLM, xb, o);
+      const int i2 = __shfl_xor_sync(FULLM, xi, o);
+      arg_merge(xb, xi, b2, i2);
+    }
+    if (lane == 0) {
+      Xch& x = sm.xch[buf];
+      x.best = xb;
+      x.idx = xi;
+      x.bad = bd;
     }
   }
   exchange<1>(sm, cl, C, buf, 0.f);
@@ -709,7 +782,14 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
     const bool kids = first_child >= 0;
     const T* dr = drf + (base + c) * (size_t)V;
     const bool dfast = kids && row_off(dr) == g.off;
-    stats_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, kids, A.a, A.a_lo);
+    // Thread n fetches the logits of child n's token; they land during the pass.
+    float czt = 0.f, czd = 0.f;
+    const bool is_child = tid > c && tid < nn && sm.par[tid] == c;
+    if (is_child) {
+      czt = logit_at(tr + sm.tok[tid]);
+      czd = logit_at(dr + sm.tok[tid]);
+    }
+    stats_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, kids, A.a);
     if (sm.res.bad || !(sm.res.st.m > -INFINITY) || (kids && !(sm.res.sd.m > -INFINITY))) {
       valid = false;
       break;
@@ -721,7 +801,12 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
     const float iSd = kids ? fmaf(-__fdiv_rn(1.f, sd.S.hi), __fdiv_rn(sd.S.lo, sd.S.hi),
                                   __fdiv_rn(1.f, sd.S.hi))
                            : 0.f;
-    WPar P{A.a, A.a_lo, st.F, iSt, sd.F, 0.f, false};
+    if (is_child) {
+      sm.czt[tid] = czt;
+      sm.czd[tid] = czd;
+    }
+    __syncthreads();
+    WPar P{A.a, st.F, iSt, sd.F, 0.f, false};
     bool totals = false;  // sm.gtot/wtot/ctot hold the weights of P
     int next = -1;
     if (kids) {
@@ -729,9 +814,8 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
       for (int n = first_child; n < nn; ++n) {
         if (sm.par[n] != c) continue;
         if (tid == 0) {
-          const int x = sm.tok[n];
-          const float px = __fmul_rn(term_precise(logit_at(tr + x), A.a, A.a_lo, st.F), iSt);
-          const float qx = __fmul_rn(term_precise(logit_at(dr + x), A.a, A.a_lo, sd.F), iSd);
+          const float px = __fmul_rn(term_precise(sm.czt[n], A.a, A.a_lo, st.F), iSt);
+          const float qx = __fmul_rn(term_precise(sm.czd[n], A.a, A.a_lo, sd.F), iSd);
           // u * q(x) < r(x) with r = max(0, p - lam q) / W, division-free.
           sm.dec = __fmul_rn(__fmul_rn(sm.u[n], qx), W.hi) < fmaxf(fmaf(-lam.hi, qx, px), 0.f);
         }
@@ -741,7 +825,7 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
           break;
         }
         lam = ff_add(lam, W);
-        P = WPar{A.a, A.a_lo, st.F, iSt, sd.F, __fmul_rn(lam.hi, iSd), true};
+        P = WPar{A.a, st.F, iSt, sd.F, __fmul_rn(lam.hi, iSd), true};
         wsum_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, P);
         if (sm.res.tot.hi > 0.f) {
           W = sm.res.tot;
@@ -764,7 +848,7 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
     }
     // Terminal sample: the residual after the last rejection, or p (leaf, or restart).
     if (!totals) {
-      P = WPar{A.a, A.a_lo, st.F, iSt, sd.F, 0.f, false};
+      P = WPar{A.a, st.F, iSt, sd.F, 0.f, false};
       wsum_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, P);
     }
     const int y = locate<T>(sm, C, rank, g, tr, dr, dfast, P, sm.u[0]);
