@@ -289,38 +289,55 @@ def run_gpu(args):
 
 def run_e2e(args, sv, g, ws, dev, tau, budget):
     """Public calls with host inputs: per step H2D of the step's inputs from pinned
-    memory, schedule + verify, D2H of the emitted tokens and accepted counts."""
+    memory, schedule + verify, D2H of the emitted tokens and accepted counts. Two device
+    input buffers alternate, so step i+1's copy (copy stream) runs under step i's
+    schedule + verify (compute stream); each step's compute waits for its own copy, and
+    a buffer is refilled only after the compute that read it has finished."""
     B, K = args.B, args.K
     host = {k: g[k].cpu().pin_memory() for k in ("target", "draft", "draft_tok", "uniforms",
                                                   "conf")}
-    dbuf = {k: torch.empty_like(g[k]) for k in host}
+    dbufs = [{k: torch.empty_like(g[k]) for k in host} for _ in range(2)]
     out_len = torch.empty(B, dtype=torch.int32, device=dev)
     out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
     out_acc = torch.empty(B, dtype=torch.int32, device=dev)
     h_tok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
     h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
     st = torch.cuda.Stream(device=dev)
+    cp = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    for e in consumed:
+        e.record(st)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = h_tok.numel() * 4 + h_acc.numel() * 4
+    step = [0]
 
     def one():
-        with torch.cuda.stream(st):
+        i = step[0] % 2
+        step[0] += 1
+        dbuf = dbufs[i]
+        with torch.cuda.stream(cp):
+            cp.wait_event(consumed[i])
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
+            copied[i].record(cp)
+        with torch.cuda.stream(st):
+            st.wait_event(copied[i])
             sv.sv_schedule(dbuf["conf"], tau, budget, ws, out_len=out_len, stream=st)
             sv.sv_verify(dbuf["target"], dbuf["draft"], dbuf["draft_tok"], out_len,
                          dbuf["uniforms"], args.T, ws, out_tok=out_tok, out_accepted=out_acc,
                          stream=st)
+            consumed[i].record(st)
             h_tok.copy_(out_tok, non_blocking=True)
             h_acc.copy_(out_acc, non_blocking=True)
 
     for _ in range(3):
         one()
-    st.synchronize()
+    torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         one()
-    st.synchronize()
+    torch.cuda.synchronize(dev)
     dt = time.perf_counter() - t0
     tokens = int(out_len.sum().item()) * args.e2e_steps
     return {"value": tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -4,6 +4,7 @@
 #include <cmath>
 
 #include "sv_common.cuh"
+#include "sv_launch.cuh"
 #include "sv_tree.cuh"
 
 namespace sv {

@@ -18,6 +18,7 @@
 //    for each position with a tested token (float64, then rounded to float32), ECE =
 //    sum_bins |accepted - sum c'| / tested, and the window restarts.
 #include "sv_common.cuh"
+#include "sv_launch.cuh"
 
 namespace sv {
 

@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 
 #include "sv_common.cuh"
+#include "sv_launch.cuh"
 
 namespace sv {
 

@@ -22,6 +22,7 @@
 //     Algorithm"), in fp64 from the device-resident load state.
 // One CTA of 1024 threads; everything lives in shared memory.
 #include "sv_common.cuh"
+#include "sv_launch.cuh"
 
 namespace sv {
 
