@@ -389,3 +389,22 @@ def _pins():
 
 
 PINS = _pins()
+
+
+def test_tree_path_bytes_counts_the_walk():
+    """The benchmark's algorithmic bytes for a tree call: target rows of the root, the
+    accepted nodes (the stop node is the last of them), and draft rows of those with
+    children (none at T == 0). Hand case: tree16 parents, path 0 -> 1 -> 5."""
+    import synth
+
+    par = np.array([synth.TREE16_PARENTS, synth.TREE16_PARENTS], np.int32)
+    path = np.full((2, 16), -1, np.int32)
+    path[0, :2] = [1, 5]  # request 0 accepted nodes 1 and 5 (node 5 has children 11, 12)
+    acc = np.array([2, -1], np.int32)  # request 1 invalid: nothing counted
+    V, e = 10, 2
+    # target rows of nodes 0, 1, 5; draft rows of 0, 1, 5 (all three have children)
+    assert synth.tree_path_bytes(path, acc, par, V, e) == 6 * V * e
+    assert synth.tree_path_bytes(path, acc, par, V, e, greedy=True) == 3 * V * e
+    path[0, :2] = [4, -1]  # node 4 is a leaf: its draft row is not read
+    acc[0] = 1
+    assert synth.tree_path_bytes(path, acc, par, V, e) == 3 * V * e
