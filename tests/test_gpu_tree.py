@@ -175,8 +175,8 @@ def test_invalid_and_unread_rows(sv, ws):
     B, N, V = 6, 5, 3000
     inp = synth.tree_inputs(B, N, V, dtype=torch.float32, temperature=1.0, shape="star",
                             seed=9)
-    # Request 0: every child accepted at u = 0 is impossible to predict, so force the
-    # walk instead: a chain 0 -> 1 -> 2 whose tests accept (u = 0), nodes 3, 4 unreached.
+    # Request 0: links 0 -> 1 -> 2 with accepting tests (u = 0 accepts whenever p(x) > 0),
+    # so the walk ends at leaf 2 and never reaches nodes 3 and 4 (also children of 0).
     inp["parent"][0] = torch.tensor([-1, 0, 1, 0, 0], dtype=torch.int32)
     inp["uniforms"][0, 1:] = 0.0
     inp["target"][0, 3] = float("nan")
