@@ -194,6 +194,16 @@ __device__ __forceinline__ float2 fma2(float2 x, float2 y, float2 z) {
   return d;
 }
 
+__device__ __forceinline__ float2 add2(float2 x, float2 y) {
+  float2 d;
+  asm("{\n\t.reg .b64 rx, ry, rd;\n\t"
+      "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, rx, ry;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return d;
+}
+
 // The VEC logits of a raw vector as VEC/2 pairs.
 template <typename T>
 __device__ __forceinline__ float2 pair_of(const uint4 v, int i) {
@@ -236,8 +246,7 @@ __device__ __forceinline__ float vexpsum(const uint4 v, float a, float nF) {
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
     const float2 y = fma2(pair_of<T>(v, i), aa, cc);
-    acc.x += ex2(y.x);
-    acc.y += ex2(y.y);
+    acc = add2(acc, make_float2(ex2(y.x), ex2(y.y)));
   }
   return acc.x + acc.y;
 }
@@ -311,7 +320,7 @@ __device__ __forceinline__ float vec_weights(const WPar& P, uint4 vt, uint4 vd, 
   const float2 aa = make_float2(P.a, P.a), ct = make_float2(-P.Ft, -P.Ft);
   const float2 st = make_float2(P.iSt, P.iSt), z0 = make_float2(0.f, 0.f);
   const float2 cd = make_float2(-P.Fd, -P.Fd), nl = make_float2(-P.lq, -P.lq);
-  float sum = 0.f;
+  float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
     const float2 yt = fma2(pair_of<T>(vt, i), aa, ct);
@@ -324,9 +333,9 @@ __device__ __forceinline__ float vec_weights(const WPar& P, uint4 vt, uint4 vd, 
     }
     w[2 * i] = pt.x;
     w[2 * i + 1] = pt.y;
-    sum += pt.x + pt.y;
+    sum = add2(sum, pt);
   }
-  return sum;
+  return sum.x + sum.y;
 }
 
 // ---------------------------------------------------------------------------
@@ -417,6 +426,16 @@ __device__ __forceinline__ Geo make_geo(const T* tr, int V, int C, int rank, int
   return g;
 }
 
+// A round of UNR tiles from tile tb on is interior when all its tiles belong to the warp
+// and every vector in them is whole (vector j covers elements j*VEC - off ..): no
+// per-vector checks then. `d_off_grid`: the draft row is off the grid (never interior).
+template <typename T>
+__device__ __forceinline__ bool interior_round(const Geo& g, int tb, bool d_off_grid) {
+  constexpr int VEC = EV<T>::VEC;
+  const int jlo = g.off > 0 ? 1 : 0, jhi = (g.V + g.off) / VEC;  // whole vectors: [jlo, jhi)
+  return !d_off_grid && tb + UNR <= g.t1 && tb * 32 >= jlo && (tb + UNR) * 32 <= jhi;
+}
+
 // Publishes this CTA's partial (already in sm.xch[buf] by thread 0), waits for the
 // cluster, and merges the C partials in rank order into sm.res (thread 0).
 template <int KIND>
@@ -479,13 +498,24 @@ __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, con
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   Soft st = soft_empty(), sd = soft_empty();
   bool bad = false;
+  const uint4* t4 = reinterpret_cast<const uint4*>(tr - g.off);  // vector 0 of the grid
+  const uint4* d4 = reinterpret_cast<const uint4*>(dr - g.off);
   for (int tb = g.t0; tb < g.t1; tb += UNR) {
     uint4 vt[UNR], vd[UNR];
+    if (interior_round<T>(g, tb, use_d && !dfast)) {  // whole vectors on both rows' grids
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) {
-      const int j = (tb + k) * 32 + lane;
-      vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, j) : neg_inf_vec<T>();
-      if (use_d) vd[k] = tb + k < g.t1 ? fetch<T>(dr, dfast, g.V, g.off, j) : neg_inf_vec<T>();
+      for (int k = 0; k < UNR; ++k) {
+        const int j = (tb + k) * 32 + lane;
+        vt[k] = __ldg(t4 + j);
+        if (use_d) vd[k] = __ldg(d4 + j);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < UNR; ++k) {
+        const int j = (tb + k) * 32 + lane;
+        vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, j) : neg_inf_vec<T>();
+        if (use_d) vd[k] = tb + k < g.t1 ? fetch<T>(dr, dfast, g.V, g.off, j) : neg_inf_vec<T>();
+      }
     }
     soft_round<T>(st, vt, a, bad);
     if (use_d) soft_round<T>(sd, vd, a, bad);
@@ -525,12 +555,19 @@ __device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, co
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
+  const uint4* t4 = reinterpret_cast<const uint4*>(tr - g.off);  // vector 0 of the grid
+  const int jlo = g.off > 0 ? 1 : 0, jhi = (g.V + g.off) / VEC;   // whole vectors
   for (int tb = g.t0; tb < g.t1; tb += UNR_G) {
     uint4 vt[UNR_G];
+    if (tb + UNR_G <= g.t1 && tb * 32 >= jlo && (tb + UNR_G) * 32 <= jhi) {
 #pragma unroll
-    for (int k = 0; k < UNR_G; ++k)
-      vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane)
-                            : neg_inf_vec<T>();
+      for (int k = 0; k < UNR_G; ++k) vt[k] = __ldg(t4 + (tb + k) * 32 + lane);
+    } else {
+#pragma unroll
+      for (int k = 0; k < UNR_G; ++k)
+        vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane)
+                              : neg_inf_vec<T>();
+    }
     float vm = vmax<T>(vt[0]);
 #pragma unroll
     for (int k = 1; k < UNR_G; ++k) vm = fmax_nan(vm, vmax<T>(vt[k]));
@@ -594,14 +631,25 @@ __device__ void wsum_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, cons
   const int gsz = group_size(nt);
   ff wt{0.f, 0.f};
   float ls = 0.f, lc = 0.f;
+  const uint4* t4 = reinterpret_cast<const uint4*>(tr - g.off);  // vector 0 of the grid
+  const uint4* d4 = reinterpret_cast<const uint4*>(dr - g.off);
   for (int tb = 0; tb < nt; tb += UNR) {
     uint4 vt[UNR], vd[UNR];
+    if (interior_round<T>(g, g.t0 + tb, P.use_d && !dfast)) {  // whole vectors on both grids
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) {
-      if (tb + k < nt) {
+      for (int k = 0; k < UNR; ++k) {
         const int j = (g.t0 + tb + k) * 32 + lane;
-        vt[k] = fetch<T>(tr, true, g.V, g.off, j);
-        if (P.use_d) vd[k] = fetch<T>(dr, dfast, g.V, g.off, j);
+        vt[k] = __ldg(t4 + j);
+        if (P.use_d) vd[k] = __ldg(d4 + j);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < UNR; ++k) {
+        if (tb + k < nt) {
+          const int j = (g.t0 + tb + k) * 32 + lane;
+          vt[k] = fetch<T>(tr, true, g.V, g.off, j);
+          if (P.use_d) vd[k] = fetch<T>(dr, dfast, g.V, g.off, j);
+        }
       }
     }
 #pragma unroll
