@@ -513,6 +513,7 @@ def run_sweep(args):
 def _graph_median_us(fn, st, n=50):
     """Median per-call time of fn() captured n times in a CUDA graph, from event-record
     nodes around each call (launch gaps excluded)."""
+    st.wait_stream(torch.cuda.current_stream(st.device))  # inputs are made on that stream
     with torch.cuda.stream(st):
         for _ in range(3):
             fn()
@@ -607,9 +608,9 @@ def run_markov(args):
 
 
 def run_tree(args):
-    """One JSON line per temperature: tree verification of B=64 trees of 16 nodes
-    (V=151,936 bf16), timed per call inside a CUDA graph with an L2 flush before each
-    call. Algorithmic bytes are the rows the walk must read (the target row of every node
+    """One JSON line per batch size and temperature: tree verification of B trees of 16
+    nodes (V=151,936 bf16; B from --tree-B, 64 by default), timed per call inside a CUDA
+    graph with an L2 flush before each call. Algorithmic bytes are the rows the walk must read (the target row of every node
     on the accepted path and of the stop node, and the draft row of each of those with
     children), from the call's own outputs."""
     import speculative_decoding_verification_79_gb300 as sv
@@ -620,12 +621,13 @@ def run_tree(args):
     peak, _ = _peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ws = sv.Workspace(1, 1, 1, device=dev)
-    for T in (1.0, 0.0):
-        inp = synth.tree_qwen3(T, seed=1, device=dev)
+    for B_t, T in [(b, t) for b in args.tree_B for t in (1.0, 0.0)]:
+        inp = synth.tree_qwen3(T, seed=1, device=dev, B=B_t)
         B, N, V = inp["target"].shape
         outs = [torch.empty((B, N), dtype=torch.int32, device=dev),
                 torch.empty(B, dtype=torch.int32, device=dev),
                 torch.empty((B, N), dtype=torch.int32, device=dev)]
+        st.wait_stream(torch.cuda.current_stream(dev))  # inputs are made on that stream
 
         def call():
             sv.sv_verify_tree(inp["target"], inp["draft"] if T > 0 else None, inp["parent"],
@@ -761,6 +763,8 @@ def main():
                     help="time the Markov logit-bias drafting loop")
     ap.add_argument("--tree", action="store_true",
                     help="time tree (multi-candidate) verification")
+    ap.add_argument("--tree-B", type=lambda x: [int(v) for v in x.split(",")], default=[64],
+                    help="batch sizes of --tree, comma-separated")
     ap.add_argument("--once", type=int, default=0,
                     help="no timing: build one input set and run N schedule+verify steps "
                          "(a short, self-contained program for profilers)")

@@ -322,7 +322,7 @@ def tree_inputs(B, N, V, *, dtype=torch.bfloat16, temperature=1.0, target_sigma=
 
 
 def tree_qwen3(temperature, seed=0, device="cpu", B=64):
-    """B=64 trees of 16 nodes (TREE16_PARENTS), V=151,936 bf16; target N(0,3^2) with
+    """B trees (64 by default) of 16 nodes (TREE16_PARENTS), V=151,936 bf16; target N(0,3^2) with
     rows peaked (+12) w.p. 0.2; draft noise N(0,1)."""
     return tree_inputs(B, 16, QWEN3_VOCAB, dtype=torch.bfloat16, temperature=temperature,
                        target_sigma=3.0, draft_sigma=1.0, peak_prob=0.2, peak_height=12.0,
