@@ -160,7 +160,7 @@ __device__ __forceinline__ void acc2(float& s, float& c, float w) {
 
 // ---------------------------------------------------------------------------
 // Softmax statistics: m = running max of the raw logits, F = fl(m*a) the frame,
-// S = sum of 2^(z*(a + a_lo) - F) (float-float).
+// S = sum of 2^(z*a - F) (float-float; a = log2(e)/T rounded to fp32).
 // ---------------------------------------------------------------------------
 struct Soft {
   float m, F;
@@ -306,7 +306,7 @@ __device__ __forceinline__ void arg_merge(float& best, int& idx, float b2, int i
 
 // ---------------------------------------------------------------------------
 // Residual and sample weights: w = max(0, p - lam*q), or p when use_d is false.
-// p = 2^(zt*(a + a_lo) - Ft) * iSt, q likewise; lq = lam * iSd.
+// p = 2^(zt*a - Ft) * iSt, q likewise; lq = lam * iSd.
 // ---------------------------------------------------------------------------
 struct WPar {
   float a, Ft, iSt, Fd, lq;
