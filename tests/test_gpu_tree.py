@@ -218,3 +218,16 @@ def test_graph_capture_and_repeat(sv, ws):
     assert (outs[0].cpu().numpy() == ref["out_tok"]).all()
     assert (outs[1].cpu().numpy() == ref["out_accepted"]).all()
     assert (outs[2].cpu().numpy() == ref["out_path"]).all()
+
+
+@needs_cuda
+def test_large_batch_dsv4_vocab(sv, ws):
+    """B=512 random trees of 8 nodes at DeepSeek-V4's vocabulary (129,280, bf16), T=0.7:
+    one CTA per request, several waves; every request against the oracle."""
+    inp = synth.tree_inputs(512, 8, synth.DSV4_VOCAB, dtype=torch.bfloat16, temperature=0.7,
+                            target_sigma=3.0, draft_sigma=1.0, shape="random",
+                            n_nodes="uniform", seed=12, device="cuda")
+    gpu = run_gpu(sv, ws, inp, 0.7)
+    nf, nd = compare(gpu, run_oracle(inp, 0.7))
+    assert gpu["status"] == sv.SV_OK
+    print(f"[tree] B=512 V=129280: {nf} flagged, {nd} decided differently")
