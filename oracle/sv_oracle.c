@@ -310,9 +310,10 @@ static int verify_one(const void *tgt, const void *drf, int dtype, const int32_t
         }
         /* First rejection: sample from normalize(max(0, p - q)) by inverse
          * CDF on the request's last uniform u_{b,K} [DD "The Speculative
-         * Decoding Solution": "sample from adjusted distribution"; the page's
-         * residual line subtracts a list of scalars from a vector, read here
-         * as the full distributions p and q]. */
+         * Decoding Solution": after a rejection the token is drawn from the
+         * residual of the two distributions; the page's residual line
+         * subtracts a list of scalars from a vector, read here as the full
+         * distributions p and q]. */
         j = k;
         for (int v = 0; v < V; v++) r[v] = p[v] - q[v] > 0.0 ? p[v] - q[v] : 0.0;
         double Z, gap;
@@ -672,8 +673,13 @@ int oracle_markov_draft(const uint16_t *L, const uint16_t *U, const uint16_t *Vm
     if (B < 0 || K < 1 || V < 1 || r < 1) return ORC_ERR_ARG;
     for (int b = 0; b < B; b++)
         if (prev[b] < 0 || prev[b] >= V) return ORC_ERR_INPUT;
-    double *x = (double *)malloc(sizeof(double) * (size_t)r);
+    /* Requests are independent: OpenMP threads take whole requests, so the result
+     * does not depend on the thread count. */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
     for (int b = 0; b < B; b++) {
+        double *x = (double *)malloc(sizeof(double) * (size_t)r);
         int y = prev[b];
         for (int k = 0; k < K; k++) {
             for (int j = 0; j < r; j++) x[j] = bf16_value(Vm[(size_t)y * r + j]);
@@ -713,8 +719,8 @@ int oracle_markov_draft(const uint16_t *L, const uint16_t *U, const uint16_t *Vm
             if (out_gap) out_gap[(size_t)b * K + k] = amax > 0 ? (top1 - top2) / amax : 0.0;
             y = best;
         }
+        free(x);
     }
-    free(x);
     return ORC_OK;
 }
 

@@ -49,12 +49,13 @@ def _compare(inp, got_corr, got_tok):
     B, K, V = L.shape
     r = U.shape[1]
     Uf, Vf, Lf = _f(U), _f(Vm), _f(L)
+    Ua = np.abs(Uf)
     near_ties = flagged = 0
     for b in range(B):
         y = int(prev[b])
         for k in range(K):
             x = Vf[y]
-            terms = np.abs(Uf) @ np.abs(x)
+            terms = Ua @ np.abs(x)
             z = Lf[b, k] + Uf @ x
             bound = 2.0 ** -24 * (r * terms + np.abs(z)) * 2
             sp = _spacing(z)
@@ -95,6 +96,15 @@ def test_markov_parity(sv, B, K, V, r):
     flagged, ties = _compare(inp, _bits(corr.cpu()), tok.cpu().numpy())
     print(f"[markov] B={B} K={K} V={V} r={r}: {flagged} elements one bf16 step apart at "
           f"rounding midpoints, {ties} near-tie tokens")
+
+
+@needs_cuda
+@pytest.mark.parametrize("r", [128, 256])
+def test_markov_parity_benchmarked_shape(sv, r):
+    """The shape the drafting kernel is timed at: B=64 requests, K=8 positions, the
+    151,936-entry vocabulary, ranks 128 and 256 ([GD] "1. The Markov Logit-Bias Head"):
+    every request and position against the oracle."""
+    test_markov_parity(sv, 64, 8, synth.QWEN3_VOCAB, r)
 
 
 @needs_cuda

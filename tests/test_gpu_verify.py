@@ -99,15 +99,13 @@ def test_ragged_schedule_then_verify(sv, budget):
 
 
 @needs_cuda
-def test_large_batch_sampled(sv):
-    """B=512, K=8, V=129,280 bf16, T=0.7, verify lengths U{1..8}: all outputs from the
-    GPU, 96 sampled requests checked against the oracle."""
+def test_large_batch(sv):
+    """B=512, K=8, V=129,280 bf16, T=0.7, verify lengths U{1..8} (the DeepSeek-V4
+    vocabulary of [DD] "The Low-Rank Trick"): every request against the oracle."""
     inp = synth.large_batch(seed=0, device="cuda")
     gpu = run_gpu(sv, inp, 0.7)
-    idx = np.sort(np.random.default_rng(0).choice(512, size=96, replace=False))
-    ref = run_oracle(inp, 0.7, idx=torch.as_tensor(idx, device="cuda"))
-    account("large batch",
-            *compare(gpu, ref, 0.7, inp["verify_len"].cpu().numpy()[idx], idx=idx))
+    ref = run_oracle(inp, 0.7)
+    account("large batch", *compare(gpu, ref, 0.7, inp["verify_len"].cpu().numpy()))
     acc = gpu["out_accepted"]
     L = inp["verify_len"].cpu().numpy()
     assert ((acc >= 0) & (acc <= L)).all()

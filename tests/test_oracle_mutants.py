@@ -5,7 +5,7 @@ import os
 import numpy as np
 import pytest
 
-from test_oracle_verify import lossless_error
+from test_oracle_verify import lossless_error, pq_error
 
 MUTANTS = {
     "residual sign q-p": (
@@ -33,6 +33,35 @@ def test_lossless_pin_catches(oracle_mod, tmp_path, name):
     lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
     T = 0.5 if "temperature" in name else 1.0
     assert lossless_error(oracle_mod, T, 0, lib=lib) > 1e-3
+
+
+# Slips confined to the block that writes the diagnostic p_k(x_k), q_k(x_k): the
+# decisions (and so the losslessness pin) are untouched, the probability pin is not.
+PQ_MUTANTS = {
+    "p and q outputs swapped": (
+        "if (out_p) out_p[(size_t)b * K + k] = p[x];\n            if (out_q) out_q[(size_t)b * K + k] = q[x];",
+        "if (out_p) out_p[(size_t)b * K + k] = q[x];\n            if (out_q) out_q[(size_t)b * K + k] = p[x];"),
+    "p from target row k+1": (
+        "row_softmax(tgt, dtype, (trow0 + k) * (size_t)V, V, T, Mt[k], p);\n"
+        "            row_softmax(drf, dtype, (drow0 + k) * (size_t)V, V, T, Md[k], q);\n"
+        "            if (out_p)",
+        "row_softmax(tgt, dtype, (trow0 + k + 1) * (size_t)V, V, T, Mt[k + 1], p);\n"
+        "            row_softmax(drf, dtype, (drow0 + k) * (size_t)V, V, T, Md[k], q);\n"
+        "            if (out_p)"),
+    "temperature dropped in the diagnostic block": (
+        "row_softmax(drf, dtype, (drow0 + k) * (size_t)V, V, T, Md[k], q);\n            if (out_p)",
+        "row_softmax(drf, dtype, (drow0 + k) * (size_t)V, V, 1.0, Md[k], q);\n            if (out_p)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PQ_MUTANTS))
+def test_probability_pin_catches(oracle_mod, tmp_path, name):
+    old, new = PQ_MUTANTS[name]
+    src = oracle_mod.source()
+    assert src.count(old) == 1, name
+    lib = oracle_mod.build_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    assert pq_error(oracle_mod, lib=lib) > 1e-3
+    assert lossless_error(oracle_mod, 1.0, 0, lib=lib) < 1e-9  # decisions unchanged
 
 
 SCHED_MUTANTS = {

@@ -301,3 +301,60 @@ def test_invalid_inputs_flagged(oracle_mod):
         assert ref["flags"][b] & oracle_mod.FLAG_INVALID
     for b in (0, 7):
         assert ref["out_accepted"][b] >= 0 and not ref["flags"][b] & oracle_mod.FLAG_INVALID
+
+
+def _bf16_round(x):
+    """float32 array -> (bf16 bit patterns, their exact float64 values), round to
+    nearest even, written out with integer arithmetic (no torch)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    return b, (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pq_error(oracle_mod, lib=None):
+    """Largest relative error of the oracle's diagnostic outputs p_k(x_k), q_k(x_k)
+    against numpy's float64 softmax of the same (exactly representable) logits, over
+    fp32 and bf16 inputs, T in {0.5, 1, 2}, ragged verify lengths and drafted tokens
+    spread over the row; inf when a position k >= L_b is not NaN or a tested one is."""
+    worst = 0.0
+    for i, dt in enumerate(("f32", "bf16")):
+        for j, T in enumerate((0.5, 1.0, 2.0)):
+            rng = np.random.default_rng(100 + 10 * i + j)
+            B, K, V = 6, 5, 700
+            t = rng.normal(0.0, 2.5, size=(B, K + 1, V)).astype(np.float32)
+            d = (t[:, :K] + rng.normal(0.0, 1.0, size=(B, K, V))).astype(np.float32)
+            if dt == "bf16":
+                (tb, tv), (db, dv) = _bf16_round(t), _bf16_round(d)
+                targ, darg = tb, db
+            else:
+                tv, dv = t.astype(np.float64), d.astype(np.float64)
+                targ, darg = t, d
+            tok = rng.integers(0, V, size=(B, K)).astype(np.int32)
+            L = np.array([0, 1, 3, 5, 2, 4], np.int32)
+            u = rng.random((B, K + 1)).astype(np.float32)
+            r = oracle_mod.verify(targ, darg, tok, L, u, T, lib=lib)
+            for b in range(B):
+                for k in range(K):
+                    if k >= L[b]:
+                        if not (np.isnan(r["p"][b, k]) and np.isnan(r["q"][b, k])):
+                            return np.inf
+                        continue
+                    pk = softmax64(tv[b, k], T)[tok[b, k]]
+                    qk = softmax64(dv[b, k], T)[tok[b, k]]
+                    for got, want in ((r["p"][b, k], pk), (r["q"][b, k], qk)):
+                        if not np.isfinite(got):
+                            return np.inf
+                        worst = max(worst, abs(got - want) / want)
+    return worst
+
+
+def test_diag_probabilities_are_softmax_at_drafted_token(oracle_mod):
+    """The oracle's p_k(x_k) and q_k(x_k) outputs (the reference for the GPU's
+    probability parity) against numpy's float64 softmax of target row k and draft row
+    k at temperature T, evaluated at the drafted token [DSpark Deep Dive, 'The
+    Speculative Decoding Solution': p and q are the softmax distributions of the target
+    and draft logits]. Both sides sum V = 700 exponentials in float64 in different
+    orders (sequential against pairwise) and round (z - M)/T against z/T - max(z/T),
+    so they agree to a few ulps (measured 2e-15): 1e-14 relative. NaN beyond each
+    request's verify length."""
+    assert pq_error(oracle_mod) < 1e-14
