@@ -254,7 +254,7 @@ sv_status sv_markov_draft(const void *logits_d, const void *U_d, const void *Vm_
  *  argmax of target row k, and the terminal token is the argmax of row j. The
  *  emitted tokens follow the target distribution exactly.
  *  Arithmetic: fp32 softmax statistics; the terminal inverse CDF is accumulated in
- *  float64 over compensated fp32 sums.
+ *  float-float (about 48 significant bits) over compensated fp32 sums.
  *  Limits: 0 <= B <= SV_MAX_B, 1 <= K <= SV_MAX_K, 1 <= V <= SV_MAX_V.
  */
 sv_status sv_verify(const void *target_d, const void *draft_d, sv_dtype dtype,
@@ -273,13 +273,41 @@ sv_status sv_verify(const void *target_d, const void *draft_d, sv_dtype dtype,
  *           position k (k <= j and k < L_b). accept/tested is the per-position
  *           acceptance rate the online calibration of [DD "Online Calibration"]
  *           compares against the predicted confidence.
+ *  near_tie_flags_d [B] int32 or NULL: per request, the decisions that were close
+ *           enough to a boundary that fp32 rounding could have changed them (the
+ *           accept rule u < min(1, p/q) and the residual sample of [DD "The
+ *           Speculative Decoding Solution"]); 0 for a request with none. Bits:
+ *             1  an accept test at a tested position (k <= j, k < L_b) had
+ *                |u_k - min(1, p/q)| < 1e-5 (min(1, p/q) read as 1 when q = 0 < p,
+ *                and 0 when p = q = 0);
+ *             2  the terminal sample's target u_{b,K} * Z lay within 1e-5 * Z of an
+ *                edge of the chosen token's inverse-CDF bucket (Z = total weight);
+ *             4  p and q were both below 1e-30 at a tested position;
+ *             8  the residual max(0, p_j - q_j) had less than 1e-5 of mass;
+ *            16  the request is invalid (out_accepted = -1).
+ *           At T == 0: 0, or 16 for an invalid request. Computed from the kernel's own
+ *           fp32 / float-float values, so a flag can differ from an exact
+ *           computation's only when the exact margin is itself within about 2e-6 of
+ *           the 1e-5 window.
  */
 sv_status sv_verify_diag(const void *target_d, const void *draft_d, sv_dtype dtype,
                          const int32_t *draft_tok_d, const int32_t *verify_len_d,
                          const float *uniforms_d, int B, int K, int V, float temperature,
                          int32_t *out_tok_d, int32_t *out_accepted_d, float *out_p_d,
                          float *out_q_d, uint32_t *accept_count_d, uint32_t *tested_count_d,
-                         void *ws_d, size_t ws_bytes, void *stream);
+                         int32_t *near_tie_flags_d, void *ws_d, size_t ws_bytes,
+                         void *stream);
+
+/*
+ * sv_set_wait_limit: bound, in GPU clock cycles, on how long a verify call's warps
+ * wait for results published by other warps (a row's partial sums, a request's
+ * decision, a queued terminal job) before the call gives up: SV_ERR_TIMEOUT in the
+ * status word, outputs unspecified, the workspace left ready for the next call.
+ * cycles <= 0 restores the default (about 2 s). Applies to calls made afterwards in
+ * this process; returns the previous bound. A testing aid: the default is far above
+ * any normal wait. The library has no counterpart on the pages.
+ */
+long long sv_set_wait_limit(long long cycles);
 
 /*
  * sv_verify_tree: verification of drafted token trees (multi-candidate rejection
@@ -339,20 +367,23 @@ sv_status sv_get_status(void *ws_d, void *stream, int clear, int32_t *status_out
 
 /*
  * sv_verify_static: sv_verify for callers that cannot allocate device memory -- for
- * example code that runs while a CUDA graph is being captured in a mode that forbids
- * cudaMalloc, or a plugin whose host application owns every allocation. The paper has
- * no counterpart; this is a convenience of this library.
+ * example a plugin whose host application owns every device allocation, or a runtime
+ * that plans all its memory up front and allows no allocation afterwards. The paper
+ * has no counterpart; this is a convenience of this library.
  *
  * Same arguments and results as sv_verify, without the workspace: the scratch is one
  * device array inside the library, SV_STATIC_SCRATCH_BYTES long, that every GPU which
  * loads the library holds until the process exits. Shapes whose workspace
  * (sv_workspace_bytes(B, K, V)) exceeds that size return SV_ERR_WORKSPACE without
  * doing anything. The call allocates nothing (no cudaMalloc, no cudaFree).
- *  - The first call on each device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
- *  - Every call shares the one array and clears its counters first (an async memset
- *    on `stream`), so calls whose work overlaps on the GPU -- on different streams, or
- *    from different threads -- race and must not be issued; order them on one stream.
+ *  - The first call on each device also looks up the array's device address (a
+ *    host-side runtime query, made with that device current).
+ *  - Every call shares the one array and keeps what the previous call left there.
+ *    Each call leaves its counters and published words at zero, and the call clears
+ *    the array's 256-byte header (an async memset on `stream`) before its kernel.
+ *    Calls whose work overlaps on the GPU -- on different streams, or from different
+ *    threads -- race on the array and must not be issued; order them on one stream.
+ *  - Arguments are checked, as for sv_verify, before anything is enqueued.
  *  - The workspace status word is cleared by every call and is not readable through
  *    this entry point; invalid device data still shows as out_accepted = -1.
  */

@@ -68,7 +68,9 @@ def load(build_if_missing: bool = True):
     lib.sv_verify.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
     lib.sv_verify.restype = i32
     lib.sv_verify_diag.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp,
-                                   vp, vp, vp, sz, vp]
+                                   vp, vp, vp, vp, sz, vp]
+    lib.sv_set_wait_limit.argtypes = [ctypes.c_longlong]
+    lib.sv_set_wait_limit.restype = ctypes.c_longlong
     lib.sv_verify_diag.restype = i32
     lib.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp,
                                    vp, sz, vp]
@@ -285,7 +287,8 @@ def sv_verify(target, draft, draft_tok, verify_len, uniforms, temperature, ws: W
 
     target [B,K+1,V], draft [B,K,V] (bf16 or fp32; draft/uniforms may be None at T=0),
     draft_tok [B,K] int32, verify_len [B] int32, uniforms [B,K+1] float32.
-    Returns (out_tok [B,K+1], out_accepted [B]) and, with diag=True, also (p, q) [B,K].
+    Returns (out_tok [B,K+1], out_accepted [B]) and, with diag=True, also (p, q) [B,K]
+    and the near-tie flags [B] int32.
     """
     target = _dev(target, "target")
     B, K1, V = target.shape
@@ -303,18 +306,25 @@ def sv_verify(target, draft, draft_tok, verify_len, uniforms, temperature, ws: W
     if diag or accept_count is not None or tested_count is not None:
         p = torch.empty((B, K), dtype=torch.float32, device=dev) if diag else None
         q = torch.empty((B, K), dtype=torch.float32, device=dev) if diag else None
+        flags = torch.empty(B, dtype=torch.int32, device=dev) if diag else None
         rc = lib.sv_verify_diag(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tok),
                                 _ptr(verify_len), _ptr(uniforms), B, K, V, float(temperature),
                                 _ptr(out_tok), _ptr(out_accepted), _ptr(p), _ptr(q),
-                                _ptr(accept_count), _ptr(tested_count), _ptr(ws.t), ws.nbytes,
-                                _stream(stream))
+                                _ptr(accept_count), _ptr(tested_count), _ptr(flags), _ptr(ws.t),
+                                ws.nbytes, _stream(stream))
         _check("sv_verify_diag", rc)
-        return (out_tok, out_accepted, p, q) if diag else (out_tok, out_accepted)
+        return (out_tok, out_accepted, p, q, flags) if diag else (out_tok, out_accepted)
     rc = lib.sv_verify(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tok),
                        _ptr(verify_len), _ptr(uniforms), B, K, V, float(temperature),
                        _ptr(out_tok), _ptr(out_accepted), _ptr(ws.t), ws.nbytes, _stream(stream))
     _check("sv_verify", rc)
     return out_tok, out_accepted
+
+
+def set_wait_limit(cycles: int) -> int:
+    """Bound (GPU clock cycles) on a verify call's waits for other warps' results;
+    cycles <= 0 restores the default. Returns the previous bound (a testing aid)."""
+    return int(load().sv_set_wait_limit(int(cycles)))
 
 
 def sv_verify_tree(target, draft, parent, draft_tok, n_nodes, uniforms, temperature,

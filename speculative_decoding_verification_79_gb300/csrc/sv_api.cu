@@ -154,12 +154,23 @@ sv_status sv_calib_update(double* stats_d, float* temps_d, int K, float lr, floa
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dtype,
+}  // extern "C"
+
+namespace sv {
+
+// Bound on a verify call's waits for other warps' results (clock cycles); a testing
+// aid can shorten it (sv_set_wait_limit).
+static std::atomic<long long> g_wait_limit{WAIT_CYCLES};
+
+// Every host-side check of a verify call, then the kernel arguments (nothing is
+// enqueued here).
+sv_status verify_prepare(const void* target_d, const void* draft_d, sv_dtype dtype,
                          const int32_t* draft_tok_d, const int32_t* verify_len_d,
                          const float* uniforms_d, int B, int K, int V, float temperature,
                          int32_t* out_tok_d, int32_t* out_accepted_d, float* out_p_d,
                          float* out_q_d, uint32_t* accept_count_d, uint32_t* tested_count_d,
-                         void* ws_d, size_t ws_bytes, void* stream) {
+                         int32_t* near_tie_flags_d, void* ws_d, size_t ws_bytes,
+                         VerifyArgs* out, int* grid_out) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || B > SV_MAX_B || K < 1 || K > SV_MAX_K || V < 1 || V > SV_MAX_V)
     return SV_ERR_SHAPE;
@@ -169,6 +180,7 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
     return SV_ERR_ARG;
   const WsLayout L = ws_layout(B, K, V);
   if (!ws_d || !aligned(ws_d, 256) || ws_bytes < L.total) return SV_ERR_WORKSPACE;
+  *grid_out = 0;
   if (B == 0) return SV_OK;
   const size_t eb = dtype == SV_BF16 ? 2 : 4;
   if (!target_d || !draft_tok_d || !verify_len_d || !out_tok_d || !out_accepted_d)
@@ -178,18 +190,19 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
       !aligned(verify_len_d, 4) || (uniforms_d && !aligned(uniforms_d, 4)) ||
       !aligned(out_tok_d, 4) || !aligned(out_accepted_d, 4) || (out_p_d && !aligned(out_p_d, 4)) ||
       (out_q_d && !aligned(out_q_d, 4)) || (accept_count_d && !aligned(accept_count_d, 4)) ||
-      (tested_count_d && !aligned(tested_count_d, 4)))
+      (tested_count_d && !aligned(tested_count_d, 4)) ||
+      (near_tie_flags_d && !aligned(near_tie_flags_d, 4)))
     return SV_ERR_ARG;
   const int sms = sm_count();
   if (sms <= 0) return SV_ERR_CUDA;
 
   unsigned char* ws = static_cast<unsigned char*>(ws_d);
-  VerifyArgs A;
+  VerifyArgs& A = *out;
   A.tgt = target_d;
-  A.drf = draft_d;
+  A.drf = greedy ? nullptr : draft_d;
   A.tok = draft_tok_d;
   A.vlen = verify_len_d;
-  A.uni = uniforms_d;
+  A.uni = greedy ? nullptr : uniforms_d;
   A.B = B;
   A.K = K;
   A.V = V;
@@ -204,12 +217,14 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.E2 = SLOT_BYTES / 2 / (int)eb;
   A.RS = L.RS;
   A.Rmax = L.Rmax;
+  A.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   A.out_tok = out_tok_d;
   A.out_acc = out_accepted_d;
   A.out_p = out_p_d;
   A.out_q = out_q_d;
   A.acc_cnt = accept_count_d;
   A.tst_cnt = tested_count_d;
+  A.out_flags = near_tie_flags_d;
   A.hdr = reinterpret_cast<WsHeader*>(ws);
   A.t_row = reinterpret_cast<uint32_t*>(ws + L.t_row);
   A.t_req = reinterpret_cast<uint32_t*>(ws + L.t_req);
@@ -221,14 +236,39 @@ sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dty
   A.jobs = reinterpret_cast<TermJob*>(ws + L.jobs);
   A.dec_flag = reinterpret_cast<uint32_t*>(ws + L.dec);
   A.lsum = reinterpret_cast<float*>(ws + L.lsum);
-
   // One persistent CTA per SM, fewer when the batch cannot give every warp a piece.
   const long long max_pieces = (long long)B * (greedy ? K + 1 : 2 * K + 1) * A.P;
   const long long want = (max_pieces + NCW - 1) / NCW;
-  const int grid = (int)(want < sms ? want : sms);
-  const cudaError_t e =
-      launch_verify(A, dtype == SV_BF16, greedy, grid, static_cast<cudaStream_t>(stream));
+  *grid_out = (int)(want < sms ? want : sms);
+  return SV_OK;
+}
+
+sv_status verify_launch(const VerifyArgs& A, sv_dtype dtype, float temperature, int grid,
+                        void* stream) {
+  if (grid <= 0) return SV_OK;
+  const cudaError_t e = launch_verify(A, dtype == SV_BF16, temperature == 0.f, grid,
+                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv
+
+extern "C" {
+
+sv_status sv_verify_diag(const void* target_d, const void* draft_d, sv_dtype dtype,
+                         const int32_t* draft_tok_d, const int32_t* verify_len_d,
+                         const float* uniforms_d, int B, int K, int V, float temperature,
+                         int32_t* out_tok_d, int32_t* out_accepted_d, float* out_p_d,
+                         float* out_q_d, uint32_t* accept_count_d, uint32_t* tested_count_d,
+                         int32_t* near_tie_flags_d, void* ws_d, size_t ws_bytes, void* stream) {
+  VerifyArgs A;
+  int grid = 0;
+  const sv_status st = verify_prepare(target_d, draft_d, dtype, draft_tok_d, verify_len_d,
+                                      uniforms_d, B, K, V, temperature, out_tok_d,
+                                      out_accepted_d, out_p_d, out_q_d, accept_count_d,
+                                      tested_count_d, near_tie_flags_d, ws_d, ws_bytes, &A, &grid);
+  if (st != SV_OK) return st;
+  return verify_launch(A, dtype, temperature, grid, stream);
 }
 
 sv_status sv_verify(const void* target_d, const void* draft_d, sv_dtype dtype,
@@ -238,7 +278,13 @@ sv_status sv_verify(const void* target_d, const void* draft_d, sv_dtype dtype,
                     void* stream) {
   return sv_verify_diag(target_d, draft_d, dtype, draft_tok_d, verify_len_d, uniforms_d, B, K, V,
                         temperature, out_tok_d, out_accepted_d, nullptr, nullptr, nullptr,
-                        nullptr, ws_d, ws_bytes, stream);
+                        nullptr, nullptr, ws_d, ws_bytes, stream);
+}
+
+long long sv_set_wait_limit(long long cycles) {
+  const long long prev = g_wait_limit.load(std::memory_order_relaxed);
+  g_wait_limit.store(cycles > 0 ? cycles : WAIT_CYCLES, std::memory_order_relaxed);
+  return prev;
 }
 
 sv_status sv_verify_tree(const void* target_d, const void* draft_d, sv_dtype dtype,

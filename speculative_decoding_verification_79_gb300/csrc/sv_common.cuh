@@ -35,7 +35,8 @@ constexpr int NSLOT = NCW * SLOTS_PER_WARP;
 constexpr int NTHREADS = 32 * NCW;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz: bound on any wait
 
-// Status word bits (sticky, in the workspace header).
+// Status word bits (sticky reports, in the workspace header; cleared only by the
+// caller).
 constexpr uint32_t ST_DEVICE_INPUT = 1u;
 constexpr uint32_t ST_TIMEOUT = 2u;
 
@@ -43,8 +44,8 @@ constexpr uint32_t ST_TIMEOUT = 2u;
 // Workspace layout (computed identically on host and device from B, K, V).
 // ---------------------------------------------------------------------------
 struct WsHeader {
-  uint32_t status;    // ST_* bits
-  uint32_t reserved;
+  uint32_t status;    // ST_* bits: sticky report
+  uint32_t abort;     // verify: set when a wait of this call gave up; reset at its end
   uint32_t cta_done;  // verify: CTAs that have finished
   uint32_t pad[61];
 };
@@ -60,7 +61,8 @@ struct __align__(32) TermJob {
   // Target and draft rows j: raw maximum M and 2^(M*a - fl(M*a)) / S, the inverse
   // row sum in the frame of the exact maximum.
   float MAt, invSt, MAd, invSd;
-  int pad[2];
+  int flags;  // near-tie flags of the decision (accept-test ties, tiny probabilities)
+  int pad;
 };
 
 struct WsLayout {
@@ -132,12 +134,14 @@ struct VerifyArgs {
   int E2;      // elements per terminal-job piece (per row)
   int RS;      // row slots per request, 2K+1
   int Rmax;    // stride of the terminal-partial array
+  long long wait_limit;  // bound, in clock cycles, on waits for other warps' results
   int32_t* out_tok;
   int32_t* out_acc;
   float* out_p;
   float* out_q;
   uint32_t* acc_cnt;
   uint32_t* tst_cnt;
+  int32_t* out_flags;
   WsHeader* hdr;
   uint32_t* t_row;
   uint32_t* t_req;
@@ -152,6 +156,18 @@ struct VerifyArgs {
 };
 
 cudaError_t launch_verify(const VerifyArgs& A, bool bf16, bool greedy, int grid, cudaStream_t st);
+
+// Host side of a verify call (sv_api.cu): every argument check, then the kernel
+// arguments and grid (grid 0: nothing to launch); and the launch itself.
+sv_status verify_prepare(const void* target_d, const void* draft_d, sv_dtype dtype,
+                         const int32_t* draft_tok_d, const int32_t* verify_len_d,
+                         const float* uniforms_d, int B, int K, int V, float temperature,
+                         int32_t* out_tok_d, int32_t* out_accepted_d, float* out_p_d,
+                         float* out_q_d, uint32_t* accept_count_d, uint32_t* tested_count_d,
+                         int32_t* near_tie_flags_d, void* ws_d, size_t ws_bytes,
+                         VerifyArgs* out, int* grid_out);
+sv_status verify_launch(const VerifyArgs& A, sv_dtype dtype, float temperature, int grid,
+                        void* stream);
 
 // ---------------------------------------------------------------------------
 // PTX wrappers.

@@ -1,8 +1,8 @@
 // sv_static.cu -- sv_verify_static: verification with no allocation at all.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA graph is being
-// captured with a capture mode that forbids it, allocator-less embedded runtimes,
-// and plugins whose host application owns every allocation. This entry point lets
+// Some callers cannot call cudaMalloc: plugins whose host application owns every
+// device allocation, runtimes that plan all their memory up front and allow no
+// allocation afterwards, and allocator-less embedded deployments. This entry point lets
 // them verify without providing a workspace: the scratch lives in one file-scope
 // device array that the library image carries, sized SV_STATIC_SCRATCH_BYTES, which
 // every GPU that loads the library keeps until the process exits.
@@ -49,15 +49,25 @@ extern "C" sv_status sv_verify_static(const void* target_d, const void* draft_d,
     return SV_ERR_SHAPE;
   const size_t need = ws_layout(B, K, V).total;
   if (need > (size_t)SV_STATIC_SCRATCH_BYTES) return SV_ERR_WORKSPACE;  // too big for the array
-  if (B == 0) return SV_OK;
-  void* ws = nullptr;
-  const sv_status st = scratch_address(&ws);
-  if (st != SV_OK) return st;
-  // The array keeps the previous call's contents: clear the header and the ticket
-  // counters, which must start at zero.
-  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + TICKET_BYTES, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  // No device work (and no address lookup) for an empty batch: its arguments are
+  // still checked.
+  void* ws = reinterpret_cast<void*>(static_cast<uintptr_t>(256));
+  if (B > 0) {
+    const sv_status sa = scratch_address(&ws);
+    if (sa != SV_OK) return sa;
+  }
+  // Every argument check runs before anything is enqueued.
+  VerifyArgs A;
+  int grid = 0;
+  const sv_status st = verify_prepare(target_d, draft_d, dtype, draft_tok_d, verify_len_d,
+                                      uniforms_d, B, K, V, temperature, out_tok_d,
+                                      out_accepted_d, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                      ws, need, &A, &grid);
+  if (st != SV_OK || grid == 0) return st;
+  // The array keeps the previous call's contents. Every call leaves its counters and
+  // published words at zero (and the array starts at zero when the library loads), so
+  // only the 256-byte header, whose status word collects reports, is cleared here.
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SV_ERR_CUDA;
-  return sv_verify(target_d, draft_d, dtype, draft_tok_d, verify_len_d, uniforms_d, B, K, V,
-                   temperature, out_tok_d, out_accepted_d, ws, need, stream);
+  return verify_launch(A, dtype, temperature, grid, stream);
 }

@@ -31,8 +31,15 @@
 //    (compensated fp32, float-float across lanes) and stores the 32 lane-range
 //    totals; the task completing a request finds the token by inverse CDF at u_{b,K}
 //    over piece totals, lane-range totals and at most one lane range of elements.
-//  Every wait is bounded in time; on expiry the kernel sets SV_ERR_TIMEOUT in the
-//  status word, lets its copies in flight land, and returns.
+//  - Near-tie flags (optional output): the deciding warp marks accept tests within
+//    1e-5 of their ratio and tests with p, q < 1e-30 among positions 0..j; the task
+//    completing the terminal sample adds a sample within 1e-5 of a CDF bucket edge
+//    and a residual of less than 1e-5 mass.
+//  Every wait is bounded: waits for another warp's result by the call's wait limit,
+//  waits for a copy to land by a fixed bound. The first wait to run out reports
+//  SV_ERR_TIMEOUT in the status word and sets the call's abort word, which every other
+//  wait checks; the warps let their copies in flight land and return, and the last
+//  CTA clears the workspace (every ticket and published word) and the abort word.
 #include <cfloat>
 #include <climits>
 
@@ -41,6 +48,13 @@
 namespace sv {
 
 enum : int { K_STREAM = 0, K_TERM = 1 };
+
+// Near-tie flag bits of a request (the oracle's meaning): an accept test within 1e-5
+// of its ratio, a terminal sample within 1e-5 (normalised) of a CDF bucket edge, p and
+// q both below 1e-30 at a test, a residual with less than 1e-5 of mass, an invalid
+// request.
+enum : int { F_ACCEPT_TIE = 1, F_CDF_EDGE = 2, F_TINY_PROB = 4, F_SMALL_RESID = 8, F_INVALID = 16 };
+constexpr float NEAR_TIE = 1e-5f;
 
 // A contiguous run of elements of one row, split by 16-byte alignment into a head
 // read directly from global memory, a body copied to shared memory, and a tail
@@ -57,6 +71,7 @@ struct __align__(16) SlotMeta {
   int jkind;          // terminal piece: J_RESID or J_BONUS
   int last;           // stream piece: the warp's row segment ends here
   int xk;             // stream piece (T > 0): the drafted token of its row, or -1
+  int tflags;         // terminal piece: near-tie flags of the request's decision
   Seg s0, s1;         // stream piece: s0; terminal piece: target (s0) and draft (s1)
   float Mt, iSt, Md, iSd;
 };
@@ -301,8 +316,14 @@ __device__ __forceinline__ bool ff_lt(ff a, ff b) {
   return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
 }
 
+__device__ __forceinline__ float ff_to_f(ff a) { return a.hi + a.lo; }
+
 __device__ __forceinline__ ff shfl_xor_ff(ff x, int o) {
   return ff{__shfl_xor_sync(FULL, x.hi, o), __shfl_xor_sync(FULL, x.lo, o)};
+}
+
+__device__ __forceinline__ ff shfl_ff(ff x, int src) {
+  return ff{__shfl_sync(FULL, x.hi, src), __shfl_sync(FULL, x.lo, src)};
 }
 
 __device__ __forceinline__ ff warp_sum_ff(ff x) {
@@ -323,6 +344,15 @@ __device__ __forceinline__ ff warp_incl_scan_ff(ff x, int lane) {
 // ---------------------------------------------------------------------------
 // Row addressing and piece splitting.
 // ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ const T* tgt_row(const VerifyArgs& A, int b, int k) {
+  return static_cast<const T*>(A.tgt) + ((size_t)b * (A.K + 1) + k) * A.V;
+}
+template <typename T>
+__device__ __forceinline__ const T* drf_row(const VerifyArgs& A, int b, int k) {
+  return static_cast<const T*>(A.drf) + ((size_t)b * A.K + k) * A.V;
+}
+
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const VerifyArgs& A, int b, int rslot, int L) {
   if (rslot <= L) return static_cast<const T*>(A.tgt) + ((size_t)b * (A.K + 1) + rslot) * A.V;
@@ -353,6 +383,17 @@ __device__ __forceinline__ int L_of_rows(int nrows, bool greedy) {
 }
 
 __device__ void raise_status(const VerifyArgs& A, uint32_t bits) { atomicOr(&A.hdr->status, bits); }
+
+// The call's abort word: set by the first wait that gives up, so that every other
+// wait of the call returns at once; the last CTA resets it. (The status word only
+// reports: a report left from an earlier call does not stop this one.)
+__device__ __forceinline__ bool call_aborted(const VerifyArgs& A) {
+  return *reinterpret_cast<volatile uint32_t*>(&A.hdr->abort) != 0;
+}
+__device__ void give_up(const VerifyArgs& A) {
+  raise_status(A, ST_TIMEOUT);
+  atomicExch(&A.hdr->abort, 1u);
+}
 
 // ---------------------------------------------------------------------------
 // Fence-free publication. Results passed between warps (row partials, row
@@ -387,9 +428,9 @@ __device__ u64 take_word(const VerifyArgs& A, u64* p) {
   if (w == 0) {
     const long long t0 = clock64();
     while ((w = ld_word(p)) == 0) {
-      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return 0;
-      if (clock64() - t0 > WAIT_CYCLES) {
-        raise_status(A, ST_TIMEOUT);
+      if (call_aborted(A)) return 0;
+      if (clock64() - t0 > A.wait_limit) {
+        give_up(A);
         return 0;
       }
       __nanosleep(32);
@@ -406,9 +447,9 @@ __device__ u64 wait_word(const VerifyArgs& A, const u64* p) {
   if (w == 0) {
     const long long t0 = clock64();
     while ((w = ld_word(p)) == 0) {
-      if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) return 0;
-      if (clock64() - t0 > WAIT_CYCLES) {
-        raise_status(A, ST_TIMEOUT);
+      if (call_aborted(A)) return 0;
+      if (clock64() - t0 > A.wait_limit) {
+        give_up(A);
         return 0;
       }
       __nanosleep(32);
@@ -424,7 +465,7 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared& S, const Veri
     if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
     if (clock64() - t0 > WAIT_CYCLES) {
       S.abort_flag = 1;
-      raise_status(A, ST_TIMEOUT);
+      give_up(A);
       return false;
     }
   }
@@ -453,6 +494,7 @@ __device__ void emit_invalid(const VerifyArgs& A, int b, int lane) {
     for (int k = lane; k < A.K; k += 32) A.out_q[(size_t)b * A.K + k] = nan;
   if (lane == 0) {
     A.out_acc[b] = -1;
+    if (A.out_flags) A.out_flags[b] = F_INVALID;
     raise_status(A, ST_DEVICE_INPUT);
     st_release(A.dec_flag + b, 2u);  // decided, no terminal sample
   }
@@ -479,7 +521,7 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   const size_t rb = (size_t)b * A.RS;
   float p = __int_as_float(0x7fc00000), q = p, MAt = 0.f, MAd = 0.f, iSt = 0.f, iSd = 0.f;
   int x = -1;
-  bool ok = true, acc = false;
+  bool ok = true, acc = false, tie = false, tiny = false;
   // Every load of the decision is issued up front. The drafted tokens' logits were
   // picked up while their rows streamed past.
   const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
@@ -516,6 +558,9 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
       iSt = __fdiv_rn(1.f, st.y);
       iSd = __fdiv_rn(1.f, sd.y);
       acc = u * q < p;
+      const float ratio = q > 0.f ? fminf(__fdiv_rn(p, q), 1.f) : (p > 0.f ? 1.f : 0.f);
+      tie = fabsf(u - ratio) < NEAR_TIE;
+      tiny = p < 1e-30f && q < 1e-30f;
     }
   }
   const bool okL = finitef(sL.x) && sL.y > 0.f && finitef(sL.y) && uK >= 0.f && uK < 1.f;
@@ -526,6 +571,10 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
   const unsigned am = __ballot_sync(FULL, lane < L && acc);
   const unsigned lm = (L >= 32) ? FULL : ((1u << L) - 1u);
   const int j = ((am & lm) == lm) ? L : (__ffs(~am) - 1);
+  // Near ties among the tests that were decisive (positions 0..j).
+  const bool tested = lane < L && lane <= j;
+  const int dflags = (__any_sync(FULL, tested && tie) ? F_ACCEPT_TIE : 0) |
+                     (__any_sync(FULL, tested && tiny) ? F_TINY_PROB : 0);
   int32_t* ot = A.out_tok + (size_t)b * (K + 1);
   for (int k = lane; k <= K; k += 32)
     if (k != j) ot[k] = (k < j) ? x : -1;
@@ -552,13 +601,15 @@ __device__ void decide_sample(const VerifyArgs& A, int b, int L, int lane) {
       J.MAd = jMdd;
       J.invSd = jSd;
     }
-    // The job's frames travel as two published words and its kind and row in the flag
-    // itself (1 | bonus << 2 | (row + 1) << 8), so neither side needs a fence.
+    // The job's frames travel as two published words and its kind, row and near-tie
+    // flags in the flag itself (1 | bonus << 2 | flags << 4 | (row + 1) << 8), so
+    // neither side needs a fence.
     u64* jw = reinterpret_cast<u64*>(A.jobs + b);
     st_word(jw, enc_pair(J.MAt, __float_as_uint(J.invSt)));
     st_word(jw + 1, enc_pair(J.MAd, __float_as_uint(J.invSd)));
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(A.dec_flag + b),
-                 "r"(1u | (J.kind == J_BONUS ? 4u : 0u) | (static_cast<uint32_t>(j + 1) << 8))
+                 "r"(1u | (J.kind == J_BONUS ? 4u : 0u) | (static_cast<uint32_t>(dflags) << 4) |
+                     (static_cast<uint32_t>(j + 1) << 8))
                  : "memory");
   }
   // The terminal rows are read again shortly by the terminal tasks: start fetching
@@ -601,7 +652,10 @@ __device__ void decide_greedy(const VerifyArgs& A, int b, int L, int lane) {
   if (A.out_q && lane < K) A.out_q[(size_t)b * K + lane] = nan;
   if (A.acc_cnt && lane < L && lane < j) atomicAdd(A.acc_cnt + lane, 1u);
   if (A.tst_cnt && lane < L && lane <= j) atomicAdd(A.tst_cnt + lane, 1u);
-  if (lane == 0) A.out_acc[b] = j;
+  if (lane == 0) {
+    A.out_acc[b] = j;
+    if (A.out_flags) A.out_flags[b] = 0;
+  }
 }
 
 // Per-lane running state of a row segment: (m, ma = fl(m*a), s) at T > 0, or
@@ -965,7 +1019,7 @@ __device__ ff range_sum_global(const T* t, const T* d, int n, const TermW& W, in
 
 // A terminal task whose ticket value has not been inspected yet.
 struct TermPend {
-  int valid, b, j, jkind;
+  int valid, b, j, jkind, tflags;
   float Mt, iSt, Md, iSd;
   uint32_t old;  // ticket value returned to lane 0
 };
@@ -990,6 +1044,7 @@ __device__ TermPend term_consume(const VerifyArgs& A, const SlotMeta& M, unsigne
   pt.b = M.b;
   pt.j = M.r;
   pt.jkind = M.jkind;
+  pt.tflags = M.tflags;
   pt.Mt = M.Mt;
   pt.iSt = M.iSt;
   pt.Md = M.Md;
@@ -1012,13 +1067,21 @@ __device__ __forceinline__ void term_ticket(const VerifyArgs& A, TermPend& pt, i
   if (lane == 0) pt.old = atom_add_release(A.t_res + pt.b, 1u);
 }
 
+// ---------------------------------------------------------------------------
+// Locating the terminal token (inverse CDF at u_{b,K}).
+// ---------------------------------------------------------------------------
+struct Located {
+  int y;
+  float gap;  // distance of the target to the nearest edge of y's bucket, over Z
+};
+
 // Element level: the first element e in [r0, r1) of rows t, d with t3 < cumulative
 // weight from r0 (or the last positive element when `past`, or when rounding leaves
 // t3 beyond the range's total). Each lane takes up to EPL consecutive elements and
 // keeps their weights in registers.
 template <typename T>
-__device__ int locate_elems(const T* t, const T* d, int r0, int r1, ff t3, bool past,
-                            const TermW& W, int lane) {
+__device__ Located locate_elems(const T* t, const T* d, int r0, int r1, ff t3, bool past, ff Z,
+                                const TermW& W, int lane) {
   constexpr int VEC = ET<T>::VEC;
   constexpr int E2 = SLOT_BYTES / 2 / (int)sizeof(T);
   constexpr int EPL = (VEC * ((E2 + 32 * VEC - 1) / (32 * VEC)) + 31) / 32;
@@ -1035,33 +1098,42 @@ __device__ int locate_elems(const T* t, const T* d, int r0, int r1, ff t3, bool 
   }
   const ff ls = two_sum_ff(hs, hc);
   const ff incl = warp_incl_scan_ff(ls, lane);
-  int y = -1;
+  Located r{-1, 0.f};
   const unsigned hit = past ? 0u : __ballot_sync(FULL, ff_lt(t3, incl));
   if (hit) {
     const int ln = __ffs(hit) - 1;
+    float gap = 0.f;
     if (lane == ln) {
       ff cum = ff_add(incl, ff_neg(ls));
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        cum = ff_add(cum, ff{w[i], 0.f});
-        if (y < 0 && e0 + i < r1 && ff_lt(t3, cum)) y = e0 + i;
+        const ff nc = ff_add(cum, ff{w[i], 0.f});
+        if (r.y < 0 && e0 + i < r1 && ff_lt(t3, nc)) {
+          r.y = e0 + i;
+          const float glo = ff_to_f(ff_add(t3, ff_neg(cum)));
+          const float ghi = ff_to_f(ff_add(nc, ff_neg(t3)));
+          gap = fminf(glo, ghi) / ff_to_f(Z);
+        }
+        cum = nc;
       }
-      if (y < 0) y = lastpos;
+      if (r.y < 0) r.y = lastpos;
     }
-    y = __shfl_sync(FULL, y, ln);
+    r.y = __shfl_sync(FULL, r.y, ln);
+    r.gap = __shfl_sync(FULL, gap, ln);
   }
-  if (y < 0) {
+  if (r.y < 0) {
     const unsigned has = __ballot_sync(FULL, lastpos >= 0);
-    y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : r0;
+    r.y = has ? __shfl_sync(FULL, lastpos, 31 - __clz(has)) : r0;
+    r.gap = 0.f;
   }
-  return y;
+  return r;
 }
 
 // Lane-range and element levels inside piece `pstar` of rows trow, drow, given each
 // lane's range total `lsv` and the target t2 relative to the piece start.
 template <typename T>
-__device__ int locate_in_piece(const VerifyArgs& A, const T* trow, const T* drow, int pstar,
-                               float lsv, ff t2, bool past, const TermW& W, int lane) {
+__device__ Located locate_in_piece(const VerifyArgs& A, const T* trow, const T* drow, int pstar,
+                                   float lsv, ff t2, bool past, ff Z, const TermW& W, int lane) {
   const ff mine{lsv, 0.f};
   const ff incl = warp_incl_scan_ff(mine, lane);
   int lstar;
@@ -1070,8 +1142,7 @@ __device__ int locate_in_piece(const VerifyArgs& A, const T* trow, const T* drow
   if (hit) {
     lstar = __ffs(hit) - 1;
     const ff ex = ff_add(incl, ff_neg(mine));
-    const ff base2{__shfl_sync(FULL, ex.hi, lstar), __shfl_sync(FULL, ex.lo, lstar)};
-    t3 = ff_add(t2, ff_neg(base2));
+    t3 = ff_add(t2, ff_neg(shfl_ff(ex, lstar)));
   } else {
     const unsigned has = __ballot_sync(FULL, lsv > 0.f);
     lstar = has ? 31 - __clz(has) : 0;
@@ -1081,13 +1152,16 @@ __device__ int locate_in_piece(const VerifyArgs& A, const T* trow, const T* drow
   const int n = min(A.E2, A.V - e0);
   const int ce = range_len<T>(n);
   const int r0 = min(n, lstar * ce), r1 = min(n, r0 + ce);
-  return e0 + locate_elems<T>(trow + e0, drow + e0, r0, r1, t3, past, W, lane);
+  Located r = locate_elems<T>(trow + e0, drow + e0, r0, r1, t3, past, Z, W, lane);
+  r.y += e0;
+  return r;
 }
 
 // No residual mass left (p == q up to rounding): sample p_j itself instead, its piece
 // totals computed here, piece by piece.
 template <typename T>
-__device__ int locate_whole_row(const VerifyArgs& A, const T* trow, float uK, TermW W, int lane) {
+__device__ Located locate_whole_row(const VerifyArgs& A, const T* trow, float uK, TermW W,
+                                    int lane) {
   W.resid = false;
   const int R = A.R;
   ff Z{0.f, 0.f};
@@ -1113,16 +1187,18 @@ __device__ int locate_whole_row(const VerifyArgs& A, const T* trow, float uK, Te
     }
     base = nb;
   }
-  return locate_in_piece<T>(A, trow, trow, pstar, lsv, ff_add(target, ff_neg(base)), past, W,
+  return locate_in_piece<T>(A, trow, trow, pstar, lsv, ff_add(target, ff_neg(base)), past, Z, W,
                             lane);
 }
 
-// Locate the terminal token of request b (row j) from its piece and lane-range totals.
+// Locate the terminal token of request b (row j) from its piece and lane-range totals
+// (whole warp). Also reports the residual's mass through `Zout` (residual jobs).
 template <typename T>
-__device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, int lane) {
+__device__ Located term_locate(const VerifyArgs& A, int b, int j, const TermW& W, float& Zout,
+                               int lane) {
   const int R = A.R, K = A.K;
-  const T* trow = static_cast<const T*>(A.tgt) + ((size_t)b * (K + 1) + j) * A.V;
-  const T* drow = W.resid ? static_cast<const T*>(A.drf) + ((size_t)b * K + j) * A.V : trow;
+  const T* trow = tgt_row<T>(A, b, j);
+  const T* drow = W.resid ? drf_row<T>(A, b, j) : trow;
   const float uK = __ldg(A.uni + (size_t)b * (K + 1) + K);
   const float2* rp = A.rpart + (size_t)b * A.Rmax;
   const int c = (R + 31) / 32;
@@ -1133,7 +1209,8 @@ __device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, in
   int lastpos = -1;
   if (c <= CREG) {
 #pragma unroll
-    for (int i = 0; i < CREG; ++i) wr[i] = (p0 + i < p1) ? __ldcg(rp + p0 + i) : make_float2(0.f, 0.f);
+    for (int i = 0; i < CREG; ++i)
+      wr[i] = (p0 + i < p1) ? __ldcg(rp + p0 + i) : make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < CREG; ++i) {
       ls = ff_add(ls, ff{wr[i].x, wr[i].y});
@@ -1147,7 +1224,8 @@ __device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, in
     }
   }
   const ff incl = warp_incl_scan_ff(ls, lane);
-  const ff Z{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
+  const ff Z = shfl_ff(incl, 31);
+  Zout = ff_to_f(Z);
   if (W.resid && !(Z.hi > 0.f && Z.hi <= 3.402823466e38f))
     return locate_whole_row<T>(A, trow, uK, W, lane);
   const ff target = ff_mul_f(Z, uK);
@@ -1190,7 +1268,7 @@ __device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, in
     }
     pstar = __shfl_sync(FULL, pstar, ln);
     past = __shfl_sync(FULL, (int)past, ln) != 0;
-    base = ff{__shfl_sync(FULL, base.hi, ln), __shfl_sync(FULL, base.lo, ln)};
+    base = shfl_ff(base, ln);
   }
   if (pstar < 0) {  // rounding put the target past the last piece
     const unsigned has = __ballot_sync(FULL, lastpos >= 0);
@@ -1199,7 +1277,7 @@ __device__ int term_locate(const VerifyArgs& A, int b, int j, const TermW& W, in
   }
   const float lsv = __ldcg(A.lsum + ((size_t)b * A.Rmax + pstar) * 32 + lane);
   const ff t2 = past ? ff{0.f, 0.f} : ff_add(target, ff_neg(base));
-  return locate_in_piece<T>(A, trow, drow, pstar, lsv, t2, past, W, lane);
+  return locate_in_piece<T>(A, trow, drow, pstar, lsv, t2, past, Z, W, lane);
 }
 
 // Inspect a terminal ticket: the task completing its request locates the token.
@@ -1210,8 +1288,17 @@ __device__ void term_settle(const VerifyArgs& A, const TermPend& pt, int lane) {
   fence_acq_rel();
   if (lane == 0) A.t_res[pt.b] = 0;
   const TermW W{A.a, pt.Mt, pt.iSt, pt.Md, pt.iSd, pt.jkind == J_RESID};
-  const int y = term_locate<T>(A, pt.b, pt.j, W, lane);
-  if (lane == 0) A.out_tok[(size_t)pt.b * (A.K + 1) + pt.j] = y;
+  float Z = 0.f;
+  const Located r = term_locate<T>(A, pt.b, pt.j, W, Z, lane);
+  if (lane == 0) {
+    A.out_tok[(size_t)pt.b * (A.K + 1) + pt.j] = r.y;
+    if (A.out_flags) {
+      int f = pt.tflags;
+      if (r.gap < NEAR_TIE) f |= F_CDF_EDGE;
+      if (W.resid && Z < NEAR_TIE) f |= F_SMALL_RESID;
+      A.out_flags[pt.b] = f;
+    }
+  }
   __syncwarp();
 }
 
@@ -1321,6 +1408,7 @@ __device__ void issue_term(const VerifyArgs& A, int b, int p, const TermJob& J, 
   meta.iSt = J.invSt;
   meta.Md = J.MAd;
   meta.iSd = J.invSd;
+  meta.tflags = J.flags;
   meta.s0 = make_seg(reinterpret_cast<const unsigned char*>(tr), n, eb);
   bool whole = meta.s0.head == 0 && meta.s0.body == n;
   if (kind == J_RESID) {
@@ -1386,6 +1474,7 @@ __device__ int refill(const VerifyArgs& A, Issuer& I, const int* prefix, bool fr
         const u64* jw = reinterpret_cast<const u64*>(A.jobs + b);
         const u64 w1 = wait_word(A, jw), w2 = wait_word(A, jw + 1);
         I.J.kind = (f & 4u) ? J_BONUS : J_RESID;
+        I.J.flags = static_cast<int>((f >> 4) & 15u);
         I.J.j = static_cast<int>(f >> 8) - 1;
         I.J.MAt = dec_x(w1);
         I.J.invSt = __uint_as_float(dec_y(w1));
@@ -1424,13 +1513,13 @@ __device__ bool wait_decided(const VerifyArgs& A, Shared& S, Issuer& I) {
     __nanosleep(256);
     if ((it & 15) != 0) continue;
     if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
-    if (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) {
+    if (call_aborted(A)) {
       S.abort_flag = 1;
       return false;
     }
-    if (clock64() - t0 > WAIT_CYCLES) {
+    if (clock64() - t0 > A.wait_limit) {
       S.abort_flag = 1;
-      raise_status(A, ST_TIMEOUT);
+      give_up(A);
       return false;
     }
   }
@@ -1690,7 +1779,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
   __syncthreads();
   if (S.last_cta) {
     __threadfence();
-    const bool dirty = (*reinterpret_cast<volatile uint32_t*>(&A.hdr->status) & ST_TIMEOUT) != 0;
+    const bool dirty = call_aborted(A);
     if (dirty) {
       // An aborted call can leave published words behind: clear them all.
       const size_t nrow = (size_t)B * A.RS;
@@ -1711,7 +1800,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sv_verify_kernel(const VerifyArgs
       reinterpret_cast<u64*>(A.jobs + i)[0] = 0ull;
       reinterpret_cast<u64*>(A.jobs + i)[1] = 0ull;
     }
-    if (tid == 0) A.hdr->cta_done = 0;
+    __syncthreads();
+    if (tid == 0) {
+      A.hdr->abort = 0;
+      A.hdr->cta_done = 0;
+    }
   }
 }
 

@@ -48,6 +48,7 @@ def run_gpu(sv, g, T, ws=None, diag=True):
     if diag:
         res["p"] = out[2].cpu().numpy()
         res["q"] = out[3].cpu().numpy()
+        res["flags"] = out[4].cpu().numpy()
     res["status"] = ws.status(clear=True)
     return res
 
@@ -95,6 +96,8 @@ def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
                     f"{g[bb, kk]:.9e} ref {r[bb, kk]:.9e} (other: gpu p {gp[bb, kk]:.6e} "
                     f"q {gq[bb, kk]:.6e}; ref p {ref['p'][bb, kk]:.6e} q {ref['q'][bb, kk]:.6e}); "
                     f"{int(badm.sum())} elements over")
+    if "flags" in gpu:
+        check_flags(gpu["flags"] if idx is None else gpu["flags"][idx], ref, T)
     positions = int((np.clip(L, 0, None) + 1).sum())
     fl = ref["flags"]
     LAST.update(requests=int(fl.size), accept_tie=int(((fl & oracle.FLAG_ACCEPT_TIE) != 0).sum()),
@@ -109,6 +112,35 @@ def compare(gpu, ref, T, verify_len, idx=None, check_p=True):
     assert (margins < MARGIN_RESOLUTION).all(), (
         f"decisions differ at oracle margins {margins.tolist()}, above the GPU's resolution")
     return int(flagged.sum()), positions, int(differ.sum()), float(margins.max(initial=0.0))
+
+
+# Near-tie flags from the GPU against the oracle's: the accept-test and CDF-edge kinds
+# together are raised exactly when a request's smallest decision margin is below 1e-5,
+# so they must agree wherever the oracle's margin is outside [1e-5 - 2e-6, 1e-5 + 2e-6]
+# (the GPU's flags come from its own fp32 values); the invalid bit must agree always.
+FLAG_BAND = MARGIN_RESOLUTION
+FLAG_COUNTS = {"requests": 0, "gpu_flagged": 0, "in_band": 0}
+
+
+def check_flags(gflags, ref, T):
+    rf = ref["flags"]
+    inv_g = (gflags & oracle.FLAG_INVALID) != 0
+    inv_r = (rf & oracle.FLAG_INVALID) != 0
+    assert np.array_equal(inv_g, inv_r), f"invalid flags differ at {np.nonzero(inv_g != inv_r)[0][:10]}"
+    if T == 0:
+        assert (gflags[~inv_g] == 0).all()
+        return
+    tie_mask = oracle.FLAG_ACCEPT_TIE | oracle.FLAG_CDF_EDGE
+    g = ((gflags & tie_mask) != 0) & ~inv_g
+    r = ((rf & tie_mask) != 0) & ~inv_r
+    m = ref["margin"]
+    band = np.abs(m - 1e-5) <= FLAG_BAND
+    bad = np.nonzero((g != r) & ~band & ~inv_r)[0]
+    assert bad.size == 0, (f"near-tie flags differ at requests {bad[:10]}: gpu {gflags[bad[:10]]} "
+                           f"oracle {rf[bad[:10]]} margins {m[bad[:10]]}")
+    FLAG_COUNTS["requests"] += int((~inv_r).sum())
+    FLAG_COUNTS["gpu_flagged"] += int(g.sum())
+    FLAG_COUNTS["in_band"] += int((band & ~inv_r).sum())
 
 
 def account(name, nf, npos, nmis, max_margin=0.0):

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     for n in ("sv_schedule", "sv_verify", "sv_verify_diag", "sv_workspace_bytes",
               "sv_workspace_init", "sv_get_status", "sv_status_string", "sv_version",
               "sv_schedule_cal", "sv_calib_stats_len", "sv_calib_observe", "sv_calib_update",
-              "sv_markov_keys_len", "sv_markov_draft", "sv_schedule_curve", "sv_verify_tree"):
+              "sv_markov_keys_len", "sv_markov_draft", "sv_schedule_curve", "sv_verify_tree",
+              "sv_verify_static", "sv_set_wait_limit"):
         assert n in names
 
 
@@ -74,6 +75,9 @@ def test_host_argument_checks(lib):
     assert lib.sv_verify(*args(drf=None)) == sv.SV_ERR_ARG
     assert lib.sv_verify(*args(dt=0, tgt=ctypes.c_void_p(258))) == sv.SV_ERR_ARG
     assert lib.sv_verify(*args(B=0)) == sv.SV_OK
+    diag = lambda flags=fake: (fake, fake, 1, fake, fake, fake, 4, 4, 100, 1.0, fake, fake,  # noqa: E731
+                               None, None, None, None, flags, fake, n, None)
+    assert lib.sv_verify_diag(*diag(flags=ctypes.c_void_p(258))) == sv.SV_ERR_ARG
     assert lib.sv_schedule(fake, 4, 4, 1.5, 10, fake, fake, n, None) == sv.SV_ERR_ARG
     assert lib.sv_schedule(fake, 4, 4, float("nan"), 10, fake, fake, n, None) == sv.SV_ERR_ARG
     assert lib.sv_schedule(fake, 4, 4, 0.3, -1, fake, fake, n, None) == sv.SV_ERR_ARG
@@ -84,10 +88,40 @@ def test_host_argument_checks(lib):
     assert sv.status_string(sv.SV_ERR_TIMEOUT) == "device wait timed out"
 
 
-def test_workspace_layout_is_shape_independent_for_counters(lib):
-    """Counters live at fixed offsets, so any workspace holds at least that region."""
-    small = lib.sv_workspace_bytes(1, 1, 1)
-    assert small >= 4 * (4096 * 65 + 2 * 4096)
+def test_workspace_fits_every_smaller_shape(lib):
+    """A workspace sized for (B, K, V) holds the layout of any call with B' <= B,
+    K' <= K, V' <= V (calls of different shapes may share it)."""
+    import itertools
+
+    shapes = list(itertools.product((1, 7, 64, 512, 4096), (1, 3, 8, 32), (1, 999, 151936)))
+    size = {sh: lib.sv_workspace_bytes(*sh) for sh in shapes}
+    for a in shapes:
+        for b in shapes:
+            if all(x <= y for x, y in zip(a, b)):
+                assert size[a] <= size[b], (a, b)
+
+
+def test_static_entry_and_wait_limit_host_side(lib):
+    """sv_verify_static checks its arguments before any device work (an empty batch
+    needs no GPU); sv_set_wait_limit returns the previous bound."""
+    import speculative_decoding_verification_79_gb300 as sv
+
+    fn = lib.sv_verify_static
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
+    fn.restype = i32
+    fake = ctypes.c_void_p(256)
+    args = lambda dt=1, B=4, K=4, V=100, T=1.0: (  # noqa: E731
+        fake, fake, dt, fake, fake, fake, B, K, V, T, fake, fake, None)
+    assert fn(*args(B=0)) == sv.SV_OK
+    assert fn(*args(B=0, dt=7)) == sv.SV_ERR_DTYPE
+    assert fn(*args(B=0, T=-1.0)) == sv.SV_ERR_ARG
+    assert fn(*args(K=33)) == sv.SV_ERR_SHAPE
+    assert fn(*args(B=4096, K=32, V=1 << 20)) == sv.SV_ERR_WORKSPACE
+    prev = lib.sv_set_wait_limit(12345)
+    assert lib.sv_set_wait_limit(prev) == 12345
+    assert lib.sv_set_wait_limit(0) == prev
+    assert lib.sv_set_wait_limit(0) == 4000000000
 
 
 def test_no_fallback_without_cuda():

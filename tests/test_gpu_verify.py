@@ -274,6 +274,35 @@ def test_cuda_graph_replay(sv):
 
 
 @needs_cuda
+def test_timeout_then_clean_call(sv):
+    """Every wait of a verify call for another warp's result is bounded. With the bound
+    cut to 300 clock cycles (a testing aid), waits that normally last microseconds (the
+    producers waiting for the last decisions, warps waiting for published words) run
+    out: the call gives up, SV_ERR_TIMEOUT is reported, and the kernel returns. The
+    next call on the same workspace, with the status still set, must match the oracle
+    exactly: the abort of one call does not leak into the next."""
+    inp = synth.sweep_point(64, 8, seed=3, device="cuda")
+    ws = sv.Workspace(64, 8, synth.QWEN3_VOCAB)
+    prev = sv.set_wait_limit(300)
+    try:
+        sv.sv_verify(inp["target"], inp["draft"], inp["draft_tok"], inp["verify_len"],
+                     inp["uniforms"], 1.0, ws)
+        torch.cuda.synchronize()
+    finally:
+        sv.set_wait_limit(prev)
+    assert ws.status() == sv.SV_ERR_TIMEOUT
+    for _ in range(2):
+        tok, acc, p, q, fl = sv.sv_verify(inp["target"], inp["draft"], inp["draft_tok"],
+                                          inp["verify_len"], inp["uniforms"], 1.0, ws, diag=True)
+        torch.cuda.synchronize()
+        gpu = {"out_tok": tok.cpu().numpy(), "out_accepted": acc.cpu().numpy(),
+               "p": p.cpu().numpy(), "q": q.cpu().numpy(), "flags": fl.cpu().numpy()}
+        compare(gpu, run_oracle(inp, 1.0), 1.0, inp["verify_len"].cpu().numpy())
+    assert ws.status(clear=True) == sv.SV_ERR_TIMEOUT  # the report stays until cleared
+    assert ws.status() == sv.SV_OK
+
+
+@needs_cuda
 def test_near_tie_summary():
     """Reading of the near-tie rule. Outside the oracle's 1e-5 near-tie windows every
     decision above was bit-exact. At V = 151,936 the mean inverse-CDF bucket (6.6e-6) is
@@ -293,4 +322,10 @@ def test_near_tie_summary():
           f"requests ({t['accept_tie'] / t['positions']:.2e} of positions); terminal sample "
           f"within 1e-5 of a CDF edge in {t['cdf_edge']} of {t['requests']} requests; "
           f"degenerate (tiny probabilities, empty residual) in {t['degenerate']}")
+    f = gpu_util.FLAG_COUNTS
+    if f["requests"]:
+        print(f"[near-ties] GPU flags (accept ties and CDF edges): {f['gpu_flagged']} of "
+              f"{f['requests']} valid requests ({f['gpu_flagged'] / t['positions']:.2e} of "
+              f"positions); {f['in_band']} requests had an oracle margin within 2e-6 of the "
+              f"1e-5 window, where the GPU's flag may differ")
     assert t["max_margin"] < gpu_util.MARGIN_RESOLUTION

@@ -1,6 +1,7 @@
 """sv_verify_static, the entry point for callers that cannot allocate device memory
-(graph-capture code that may not call cudaMalloc, plugins whose host owns every
-allocation): it keeps its scratch in a fixed device array inside the library.
+(plugins whose host application owns every device allocation, runtimes that plan all
+their memory up front): it keeps its scratch in a fixed device array inside the
+library.
 
 Called through the C-ABI and checked against sv_verify (the workspace entry point) on
 two calls in a row with different inputs: the decisions must be identical, the bar of
@@ -66,3 +67,38 @@ def test_static_scratch_rejects_oversized_shapes():
     d = ctypes.c_void_p(dummy.data_ptr())
     rc = fn(d, d, 1, d, d, d, 4096, 32, 1 << 20, 1.0, d, d, None)
     assert rc == sv.SV_ERR_WORKSPACE
+
+
+@needs_cuda
+def test_static_scratch_after_invalid_device_data():
+    """A call with invalid device data (a drafted token outside [0, V)) marks that
+    request -1; the next call on the shared array must again match sv_verify."""
+    import speculative_decoding_verification_79_gb300 as sv
+
+    lib = sv.load()
+    fn = _static_fn(lib)
+    stream = torch.cuda.current_stream()
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    B, K, V = 16, 6, 40000
+    bad = synth.verify_inputs(B, K, V, dtype=torch.bfloat16, temperature=1.0, seed=31,
+                              device="cuda", verify_len="uniform")
+    bad["draft_tok"][3, 0] = V
+    bad["verify_len"][3] = K
+    good = synth.verify_inputs(B, K, V, dtype=torch.bfloat16, temperature=1.0, seed=32,
+                               device="cuda", verify_len="uniform")
+    ws = sv.Workspace(B, K, V)
+    ref_tok, ref_acc = sv.sv_verify(good["target"], good["draft"], good["draft_tok"],
+                                    good["verify_len"], good["uniforms"], 1.0, ws)
+    for g, check in ((bad, False), (good, True)):
+        out_tok = torch.full((B, K + 1), -7, dtype=torch.int32, device="cuda")
+        out_acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        rc = fn(P(g["target"]), P(g["draft"]), 1, P(g["draft_tok"]), P(g["verify_len"]),
+                P(g["uniforms"]), B, K, V, 1.0, P(out_tok), P(out_acc),
+                ctypes.c_void_p(stream.cuda_stream))
+        assert rc == sv.SV_OK, sv.status_string(rc)
+        torch.cuda.synchronize()
+        if not check:
+            assert int(out_acc[3]) == -1 and (out_tok[3] == -1).all()
+            continue
+        assert np.array_equal(out_acc.cpu().numpy(), ref_acc.cpu().numpy())
+        assert np.array_equal(out_tok.cpu().numpy(), ref_tok.cpu().numpy())
