@@ -195,8 +195,14 @@ def run_gpu(args):
                for _ in range(n_graph)]
     except TypeError:
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_graph)]
+    # The timed graph holds the launches only; a second graph of the same steps with
+    # event-record nodes between the launches gives the per-launch times.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=st):
+        for i in range(n_graph):
+            step(i)
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=st):
         for i in range(n_graph):
             step(i, evs[i])
     rem = args.steps % n_graph
@@ -230,10 +236,15 @@ def run_gpu(args):
         torch.distributed.barrier()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     clocks = clk.summary()
+    with torch.cuda.stream(st):  # per-launch times, after the timed region
+        for _ in range(2):
+            graph_ev.replay()
+    st.synchronize()
     try:
         ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
         sch_ms = [e[0].elapsed_time(e[1]) for e in evs]
-        timing_src = f"event-record nodes in the graph, last of {reps} replays"
+        timing_src = ("event-record nodes around each launch in a replay of the same steps "
+                      "after the timed region (the timed graph holds the launches only)")
     except RuntimeError:
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_graph)]
         with torch.cuda.stream(st):
@@ -249,11 +260,22 @@ def run_gpu(args):
     L = out_len.cpu()
     tokens_per_step = int(L.sum().item())
     bytes_per_launch = synth.logit_bytes(L, V, 2, greedy=(T == 0.0))
+    # For context: the rows a verifier would need if it stopped reading each request at
+    # its first rejection j_b (positions 0..j_b, plus one row), from the last step's
+    # outputs.
+    jb = out_acc.cpu().clamp(min=0)
+    early_exit = int(((2 * torch.minimum(jb + 1, L) + 1) * V * 2).sum().item())
     value = job_rate(tokens_per_step, args.steps, world, elapsed_ms)
     ver_avg = sum(ver_ms) / len(ver_ms)
     peak, peak_kind = _peaks()
     achieved = bytes_per_launch / (ver_avg / 1e3) / 1e9
 
+    traffic = _profiled_traffic()
+    traffic_src = (f"dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of this "
+                   f"workload, from the committed summary {os.path.relpath(PROFILE, ROOT)}, "
+                   f"taken on the same kernel sources (sha {kernel_sha()}); not measured in "
+                   f"this run") if traffic is not None else (
+                   "null: the committed ncu summary was taken on other kernel sources")
     e2e = run_e2e(args, sv, sets[0], ws, dev, tau, budget) if args.e2e_steps > 0 else None
     cpu = cpu_baseline(args) if (rank == 0 and not args.no_cpu) else None
 
@@ -271,11 +293,14 @@ def run_gpu(args):
         "logit_gbs": job_rate(bytes_per_launch, args.steps, world, elapsed_ms) / 1e9,
         "verify_us_avg": ver_avg * 1e3, "schedule_us_avg": sum(sch_ms) / len(sch_ms) * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "frac": achieved / peak, "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                      "kernel": "sv_verify_kernel<bf16, T>0>",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "per_launch_timing": timing_src},
+                     "per_launch_timing": timing_src,
+                     "early_exit_min_bytes": early_exit,
+                     "early_exit_min_frac_of_algorithmic": early_exit / bytes_per_launch},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -353,35 +378,67 @@ def _oracle_args(inp, vlen=None):
             inp["uniforms"].numpy()]
 
 
-def cpu_baseline(args):
-    """The float64 oracle, as it stands, on a bounded sample of the same workload, on all
-    host cores, scaled to verified draft tokens/s. The sample is the workload's batch of
-    B requests (fewer if one batch alone would take longer than the time budget), run
-    as many times as fit in about --cpu-seconds of wall time."""
+def _cpu_model():
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else platform)."""
+    import platform
+    import subprocess
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_rate(args, threads, seconds, seed):
+    """Verified draft tokens/s of the float64 oracle (schedule + verify) on `threads`
+    host threads, over as many passes of a sample batch as fit in about `seconds`."""
     import oracle
 
-    cores = os.cpu_count() or 1
-    inp = _inputs(1, args.K, args.V, args.T, 7, "cpu")
+    inp = _inputs(1, args.K, args.V, args.T, seed, "cpu")
     t0 = time.perf_counter()
     oracle.verify(*_oracle_args(inp), args.T, nthreads=1, diag=False)
     one = time.perf_counter() - t0
-    n_req = max(1, min(args.B, int(args.cpu_seconds * cores / max(one, 1e-6))))
-    inp = _inputs(n_req, args.K, args.V, args.T, 8, "cpu")
+    n_req = max(1, min(args.B, int(seconds * threads / max(one, 1e-6))))
+    inp = _inputs(n_req, args.K, args.V, args.T, seed + 1, "cpu")
     conf = inp["conf"].numpy()
     oargs = _oracle_args(inp)
-    threads = min(cores, n_req)
+    threads = min(threads, n_req)
     reps, dt = 0, 0.0
     t0 = time.perf_counter()
-    while reps == 0 or dt < args.cpu_seconds:
+    while reps == 0 or dt < seconds:
         oracle.schedule(conf, 0.0, n_req * args.K)
         oracle.verify(*oargs, args.T, nthreads=threads, diag=False)
         reps += 1
         dt = time.perf_counter() - t0
-    return {"value": reps * n_req * args.K / dt, "unit": UNIT, "cores": threads,
-            "kind": "oracle",
+    return reps * n_req * args.K / dt, threads, reps, n_req, dt
+
+
+def cpu_baseline(args):
+    """The float64 oracle, as it stands, on a bounded sample of the same workload, scaled
+    to verified draft tokens/s: on all host cores (the line's value) and on one core.
+    The sample is the workload's batch of B requests (fewer if one batch alone would
+    take longer than the time budget), run as many times as fit in about --cpu-seconds
+    of wall time (half of it for the one-core figure)."""
+    cores = os.cpu_count() or 1
+    v, threads, reps, n_req, dt = _oracle_rate(args, cores, args.cpu_seconds, 7)
+    v1, _, reps1, n1, dt1 = _oracle_rate(args, 1, args.cpu_seconds / 2, 17)
+    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "value_1core": v1, "host_cpus": cores, "cpu_model": _cpu_model(),
             "sample": f"{reps} passes over {n_req} of the {args.B} requests (K={args.K}, "
                       f"V={args.V}, bf16 inputs, T={args.T}), schedule + verify, "
-                      f"{dt:.1f} s wall on {threads} threads"}
+                      f"{dt:.1f} s wall on {threads} threads; one core: {reps1} passes over "
+                      f"{n1} requests, {dt1:.1f} s"}
 
 
 def run_reference(args):
