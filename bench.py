@@ -508,8 +508,8 @@ def run_sweep(args):
     temps = [float(t) for t in args.sweep_T.split(",")] if args.sweep_T else [args.T]
     st = torch.cuda.Stream(device=dev)
     for T in temps:
-        for K in synth.SWEEP_K:
-            for B in synth.SWEEP_B:
+        for K in (args.sweep_K or synth.SWEEP_K):
+            for B in (args.sweep_B or synth.SWEEP_B):
                 nbytes1 = synth.logit_bytes([K] * B, synth.QWEN3_VOCAB, 2, greedy=(T == 0.0))
                 nsets = max(2, -(-2 * (129 << 20) // max(1, nbytes1)))  # > 2x L2 in total
                 sets = [synth.sweep_point(B, K, seed=s, device=dev) for s in range(nsets)]
@@ -822,6 +822,8 @@ def main():
                     help="time tree (multi-candidate) verification")
     ap.add_argument("--tree-B", type=lambda x: [int(v) for v in x.split(",")], default=[64],
                     help="batch sizes of --tree, comma-separated")
+    ap.add_argument("--sweep-B", type=lambda x: [int(v) for v in x.split(",")], default=None)
+    ap.add_argument("--sweep-K", type=lambda x: [int(v) for v in x.split(",")], default=None)
     ap.add_argument("--once", type=int, default=0,
                     help="no timing: build one input set and run N schedule+verify steps "
                          "(a short, self-contained program for profilers)")
