@@ -7,31 +7,47 @@
 // and the next token is drafted from L'_k (greedy here: the lowest-index argmax, as
 // in the page's sketch), so the positions run one after another.
 //
-// One launch per position. For a batch of B requests the correction is a product of
-// U [V, r] with X [r, B], X's columns the gathered rows Vm[y_b, :]: a dense
-// contraction, done on the tensor cores (bf16 inputs, fp32 accumulation) by
-// mma.sync.m16n8k16. A CTA owns 128 vocabulary rows and up to 64 requests: it copies
-// its U tile (kept in L2 across positions: evict_last) and the 64 gathered rows of Vm
-// into shared memory with cp.async while each thread loads the raw logits of its own
-// accumulator elements into registers, multiplies (8 warps x 16 rows x 64 columns),
-// adds, rounds once to bf16 and stores from the registers, and folds the tile's
-// argmax of each request into a 64-bit key per (position, request) with atomicMax:
-// key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v), so the
-// largest value wins and, among equal values, the lowest index; max is order-free,
-// so results do not depend on CTA scheduling. The next position reads y from those
-// keys; a last small launch writes the drafted tokens.
+// One launch per position. For a group of up to 128 requests the correction is the
+// product D = X U^T, X [128, r] the gathered rows Vm[y_b, :] (zero past the batch),
+// U [V, r]: a dense contraction on the fifth-generation tensor cores. A persistent CTA
+// per SM (and request group) gathers X once into shared memory in the canonical
+// K-major 128-byte-swizzled layout, then walks its vocabulary tiles of 64 rows with
+// three roles coupled only by mbarriers (a TMA warp, an MMA warp, four epilogue warps):
+//  - U tiles of 64 rows come by 2-D tensor-map TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle, one box of 64 rows x 64 columns per 64 of r; rows past V and columns past
+//    r are filled with zeros) into a ring of four shared-memory buffers, so three
+//    copies run ahead of the tile being multiplied;
+//  - one thread issues the tile's tcgen05.mma (kind::f16, bf16 inputs, M = 128 requests,
+//    N = 64 vocabulary rows, K = 16 each) into one of two TMEM accumulators of 64 fp32
+//    columns and commits them to an mbarrier;
+//  - while the next tile multiplies, the four warps read the previous accumulator with
+//    tcgen05.ld (thread t holds request t's 64 values), add the raw logits (16-byte
+//    loads of one request's row), round once to bf16, store, and keep the request's
+//    running maximum and its first index.
+// key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v): the largest
+// value wins and, among equal values, the lowest index. Each CTA ends with one
+// atomicMax per request; max is order-free, so results do not depend on scheduling.
+// The next position reads y from those keys; a last small launch writes the tokens.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "sv_common.cuh"
 #include "sv_launch.cuh"
 
 namespace sv {
 
-constexpr int MK_ROWS = 128;   // vocabulary rows per CTA
-constexpr int MK_COLS = 64;    // requests per CTA
-constexpr int MK_WARPS = 8;    // 16 rows each
-constexpr int MK_THREADS = MK_WARPS * 32;
-constexpr int MK_PAD = 8;      // bf16 elements of padding per shared-memory row
+constexpr int MK_M = 128;        // requests per group (UMMA M; rows past the batch are zero)
+constexpr int MK_N = 64;         // vocabulary rows per tile (UMMA N)
+constexpr int MK_KB = 64;        // K elements per 128-byte swizzle block
+constexpr int MK_EPI_WARPS = 4;  // epilogue warps: warp w reads TMEM lanes 32 (w % 4) + 0..31
+constexpr int MK_THREADS = 32 * (2 + MK_EPI_WARPS);  // and a TMA warp and an MMA warp
+constexpr int MK_XBLK = MK_M * 128;      // one block of X: 128 rows x 128 bytes
+constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 64 rows x 128 bytes
+constexpr int MK_RING = 4;               // U tiles in flight
+constexpr uint32_t MK_TMEM_COLS = 2 * MK_N;  // two accumulators
 
 struct MarkovArgs {
   const uint16_t* L;     // [B, K, V] raw logits (bf16 bits)
@@ -62,24 +78,84 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3,
-                                        const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-               : "r"(smem_addr(p)));
+// ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) and tensor-map TMA wrappers.
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor of a K-major operand in the canonical 128-byte
+// swizzled layout: 8-row groups 1024 bytes apart (stride byte offset), rows of 128
+// bytes, the leading byte offset unused; descriptor version 1, swizzle mode 128 B.
+// The buffer must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_desc(const void* smem) {
+  const uint32_t a = smem_addr(smem);
+  return static_cast<uint64_t>((a >> 4) & 0x3fffu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t& b0, uint32_t& b1, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-               : "=r"(b0), "=r"(b1)
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// N = MK_N, M = MK_M.
+constexpr uint32_t MK_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                              (static_cast<uint32_t>(MK_N >> 3) << 17) |
+                              (static_cast<uint32_t>(MK_M >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(MK_IDESC), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Tile (x = column, y = row) of a 2-D tensor map into shared memory, with an L2 cache
+// policy.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Bounded wait for an mbarrier phase; false (and a status report) when it runs out.
+__device__ bool mk_wait(uint64_t* bar, uint32_t parity, const MarkovArgs& A) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (clock64() - t0 > WAIT_CYCLES) {
+      atomicOr(&A.hdr->status, ST_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 // The token drafted at position k-1 of request b (k > 0), or prev[b]; -1 if invalid.
@@ -93,105 +169,215 @@ __device__ __forceinline__ int prev_token(const MarkovArgs& A, int b) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
 }
 
-__global__ void __launch_bounds__(MK_THREADS, 2) sv_markov_step_kernel(const MarkovArgs A) {
-  extern __shared__ __align__(128) unsigned char dsm[];
-  const int r = A.r, rs = r + MK_PAD;  // shared row stride (bf16 elements)
-  uint16_t* Us = reinterpret_cast<uint16_t*>(dsm);                 // [MK_ROWS][rs]
-  uint16_t* Xs = Us + (size_t)MK_ROWS * rs;                         // [MK_COLS][rs]
+// Shared memory of the step kernel: X (nkb blocks of 128 rows x 128 bytes), then the
+// ring of U tiles (nkb blocks of 64 rows x 128 bytes each), 1024-byte aligned; at least
+// 116 KB, so that one CTA is resident per SM.
+size_t markov_smem_bytes(int r) {
+  const int nkb = (r + MK_KB - 1) / MK_KB;
+  const size_t need = 1024 + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK);
+  return need > (size_t)116 * 1024 ? need : (size_t)116 * 1024;
+}
+
+__global__ void __launch_bounds__(MK_THREADS, 1)
+    sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU) {
+  extern __shared__ __align__(1024) unsigned char dsm_raw[];
+  unsigned char* dsm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // ufull: U tile landed; uempty: its product is done (the buffer may be refilled);
+  // afull: accumulator ready; aempty: the epilogue warps have read it.
+  __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[2], aempty[2];
+  __shared__ uint32_t tmem_base;
+  const int r = A.r, V = A.V, B = A.B;
+  const int nkb = (r + MK_KB - 1) / MK_KB;
+  unsigned char* Xs = dsm;
+  auto ubuf = [&](int q) { return dsm + (size_t)nkb * (MK_XBLK + q * MK_UBLK); };
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int v0 = blockIdx.x * MK_ROWS, b0 = blockIdx.y * MK_COLS;
-  const int nrows = min(MK_ROWS, A.V - v0), ncols = min(MK_COLS, A.B - b0);
-  const uint64_t keep = policy_evict_last();
-  const int cpr = r / 8;  // 16-byte chunks per row of U / Vm
+  const int g0 = blockIdx.y * MK_M;                 // first request of the group
+  const int nb = min(MK_M, B - g0);                 // requests in the group
+  const int ntiles = (V + MK_N - 1) / MK_N;
+  const uint32_t tile_bytes = static_cast<uint32_t>(nkb) * MK_UBLK;
+  int nmine = 0;  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
 
-  // Copies: the U tile and the gathered rows of Vm (zero rows past the ends).
-  for (int i = tid; i < MK_ROWS * cpr; i += MK_THREADS) {
-    const int row = i / cpr, c = i - row * cpr;
-    uint16_t* dst = Us + (size_t)row * rs + c * 8;
-    if (row < nrows)
-      cp_async16(dst, A.U + (size_t)(v0 + row) * r + c * 8, keep);
-    else
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-  }
-  for (int i = tid; i < MK_COLS * cpr; i += MK_THREADS) {
-    const int col = i / cpr, c = i - col * cpr;
-    uint16_t* dst = Xs + (size_t)col * rs + c * 8;
-    const int y = (col < ncols) ? prev_token(A, b0 + col) : -1;
-    if (y >= 0)
-      cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
-    else
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-  }
-  // The raw logits of this thread's accumulator elements, straight into registers
-  // (their latency overlaps the copies above and the product below): element (n, e)
-  // is row 16w + g (+8 for e >= 2), column 8n + 2t (+1 for odd e).
-  const int g = lane >> 2, tq = lane & 3;
-  const size_t KV = (size_t)A.K * A.V;
-  uint16_t lraw[8][4];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = 16 * w + g + ((e & 2) ? 8 : 0), col = 8 * n + 2 * tq + (e & 1);
-      lraw[n][e] = (row < nrows && col < ncols)
-                       ? __ldcs(A.L + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + row)
-                       : static_cast<uint16_t>(0);
+  if (tid == 0) {
+    for (int q = 0; q < MK_RING; ++q) {
+      mbar_init(&ufull[q], 1);
+      mbar_init(&uempty[q], 1);
     }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&afull[q], 1);
+      mbar_init(&aempty[q], MK_EPI_WARPS);
+    }
+    fence_mbar_init();
   }
-  cp_async_wait_all();
+  if (w == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(MK_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // X: row m = request g0 + m, the gathered Vm row, zero past the group, past r, or for
+  // an invalid previous token; 16-byte chunks placed in the swizzled layout.
+  {
+    const uint64_t keep = policy_evict_last();
+    const int cpr = nkb * (MK_KB / 8);  // 16-byte chunks per padded row
+    for (int i = tid; i < MK_M * cpr; i += MK_THREADS) {
+      const int m = i / cpr, c = i - m * cpr;
+      const int kb = c >> 3, cc = c & 7;
+      unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
+      const int y = (m < nb && c * 8 < r) ? prev_token(A, g0 + m) : -1;
+      if (y >= 0)
+        cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_wait_all();
+    // The tensor cores read X through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tmem_fence_before();
   __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = tmem_base;
 
-  // Correction tile: warp w takes rows 16w..16w+15 and all 64 columns.
-  float acc[8][4];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  const uint16_t* arow = Us + (size_t)(16 * w + (lane & 15)) * rs + (lane >> 4) * 8;
-  const uint16_t* brow = Xs + (size_t)(lane & 7) * rs + ((lane >> 3) & 1) * 8;
-  for (int k0 = 0; k0 < r; k0 += 16) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(a0, a1, a2, a3, arow + k0);
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      uint32_t b0r, b1r;
-      ldsm_x2(b0r, b1r, brow + (size_t)(8 * n) * rs + k0);
-      mma_bf16(acc[n], a0, a1, a2, a3, b0r, b1r);
-    }
-  }
-
-  // Raw logits + correction, rounded once to bf16, stored from the registers; each
-  // column's best key over the warp's 16 rows, then over the 8 warps in shared memory.
-  __shared__ unsigned long long red[MK_WARPS][MK_COLS];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) {
-    unsigned long long kb[2] = {0ull, 0ull};  // columns 8n + 2t and 8n + 2t + 1
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = 16 * w + g + ((e & 2) ? 8 : 0), col = 8 * n + 2 * tq + (e & 1);
-      const uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf2f(lraw[n][e]), acc[n][e])));
-      if (row < nrows && col < ncols) {
-        __stcs(A.out + (size_t)(b0 + col) * KV + (size_t)A.k * A.V + v0 + row, h);
-        const unsigned long long key = (static_cast<unsigned long long>(bf_order(h)) << 32) |
-                                       static_cast<unsigned long long>(0xffffffffu - (uint32_t)(v0 + row));
-        kb[e & 1] = key > kb[e & 1] ? key : kb[e & 1];
+  if (w == 0) {
+    // TMA producer (lane 0): U tiles into the ring, each once its buffer's previous
+    // product is done. U is read again at every position: keep it in L2.
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      for (int i = 0; i < nmine; ++i) {
+        const int q = i % MK_RING;
+        if (i >= MK_RING && !mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A))
+          break;
+        mbar_arrive_expect_tx(&ufull[q], tile_bytes);
+        const int t = blockIdx.x + i * gridDim.x;
+        for (int kb = 0; kb < nkb; ++kb)
+          tma_load_2d(ubuf(q) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[q], keep);
       }
     }
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      unsigned long long m = kb[c];
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {  // over g: lanes with the same t hold the same column
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, m, o);
-        m = y > m ? y : m;
+  } else if (w == 1) {
+    // MMA issuer (lane 0): tile i's product into accumulator i & 1 once its U tile has
+    // landed and the epilogue warps have read that accumulator's previous tile.
+    if (lane == 0) {
+      const uint64_t ad = sw128_desc(Xs);
+      const int nk = r / 16;
+      for (int i = 0; i < nmine; ++i) {
+        const int q = i % MK_RING, a = i & 1;
+        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / MK_RING) & 1), A)) break;
+        if (i >= 2 && !mk_wait(&aempty[a], static_cast<uint32_t>((i / 2 - 1) & 1), A)) break;
+        tmem_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(a * MK_N);
+        const uint64_t bd = sw128_desc(ubuf(q));
+        for (int kk = 0; kk < nk; ++kk) {
+          // 16 elements = 32 bytes along K inside a 128-byte block; X's blocks are 16 KB
+          // apart, the U tile's 8 KB.
+          const uint64_t sub = static_cast<uint64_t>((kk & 3) * 2);
+          umma_bf16(d, ad + static_cast<uint64_t>((kk >> 2) * (MK_XBLK >> 4)) + sub,
+                    bd + static_cast<uint64_t>((kk >> 2) * (MK_UBLK >> 4)) + sub, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&uempty[q]);  // the U buffer is free when these products are done
+        umma_commit(&afull[a]);   // and the accumulator is ready
       }
-      if (g == 0) red[w][8 * n + 2 * tq + c] = m;
     }
-  }
-  __syncthreads();
-  if (tid < MK_COLS && tid < ncols) {
-    unsigned long long m = 0ull;
+  } else {
+    // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. thread e holds the
+    // 64 values of request g0 + m, m = 32 (w % 4) + lane.
+    const int m = 32 * (w & 3) + lane;
+    const size_t KV = (size_t)A.K * V;
+    const int b = g0 + m;
+    const bool live = m < nb;
+    const uint16_t* Lrow = A.L + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
+    uint16_t* Orow = A.out + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
+    const bool vec = (V & 7) == 0;  // rows 16-byte aligned: vector loads and stores
+    uint32_t best = 0;   // order-preserving code (+1) of the request's largest value so far
+    int best_v = -1;     // its first index (values are visited in increasing v)
+    auto see = [&](uint16_t h, int v) {
+      const uint32_t c = bf_order(h) + 1u;
+      if (c > best) {
+        best = c;
+        best_v = v;
+      }
+    };
+    // Raw logits of tile i (16-byte vectors), loaded one tile ahead of their use.
+    uint4 raw[MK_N / 8], nxt[MK_N / 8];
+    auto load_raw = [&](int i, uint4* dst) {
+      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
+      if (vec && live && i < nmine && v0 + MK_N <= V) {
 #pragma unroll
-    for (int q = 0; q < MK_WARPS; ++q) m = red[q][tid] > m ? red[q][tid] : m;
-    if (m) atomicMax(A.keys + (size_t)A.k * A.B + b0 + tid, m);
+        for (int j = 0; j < MK_N / 8; ++j) dst[j] = __ldcs(reinterpret_cast<const uint4*>(Lrow + v0) + j);
+      }
+    };
+    load_raw(0, nxt);
+    for (int i = 0; i < nmine; ++i) {
+#pragma unroll
+      for (int j = 0; j < MK_N / 8; ++j) raw[j] = nxt[j];
+      load_raw(i + 1, nxt);
+      const int a = i & 1;
+      bool ok = true;
+      if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / 2) & 1), A);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      tmem_fence_after();
+      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
+      const bool full = vec && live && v0 + MK_N <= V;
+      const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
+                            static_cast<uint32_t>(a * MK_N);
+      float acc0[32], acc1[32];
+      tmem_ld32(tcol, acc0);
+      tmem_ld32(tcol + 32, acc1);
+      // The accumulator is in registers: release it to the MMA issuer.
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[a]);
+#pragma unroll
+      for (int q = 0; q < MK_N / 32; ++q) {
+        const float* acc = q ? acc1 : acc0;
+        const int vq = v0 + q * 32;
+        if (full) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 rw = raw[q * 4 + j];
+            const uint32_t wv[4] = {rw.x, rw.y, rw.z, rw.w};
+            uint32_t hp[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = j * 8 + e2 * 2;  // elements e (low half) and e + 1 (high half)
+              const uint16_t lo =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf_lo(wv[e2]), acc[e])));
+              const uint16_t hi =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf_hi(wv[e2]), acc[e + 1])));
+              hp[e2] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+              see(lo, vq + e);
+              see(hi, vq + e + 1);
+            }
+            __stcs(reinterpret_cast<uint4*>(Orow + vq) + j, make_uint4(hp[0], hp[1], hp[2], hp[3]));
+          }
+        } else if (live) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (vq + e >= V) continue;
+            const uint16_t hv = __bfloat16_as_ushort(
+                __float2bfloat16_rn(__fadd_rn(bf2f(__ldcs(Lrow + vq + e)), acc[e])));
+            __stcs(Orow + vq + e, hv);
+            see(hv, vq + e);
+          }
+        }
+      }
+    }
+    if (live && best_v >= 0)
+      atomicMax(A.keys + (size_t)A.k * B + b,
+                (static_cast<unsigned long long>(best - 1u) << 32) |
+                    (0xffffffffull - static_cast<unsigned>(best_v)));
+  }
+
+  tmem_fence_before();
+  __syncthreads();
+  if (w == 0) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(MK_TMEM_COLS)
+                 : "memory");
   }
 }
 
@@ -209,8 +395,21 @@ __global__ void sv_markov_finish_kernel(const MarkovArgs A) {
   }
 }
 
-// The U tile and the gathered Vm rows.
-size_t markov_smem_bytes(int r) { return (size_t)(MK_ROWS + MK_COLS) * (r + MK_PAD) * 2; }
+// The driver's tensor-map encoder, looked up once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
 
 cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* Vm,
                           const int32_t* prev, int B, int K, int V, int r, uint16_t* out,
@@ -223,13 +422,31 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // U as a 2-D tensor [V rows, r columns] of bf16: boxes of 64 rows x 64 columns (128
+  // bytes, 128-byte swizzle), zeros outside the tensor.
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tm;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(r) * 2};
+  const cuuint32_t box[2] = {MK_KB, MK_N};  // 64 columns (128 bytes) x 64 rows
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(U), gdim, gstride, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)K * B, st);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   MarkovArgs A{L, U, Vm, prev, out, keys, tok, hdr, B, K, V, r, 0};
-  const dim3 grid((V + MK_ROWS - 1) / MK_ROWS, (B + MK_COLS - 1) / MK_COLS);
+  const int ntiles = (V + MK_N - 1) / MK_N;
+  const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms),
+                  static_cast<unsigned>((B + MK_M - 1) / MK_M));
   for (int k = 0; k < K; ++k) {
     A.k = k;
-    sv_markov_step_kernel<<<grid, MK_THREADS, markov_smem_bytes(r), st>>>(A);
+    sv_markov_step_kernel<<<grid, MK_THREADS, markov_smem_bytes(r), st>>>(A, tm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   sv_markov_finish_kernel<<<(B + 127) / 128, 128, 0, st>>>(A);
