@@ -12,18 +12,19 @@
 // U [V, r]: a dense contraction on the fifth-generation tensor cores. A persistent CTA
 // per SM (and request group) gathers X once into shared memory in the canonical
 // K-major 128-byte-swizzled layout, then walks its vocabulary tiles of 64 rows with
-// three roles coupled only by mbarriers (a TMA warp, an MMA warp, four epilogue warps):
+// three roles coupled only by mbarriers (a TMA warp, an MMA warp, eight epilogue warps):
 //  - U tiles of 64 rows come by 2-D tensor-map TMA (cp.async.bulk.tensor, 128-byte
 //    swizzle, one box of 64 rows x 64 columns per 64 of r; rows past V and columns past
 //    r are filled with zeros) into a ring of four shared-memory buffers, so three
 //    copies run ahead of the tile being multiplied;
 //  - one thread issues the tile's tcgen05.mma (kind::f16, bf16 inputs, M = 128 requests,
-//    N = 64 vocabulary rows, K = 16 each) into one of two TMEM accumulators of 64 fp32
+//    N = 64 vocabulary rows, K = 16 each) into one of four TMEM accumulators of 64 fp32
 //    columns and commits them to an mbarrier;
-//  - while the next tile multiplies, the four warps read the previous accumulator with
-//    tcgen05.ld (thread t holds request t's 64 values), add the raw logits (16-byte
-//    loads of one request's row), round once to bf16, store, and keep the request's
-//    running maximum and its first index.
+//  - while the next tile multiplies, eight epilogue warps read the previous accumulator
+//    with tcgen05.ld (two warps per group of 32 TMEM lanes, 32 columns each: a thread
+//    holds 32 consecutive values of one request), add the raw logits (16-byte loads of
+//    the request's row, fetched one tile ahead), round once to bf16, store, and keep the
+//    request's running maximum and its first index.
 // key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v): the largest
 // value wins and, among equal values, the lowest index. Each CTA ends with one
 // atomicMax per request; max is order-free, so results do not depend on scheduling.
@@ -42,12 +43,13 @@ namespace sv {
 constexpr int MK_M = 128;        // requests per group (UMMA M; rows past the batch are zero)
 constexpr int MK_N = 64;         // vocabulary rows per tile (UMMA N)
 constexpr int MK_KB = 64;        // K elements per 128-byte swizzle block
-constexpr int MK_EPI_WARPS = 4;  // epilogue warps: warp w reads TMEM lanes 32 (w % 4) + 0..31
+constexpr int MK_EPI_WARPS = 8;  // epilogue warps: two per TMEM lane group, half a tile each
 constexpr int MK_THREADS = 32 * (2 + MK_EPI_WARPS);  // and a TMA warp and an MMA warp
 constexpr int MK_XBLK = MK_M * 128;      // one block of X: 128 rows x 128 bytes
 constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 64 rows x 128 bytes
 constexpr int MK_RING = 4;               // U tiles in flight
-constexpr uint32_t MK_TMEM_COLS = 2 * MK_N;  // two accumulators
+constexpr int MK_ACC = 4;                    // accumulator stages in TMEM
+constexpr uint32_t MK_TMEM_COLS = MK_ACC * MK_N;
 
 struct MarkovArgs {
   const uint16_t* L;     // [B, K, V] raw logits (bf16 bits)
@@ -146,10 +148,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Probe of an mbarrier phase that may suspend the thread for up to `ns` nanoseconds
+// (or until the phase completes), so waiting lanes do not spin through issue slots.
+__device__ __forceinline__ bool mbar_try_ns(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for an mbarrier phase; false (and a status report) when it runs out.
 __device__ bool mk_wait(uint64_t* bar, uint32_t parity, const MarkovArgs& A) {
   const long long t0 = clock64();
-  while (!mbar_try(bar, parity)) {
+  while (!mbar_try_ns(bar, parity, 2000u)) {
     if (clock64() - t0 > WAIT_CYCLES) {
       atomicOr(&A.hdr->status, ST_TIMEOUT);
       return false;
@@ -185,7 +201,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // ufull: U tile landed; uempty: its product is done (the buffer may be refilled);
   // afull: accumulator ready; aempty: the epilogue warps have read it.
-  __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[2], aempty[2];
+  __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[MK_ACC], aempty[MK_ACC];
   __shared__ uint32_t tmem_base;
   const int r = A.r, V = A.V, B = A.B;
   const int nkb = (r + MK_KB - 1) / MK_KB;
@@ -204,7 +220,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       mbar_init(&ufull[q], 1);
       mbar_init(&uempty[q], 1);
     }
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < MK_ACC; ++q) {
       mbar_init(&afull[q], 1);
       mbar_init(&aempty[q], MK_EPI_WARPS);
     }
@@ -258,15 +274,16 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       }
     }
   } else if (w == 1) {
-    // MMA issuer (lane 0): tile i's product into accumulator i & 1 once its U tile has
-    // landed and the epilogue warps have read that accumulator's previous tile.
+    // MMA issuer (lane 0): tile i's product into accumulator i % MK_ACC once its U tile
+    // has landed and the epilogue warps have read that accumulator's previous tile.
     if (lane == 0) {
       const uint64_t ad = sw128_desc(Xs);
       const int nk = r / 16;
       for (int i = 0; i < nmine; ++i) {
-        const int q = i % MK_RING, a = i & 1;
+        const int q = i % MK_RING, a = i % MK_ACC;
         if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / MK_RING) & 1), A)) break;
-        if (i >= 2 && !mk_wait(&aempty[a], static_cast<uint32_t>((i / 2 - 1) & 1), A)) break;
+        if (i >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>((i / MK_ACC - 1) & 1), A))
+          break;
         tmem_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(a * MK_N);
         const uint64_t bd = sw128_desc(ubuf(q));
@@ -282,9 +299,11 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       }
     }
   } else {
-    // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. thread e holds the
-    // 64 values of request g0 + m, m = 32 (w % 4) + lane.
+    // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. request g0 + m,
+    // m = 32 (w % 4) + lane, and columns 32 h .. 32 h + 31 of each tile (h: which of the
+    // two warps of its lane group).
     const int m = 32 * (w & 3) + lane;
+    const int h = (w - 2) >> 2;
     const size_t KV = (size_t)A.K * V;
     const int b = g0 + m;
     const bool live = m < nb;
@@ -300,44 +319,41 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         best_v = v;
       }
     };
-    // Raw logits of tile i (16-byte vectors), loaded one tile ahead of their use.
-    uint4 raw[MK_N / 8], nxt[MK_N / 8];
+    // Raw logits of this warp's 32 columns of tile i (16-byte vectors), loaded one tile
+    // ahead of their use.
+    uint4 raw[4], nxt[4];
     auto load_raw = [&](int i, uint4* dst) {
-      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
-      if (vec && live && i < nmine && v0 + MK_N <= V) {
+      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
+      if (vec && live && i < nmine && v0 + 32 <= V) {
 #pragma unroll
-        for (int j = 0; j < MK_N / 8; ++j) dst[j] = __ldcs(reinterpret_cast<const uint4*>(Lrow + v0) + j);
+        for (int j = 0; j < 4; ++j) dst[j] = __ldcs(reinterpret_cast<const uint4*>(Lrow + v0) + j);
       }
     };
     load_raw(0, nxt);
     for (int i = 0; i < nmine; ++i) {
 #pragma unroll
-      for (int j = 0; j < MK_N / 8; ++j) raw[j] = nxt[j];
+      for (int j = 0; j < 4; ++j) raw[j] = nxt[j];
       load_raw(i + 1, nxt);
-      const int a = i & 1;
+      const int a = i % MK_ACC;
       bool ok = true;
-      if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / 2) & 1), A);
+      if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / MK_ACC) & 1), A);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       tmem_fence_after();
-      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
-      const bool full = vec && live && v0 + MK_N <= V;
+      const int vq = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
+      const bool full = vec && live && vq + 32 <= V;
       const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
-                            static_cast<uint32_t>(a * MK_N);
-      float acc0[32], acc1[32];
-      tmem_ld32(tcol, acc0);
-      tmem_ld32(tcol + 32, acc1);
+                            static_cast<uint32_t>(a * MK_N + 32 * h);
+      float acc[32];
+      tmem_ld32(tcol, acc);
       // The accumulator is in registers: release it to the MMA issuer.
       tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aempty[a]);
-#pragma unroll
-      for (int q = 0; q < MK_N / 32; ++q) {
-        const float* acc = q ? acc1 : acc0;
-        const int vq = v0 + q * 32;
+      {
         if (full) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint4 rw = raw[q * 4 + j];
+            const uint4 rw = raw[j];
             const uint32_t wv[4] = {rw.x, rw.y, rw.z, rw.w};
             uint32_t hp[4];
 #pragma unroll
