@@ -241,26 +241,34 @@ __device__ __forceinline__ void soft_round(Soft& s, const uint4* v, float a, boo
   s.S = ff_norm(r.hi, __fadd_rn(r.lo, s.S.lo));
 }
 
-// Merge of two statistics; symmetric bit for bit.
-__device__ __forceinline__ Soft soft_merge(const Soft& x, const Soft& y, float a) {
-  if (y.m == -INFINITY) return x;
-  if (x.m == -INFINITY) return y;
-  const float mn = fmaxf(x.m, y.m);
-  const float Fn = __fmul_rn(mn, a);
-  const float fx = (x.m == mn) ? 1.f : ex2(__fsub_rn(x.F, Fn));
-  const float fy = (y.m == mn) ? 1.f : ex2(__fsub_rn(y.F, Fn));
-  return Soft{mn, Fn, ff_add(ff_mul_f(x.S, fx), ff_mul_f(y.S, fy))};
-}
-
-__device__ __forceinline__ Soft soft_shfl_xor(const Soft& s, int o) {
-  return Soft{__shfl_xor_sync(FULLM, s.m, o), __shfl_xor_sync(FULLM, s.F, o),
-              ff_shfl_xor(s.S, o)};
-}
-
-__device__ __forceinline__ Soft soft_warp(Soft s, float a) {
+// Warp merge in one frame: the warp's maximum first, then each lane's sum rescaled once
+// into it and the sums added by a butterfly (every lane ends with the same bits). Lanes
+// whose statistics hold nothing (m = -inf) add nothing.
+__device__ __forceinline__ Soft soft_warp1(const Soft& s, float a) {
+  float m = s.m;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) s = soft_merge(s, soft_shfl_xor(s, o), a);
-  return s;
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULLM, m, o));
+  if (!(m > -INFINITY)) return soft_empty();
+  const float F = __fmul_rn(m, a);
+  const ff S = s.m > -INFINITY ? ff_mul_f(s.S, ex2(__fsub_rn(s.F, F))) : ff{0.f, 0.f};
+  return Soft{m, F, ff_warp_sum(S)};
+}
+
+// The same over PER statistics per lane (added in index order, then the butterfly).
+template <int PER>
+__device__ __forceinline__ Soft soft_frame_merge(const Soft* s, float a) {
+  float m = s[0].m;
+#pragma unroll
+  for (int i = 1; i < PER; ++i) m = fmaxf(m, s[i].m);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULLM, m, o));
+  if (!(m > -INFINITY)) return soft_empty();
+  const float F = __fmul_rn(m, a);
+  ff S{0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (s[i].m > -INFINITY) S = ff_add(S, ff_mul_f(s[i].S, ex2(__fsub_rn(s[i].F, F))));
+  return Soft{m, F, ff_warp_sum(S)};
 }
 
 // Argmax with ties to the lowest index.

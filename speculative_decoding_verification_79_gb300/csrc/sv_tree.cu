@@ -23,9 +23,11 @@
 // tiles, each warp a contiguous sub-range (lanes read consecutive vectors: coalesced).
 // Per visited node the cluster makes one pass for the softmax statistics of both rows
 // (argmax of the target row at T == 0), one pass per rejection for W, and samples from
-// the last pass's totals in three levels (CTA, warp group of tiles, element). Partial
-// results meet in distributed shared memory behind hardware cluster barriers; every CTA
-// merges the C partials in rank order, so all CTAs reach bit-identical values, take the
+// the last pass's totals in three levels (CTA, warp group of tiles, element). Every
+// warp leaves its partial result in shared memory; after one hardware cluster barrier
+// warp 0 of every CTA reads all C x 16 partials over distributed shared memory and
+// merges them in a fixed order (softmax statistics in one frame: the maximum first,
+// then each partial rescaled once), so all CTAs reach bit-identical values, take the
 // same branches and arrive at the same barriers. Only rows the walk reaches are read.
 #include <cfloat>
 #include <atomic>
@@ -51,12 +53,22 @@ constexpr int MAXC = 8;         // largest cluster
 // ---------------------------------------------------------------------------
 // Shared state of one CTA.
 // ---------------------------------------------------------------------------
-struct Xch {  // one CTA's partial result, read by the cluster
+struct Xch {  // a partial or merged result
   Soft st, sd;
   float best;
   int idx;
   int bad;
   ff tot;
+};
+
+struct __align__(16) Xw {  // one warp's partial result, read by every CTA of the cluster
+  Soft st, sd;
+  float best;
+  int idx;
+  int bad;
+  int pad;
+  ff tot;
+  ff pad2;
 };
 
 struct Smem {
@@ -69,15 +81,11 @@ struct Smem {
   int dec;
   int sel_w, sel_g;
   ff sel_cum;
-  Soft wst[TW], wsd[TW];
-  float wbest[TW];
-  int widx[TW];
-  int wbad[TW];
-  ff wtot[TW];
   ff gtot[TW][NGRP];
   ff ctot[MAXC];
-  Xch xch[2];
+  Xw xw[2][TW];  // per-warp partials, alternating between passes
   Xch res;
+  int lastbuf;   // the xw buffer of the last pass
 };
 
 // Tiles [t0, t1) of warp w in CTA `rank` of C, for a row of `ntiles` tiles.
@@ -124,15 +132,20 @@ __device__ __forceinline__ bool interior_round(const Geo& g, int tb, bool d_off_
   return !d_off_grid && tb + UNR <= g.t1 && tb * 32 >= jlo && (tb + UNR) * 32 <= jhi;
 }
 
-// Publishes this CTA's partial (already in sm.xch[buf] by thread 0), waits for the
-// cluster, and merges the C partials in rank order into sm.res (thread 0).
+// Waits for every warp of the cluster to have stored its partial in sm.xw[buf], then
+// warp 0 of each CTA merges the C x TW partials (over distributed shared memory) in a
+// fixed order into sm.res, so all CTAs reach bit-identical values: the statistics in
+// one frame (the maximum first, then each partial rescaled once into it), the argmax,
+// or the weight totals per CTA (warps in order; into sm.ctot) and over the cluster
+// (CTAs in rank order).
 template <int KIND>
 __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C, int buf,
                                          float a) {
-  cl.sync();
+  cl.sync();  // also a CTA barrier
   if (threadIdx.x < 32) {
-    // Lane k < C reads CTA k's partial; the merge is the same fixed tree in every CTA.
     const int lane = threadIdx.x;
+    const int n = C * TW;
+    constexpr int PER = MAXC * TW / 32;  // entries per lane at most
     Xch r;
     r.st = soft_empty();
     r.sd = soft_empty();
@@ -140,24 +153,35 @@ __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C,
     r.idx = INT_MAX;
     r.bad = 0;
     r.tot = ff{0.f, 0.f};
-    if (lane < C) {
-      const Xch* x = cl.map_shared_rank(&sm.xch[buf], lane);
-      r.bad = x->bad;
-      if (KIND == 0) {
-        r.st = x->st;
-        r.sd = x->sd;
-      } else if (KIND == 1) {
-        r.best = x->best;
-        r.idx = x->idx;
-      } else {
-        r.tot = x->tot;
-      }
-    }
-    r.bad = __any_sync(FULLM, r.bad);
     if (KIND == 0) {
-      r.st = soft_warp(r.st, a);
-      r.sd = soft_warp(r.sd, a);
+      Soft et[PER], ed[PER];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        et[i] = ed[i] = soft_empty();
+        if (e < n) {
+          const Xw* x = cl.map_shared_rank(&sm.xw[buf][e % TW], e / TW);
+          et[i] = x->st;
+          ed[i] = x->sd;
+          bad |= x->bad != 0;
+        }
+      }
+      r.bad = __any_sync(FULLM, bad);
+      r.st = soft_frame_merge<PER>(et, a);
+      r.sd = soft_frame_merge<PER>(ed, a);
     } else if (KIND == 1) {
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < n) {
+          const Xw* x = cl.map_shared_rank(&sm.xw[buf][e % TW], e / TW);
+          arg_merge(r.best, r.idx, x->best, x->idx);
+          bad |= x->bad != 0;
+        }
+      }
+      r.bad = __any_sync(FULLM, bad);
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
         const float b2 = __shfl_xor_sync(FULLM, r.best, o);
@@ -165,16 +189,25 @@ __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C,
         arg_merge(r.best, r.idx, b2, i2);
       }
     } else {
-      // Totals add up in rank order, the order the sample's search walks them.
+      // Lane k < C adds CTA k's warp totals in warp order (loads all in flight).
       ff t{0.f, 0.f};
-      for (int k = 0; k < C; ++k) {
-        const ff tk{__shfl_sync(FULLM, r.tot.hi, k), __shfl_sync(FULLM, r.tot.lo, k)};
-        if (lane == 0) sm.ctot[k] = tk;
-        t = ff_add(t, tk);
+      if (lane < C) {
+        ff v[TW];
+#pragma unroll
+        for (int w = 0; w < TW; ++w) v[w] = cl.map_shared_rank(&sm.xw[buf][w], lane)->tot;
+#pragma unroll
+        for (int w = 0; w < TW; ++w) t = ff_add(t, v[w]);
+        sm.ctot[lane] = t;
       }
-      r.tot = t;
+      // Totals add up in rank order, the order the sample's search walks them.
+      ff c{0.f, 0.f};
+      for (int k = 0; k < C; ++k) c = ff_add(c, ff{__shfl_sync(FULLM, t.hi, k), __shfl_sync(FULLM, t.lo, k)});
+      r.tot = c;
     }
-    if (lane == 0) sm.res = r;
+    if (lane == 0) {
+      sm.res = r;
+      sm.lastbuf = buf;
+    }
   }
   __syncthreads();
 }
@@ -208,27 +241,14 @@ __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, con
     soft_round<T, UNR>(st, vt, a, bad);
     if (use_d) soft_round<T, UNR>(sd, vd, a, bad);
   }
-  st = soft_warp(st, a);
-  if (use_d) sd = soft_warp(sd, a);
+  st = soft_warp1(st, a);
+  sd = use_d ? soft_warp1(sd, a) : soft_empty();
   const bool wb = __any_sync(FULLM, bad);
   if (lane == 0) {
-    sm.wst[w] = st;
-    sm.wsd[w] = sd;
-    sm.wbad[w] = wb;
-  }
-  __syncthreads();
-  if (w == 0) {
-    Soft xs = lane < TW ? sm.wst[lane] : soft_empty();
-    Soft xd = (use_d && lane < TW) ? sm.wsd[lane] : soft_empty();
-    const bool xb = __any_sync(FULLM, lane < TW && sm.wbad[lane]);
-    xs = soft_warp(xs, a);
-    if (use_d) xd = soft_warp(xd, a);
-    if (lane == 0) {
-      Xch& x = sm.xch[buf];
-      x.st = xs;
-      x.sd = xd;
-      x.bad = xb;
-    }
+    Xw& x = sm.xw[buf][w];
+    x.st = st;
+    x.sd = sd;
+    x.bad = wb;
   }
   exchange<0>(sm, cl, C, buf, a);
   buf ^= 1;
@@ -282,27 +302,10 @@ __device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, co
   }
   const bool wb = __any_sync(FULLM, bad);
   if (lane == 0) {
-    sm.wbest[w] = best;
-    sm.widx[w] = idx;
-    sm.wbad[w] = wb;
-  }
-  __syncthreads();
-  if (w == 0) {
-    float xb = lane < TW ? sm.wbest[lane] : -INFINITY;
-    int xi = lane < TW ? sm.widx[lane] : INT_MAX;
-    const bool bd = __any_sync(FULLM, lane < TW && sm.wbad[lane]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float b2 = __shfl_xor_sync(FULLM, xb, o);
-      const int i2 = __shfl_xor_sync(FULLM, xi, o);
-      arg_merge(xb, xi, b2, i2);
-    }
-    if (lane == 0) {
-      Xch& x = sm.xch[buf];
-      x.best = xb;
-      x.idx = xi;
-      x.bad = bd;
-    }
+    Xw& x = sm.xw[buf][w];
+    x.best = best;
+    x.idx = idx;
+    x.bad = wb;
   }
   exchange<1>(sm, cl, C, buf, 0.f);
   buf ^= 1;
@@ -356,13 +359,9 @@ __device__ void wsum_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, cons
       }
     }
   }
-  if (lane == 0) sm.wtot[w] = wt;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ff t{0.f, 0.f};
-    for (int k = 0; k < TW; ++k) t = ff_add(t, sm.wtot[k]);
-    sm.xch[buf].tot = t;
-    sm.xch[buf].bad = 0;
+  if (lane == 0) {
+    sm.xw[buf][w].tot = wt;
+    sm.xw[buf][w].bad = 0;
   }
   exchange<2>(sm, cl, C, buf, 0.f);
   buf ^= 1;
@@ -382,7 +381,9 @@ __device__ int locate(Smem& sm, int C, int rank, const Geo& g, const T* tr, cons
   if (cs < 0) cs = 0;  // no mass at all cannot happen (the largest p weight is ~1)
   if (cs != rank) return -1;
   if (threadIdx.x == 0) {
-    int ws = select_item(sm.wtot, TW, target, cum);
+    ff wtot[TW];
+    for (int k = 0; k < TW; ++k) wtot[k] = sm.xw[sm.lastbuf][k].tot;
+    int ws = select_item(wtot, TW, target, cum);
     if (ws < 0) ws = 0;
     int t0, t1;
     warp_tiles(g.ntiles, C, rank, ws, t0, t1);
