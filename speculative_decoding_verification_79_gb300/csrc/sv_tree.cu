@@ -84,6 +84,8 @@ struct Smem {
   ff gtot[TW][NGRP];
   ff ctot[MAXC];
   Xw xw[2][TW];  // per-warp partials, alternating between passes
+  Soft sst[TW];  // per-warp statistics of the target row from the node's statistics pass
+  ff pw[TW];     // per-warp totals of p (sample without a weight pass)
   Xch res;
   int lastbuf;   // the xw buffer of the last pass
 };
@@ -249,6 +251,7 @@ __device__ void stats_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, con
     x.st = st;
     x.sd = sd;
     x.bad = wb;
+    sm.sst[w] = st;
   }
   exchange<0>(sm, cl, C, buf, a);
   buf ^= 1;
@@ -367,40 +370,109 @@ __device__ void wsum_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, cons
   buf ^= 1;
 }
 
-// Inverse CDF over the weights of the last wsum_pass at target = u * total: CTA, then
-// warp and group (thread 0 of that CTA), then element (that warp). Returns the element
-// in the lane that found it and -1 elsewhere; only the owning CTA finds one.
+// Inverse CDF at target = u * total: CTA, then warp and group of tiles, then element
+// (one warp). Weights of the last wsum_pass (from_s false: totals kept by that pass), or
+// p itself (from_s: CTA and warp totals rescaled from the statistics pass's per-warp
+// partials, group totals of the chosen warp's tiles summed by all warps of the CTA, so
+// no pass over the whole row). Returns the element in lane 0 of the warp that found it
+// and -1 elsewhere; only the owning CTA finds one.
 template <typename T>
-__device__ int locate(Smem& sm, int C, int rank, const Geo& g, const T* tr, const T* dr,
-                      bool dfast, const WPar& P, float u) {
+__device__ int locate(Smem& sm, cg::cluster_group& cl, int C, int rank, const Geo& g,
+                      const T* tr, const T* dr, bool dfast, const WPar& P, float u,
+                      bool from_s) {
   constexpr int VEC = EV<T>::VEC;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (from_s) {
+    if (threadIdx.x < 32) {
+      // Lane k < C: CTA k's warp totals of p (loads in flight), in warp order.
+      ff t{0.f, 0.f};
+      if (lane < C) {
+        Soft v[TW];
+#pragma unroll
+        for (int k = 0; k < TW; ++k) v[k] = *cl.map_shared_rank(&sm.sst[k], lane);
+#pragma unroll
+        for (int k = 0; k < TW; ++k) {
+          const ff pk = v[k].m > -INFINITY
+                            ? ff_mul_f(ff_mul_f(v[k].S, ex2(__fsub_rn(v[k].F, P.Ft))), P.iSt)
+                            : ff{0.f, 0.f};
+          t = ff_add(t, pk);
+          if (lane == rank) sm.pw[k] = pk;
+        }
+        sm.ctot[lane] = t;
+      }
+      ff c{0.f, 0.f};
+      for (int k = 0; k < C; ++k) c = ff_add(c, ff{__shfl_sync(FULLM, t.hi, k), __shfl_sync(FULLM, t.lo, k)});
+      if (lane == 0) sm.res.tot = c;
+    }
+    __syncthreads();
+  }
   const ff target = ff_mul_f(sm.res.tot, u);
   ff cum{0.f, 0.f};
   int cs = select_item(sm.ctot, C, target, cum);
   if (cs < 0) cs = 0;  // no mass at all cannot happen (the largest p weight is ~1)
   if (cs != rank) return -1;
-  if (threadIdx.x == 0) {
-    ff wtot[TW];
-    for (int k = 0; k < TW; ++k) wtot[k] = sm.xw[sm.lastbuf][k].tot;
-    int ws = select_item(wtot, TW, target, cum);
-    if (ws < 0) ws = 0;
+  int ga, gb, scan_w;
+  if (!from_s) {
+    if (threadIdx.x == 0) {
+      ff wtot[TW];
+      for (int k = 0; k < TW; ++k) wtot[k] = sm.xw[sm.lastbuf][k].tot;
+      int ws = select_item(wtot, TW, target, cum);
+      if (ws < 0) ws = 0;
+      int t0, t1;
+      warp_tiles(g.ntiles, C, rank, ws, t0, t1);
+      const int nt = t1 - t0;
+      const int gsz = group_size(nt);
+      int gs = select_item(sm.gtot[ws], (nt + gsz - 1) / gsz, target, cum);
+      if (gs < 0) gs = 0;
+      sm.sel_w = ws;
+      sm.sel_g = gs;
+      sm.sel_cum = cum;
+    }
+    __syncthreads();
+    scan_w = sm.sel_w;
     int t0, t1;
-    warp_tiles(g.ntiles, C, rank, ws, t0, t1);
+    warp_tiles(g.ntiles, C, rank, scan_w, t0, t1);
+    const int gsz = group_size(t1 - t0);
+    ga = t0 + sm.sel_g * gsz;
+    gb = min(t1, ga + gsz);
+  } else {
+    if (threadIdx.x == 0) {
+      int ws = select_item(sm.pw, TW, target, cum);
+      if (ws < 0) ws = 0;
+      sm.sel_w = ws;
+      sm.sel_cum = cum;
+    }
+    __syncthreads();
+    int t0, t1;
+    warp_tiles(g.ntiles, C, rank, sm.sel_w, t0, t1);
     const int nt = t1 - t0;
-    const int gsz = group_size(nt);
-    int gs = select_item(sm.gtot[ws], (nt + gsz - 1) / gsz, target, cum);
-    if (gs < 0) gs = 0;
-    sm.sel_w = ws;
-    sm.sel_g = gs;
-    sm.sel_cum = cum;
+    const int gsz = max(1, (nt + NGRP - 1) / NGRP);
+    const int ngrp = (nt + gsz - 1) / gsz;
+    for (int grp = w; grp < ngrp; grp += TW) {  // group totals of p, dealt over the warps
+      float ls = 0.f, lc = 0.f;
+      const int te = min(t1, t0 + (grp + 1) * gsz);
+      for (int t = t0 + grp * gsz; t < te; ++t) {
+        const uint4 vt = fetch<T>(tr, true, g.V, g.off, t * 32 + lane);
+        float wv[VEC];
+        acc2(ls, lc, vec_weights<T>(P, vt, vt, wv));
+      }
+      const ff gt = ff_warp_sum(ff_two_sum(ls, lc));
+      if (lane == 0) sm.gtot[0][grp] = gt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      cum = sm.sel_cum;
+      int gs = select_item(sm.gtot[0], ngrp, target, cum);
+      if (gs < 0) gs = 0;
+      sm.sel_g = gs;
+      sm.sel_cum = cum;
+    }
+    __syncthreads();
+    scan_w = 0;
+    ga = t0 + sm.sel_g * gsz;
+    gb = min(t1, ga + gsz);
   }
-  __syncthreads();
-  if (w != sm.sel_w) return -1;
-  int t0, t1;
-  warp_tiles(g.ntiles, C, rank, w, t0, t1);
-  const int gsz = group_size(t1 - t0);
-  const int ga = t0 + sm.sel_g * gsz, gb = min(t1, ga + gsz);
+  if (w != scan_w) return -1;
   cum = sm.sel_cum;
   int found = -1, last_pos = -1;
   for (int t = ga; t < gb; ++t) {
@@ -440,6 +512,7 @@ __device__ int locate(Smem& sm, int C, int rank, const Geo& g, const T* tr, cons
     cum = ff_add(cum, ff{__shfl_sync(FULLM, incl.hi, 31), __shfl_sync(FULLM, incl.lo, 31)});
   }
   if (found < 0) found = last_pos;
+  if (found < 0) found = max(0, ga * 32 * VEC - g.off);  // a group whose weights all rounded to 0
   return lane == 0 ? found : -1;
 }
 
@@ -583,12 +656,10 @@ __global__ void __launch_bounds__(TT, 1) tree_kernel(const TreeArgs A) {
       c = next;
       continue;
     }
-    // Terminal sample: the residual after the last rejection, or p (leaf, or restart).
-    if (!totals) {
-      P = WPar{A.a, st.F, iSt, sd.F, 0.f, false};
-      wsum_pass<T>(sm, cl, C, buf, g, tr, dr, dfast, P);
-    }
-    const int y = locate<T>(sm, C, rank, g, tr, dr, dfast, P, sm.u[0]);
+    // Terminal sample: the residual after the last rejection (its totals kept by that
+    // pass), or p (leaf, or restart) from the statistics pass's partials.
+    if (!totals) P = WPar{A.a, st.F, iSt, sd.F, 0.f, false};
+    const int y = locate<T>(sm, cl, C, rank, g, tr, dr, dfast, P, sm.u[0], !totals);
     if (y >= 0) otok[depth] = y;
     break;
   }
