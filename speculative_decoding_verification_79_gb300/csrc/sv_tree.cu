@@ -47,6 +47,7 @@ constexpr int TW = 16;          // warps per CTA
 constexpr int TT = 32 * TW;     // threads per CTA
 constexpr int UNR = 4;          // tiles a lane has in flight per row (two-row passes)
 constexpr int UNR_G = 8;        // the same for the one-row greedy pass
+static_assert(32 % TW == 0, "a CTA's warp partials fill whole halves of a warp");
 constexpr int NGRP = 32;        // group totals kept per warp for the inverse CDF
 constexpr int MAXC = 8;         // largest cluster
 
@@ -191,19 +192,26 @@ __device__ __forceinline__ void exchange(Smem& sm, cg::cluster_group& cl, int C,
         arg_merge(r.best, r.idx, b2, i2);
       }
     } else {
-      // Lane k < C adds CTA k's warp totals in warp order (loads all in flight).
-      ff t{0.f, 0.f};
-      if (lane < C) {
-        ff v[TW];
+      // Entry e = lane + 32 i is warp e % TW of CTA e / TW (all loads in flight); a
+      // fixed butterfly over each TW-lane half adds a CTA's warps, and the cluster's
+      // total adds the CTAs in rank order, the order the sample's search walks them.
+      ff v[PER];
 #pragma unroll
-        for (int w = 0; w < TW; ++w) v[w] = cl.map_shared_rank(&sm.xw[buf][w], lane)->tot;
-#pragma unroll
-        for (int w = 0; w < TW; ++w) t = ff_add(t, v[w]);
-        sm.ctot[lane] = t;
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < n ? cl.map_shared_rank(&sm.xw[buf][e % TW], e / TW)->tot : ff{0.f, 0.f};
       }
-      // Totals add up in rank order, the order the sample's search walks them.
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        ff t = v[i];
+#pragma unroll
+        for (int o = TW / 2; o; o >>= 1) t = ff_add(t, ff_shfl_xor(t, o));
+        const int k = (lane + 32 * i) / TW;
+        if (lane % TW == 0 && k < C) sm.ctot[k] = t;
+      }
+      __syncwarp();
       ff c{0.f, 0.f};
-      for (int k = 0; k < C; ++k) c = ff_add(c, ff{__shfl_sync(FULLM, t.hi, k), __shfl_sync(FULLM, t.lo, k)});
+      for (int k = 0; k < C; ++k) c = ff_add(c, sm.ctot[k]);
       r.tot = c;
     }
     if (lane == 0) {
@@ -384,24 +392,31 @@ __device__ int locate(Smem& sm, cg::cluster_group& cl, int C, int rank, const Ge
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (from_s) {
     if (threadIdx.x < 32) {
-      // Lane k < C: CTA k's warp totals of p (loads in flight), in warp order.
-      ff t{0.f, 0.f};
-      if (lane < C) {
-        Soft v[TW];
+      // Entry e = lane + 32 i is warp e % TW of CTA e / TW: its statistics rescaled to
+      // p's frame (all loads in flight); a fixed butterfly over each TW-lane half adds a
+      // CTA's warps; the cluster's total adds the CTAs in rank order.
+      const int n = C * TW;
+      constexpr int PER = MAXC * TW / 32;
+      Soft v[PER];
 #pragma unroll
-        for (int k = 0; k < TW; ++k) v[k] = *cl.map_shared_rank(&sm.sst[k], lane);
-#pragma unroll
-        for (int k = 0; k < TW; ++k) {
-          const ff pk = v[k].m > -INFINITY
-                            ? ff_mul_f(ff_mul_f(v[k].S, ex2(__fsub_rn(v[k].F, P.Ft))), P.iSt)
-                            : ff{0.f, 0.f};
-          t = ff_add(t, pk);
-          if (lane == rank) sm.pw[k] = pk;
-        }
-        sm.ctot[lane] = t;
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < n ? *cl.map_shared_rank(&sm.sst[e % TW], e / TW) : soft_empty();
       }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i, k = e / TW;
+        ff t = v[i].m > -INFINITY
+                   ? ff_mul_f(ff_mul_f(v[i].S, ex2(__fsub_rn(v[i].F, P.Ft))), P.iSt)
+                   : ff{0.f, 0.f};
+        if (k == rank && e < n) sm.pw[e % TW] = t;
+#pragma unroll
+        for (int o = TW / 2; o; o >>= 1) t = ff_add(t, ff_shfl_xor(t, o));
+        if (lane % TW == 0 && k < C) sm.ctot[k] = t;
+      }
+      __syncwarp();
       ff c{0.f, 0.f};
-      for (int k = 0; k < C; ++k) c = ff_add(c, ff{__shfl_sync(FULLM, t.hi, k), __shfl_sync(FULLM, t.lo, k)});
+      for (int k = 0; k < C; ++k) c = ff_add(c, sm.ctot[k]);
       if (lane == 0) sm.res.tot = c;
     }
     __syncthreads();
