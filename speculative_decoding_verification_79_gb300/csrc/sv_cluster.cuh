@@ -201,6 +201,24 @@ __device__ __forceinline__ float vmax(const uint4 v) {
   }
 }
 
+// Maximum of n vectors; NaN if any element is NaN. bf16 vectors are combined as packed
+// pairs and unpacked once.
+template <typename T, int n>
+__device__ __forceinline__ float vmax_n(const uint4* v) {
+  if constexpr (EV<T>::VEC == 8) {
+    uint32_t m = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
+#pragma unroll
+    for (int k = 1; k < n; ++k)
+      m = bmax2_nan(m, bmax2_nan(bmax2_nan(v[k].x, v[k].y), bmax2_nan(v[k].z, v[k].w)));
+    return fmax_nan(bf_lo(m), bf_hi(m));
+  } else {
+    float m = vmax<T>(v[0]);
+#pragma unroll
+    for (int k = 1; k < n; ++k) m = fmax_nan(m, vmax<T>(v[k]));
+    return m;
+  }
+}
+
 // Sum of 2^(z*a - F) over a vector (nF = -F): each element's unnormalised weight in
 // frame F (0 for -inf). The rounding of a = log2(e)/T moves every exponent by
 // (z - M)*a_lo plus a constant that the normalisation cancels: below 1e-6 relative for
@@ -222,9 +240,7 @@ __device__ __forceinline__ float vexpsum(const uint4 v, float a, float nF) {
 // the exponentials. `bad` collects NaN and +inf.
 template <typename T, int UNR>
 __device__ __forceinline__ void soft_round(Soft& s, const uint4* v, float a, bool& bad) {
-  float vm = vmax<T>(v[0]);
-#pragma unroll
-  for (int k = 1; k < UNR; ++k) vm = fmax_nan(vm, vmax<T>(v[k]));
+  const float vm = vmax_n<T, UNR>(v);
   bad |= (vm != vm) || (vm == INFINITY);
   if (vm > s.m) {
     const float Fn = __fmul_rn(vm, a);

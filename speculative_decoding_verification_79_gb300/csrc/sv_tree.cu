@@ -287,9 +287,7 @@ __device__ void argmax_pass(Smem& sm, cg::cluster_group& cl, int C, int& buf, co
         vt[k] = tb + k < g.t1 ? fetch<T>(tr, true, g.V, g.off, (tb + k) * 32 + lane)
                               : neg_inf_vec<T>();
     }
-    float vm = vmax<T>(vt[0]);
-#pragma unroll
-    for (int k = 1; k < UNR_G; ++k) vm = fmax_nan(vm, vmax<T>(vt[k]));
+    const float vm = vmax_n<T, UNR_G>(vt);
     bad |= (vm != vm) || (vm == INFINITY);
     if (vm > best) {  // rare: find the round's first element equal to its maximum
       best = vm;
