@@ -24,7 +24,9 @@
 //    with tcgen05.ld (two warps per group of 32 TMEM lanes, 32 columns each: a thread
 //    holds 32 consecutive values of one request), add the raw logits (16-byte loads of
 //    the request's row, fetched one tile ahead), round once to bf16, store, and keep the
-//    request's running maximum and its first index.
+//    request's running maximum and its first index. A group of at most 64 requests
+//    fills X twice (rows 64..127 repeat rows 0..63), so that all four lane groups hold
+//    its products and the warps of lane groups 0-1 and 2-3 take alternate tiles.
 // key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v): the largest
 // value wins and, among equal values, the lowest index. Each CTA ends with one
 // atomicMax per request; max is order-free, so results do not depend on scheduling.
@@ -212,6 +214,10 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const int nb = min(MK_M, B - g0);                 // requests in the group
   const int ntiles = (V + MK_N - 1) / MK_N;
   const uint32_t tile_bytes = static_cast<uint32_t>(nkb) * MK_UBLK;
+  // A group of at most 64 requests is multiplied twice (rows 64..127 of X repeat rows
+  // 0..63), so that the epilogue warps of all four TMEM lane quadrants hold its products
+  // and the two halves take alternate tiles.
+  const bool dup = nb <= MK_M / 2;
   int nmine = 0;  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
 
@@ -222,7 +228,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     }
     for (int q = 0; q < MK_ACC; ++q) {
       mbar_init(&afull[q], 1);
-      mbar_init(&aempty[q], MK_EPI_WARPS);
+      mbar_init(&aempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
     fence_mbar_init();
   }
@@ -243,7 +249,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       const int m = i / cpr, c = i - m * cpr;
       const int kb = c >> 3, cc = c & 7;
       unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
-      const int y = (m < nb && c * 8 < r) ? prev_token(A, g0 + m) : -1;
+      const int mr = dup ? (m & (MK_M / 2 - 1)) : m;  // the request of row m
+      const int y = (mr < nb && c * 8 < r) ? prev_token(A, g0 + mr) : -1;
       if (y >= 0)
         cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
       else
@@ -302,11 +309,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. request g0 + m,
     // m = 32 (w % 4) + lane, and columns 32 h .. 32 h + 31 of each tile (h: which of the
     // two warps of its lane group).
-    const int m = 32 * (w & 3) + lane;
+    const int m = 32 * (w & 3) + lane;        // TMEM lane (row of the product)
+    // With the group doubled, quadrants 0-1 take even tiles and 2-3 odd ones.
+    const int par = dup ? ((w & 3) >> 1) : 0;
+    const int step = dup ? 2 : 1;
+    const int mreq = dup ? (m & (MK_M / 2 - 1)) : m;
     const int h = (w - 2) >> 2;
     const size_t KV = (size_t)A.K * V;
-    const int b = g0 + m;
-    const bool live = m < nb;
+    const int b = g0 + mreq;
+    const bool live = mreq < nb;
     const uint16_t* Lrow = A.L + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
     uint16_t* Orow = A.out + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
     const bool vec = (V & 7) == 0;  // rows 16-byte aligned: vector loads and stores
@@ -319,8 +330,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         best_v = v;
       }
     };
-    // Raw logits of this warp's 32 columns of tile i (16-byte vectors), loaded one tile
-    // ahead of their use.
+    // Raw logits of this warp's 32 columns of tile i (16-byte vectors), loaded one of
+    // its tiles ahead of their use.
     uint4 raw[4], nxt[4];
     auto load_raw = [&](int i, uint4* dst) {
       const int v0 = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
@@ -329,11 +340,11 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         for (int j = 0; j < 4; ++j) dst[j] = __ldcs(reinterpret_cast<const uint4*>(Lrow + v0) + j);
       }
     };
-    load_raw(0, nxt);
-    for (int i = 0; i < nmine; ++i) {
+    load_raw(par, nxt);
+    for (int i = par; i < nmine; i += step) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) raw[j] = nxt[j];
-      load_raw(i + 1, nxt);
+      load_raw(i + step, nxt);
       const int a = i % MK_ACC;
       bool ok = true;
       if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / MK_ACC) & 1), A);
