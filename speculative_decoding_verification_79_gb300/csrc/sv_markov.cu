@@ -231,6 +231,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       mbar_init(&aempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
     fence_mbar_init();
+    // U does not depend on X: the first tiles of the ring start landing while X is
+    // gathered (this thread is the TMA producer).
+    const uint64_t keep = policy_evict_last();
+    for (int i = 0; i < MK_RING && i < nmine; ++i) {
+      mbar_arrive_expect_tx(&ufull[i], tile_bytes);
+      const int t = blockIdx.x + i * gridDim.x;
+      for (int kb = 0; kb < nkb; ++kb)
+        tma_load_2d(ubuf(i) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[i], keep);
+    }
   }
   if (w == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -266,14 +275,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const uint32_t tmem = tmem_base;
 
   if (w == 0) {
-    // TMA producer (lane 0): U tiles into the ring, each once its buffer's previous
-    // product is done. U is read again at every position: keep it in L2.
+    // TMA producer (lane 0): U tiles into the ring (the first MK_RING are already on
+    // their way), each once its buffer's previous product is done. U is read again at
+    // every position: keep it in L2.
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
-      for (int i = 0; i < nmine; ++i) {
+      for (int i = MK_RING; i < nmine; ++i) {
         const int q = i % MK_RING;
-        if (i >= MK_RING && !mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A))
-          break;
+        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A)) break;
         mbar_arrive_expect_tx(&ufull[q], tile_bytes);
         const int t = blockIdx.x + i * gridDim.x;
         for (int kb = 0; kb < nkb; ++kb)
