@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   // afull: accumulator ready; aempty: the epilogue warps have read it.
   __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[MK_ACC], aempty[MK_ACC];
   __shared__ uint32_t tmem_base;
+  __shared__ int yrow[MK_M];  // the previous token of each row of X (-1: a zero row)
   const int r = A.r, V = A.V, B = A.B;
   const int nkb = (r + MK_KB - 1) / MK_KB;
   unsigned char* Xs = dsm;
@@ -241,6 +242,10 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         tma_load_2d(ubuf(i) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[i], keep);
     }
   }
+  if (tid < MK_M) {  // one read of each request's previous token
+    const int mr = dup ? (tid & (MK_M / 2 - 1)) : tid;
+    yrow[tid] = mr < nb ? prev_token(A, g0 + mr) : -1;
+  }
   if (w == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base)),
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 
   // X: row m = request g0 + m, the gathered Vm row, zero past the group, past r, or for
   // an invalid previous token; 16-byte chunks placed in the swizzled layout.
+  __syncthreads();  // yrow
   {
     const uint64_t keep = policy_evict_last();
     const int cpr = nkb * (MK_KB / 8);  // 16-byte chunks per padded row
@@ -258,8 +264,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       const int m = i / cpr, c = i - m * cpr;
       const int kb = c >> 3, cc = c & 7;
       unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
-      const int mr = dup ? (m & (MK_M / 2 - 1)) : m;  // the request of row m
-      const int y = (mr < nb && c * 8 < r) ? prev_token(A, g0 + mr) : -1;
+      const int y = c * 8 < r ? yrow[m] : -1;
       if (y >= 0)
         cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
       else
