@@ -22,9 +22,15 @@
 //    columns and commits them to an mbarrier;
 //  - while the next tile multiplies, eight epilogue warps read the previous accumulator
 //    with tcgen05.ld (two warps per group of 32 TMEM lanes, 32 columns each: a thread
-//    holds 32 consecutive values of one request), add the raw logits (16-byte loads of
-//    the request's row, fetched one tile ahead), round once to bf16, store, and keep the
-//    request's running maximum and its first index. A group of at most 64 requests
+//    holds 32 consecutive values of one request), add the raw logits, round once to
+//    bf16, store, and keep the request's running maximum and its first index;
+//  - a fourth role, one warp, copies the raw logits of each tile (the group's rows x 64
+//    columns) into a second ring of stages, so that each SM keeps 32-64 KB of them in
+//    flight (loads held in registers one tile ahead kept only ~16 KB in flight and left
+//    the epilogue waiting on HBM latency): by 3-D tensor-map TMA when a U tile is at
+//    most two 64-column blocks (r <= 128), else by 16-byte cp.async, which leaves the
+//    TMA unit to the larger U tiles (measured both ways at r = 128 and 256).
+// A group of at most 64 requests
 //    fills X twice (rows 64..127 repeat rows 0..63), so that all four lane groups hold
 //    its products and the warps of lane groups 0-1 and 2-3 take alternate tiles.
 // key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v): the largest
@@ -46,12 +52,35 @@ constexpr int MK_M = 128;        // requests per group (UMMA M; rows past the ba
 constexpr int MK_N = 64;         // vocabulary rows per tile (UMMA N)
 constexpr int MK_KB = 64;        // K elements per 128-byte swizzle block
 constexpr int MK_EPI_WARPS = 8;  // epilogue warps: two per TMEM lane group, half a tile each
-constexpr int MK_THREADS = 32 * (2 + MK_EPI_WARPS);  // and a TMA warp and an MMA warp
+// and a U TMA warp, an MMA warp and a raw-logit TMA warp
+constexpr int MK_THREADS = 32 * (3 + MK_EPI_WARPS);
 constexpr int MK_XBLK = MK_M * 128;      // one block of X: 128 rows x 128 bytes
 constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 64 rows x 128 bytes
-constexpr int MK_RING = 4;               // U tiles in flight
+constexpr int MK_RING = 4;               // most U tiles in flight
 constexpr int MK_ACC = 4;                    // accumulator stages in TMEM
 constexpr uint32_t MK_TMEM_COLS = MK_ACC * MK_N;
+constexpr int MK_RAWBOX = 64 * 128;  // raw logits of 64 requests x 64 columns (bf16)
+constexpr int MK_RSTAGES = 16;       // most raw-logit stages
+#ifndef SV_MK_RAW_MAX
+#define SV_MK_RAW_MAX 65536
+#endif
+#ifndef SV_MK_U3
+#define SV_MK_U3 0
+#endif
+// U buffers for nkb blocks of K: four, or three at r > 192 (SV_MK_U3) to leave the raw
+// logits room.
+__host__ __device__ constexpr int mk_uring(int nkb) {
+  return (SV_MK_U3 && nkb > 3) ? MK_RING - 1 : MK_RING;
+}
+// Bytes of the raw-logit ring: what the 227 KB of shared memory leave next to X, the U
+// ring, 1 KB of alignment and 1 KB of static variables, in 16 KB steps, at most
+// SV_MK_RAW_MAX.
+__host__ __device__ constexpr int mk_raw_bytes(int nkb) {
+  return (227 * 1024 - 2048 - nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK)) / 16384 * 16384 <
+                 SV_MK_RAW_MAX
+             ? (227 * 1024 - 2048 - nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK)) / 16384 * 16384
+             : SV_MK_RAW_MAX;
+}
 
 struct MarkovArgs {
   const uint16_t* L;     // [B, K, V] raw logits (bf16 bits)
@@ -76,6 +105,29 @@ __device__ __forceinline__ uint32_t bf_order(uint16_t h) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t pol) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
                "l"(src), "l"(pol)
+               : "memory");
+}
+// Box (x = column, y = position, z = request) of a 3-D tensor map into shared memory.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// 16 bytes, or 16 zero bytes when `n` is 0 (nothing is read then).
+__device__ __forceinline__ void cp_async16_n(void* dst, const void* src, uint32_t n, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(n), "l"(pol)
+               : "memory");
+}
+// The mbarrier receives one arrival when all of this thread's earlier cp.async are done.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
@@ -187,23 +239,30 @@ __device__ __forceinline__ int prev_token(const MarkovArgs& A, int b) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
 }
 
-// Shared memory of the step kernel: X (nkb blocks of 128 rows x 128 bytes), then the
-// ring of U tiles (nkb blocks of 64 rows x 128 bytes each), 1024-byte aligned; at least
-// 116 KB, so that one CTA is resident per SM.
+// Shared memory of the step kernel: X (nkb blocks of 128 rows x 128 bytes), the ring
+// of U tiles (nkb blocks of 64 rows x 128 bytes each), then the raw-logit ring,
+// 1024-byte aligned; at least 116 KB, so that one CTA is resident per SM.
 size_t markov_smem_bytes(int r) {
   const int nkb = (r + MK_KB - 1) / MK_KB;
-  const size_t need = 1024 + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK);
+  const size_t need =
+      1024 + (size_t)nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK) + (size_t)mk_raw_bytes(nkb);
   return need > (size_t)116 * 1024 ? need : (size_t)116 * 1024;
 }
 
+// RING: how the raw logits reach the epilogue (0: plain loads, 1: the ring filled by
+// cp.async, 2: the ring filled by TMA from tmL).
+template <int RING>
 __global__ void __launch_bounds__(MK_THREADS, 1)
-    sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU) {
+    sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU,
+                          const __grid_constant__ CUtensorMap tmL) {
   extern __shared__ __align__(1024) unsigned char dsm_raw[];
   unsigned char* dsm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // ufull: U tile landed; uempty: its product is done (the buffer may be refilled);
   // afull: accumulator ready; aempty: the epilogue warps have read it.
+  // rfull / rempty: a raw-logit stage landed / was read by its epilogue warps.
   __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[MK_ACC], aempty[MK_ACC];
+  __shared__ uint64_t rfull[MK_RSTAGES], rempty[MK_RSTAGES];
   __shared__ uint32_t tmem_base;
   __shared__ int yrow[MK_M];  // the previous token of each row of X (-1: a zero row)
   const int r = A.r, V = A.V, B = A.B;
@@ -221,9 +280,40 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const bool dup = nb <= MK_M / 2;
   int nmine = 0;  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
+  // Raw-logit stages: 64 rows of 128 bytes (64 requests x 64 columns) per tile, twice
+  // that for a group of more; row j's 16-byte chunk c sits at chunk c ^ (j & 7), so that
+  // the epilogue's reads of 32 rows spread over all banks.
+  constexpr bool rt = RING != 0, rtma = RING == 2;
+  const int rsb = dup ? MK_RAWBOX : 2 * MK_RAWBOX;
+  const int nrs = min(MK_RSTAGES, mk_raw_bytes(nkb) / rsb);
+  const int nur = mk_uring(nkb);
+  unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + nur * MK_UBLK);
+  constexpr int RAW_W = 2 + MK_EPI_WARPS;  // the raw-logit copy warp
+  auto issue_raw = [&](int i) {  // tile i's raw logits into stage i % nrs (whole warp)
+    const int q = i % nrs;
+    const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
+    const uint64_t once = policy_evict_first();
+    unsigned char* stg = rawq + (size_t)q * rsb;
+    if constexpr (rtma) {  // boxes of 64 requests x 1 position x 64 columns, 128-byte swizzle
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&rfull[q], static_cast<uint32_t>(rsb));
+        for (int h = 0; h * MK_RAWBOX < rsb; ++h)
+          tma_load_3d(stg + h * MK_RAWBOX, &tmL, v0, A.k, g0 + 64 * h, &rfull[q], once);
+      }
+      return;
+    }
+    const size_t KV = (size_t)A.K * V;
+    for (int c = lane; c < rsb / 16; c += 32) {
+      const int j = c >> 3, cc = c & 7, v = v0 + cc * 8;
+      const bool in = g0 + j < B && v < V;  // V is a multiple of 8 here
+      const uint16_t* src = in ? A.L + (size_t)(g0 + j) * KV + (size_t)A.k * V + v : A.L;
+      cp_async16_n(stg + j * 128 + ((cc ^ (j & 7)) << 4), src, in ? 16u : 0u, once);
+    }
+    cp_async_arrive(&rfull[q]);
+  };
 
   if (tid == 0) {
-    for (int q = 0; q < MK_RING; ++q) {
+    for (int q = 0; q < nur; ++q) {
       mbar_init(&ufull[q], 1);
       mbar_init(&uempty[q], 1);
     }
@@ -231,11 +321,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       mbar_init(&afull[q], 1);
       mbar_init(&aempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
+    for (int q = 0; q < nrs; ++q) {
+      mbar_init(&rfull[q], rtma ? 1 : 32);  // the expect_tx, or each lane's cp.async
+      mbar_init(&rempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
+    }
     fence_mbar_init();
     // U does not depend on X: the first tiles of the ring start landing while X is
     // gathered (this thread is the TMA producer).
     const uint64_t keep = policy_evict_last();
-    for (int i = 0; i < MK_RING && i < nmine; ++i) {
+    for (int i = 0; i < nur && i < nmine; ++i) {
       mbar_arrive_expect_tx(&ufull[i], tile_bytes);
       const int t = blockIdx.x + i * gridDim.x;
       for (int kb = 0; kb < nkb; ++kb)
@@ -256,11 +350,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 
   // X: row m = request g0 + m, the gathered Vm row, zero past the group, past r, or for
   // an invalid previous token; 16-byte chunks placed in the swizzled layout.
-  __syncthreads();  // yrow
-  {
+  __syncthreads();  // yrow and the barriers
+  if (w == RAW_W) {
+    // The copy warp starts the raw-logit ring while the others gather X.
+    if (rt)
+      for (int i = 0; i < nrs && i < nmine; ++i) issue_raw(i);
+  } else {
     const uint64_t keep = policy_evict_last();
     const int cpr = nkb * (MK_KB / 8);  // 16-byte chunks per padded row
-    for (int i = tid; i < MK_M * cpr; i += MK_THREADS) {
+    for (int i = tid; i < MK_M * cpr; i += 32 * RAW_W) {
       const int m = i / cpr, c = i - m * cpr;
       const int kb = c >> 3, cc = c & 7;
       unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
@@ -280,14 +378,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const uint32_t tmem = tmem_base;
 
   if (w == 0) {
-    // TMA producer (lane 0): U tiles into the ring (the first MK_RING are already on
+    // TMA producer (lane 0): U tiles into the ring (the first of them are already on
     // their way), each once its buffer's previous product is done. U is read again at
     // every position: keep it in L2.
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
-      for (int i = MK_RING; i < nmine; ++i) {
-        const int q = i % MK_RING;
-        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A)) break;
+      for (int i = nur; i < nmine; ++i) {
+        const int q = i % nur;
+        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / nur - 1) & 1), A)) break;
         mbar_arrive_expect_tx(&ufull[q], tile_bytes);
         const int t = blockIdx.x + i * gridDim.x;
         for (int kb = 0; kb < nkb; ++kb)
@@ -301,8 +399,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       const uint64_t ad = sw128_desc(Xs);
       const int nk = r / 16;
       for (int i = 0; i < nmine; ++i) {
-        const int q = i % MK_RING, a = i % MK_ACC;
-        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / MK_RING) & 1), A)) break;
+        const int q = i % nur, a = i % MK_ACC;
+        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / nur) & 1), A)) break;
         if (i >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>((i / MK_ACC - 1) & 1), A))
           break;
         tmem_fence_after();
@@ -319,7 +417,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         umma_commit(&afull[a]);   // and the accumulator is ready
       }
     }
-  } else {
+  } else if (w < 2 + MK_EPI_WARPS) {
     // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. request g0 + m,
     // m = 32 (w % 4) + lane, and columns 32 h .. 32 h + 31 of each tile (h: which of the
     // two warps of its lane group).
@@ -334,7 +432,6 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     const bool live = mreq < nb;
     const uint16_t* Lrow = A.L + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
     uint16_t* Orow = A.out + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
-    const bool vec = (V & 7) == 0;  // rows 16-byte aligned: vector loads and stores
     uint32_t best = 0;   // order-preserving code (+1) of the request's largest value so far
     int best_v = -1;     // its first index (values are visited in increasing v)
     auto see = [&](uint16_t h, int v) {
@@ -344,33 +441,32 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         best_v = v;
       }
     };
-    // Raw logits of this warp's 32 columns of tile i (16-byte vectors), loaded one of
-    // its tiles ahead of their use.
-    uint4 raw[4], nxt[4];
-    auto load_raw = [&](int i, uint4* dst) {
-      const int v0 = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
-      if (vec && live && i < nmine && v0 + 32 <= V) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = __ldcs(reinterpret_cast<const uint4*>(Lrow + v0) + j);
-      }
-    };
-    load_raw(par, nxt);
     for (int i = par; i < nmine; i += step) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) raw[j] = nxt[j];
-      load_raw(i + step, nxt);
-      const int a = i % MK_ACC;
+      const int a = i % MK_ACC, q = i % nrs;
       bool ok = true;
       if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / MK_ACC) & 1), A);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      // Every lane reads the stage, so every lane observes its phase: the copy's writes
+      // are visible to a thread through its own wait on the barrier.
+      if (rt && !__all_sync(0xffffffffu, mk_wait(&rfull[q], static_cast<uint32_t>((i / nrs) & 1), A)))
+        break;
       tmem_fence_after();
       const int vq = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
-      const bool full = vec && live && vq + 32 <= V;
+      const bool full = rt && live && vq + 32 <= V;
+      // This warp's 32 columns of the request's row in the stage: 16-byte chunks
+      // 4h .. 4h + 3 of row mreq, placed by the 128-byte swizzle.
+      uint4 raw[4];
+      if (rt) {
+        const unsigned char* rp = rawq + (size_t)q * rsb + mreq * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          raw[j] = *reinterpret_cast<const uint4*>(rp + (((4 * h + j) ^ (mreq & 7)) << 4));
+      }
       const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
                             static_cast<uint32_t>(a * MK_N + 32 * h);
       float acc[32];
       tmem_ld32(tcol, acc);
-      // The accumulator is in registers: release it to the MMA issuer.
+      // The accumulator is in registers (tcgen05.wait::ld): release it to the MMA issuer.
       tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aempty[a]);
@@ -405,11 +501,28 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
           }
         }
       }
+      // The raw-logit stage is released only once every lane has used its values: a
+      // load whose result is still pending does not hold the stage, and a refill issued
+      // on an earlier release could overwrite it before it is read.
+      if (rt) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[q]);
+      }
     }
     if (live && best_v >= 0)
       atomicMax(A.keys + (size_t)A.k * B + b,
                 (static_cast<unsigned long long>(best - 1u) << 32) |
                     (0xffffffffull - static_cast<unsigned>(best_v)));
+  } else if (rt) {
+    // Raw-logit copy warp: tile i once its stage's previous tile has been read (the
+    // first stages are already on their way).
+    for (int i = nrs; i < nmine; ++i) {
+      if (!__all_sync(0xffffffffu,
+                      mk_wait(&rempty[i % nrs], static_cast<uint32_t>((i / nrs - 1) & 1), A)))
+        break;
+      issue_raw(i);
+    }
+    cp_async_wait_all();  // no copy outlives the CTA, even after a timeout
   }
 
   tmem_fence_before();
@@ -457,9 +570,15 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
                           int32_t* tok, unsigned long long* keys, WsHeader* hdr, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(sv_markov_step_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)markov_smem_bytes(SV_MAX_MARKOV_R));
+    const int smax = (int)markov_smem_bytes(SV_MAX_MARKOV_R);
+    cudaError_t e = cudaFuncSetAttribute(sv_markov_step_kernel<0>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sv_markov_step_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sv_markov_step_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -476,6 +595,25 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // The raw logits go through the shared-memory ring when their rows are 16-byte
+  // aligned (otherwise the kernel reads them with plain loads); at r <= 128 by TMA, as
+  // a 3-D tensor [B][K][V] of bf16 in boxes of 64 columns (128 bytes, 128-byte
+  // swizzle) x 1 position x 64 requests, zeros past V and B.
+  int rawring = (V % 8 == 0 && reinterpret_cast<uintptr_t>(L) % 16 == 0) ? 1 : 0;
+  CUtensorMap tl = tm;  // a valid map, unused unless rawring == 2
+  if (rawring && r <= 2 * MK_KB) {
+    const cuuint64_t ldim[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(K),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t lstride[2] = {static_cast<cuuint64_t>(V) * 2,
+                                   static_cast<cuuint64_t>(K) * static_cast<cuuint64_t>(V) * 2};
+    const cuuint32_t lbox[3] = {MK_N, 1, 64};
+    const cuuint32_t lestr[3] = {1, 1, 1};
+    if (enc(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(L), ldim, lstride,
+            lbox, lestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    rawring = 2;
+  }
   cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)K * B, st);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -487,7 +625,13 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
                   static_cast<unsigned>((B + MK_M - 1) / MK_M));
   for (int k = 0; k < K; ++k) {
     A.k = k;
-    sv_markov_step_kernel<<<grid, MK_THREADS, markov_smem_bytes(r), st>>>(A, tm);
+    const size_t smem = markov_smem_bytes(r);
+    if (rawring == 2)
+      sv_markov_step_kernel<2><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
+    else if (rawring == 1)
+      sv_markov_step_kernel<1><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
+    else
+      sv_markov_step_kernel<0><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   sv_markov_finish_kernel<<<(B + 127) / 128, 128, 0, st>>>(A);
