@@ -24,12 +24,11 @@
 //    with tcgen05.ld (two warps per group of 32 TMEM lanes, 32 columns each: a thread
 //    holds 32 consecutive values of one request), add the raw logits, round once to
 //    bf16, store, and keep the request's running maximum and its first index;
-//  - a fourth role, one warp, copies the raw logits of each tile (the group's rows x 64
-//    columns) into a second ring of stages, so that each SM keeps 32-64 KB of them in
-//    flight (loads held in registers one tile ahead kept only ~16 KB in flight and left
-//    the epilogue waiting on HBM latency): by 3-D tensor-map TMA when a U tile is at
-//    most two 64-column blocks (r <= 128), else by 16-byte cp.async, which leaves the
-//    TMA unit to the larger U tiles (measured both ways at r = 128 and 256).
+//  - a fourth role, one thread, copies the raw logits of each tile (the group's rows x 64
+//    columns) by 3-D tensor-map TMA into a second ring of stages, so that each SM keeps
+//    32-64 KB of them in flight (loads held in registers one tile ahead kept only
+//    ~16 KB in flight and left the epilogue waiting on HBM latency). A stage is released
+//    only after its values have been used.
 // A group of at most 64 requests
 //    fills X twice (rows 64..127 repeat rows 0..63), so that all four lane groups hold
 //    its products and the warps of lane groups 0-1 and 2-3 take alternate tiles.
@@ -56,31 +55,14 @@ constexpr int MK_EPI_WARPS = 8;  // epilogue warps: two per TMEM lane group, hal
 constexpr int MK_THREADS = 32 * (3 + MK_EPI_WARPS);
 constexpr int MK_XBLK = MK_M * 128;      // one block of X: 128 rows x 128 bytes
 constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 64 rows x 128 bytes
-constexpr int MK_RING = 4;               // most U tiles in flight
+constexpr int MK_RING = 4;               // U tiles in flight
 constexpr int MK_ACC = 4;                    // accumulator stages in TMEM
 constexpr uint32_t MK_TMEM_COLS = MK_ACC * MK_N;
 constexpr int MK_RAWBOX = 64 * 128;  // raw logits of 64 requests x 64 columns (bf16)
-constexpr int MK_RSTAGES = 16;       // most raw-logit stages
-#ifndef SV_MK_RAW_MAX
-#define SV_MK_RAW_MAX 65536
-#endif
-#ifndef SV_MK_U3
-#define SV_MK_U3 0
-#endif
-// U buffers for nkb blocks of K: four, or three at r > 192 (SV_MK_U3) to leave the raw
-// logits room.
-__host__ __device__ constexpr int mk_uring(int nkb) {
-  return (SV_MK_U3 && nkb > 3) ? MK_RING - 1 : MK_RING;
-}
-// Bytes of the raw-logit ring: what the 227 KB of shared memory leave next to X, the U
-// ring, 1 KB of alignment and 1 KB of static variables, in 16 KB steps, at most
-// SV_MK_RAW_MAX.
-__host__ __device__ constexpr int mk_raw_bytes(int nkb) {
-  return (227 * 1024 - 2048 - nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK)) / 16384 * 16384 <
-                 SV_MK_RAW_MAX
-             ? (227 * 1024 - 2048 - nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK)) / 16384 * 16384
-             : SV_MK_RAW_MAX;
-}
+constexpr int MK_RSTAGES = 8;        // most raw-logit stages
+// Bytes of the raw-logit ring: 64 KB, or at r > 192 the 32 KB that the 227 KB of
+// shared memory leave next to X, the U ring, alignment and static variables.
+__host__ __device__ constexpr int mk_raw_bytes(int nkb) { return nkb <= 3 ? 65536 : 32768; }
 
 struct MarkovArgs {
   const uint16_t* L;     // [B, K, V] raw logits (bf16 bits)
@@ -118,18 +100,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// 16 bytes, or 16 zero bytes when `n` is 0 (nothing is read then).
-__device__ __forceinline__ void cp_async16_n(void* dst, const void* src, uint32_t n, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(n), "l"(pol)
-               : "memory");
-}
-// The mbarrier receives one arrival when all of this thread's earlier cp.async are done.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
@@ -245,13 +215,13 @@ __device__ __forceinline__ int prev_token(const MarkovArgs& A, int b) {
 size_t markov_smem_bytes(int r) {
   const int nkb = (r + MK_KB - 1) / MK_KB;
   const size_t need =
-      1024 + (size_t)nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK) + (size_t)mk_raw_bytes(nkb);
+      1024 + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK) + (size_t)mk_raw_bytes(nkb);
   return need > (size_t)116 * 1024 ? need : (size_t)116 * 1024;
 }
 
-// RING: how the raw logits reach the epilogue (0: plain loads, 1: the ring filled by
-// cp.async, 2: the ring filled by TMA from tmL).
-template <int RING>
+// RING: the raw logits reach the epilogue through the shared-memory ring, filled by TMA
+// from tmL (rows 16-byte aligned); otherwise by plain loads.
+template <bool RING>
 __global__ void __launch_bounds__(MK_THREADS, 1)
     sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU,
                           const __grid_constant__ CUtensorMap tmL) {
@@ -281,39 +251,27 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   int nmine = 0;  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
   // Raw-logit stages: 64 rows of 128 bytes (64 requests x 64 columns) per tile, twice
-  // that for a group of more; row j's 16-byte chunk c sits at chunk c ^ (j & 7), so that
-  // the epilogue's reads of 32 rows spread over all banks.
-  constexpr bool rt = RING != 0, rtma = RING == 2;
+  // that for a group of more; the 128-byte swizzle puts row j's 16-byte chunk c at chunk
+  // c ^ (j & 7), so that the epilogue's reads of 32 rows spread over all banks.
+  constexpr bool rt = RING;
   const int rsb = dup ? MK_RAWBOX : 2 * MK_RAWBOX;
   const int nrs = min(MK_RSTAGES, mk_raw_bytes(nkb) / rsb);
-  const int nur = mk_uring(nkb);
-  unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + nur * MK_UBLK);
+  unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK);
   constexpr int RAW_W = 2 + MK_EPI_WARPS;  // the raw-logit copy warp
-  auto issue_raw = [&](int i) {  // tile i's raw logits into stage i % nrs (whole warp)
+  // Tile i's raw logits into stage i % nrs (one thread): boxes of 64 requests x 1
+  // position x 64 columns.
+  auto issue_raw = [&](int i) {
     const int q = i % nrs;
     const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
     const uint64_t once = policy_evict_first();
-    unsigned char* stg = rawq + (size_t)q * rsb;
-    if constexpr (rtma) {  // boxes of 64 requests x 1 position x 64 columns, 128-byte swizzle
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&rfull[q], static_cast<uint32_t>(rsb));
-        for (int h = 0; h * MK_RAWBOX < rsb; ++h)
-          tma_load_3d(stg + h * MK_RAWBOX, &tmL, v0, A.k, g0 + 64 * h, &rfull[q], once);
-      }
-      return;
-    }
-    const size_t KV = (size_t)A.K * V;
-    for (int c = lane; c < rsb / 16; c += 32) {
-      const int j = c >> 3, cc = c & 7, v = v0 + cc * 8;
-      const bool in = g0 + j < B && v < V;  // V is a multiple of 8 here
-      const uint16_t* src = in ? A.L + (size_t)(g0 + j) * KV + (size_t)A.k * V + v : A.L;
-      cp_async16_n(stg + j * 128 + ((cc ^ (j & 7)) << 4), src, in ? 16u : 0u, once);
-    }
-    cp_async_arrive(&rfull[q]);
+    mbar_arrive_expect_tx(&rfull[q], static_cast<uint32_t>(rsb));
+    for (int h = 0; h * MK_RAWBOX < rsb; ++h)
+      tma_load_3d(rawq + (size_t)q * rsb + h * MK_RAWBOX, &tmL, v0, A.k, g0 + 64 * h, &rfull[q],
+                  once);
   };
 
   if (tid == 0) {
-    for (int q = 0; q < nur; ++q) {
+    for (int q = 0; q < MK_RING; ++q) {
       mbar_init(&ufull[q], 1);
       mbar_init(&uempty[q], 1);
     }
@@ -322,14 +280,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       mbar_init(&aempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
     for (int q = 0; q < nrs; ++q) {
-      mbar_init(&rfull[q], rtma ? 1 : 32);  // the expect_tx, or each lane's cp.async
+      mbar_init(&rfull[q], 1);
       mbar_init(&rempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
     fence_mbar_init();
     // U does not depend on X: the first tiles of the ring start landing while X is
     // gathered (this thread is the TMA producer).
     const uint64_t keep = policy_evict_last();
-    for (int i = 0; i < nur && i < nmine; ++i) {
+    for (int i = 0; i < MK_RING && i < nmine; ++i) {
       mbar_arrive_expect_tx(&ufull[i], tile_bytes);
       const int t = blockIdx.x + i * gridDim.x;
       for (int kb = 0; kb < nkb; ++kb)
@@ -352,8 +310,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   // an invalid previous token; 16-byte chunks placed in the swizzled layout.
   __syncthreads();  // yrow and the barriers
   if (w == RAW_W) {
-    // The copy warp starts the raw-logit ring while the others gather X.
-    if (rt)
+    // The copy thread starts the raw-logit ring while the others gather X.
+    if (rt && lane == 0)
       for (int i = 0; i < nrs && i < nmine; ++i) issue_raw(i);
   } else {
     const uint64_t keep = policy_evict_last();
@@ -383,14 +341,18 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     // every position: keep it in L2.
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
-      for (int i = nur; i < nmine; ++i) {
-        const int q = i % nur;
-        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / nur - 1) & 1), A)) break;
+      int i = MK_RING;
+      for (; i < nmine; ++i) {
+        const int q = i % MK_RING;
+        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A)) break;
         mbar_arrive_expect_tx(&ufull[q], tile_bytes);
         const int t = blockIdx.x + i * gridDim.x;
         for (int kb = 0; kb < nkb; ++kb)
           tma_load_2d(ubuf(q) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[q], keep);
       }
+      // After a timeout, let the copies already issued land before the CTA exits.
+      for (int j = max(0, min(i, nmine) - MK_RING); j < min(i, nmine); ++j)
+        mk_wait(&ufull[j % MK_RING], static_cast<uint32_t>((j / MK_RING) & 1), A);
     }
   } else if (w == 1) {
     // MMA issuer (lane 0): tile i's product into accumulator i % MK_ACC once its U tile
@@ -399,8 +361,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       const uint64_t ad = sw128_desc(Xs);
       const int nk = r / 16;
       for (int i = 0; i < nmine; ++i) {
-        const int q = i % nur, a = i % MK_ACC;
-        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / nur) & 1), A)) break;
+        const int q = i % MK_RING, a = i % MK_ACC;
+        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / MK_RING) & 1), A)) break;
         if (i >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>((i / MK_ACC - 1) & 1), A))
           break;
         tmem_fence_after();
@@ -513,16 +475,18 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       atomicMax(A.keys + (size_t)A.k * B + b,
                 (static_cast<unsigned long long>(best - 1u) << 32) |
                     (0xffffffffull - static_cast<unsigned>(best_v)));
-  } else if (rt) {
-    // Raw-logit copy warp: tile i once its stage's previous tile has been read (the
+  } else if (rt && lane == 0) {
+    // Raw-logit copy thread: tile i once its stage's previous tile has been used (the
     // first stages are already on their way).
-    for (int i = nrs; i < nmine; ++i) {
-      if (!__all_sync(0xffffffffu,
-                      mk_wait(&rempty[i % nrs], static_cast<uint32_t>((i / nrs - 1) & 1), A)))
-        break;
+    int i = nrs;
+    for (; i < nmine; ++i) {
+      if (!mk_wait(&rempty[i % nrs], static_cast<uint32_t>((i / nrs - 1) & 1), A)) break;
       issue_raw(i);
     }
-    cp_async_wait_all();  // no copy outlives the CTA, even after a timeout
+    // After a timeout, let the copies already issued land before the CTA exits (at
+    // once otherwise: each of these phases has been consumed).
+    for (int j = max(0, min(i, nmine) - nrs); j < min(i, nmine); ++j)
+      mk_wait(&rfull[j % nrs], static_cast<uint32_t>((j / nrs) & 1), A);
   }
 
   tmem_fence_before();
@@ -571,13 +535,10 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
   static bool attr_set = false;
   if (!attr_set) {
     const int smax = (int)markov_smem_bytes(SV_MAX_MARKOV_R);
-    cudaError_t e = cudaFuncSetAttribute(sv_markov_step_kernel<0>,
+    cudaError_t e = cudaFuncSetAttribute(sv_markov_step_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sv_markov_step_kernel<1>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sv_markov_step_kernel<2>,
+      e = cudaFuncSetAttribute(sv_markov_step_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -596,12 +557,12 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   // The raw logits go through the shared-memory ring when their rows are 16-byte
-  // aligned (otherwise the kernel reads them with plain loads); at r <= 128 by TMA, as
-  // a 3-D tensor [B][K][V] of bf16 in boxes of 64 columns (128 bytes, 128-byte
-  // swizzle) x 1 position x 64 requests, zeros past V and B.
-  int rawring = (V % 8 == 0 && reinterpret_cast<uintptr_t>(L) % 16 == 0) ? 1 : 0;
-  CUtensorMap tl = tm;  // a valid map, unused unless rawring == 2
-  if (rawring && r <= 2 * MK_KB) {
+  // aligned (otherwise the kernel reads them with plain loads): by TMA, as a 3-D tensor
+  // [B][K][V] of bf16 in boxes of 64 columns (128 bytes, 128-byte swizzle) x 1 position
+  // x 64 requests, zeros past V and B.
+  const bool ring = V % 8 == 0 && reinterpret_cast<uintptr_t>(L) % 16 == 0;
+  CUtensorMap tl = tm;  // a valid map, unused without the ring
+  if (ring) {
     const cuuint64_t ldim[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(K),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t lstride[2] = {static_cast<cuuint64_t>(V) * 2,
@@ -612,7 +573,6 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
             lbox, lestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    rawring = 2;
   }
   cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)K * B, st);
   if (e != cudaSuccess) return e;
@@ -626,12 +586,10 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
   for (int k = 0; k < K; ++k) {
     A.k = k;
     const size_t smem = markov_smem_bytes(r);
-    if (rawring == 2)
-      sv_markov_step_kernel<2><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
-    else if (rawring == 1)
-      sv_markov_step_kernel<1><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
+    if (ring)
+      sv_markov_step_kernel<true><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
     else
-      sv_markov_step_kernel<0><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
+      sv_markov_step_kernel<false><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   sv_markov_finish_kernel<<<(B + 127) / 128, 128, 0, st>>>(A);
