@@ -213,9 +213,13 @@ sv_status sv_calib_update(double *stats_d, float *temps_d, int K, float lr, floa
  *  draft_tok_d [B, K] int32 out: y_k (-1 for a request whose prev_tok is invalid; its
  *              corrected rows are then unspecified and SV_ERR_DEVICE_INPUT is set).
  *  keys_d      [K * B] uint64 scratch (sv_markov_keys_len), overwritten.
- *  ws_d        a workspace (its status word only; any size from sv_workspace_bytes).
- *  K + 1 launches (one per position, then one that writes the tokens) after zeroing
- *  keys_d; capturable in a CUDA graph. logits_d and corrected_d must be 16-byte
+ *  ws_d        a workspace (its status word and a counter in its header; any size
+ *              from sv_workspace_bytes).
+ *  After zeroing keys_d: at B <= 128 one cooperative launch runs all K positions (one
+ *  CTA per SM; the CTAs meet at a grid barrier between positions, whose counter sits
+ *  in the workspace header and is reset by the last launch), otherwise one launch per
+ *  position; then one launch writes the tokens. Capturable in a CUDA graph. A wait
+ *  that runs out (~2 s) sets SV_ERR_TIMEOUT. logits_d and corrected_d must be 16-byte
  *  aligned, U_d and Vm_d too. Limits: 0 <= B <= SV_MAX_B, 1 <= K <= SV_MAX_K,
  *  1 <= V <= SV_MAX_V.
  */

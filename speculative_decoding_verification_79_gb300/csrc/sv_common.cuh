@@ -47,7 +47,8 @@ struct WsHeader {
   uint32_t status;    // ST_* bits: sticky report
   uint32_t abort;     // verify: set when a wait of this call gave up; reset at its end
   uint32_t cta_done;  // verify: CTAs that have finished
-  uint32_t pad[61];
+  uint32_t mk_pos;    // Markov: CTAs through the position barriers (reset after each call)
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

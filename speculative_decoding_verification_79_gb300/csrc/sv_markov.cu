@@ -73,7 +73,8 @@ struct MarkovArgs {
   unsigned long long* keys;  // [K, B]
   int32_t* tok;          // [B, K]
   WsHeader* hdr;
-  int B, K, V, r, k;
+  int B, K, V, r;
+  int k, kend;  // positions k .. kend - 1 in this launch
 };
 
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
@@ -186,6 +187,11 @@ __device__ __forceinline__ bool mbar_try_ns(uint64_t* bar, uint32_t parity, uint
   return ok != 0;
 }
 
+// Barrier `id` among the first `n` threads that reach it (whole warps).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Bounded wait for an mbarrier phase; false (and a status report) when it runs out.
 __device__ bool mk_wait(uint64_t* bar, uint32_t parity, const MarkovArgs& A) {
   const long long t0 = clock64();
@@ -198,13 +204,14 @@ __device__ bool mk_wait(uint64_t* bar, uint32_t parity, const MarkovArgs& A) {
   return true;
 }
 
-// The token drafted at position k-1 of request b (k > 0), or prev[b]; -1 if invalid.
-__device__ __forceinline__ int prev_token(const MarkovArgs& A, int b) {
-  if (A.k == 0) {
+// The token drafted at position kk-1 of request b (kk > 0), or prev[b]; -1 if invalid.
+// The keys are read from L2: other CTAs of the same launch may have written them.
+__device__ __forceinline__ int prev_token(const MarkovArgs& A, int kk, int b) {
+  if (kk == 0) {
     const int y = __ldg(A.prev + b);
     return (y >= 0 && y < A.V) ? y : -1;
   }
-  const unsigned long long key = A.keys[(size_t)(A.k - 1) * A.B + b];
+  const unsigned long long key = __ldcg(A.keys + (size_t)(kk - 1) * A.B + b);
   if (key == 0ull) return -1;
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
 }
@@ -221,6 +228,12 @@ size_t markov_smem_bytes(int r) {
 
 // RING: the raw logits reach the epilogue through the shared-memory ring, filled by TMA
 // from tmL (rows 16-byte aligned); otherwise by plain loads.
+// Positions A.k .. A.kend - 1 run in this launch. With more than one, the launch is
+// cooperative (one CTA per SM, gridDim.y == 1): between positions the epilogue warps of
+// every CTA meet at a grid barrier (a counter in the workspace header) before they read
+// the previous position's argmax and gather the next X, while U and the raw logits of
+// the next position keep streaming into their rings. Every (position, tile) pair of the
+// CTA has one running index g, which the rings and accumulator stages follow.
 template <bool RING>
 __global__ void __launch_bounds__(MK_THREADS, 1)
     sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU,
@@ -229,11 +242,13 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   unsigned char* dsm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // ufull: U tile landed; uempty: its product is done (the buffer may be refilled);
-  // afull: accumulator ready; aempty: the epilogue warps have read it.
-  // rfull / rempty: a raw-logit stage landed / was read by its epilogue warps.
+  // afull: accumulator ready; aempty: the epilogue warps have read it;
+  // rfull / rempty: a raw-logit stage landed / was used by its epilogue warps;
+  // xfull: X of the next position gathered.
   __shared__ uint64_t ufull[MK_RING], uempty[MK_RING], afull[MK_ACC], aempty[MK_ACC];
-  __shared__ uint64_t rfull[MK_RSTAGES], rempty[MK_RSTAGES];
+  __shared__ uint64_t rfull[MK_RSTAGES], rempty[MK_RSTAGES], xfull;
   __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;     // a grid barrier gave up: skip the remaining ones
   __shared__ int yrow[MK_M];  // the previous token of each row of X (-1: a zero row)
   const int r = A.r, V = A.V, B = A.B;
   const int nkb = (r + MK_KB - 1) / MK_KB;
@@ -248,26 +263,63 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   // 0..63), so that the epilogue warps of all four TMEM lane quadrants hold its products
   // and the two halves take alternate tiles.
   const bool dup = nb <= MK_M / 2;
-  int nmine = 0;  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  int nmine = 0;  // tiles of this CTA per position: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
+  const int npos = A.kend - A.k;
+  const int total = npos * nmine;  // (position, tile) pairs, position-major
   // Raw-logit stages: 64 rows of 128 bytes (64 requests x 64 columns) per tile, twice
   // that for a group of more; the 128-byte swizzle puts row j's 16-byte chunk c at chunk
-  // c ^ (j & 7), so that the epilogue's reads of 32 rows spread over all banks.
+  // c ^ (j & 7), so that the epilogue's reads of 32 rows spread over all banks. The
+  // number of stages is a power of two (2, 4 or 8).
   constexpr bool rt = RING;
   const int rsb = dup ? MK_RAWBOX : 2 * MK_RAWBOX;
   const int nrs = min(MK_RSTAGES, mk_raw_bytes(nkb) / rsb);
+  const int lgr = 31 - __clz(nrs);
   unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK);
   constexpr int RAW_W = 2 + MK_EPI_WARPS;  // the raw-logit copy warp
-  // Tile i's raw logits into stage i % nrs (one thread): boxes of 64 requests x 1
-  // position x 64 columns.
-  auto issue_raw = [&](int i) {
-    const int q = i % nrs;
+  constexpr int EPI0 = 64;                 // first thread of the epilogue warps
+  // Pair g (position kk, tile i)'s raw logits into stage g % nrs (one thread): boxes of
+  // 64 requests x 1 position x 64 columns.
+  auto issue_raw = [&](int g, int kk, int i) {
+    const int q = g & (nrs - 1);
     const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
     const uint64_t once = policy_evict_first();
     mbar_arrive_expect_tx(&rfull[q], static_cast<uint32_t>(rsb));
     for (int h = 0; h * MK_RAWBOX < rsb; ++h)
-      tma_load_3d(rawq + (size_t)q * rsb + h * MK_RAWBOX, &tmL, v0, A.k, g0 + 64 * h, &rfull[q],
+      tma_load_3d(rawq + (size_t)q * rsb + h * MK_RAWBOX, &tmL, v0, kk, g0 + 64 * h, &rfull[q],
                   once);
+  };
+  auto issue_u = [&](int g, int i) {  // U tile i into buffer g % MK_RING (one thread)
+    const int q = g & (MK_RING - 1);
+    const uint64_t keep = policy_evict_last();  // U is read again at every position
+    mbar_arrive_expect_tx(&ufull[q], tile_bytes);
+    const int t = blockIdx.x + i * gridDim.x;
+    for (int kb = 0; kb < nkb; ++kb)
+      tma_load_2d(ubuf(q) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[q], keep);
+  };
+  // X of position kk by threads t0 .. t0 + nthr - 1 (yrow holds its previous tokens): row
+  // m = request g0 + m, the gathered Vm row, zero past the group, past r, or for an
+  // invalid previous token; 16-byte chunks placed in the swizzled layout.
+  auto gather_x = [&](int t0, int nthr) {
+    const uint64_t keep = policy_evict_last();
+    const int cpr = nkb * (MK_KB / 8);  // 16-byte chunks per padded row
+    for (int i = tid - t0; i < MK_M * cpr; i += nthr) {
+      const int m = i / cpr, c = i - m * cpr;
+      const int kb = c >> 3, cc = c & 7;
+      unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
+      const int y = c * 8 < r ? yrow[m] : -1;
+      if (y >= 0)
+        cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_wait_all();
+    // The tensor cores read X through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  };
+  auto set_yrow = [&](int kk, int j) {  // thread j < MK_M: row j's previous token
+    const int mr = dup ? (j & (MK_M / 2 - 1)) : j;
+    yrow[j] = mr < nb ? prev_token(A, kk, g0 + mr) : -1;
   };
 
   if (tid == 0) {
@@ -283,21 +335,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       mbar_init(&rfull[q], 1);
       mbar_init(&rempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
     }
+    mbar_init(&xfull, 1);
+    s_abort = 0;
     fence_mbar_init();
     // U does not depend on X: the first tiles of the ring start landing while X is
     // gathered (this thread is the TMA producer).
-    const uint64_t keep = policy_evict_last();
-    for (int i = 0; i < MK_RING && i < nmine; ++i) {
-      mbar_arrive_expect_tx(&ufull[i], tile_bytes);
-      const int t = blockIdx.x + i * gridDim.x;
-      for (int kb = 0; kb < nkb; ++kb)
-        tma_load_2d(ubuf(i) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[i], keep);
-    }
+    for (int g = 0; g < MK_RING && g < total; ++g) issue_u(g, g % nmine);
   }
-  if (tid < MK_M) {  // one read of each request's previous token
-    const int mr = dup ? (tid & (MK_M / 2 - 1)) : tid;
-    yrow[tid] = mr < nb ? prev_token(A, g0 + mr) : -1;
-  }
+  if (tid < MK_M) set_yrow(A.k, tid);  // one read of each request's previous token
   if (w == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base)),
@@ -305,30 +350,13 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  // X: row m = request g0 + m, the gathered Vm row, zero past the group, past r, or for
-  // an invalid previous token; 16-byte chunks placed in the swizzled layout.
   __syncthreads();  // yrow and the barriers
   if (w == RAW_W) {
     // The copy thread starts the raw-logit ring while the others gather X.
     if (rt && lane == 0)
-      for (int i = 0; i < nrs && i < nmine; ++i) issue_raw(i);
+      for (int g = 0; g < nrs && g < total; ++g) issue_raw(g, A.k + g / nmine, g % nmine);
   } else {
-    const uint64_t keep = policy_evict_last();
-    const int cpr = nkb * (MK_KB / 8);  // 16-byte chunks per padded row
-    for (int i = tid; i < MK_M * cpr; i += 32 * RAW_W) {
-      const int m = i / cpr, c = i - m * cpr;
-      const int kb = c >> 3, cc = c & 7;
-      unsigned char* dst = Xs + (size_t)kb * MK_XBLK + m * 128 + ((cc ^ (m & 7)) << 4);
-      const int y = c * 8 < r ? yrow[m] : -1;
-      if (y >= 0)
-        cp_async16(dst, A.Vm + (size_t)y * r + c * 8, keep);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    cp_async_wait_all();
-    // The tensor cores read X through the async proxy.
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    gather_x(0, 32 * RAW_W);
   }
   tmem_fence_before();
   __syncthreads();
@@ -336,34 +364,32 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const uint32_t tmem = tmem_base;
 
   if (w == 0) {
-    // TMA producer (lane 0): U tiles into the ring (the first of them are already on
-    // their way), each once its buffer's previous product is done. U is read again at
-    // every position: keep it in L2.
+    // U producer (lane 0): pair g's tile once its buffer's previous product is done.
     if (lane == 0) {
-      const uint64_t keep = policy_evict_last();
-      int i = MK_RING;
-      for (; i < nmine; ++i) {
-        const int q = i % MK_RING;
-        if (!mk_wait(&uempty[q], static_cast<uint32_t>((i / MK_RING - 1) & 1), A)) break;
-        mbar_arrive_expect_tx(&ufull[q], tile_bytes);
-        const int t = blockIdx.x + i * gridDim.x;
-        for (int kb = 0; kb < nkb; ++kb)
-          tma_load_2d(ubuf(q) + (size_t)kb * MK_UBLK, &tmU, kb * MK_KB, t * MK_N, &ufull[q], keep);
+      int g = MK_RING, i = MK_RING % max(nmine, 1);
+      for (; g < total; ++g) {
+        if (!mk_wait(&uempty[g & (MK_RING - 1)], static_cast<uint32_t>(((g >> 2) - 1) & 1), A))
+          break;
+        issue_u(g, i);
+        if (++i == nmine) i = 0;
       }
       // After a timeout, let the copies already issued land before the CTA exits.
-      for (int j = max(0, min(i, nmine) - MK_RING); j < min(i, nmine); ++j)
-        mk_wait(&ufull[j % MK_RING], static_cast<uint32_t>((j / MK_RING) & 1), A);
+      for (int j = max(0, min(g, total) - MK_RING); j < min(g, total); ++j)
+        mk_wait(&ufull[j & (MK_RING - 1)], static_cast<uint32_t>((j >> 2) & 1), A);
     }
   } else if (w == 1) {
-    // MMA issuer (lane 0): tile i's product into accumulator i % MK_ACC once its U tile
-    // has landed and the epilogue warps have read that accumulator's previous tile.
+    // MMA issuer (lane 0): pair g's product into accumulator g % MK_ACC once its U tile
+    // has landed, the epilogue warps have read that accumulator's previous tile, and (at
+    // the first tile of a later position) that position's X is gathered.
     if (lane == 0) {
       const uint64_t ad = sw128_desc(Xs);
       const int nk = r / 16;
-      for (int i = 0; i < nmine; ++i) {
-        const int q = i % MK_RING, a = i % MK_ACC;
-        if (!mk_wait(&ufull[q], static_cast<uint32_t>((i / MK_RING) & 1), A)) break;
-        if (i >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>((i / MK_ACC - 1) & 1), A))
+      int i = 0, pos = 0;
+      for (int g = 0; g < total; ++g) {
+        const int q = g & (MK_RING - 1), a = g & (MK_ACC - 1);
+        if (i == 0 && pos > 0 && !mk_wait(&xfull, static_cast<uint32_t>((pos - 1) & 1), A)) break;
+        if (!mk_wait(&ufull[q], static_cast<uint32_t>((g >> 2) & 1), A)) break;
+        if (g >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>(((g >> 2) - 1) & 1), A))
           break;
         tmem_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(a * MK_N);
@@ -377,6 +403,10 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         }
         umma_commit(&uempty[q]);  // the U buffer is free when these products are done
         umma_commit(&afull[a]);   // and the accumulator is ready
+        if (++i == nmine) {
+          i = 0;
+          ++pos;
+        }
       }
     }
   } else if (w < 2 + MK_EPI_WARPS) {
@@ -384,103 +414,109 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     // m = 32 (w % 4) + lane, and columns 32 h .. 32 h + 31 of each tile (h: which of the
     // two warps of its lane group).
     const int m = 32 * (w & 3) + lane;        // TMEM lane (row of the product)
-    // With the group doubled, quadrants 0-1 take even tiles and 2-3 odd ones.
+    // With the group doubled, quadrants 0-1 take even pairs g and 2-3 odd ones.
     const int par = dup ? ((w & 3) >> 1) : 0;
-    const int step = dup ? 2 : 1;
     const int mreq = dup ? (m & (MK_M / 2 - 1)) : m;
     const int h = (w - 2) >> 2;
     const size_t KV = (size_t)A.K * V;
     const int b = g0 + mreq;
     const bool live = mreq < nb;
-    const uint16_t* Lrow = A.L + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
-    uint16_t* Orow = A.out + (size_t)(live ? b : 0) * KV + (size_t)A.k * V;
-    uint32_t best = 0;   // order-preserving code (+1) of the request's largest value so far
-    int best_v = -1;     // its first index (values are visited in increasing v)
-    auto see = [&](uint16_t h, int v) {
-      const uint32_t c = bf_order(h) + 1u;
-      if (c > best) {
-        best = c;
-        best_v = v;
-      }
-    };
-    for (int i = par; i < nmine; i += step) {
-      const int a = i % MK_ACC, q = i % nrs;
-      bool ok = true;
-      if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((i / MK_ACC) & 1), A);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      // Every lane reads the stage, so every lane observes its phase: the copy's writes
-      // are visible to a thread through its own wait on the barrier.
-      if (rt && !__all_sync(0xffffffffu, mk_wait(&rfull[q], static_cast<uint32_t>((i / nrs) & 1), A)))
-        break;
-      tmem_fence_after();
-      const int vq = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
-      const bool full = rt && live && vq + 32 <= V;
-      // This warp's 32 columns of the request's row in the stage: 16-byte chunks
-      // 4h .. 4h + 3 of row mreq, placed by the 128-byte swizzle.
-      uint4 raw[4];
-      if (rt) {
-        const unsigned char* rp = rawq + (size_t)q * rsb + mreq * 128;
+    bool dead = false;  // a wait gave up: skip the work, keep meeting the other warps
+    int g = 0;
+    for (int kk = A.k; kk < A.kend; ++kk) {
+      const uint16_t* Lrow = A.L + (size_t)(live ? b : 0) * KV + (size_t)kk * V;
+      uint16_t* Orow = A.out + (size_t)(live ? b : 0) * KV + (size_t)kk * V;
+      uint32_t best = 0;   // order-preserving code (+1) of the request's largest value so far
+      int best_v = -1;     // its first index (values are visited in increasing v)
+      auto see = [&](uint16_t hv, int v) {
+        const uint32_t c = bf_order(hv) + 1u;
+        if (c > best) {
+          best = c;
+          best_v = v;
+        }
+      };
+      for (int i = 0; i < nmine; ++i, ++g) {
+        if ((dup && (g & 1) != par) || dead) continue;
+        const int a = g & (MK_ACC - 1), q = g & (nrs - 1);
+        bool ok = true;
+        if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((g >> 2) & 1), A);
+        // Every lane reads the stage, so every lane observes its phase: the copy's
+        // writes are visible to a thread through its own wait on the barrier.
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) ||
+            (rt && !__all_sync(0xffffffffu,
+                               mk_wait(&rfull[q], static_cast<uint32_t>((g >> lgr) & 1), A)))) {
+          dead = true;
+          continue;
+        }
+        tmem_fence_after();
+        const int vq = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
+        const bool full = rt && live && vq + 32 <= V;
+        // This warp's 32 columns of the request's row in the stage: 16-byte chunks
+        // 4h .. 4h + 3 of row mreq, placed by the 128-byte swizzle.
+        uint4 raw[4];
+        if (rt) {
+          const unsigned char* rp = rawq + (size_t)q * rsb + mreq * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          raw[j] = *reinterpret_cast<const uint4*>(rp + (((4 * h + j) ^ (mreq & 7)) << 4));
-      }
-      const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
-                            static_cast<uint32_t>(a * MK_N + 32 * h);
-      float acc[32];
-      tmem_ld32(tcol, acc);
-      // The accumulator is in registers (tcgen05.wait::ld): release it to the MMA issuer.
-      tmem_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&aempty[a]);
-      {
+          for (int j = 0; j < 4; ++j)
+            raw[j] = *reinterpret_cast<const uint4*>(rp + (((4 * h + j) ^ (mreq & 7)) << 4));
+        }
+        const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
+                              static_cast<uint32_t>(a * MK_N + 32 * h);
+        float acc[32];
+        tmem_ld32(tcol, acc);
+        // The accumulator is in registers (tcgen05.wait::ld): release it to the MMA
+        // issuer.
+        tmem_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aempty[a]);
         if (full) {
-          // Pairs of values: one packed fp32x2 add, one rounding to bf16x2 (round to
-          // nearest even, as the per-value path), then the tile's maximum by packed
-          // NaN-propagating max. Only a tile whose maximum beats the running best looks
-          // for its first index; a tile with a NaN takes the per-value rule.
-          uint32_t hp[16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const int e = j * 8 + e2 * 2;  // elements e (low half) and e + 1 (high half)
-              float2 z;
-              asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-                  "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-                  "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-                  : "=f"(z.x), "=f"(z.y)
-                  : "f"(bf_lo(wv[e2])), "f"(bf_hi(wv[e2])), "f"(acc[e]), "f"(acc[e + 1]));
-              const __nv_bfloat162 o = __floats2bfloat162_rn(z.x, z.y);
-              hp[j * 4 + e2] = *reinterpret_cast<const uint32_t*>(&o);
-            }
-            __stcs(reinterpret_cast<uint4*>(Orow + vq) + j,
-                   make_uint4(hp[j * 4], hp[j * 4 + 1], hp[j * 4 + 2], hp[j * 4 + 3]));
-          }
-          __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&hp[0]);
-#pragma unroll
-          for (int t = 1; t < 16; ++t)
-            m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&hp[t]));
-          const __nv_bfloat16 m = __hmax_nan(m2.x, m2.y);
-          if (__hisnan(m)) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              see(static_cast<uint16_t>(hp[t] & 0xffffu), vq + 2 * t);
-              see(static_cast<uint16_t>(hp[t] >> 16), vq + 2 * t + 1);
-            }
-          } else {
-            const uint32_t c = bf_order(__bfloat16_as_ushort(m)) + 1u;
-            if (c > best) {  // the first column holding the maximum (-0 counts as +0)
-              int e = 31;
-#pragma unroll
-              for (int t = 15; t >= 0; --t) {
-                if (bf_order(static_cast<uint16_t>(hp[t] >> 16)) + 1u == c) e = 2 * t + 1;
-                if (bf_order(static_cast<uint16_t>(hp[t] & 0xffffu)) + 1u == c) e = 2 * t;
+            // Pairs of values: one packed fp32x2 add, one rounding to bf16x2 (round to
+            // nearest even, as the per-value path), then the tile's maximum by packed
+            // NaN-propagating max. Only a tile whose maximum beats the running best looks
+            // for its first index; a tile with a NaN takes the per-value rule.
+            uint32_t hp[16];
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+  #pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int e = j * 8 + e2 * 2;  // elements e (low half) and e + 1 (high half)
+                float2 z;
+                asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+                    "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+                    "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+                    : "=f"(z.x), "=f"(z.y)
+                    : "f"(bf_lo(wv[e2])), "f"(bf_hi(wv[e2])), "f"(acc[e]), "f"(acc[e + 1]));
+                const __nv_bfloat162 o = __floats2bfloat162_rn(z.x, z.y);
+                hp[j * 4 + e2] = *reinterpret_cast<const uint32_t*>(&o);
               }
-              best = c;
-              best_v = vq + e;
+              __stcs(reinterpret_cast<uint4*>(Orow + vq) + j,
+                     make_uint4(hp[j * 4], hp[j * 4 + 1], hp[j * 4 + 2], hp[j * 4 + 3]));
             }
-          }
+            __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&hp[0]);
+  #pragma unroll
+            for (int t = 1; t < 16; ++t)
+              m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&hp[t]));
+            const __nv_bfloat16 m = __hmax_nan(m2.x, m2.y);
+            if (__hisnan(m)) {
+  #pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                see(static_cast<uint16_t>(hp[t] & 0xffffu), vq + 2 * t);
+                see(static_cast<uint16_t>(hp[t] >> 16), vq + 2 * t + 1);
+              }
+            } else {
+              const uint32_t c = bf_order(__bfloat16_as_ushort(m)) + 1u;
+              if (c > best) {  // the first column holding the maximum (-0 counts as +0)
+                int e = 31;
+  #pragma unroll
+                for (int t = 15; t >= 0; --t) {
+                  if (bf_order(static_cast<uint16_t>(hp[t] >> 16)) + 1u == c) e = 2 * t + 1;
+                  if (bf_order(static_cast<uint16_t>(hp[t] & 0xffffu)) + 1u == c) e = 2 * t;
+                }
+                best = c;
+                best_v = vq + e;
+              }
+            }
         } else if (live) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -491,31 +527,62 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
             see(hv, vq + e);
           }
         }
+        // The raw-logit stage is released only once every lane has used its values: a
+        // load whose result is still pending does not hold the stage, and a refill
+        // issued on an earlier release could overwrite it before it is read.
+        if (rt) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rempty[q]);
+        }
       }
-      // The raw-logit stage is released only once every lane has used its values: a
-      // load whose result is still pending does not hold the stage, and a refill issued
-      // on an earlier release could overwrite it before it is read.
-      if (rt) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rempty[q]);
+      if (live && best_v >= 0)
+        atomicMax(A.keys + (size_t)kk * B + b,
+                  (static_cast<unsigned long long>(best - 1u) << 32) |
+                      (0xffffffffull - static_cast<unsigned>(best_v)));
+      if (kk + 1 == A.kend) break;
+      // Next position: every CTA's argmax of this one must be in before its previous
+      // tokens are read. The epilogue warps of this CTA meet (named barrier 1); one
+      // thread counts the CTA in and waits for all.
+      named_bar_sync(1, 32 * MK_EPI_WARPS);
+      if (tid == EPI0) {
+        // One release-ordered add: the CTA's maxima (ordered before it by the named
+        // barrier) are visible to whoever reads the count with acquire.
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&A.hdr->mk_pos) : "memory");
+        const uint32_t want = gridDim.x * static_cast<uint32_t>(kk + 1 - A.k);
+        const long long t0 = clock64();
+        while (!s_abort && ld_acquire(&A.hdr->mk_pos) < want) {
+          if (clock64() - t0 > WAIT_CYCLES) {
+            atomicOr(&A.hdr->status, ST_TIMEOUT);
+            s_abort = 1;
+          }
+        }
       }
+      named_bar_sync(1, 32 * MK_EPI_WARPS);
+      if (tid - EPI0 < MK_M) set_yrow(kk + 1, tid - EPI0);
+      named_bar_sync(1, 32 * MK_EPI_WARPS);
+      // The products of this position are done (every accumulator was waited for), so
+      // X may be overwritten.
+      gather_x(EPI0, 32 * MK_EPI_WARPS);
+      named_bar_sync(1, 32 * MK_EPI_WARPS);
+      if (tid == EPI0) mbar_arrive(&xfull);
     }
-    if (live && best_v >= 0)
-      atomicMax(A.keys + (size_t)A.k * B + b,
-                (static_cast<unsigned long long>(best - 1u) << 32) |
-                    (0xffffffffull - static_cast<unsigned>(best_v)));
   } else if (rt && lane == 0) {
-    // Raw-logit copy thread: tile i once its stage's previous tile has been used (the
+    // Raw-logit copy thread: pair g once its stage's previous pair has been used (the
     // first stages are already on their way).
-    int i = nrs;
-    for (; i < nmine; ++i) {
-      if (!mk_wait(&rempty[i % nrs], static_cast<uint32_t>((i / nrs - 1) & 1), A)) break;
-      issue_raw(i);
+    int g = nrs, kk = A.k + nrs / nmine, i = nrs % nmine;
+    for (; g < total; ++g) {
+      if (!mk_wait(&rempty[g & (nrs - 1)], static_cast<uint32_t>(((g >> lgr) - 1) & 1), A))
+        break;
+      issue_raw(g, kk, i);
+      if (++i == nmine) {
+        i = 0;
+        ++kk;
+      }
     }
     // After a timeout, let the copies already issued land before the CTA exits (at
     // once otherwise: each of these phases has been consumed).
-    for (int j = max(0, min(i, nmine) - nrs); j < min(i, nmine); ++j)
-      mk_wait(&rfull[j % nrs], static_cast<uint32_t>((j / nrs) & 1), A);
+    for (int j = max(0, min(g, total) - nrs); j < min(g, total); ++j)
+      mk_wait(&rfull[j & (nrs - 1)], static_cast<uint32_t>((j >> lgr) & 1), A);
   }
 
   tmem_fence_before();
@@ -532,6 +599,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 __global__ void sv_markov_finish_kernel(const MarkovArgs A) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= A.B) return;
+  if (b == 0) A.hdr->mk_pos = 0;  // the position barrier's counter, for the next call
   const int y0 = __ldg(A.prev + b);
   const bool ok = y0 >= 0 && y0 < A.V;
   if (!ok) atomicOr(&A.hdr->status, ST_DEVICE_INPUT);
@@ -608,18 +676,34 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  MarkovArgs A{L, U, Vm, prev, out, keys, tok, hdr, B, K, V, r, 0};
+  MarkovArgs A{L, U, Vm, prev, out, keys, tok, hdr, B, K, V, r, 0, K};
   const int ntiles = (V + MK_N - 1) / MK_N;
   const dim3 grid(static_cast<unsigned>(ntiles < sms ? ntiles : sms),
                   static_cast<unsigned>((B + MK_M - 1) / MK_M));
-  for (int k = 0; k < K; ++k) {
+  const size_t smem = markov_smem_bytes(r);
+  // One group of requests (B <= 128): all K positions in one cooperative launch (its
+  // CTAs, one per SM, meet at a grid barrier between positions). Otherwise one launch
+  // per position.
+  int coop = 0;
+  if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
+    return e;
+  const bool loop = grid.y == 1 && coop != 0;
+  for (int k = 0; k < K; k = A.kend) {
     A.k = k;
-    const size_t smem = markov_smem_bytes(r);
-    if (ring)
-      sv_markov_step_kernel<true><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
-    else
-      sv_markov_step_kernel<false><<<grid, MK_THREADS, smem, st>>>(A, tm, tl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    A.kend = loop ? K : k + 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(MK_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = loop ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = ring ? cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<true>, A, tm, tl)
+             : cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<false>, A, tm, tl);
+    if (e != cudaSuccess) return e;
   }
   sv_markov_finish_kernel<<<(B + 127) / 128, 128, 0, st>>>(A);
   return cudaGetLastError();

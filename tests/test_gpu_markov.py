@@ -82,7 +82,7 @@ def _compare(inp, got_corr, got_tok):
 
 
 CASES = [(1, 1, 1000, 16), (3, 4, 1003, 128), (64, 4, 4096, 256), (65, 2, 2048, 64),
-         (16, 8, 777, 32), (130, 1, 512, 256), (8, 3, 2048, 192)]
+         (16, 8, 777, 32), (130, 1, 512, 256), (8, 3, 2048, 192), (130, 3, 1000, 64)]
 
 
 @needs_cuda
