@@ -660,7 +660,9 @@ def run_markov(args):
                           "gbs": nbytes / (us / 1e6) / 1e9,
                           "frac_hbm": nbytes / (us / 1e6) / 1e9 / peak,
                           "tflops": flops / (us / 1e6) / 1e12,
-                          "timing": "median of 20 in-graph call events (K+2 launches each)"}),
+                          "timing": "median of 20 in-graph call events (a memset, one "
+                                    "launch for the K positions at B <= 128, one token "
+                                    "launch)"}),
               flush=True)
 
 
