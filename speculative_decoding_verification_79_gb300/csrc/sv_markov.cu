@@ -470,53 +470,58 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&aempty[a]);
         if (full) {
-            // Pairs of values: one packed fp32x2 add, one rounding to bf16x2 (round to
-            // nearest even, as the per-value path), then the tile's maximum by packed
-            // NaN-propagating max. Only a tile whose maximum beats the running best looks
-            // for its first index; a tile with a NaN takes the per-value rule.
-            uint32_t hp[16];
-  #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-  #pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const int e = j * 8 + e2 * 2;  // elements e (low half) and e + 1 (high half)
-                float2 z;
-                asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-                    "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-                    "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-                    : "=f"(z.x), "=f"(z.y)
-                    : "f"(bf_lo(wv[e2])), "f"(bf_hi(wv[e2])), "f"(acc[e]), "f"(acc[e + 1]));
-                const __nv_bfloat162 o = __floats2bfloat162_rn(z.x, z.y);
-                hp[j * 4 + e2] = *reinterpret_cast<const uint32_t*>(&o);
-              }
-              __stcs(reinterpret_cast<uint4*>(Orow + vq) + j,
-                     make_uint4(hp[j * 4], hp[j * 4 + 1], hp[j * 4 + 2], hp[j * 4 + 3]));
+          // Pairs of values: one packed fp32x2 add, one rounding to bf16x2 (round to
+          // nearest even, as the per-value path), then the tile's maximum by packed
+          // NaN-propagating max. Only a tile whose maximum beats the running best looks
+          // for its first index; a tile with a NaN takes the per-value rule.
+          uint32_t hp[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = j * 8 + e2 * 2;  // elements e (low half) and e + 1 (high half)
+              float2 z;
+              asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+                  "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+                  "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+                  : "=f"(z.x), "=f"(z.y)
+                  : "f"(bf_lo(wv[e2])), "f"(bf_hi(wv[e2])), "f"(acc[e]), "f"(acc[e + 1]));
+              const __nv_bfloat162 o = __floats2bfloat162_rn(z.x, z.y);
+              hp[j * 4 + e2] = *reinterpret_cast<const uint32_t*>(&o);
             }
-            __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&hp[0]);
-  #pragma unroll
-            for (int t = 1; t < 16; ++t)
-              m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&hp[t]));
-            const __nv_bfloat16 m = __hmax_nan(m2.x, m2.y);
-            if (__hisnan(m)) {
-  #pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                see(static_cast<uint16_t>(hp[t] & 0xffffu), vq + 2 * t);
-                see(static_cast<uint16_t>(hp[t] >> 16), vq + 2 * t + 1);
-              }
-            } else {
-              const uint32_t c = bf_order(__bfloat16_as_ushort(m)) + 1u;
-              if (c > best) {  // the first column holding the maximum (-0 counts as +0)
-                int e = 31;
-  #pragma unroll
-                for (int t = 15; t >= 0; --t) {
-                  if (bf_order(static_cast<uint16_t>(hp[t] >> 16)) + 1u == c) e = 2 * t + 1;
-                  if (bf_order(static_cast<uint16_t>(hp[t] & 0xffffu)) + 1u == c) e = 2 * t;
-                }
-                best = c;
-                best_v = vq + e;
-              }
+            __stcs(reinterpret_cast<uint4*>(Orow + vq) + j,
+                   make_uint4(hp[j * 4], hp[j * 4 + 1], hp[j * 4 + 2], hp[j * 4 + 3]));
+          }
+          // A tree of depth four over the 16 packed pairs (a chain would be 15 deep).
+          __nv_bfloat162 mt[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            mt[t] = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&hp[2 * t]),
+                                *reinterpret_cast<const __nv_bfloat162*>(&hp[2 * t + 1]));
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mt[t] = __hmax2_nan(mt[2 * t], mt[2 * t + 1]);
+          mt[0] = __hmax2_nan(__hmax2_nan(mt[0], mt[1]), __hmax2_nan(mt[2], mt[3]));
+          const __nv_bfloat16 m = __hmax_nan(mt[0].x, mt[0].y);
+          if (__hisnan(m)) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              see(static_cast<uint16_t>(hp[t] & 0xffffu), vq + 2 * t);
+              see(static_cast<uint16_t>(hp[t] >> 16), vq + 2 * t + 1);
             }
+          } else {
+            const uint32_t c = bf_order(__bfloat16_as_ushort(m)) + 1u;
+            if (c > best) {  // the first column holding the maximum (-0 counts as +0)
+              int e = 31;
+#pragma unroll
+              for (int t = 15; t >= 0; --t) {
+                if (bf_order(static_cast<uint16_t>(hp[t] >> 16)) + 1u == c) e = 2 * t + 1;
+                if (bf_order(static_cast<uint16_t>(hp[t] & 0xffffu)) + 1u == c) e = 2 * t;
+              }
+              best = c;
+              best_v = vq + e;
+            }
+          }
         } else if (live) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
