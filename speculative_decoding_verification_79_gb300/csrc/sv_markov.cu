@@ -48,18 +48,20 @@
 namespace sv {
 
 constexpr int MK_M = 128;        // requests per group (UMMA M; rows past the batch are zero)
-constexpr int MK_N = 64;         // vocabulary rows per tile (UMMA N)
+constexpr int MK_N = 128;        // vocabulary rows per tile (UMMA N)
 constexpr int MK_KB = 64;        // K elements per 128-byte swizzle block
 constexpr int MK_EPI_WARPS = 8;  // epilogue warps: two per TMEM lane group, half a tile each
 // and a U TMA warp, an MMA warp and a raw-logit TMA warp
 constexpr int MK_THREADS = 32 * (3 + MK_EPI_WARPS);
 constexpr int MK_XBLK = MK_M * 128;      // one block of X: 128 rows x 128 bytes
-constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 64 rows x 128 bytes
-constexpr int MK_RING = 4;               // U tiles in flight
+constexpr int MK_UBLK = MK_N * 128;      // one block of a U tile: 128 rows x 128 bytes
+constexpr int MK_RING = 4;               // most U tiles in flight
 constexpr int MK_ACC = 4;                    // accumulator stages in TMEM
 constexpr uint32_t MK_TMEM_COLS = MK_ACC * MK_N;
 constexpr int MK_RAWBOX = 64 * 128;  // raw logits of 64 requests x 64 columns (bf16)
 constexpr int MK_RSTAGES = 8;        // most raw-logit stages
+// U buffers: four at r <= 128, two above (shared memory).
+__host__ __device__ constexpr int mk_uring(int nkb) { return nkb <= 2 ? 4 : 2; }
 // Bytes of the raw-logit ring: 64 KB, or at r > 192 the 32 KB that the 227 KB of
 // shared memory leave next to X, the U ring, alignment and static variables.
 __host__ __device__ constexpr int mk_raw_bytes(int nkb) { return nkb <= 3 ? 65536 : 32768; }
@@ -222,7 +224,7 @@ __device__ __forceinline__ int prev_token(const MarkovArgs& A, int kk, int b) {
 size_t markov_smem_bytes(int r) {
   const int nkb = (r + MK_KB - 1) / MK_KB;
   const size_t need =
-      1024 + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK) + (size_t)mk_raw_bytes(nkb);
+      1024 + (size_t)nkb * (MK_XBLK + mk_uring(nkb) * MK_UBLK) + (size_t)mk_raw_bytes(nkb);
   return need > (size_t)116 * 1024 ? need : (size_t)116 * 1024;
 }
 
@@ -234,7 +236,7 @@ size_t markov_smem_bytes(int r) {
 // the previous position's argmax and gather the next X, while U and the raw logits of
 // the next position keep streaming into their rings. Every (position, tile) pair of the
 // CTA has one running index g, which the rings and accumulator stages follow.
-template <bool RING>
+template <bool RING, int NUR>
 __global__ void __launch_bounds__(MK_THREADS, 1)
     sv_markov_step_kernel(const MarkovArgs A, const __grid_constant__ CUtensorMap tmU,
                           const __grid_constant__ CUtensorMap tmL) {
@@ -272,25 +274,30 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   // c ^ (j & 7), so that the epilogue's reads of 32 rows spread over all banks. The
   // number of stages is a power of two (2, 4 or 8).
   constexpr bool rt = RING;
-  const int rsb = dup ? MK_RAWBOX : 2 * MK_RAWBOX;
+  constexpr int LGU = NUR == 4 ? 2 : 1;  // log2 of the U buffers
+  static_assert(NUR == 2 || NUR == 4, "U ring");
+  const int nbox = dup ? 1 : 2;          // 64-request blocks of a raw stage
+  const int rsb = nbox * 2 * MK_RAWBOX;  // and two 64-column halves
   const int nrs = min(MK_RSTAGES, mk_raw_bytes(nkb) / rsb);
   const int lgr = 31 - __clz(nrs);
-  unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + MK_RING * MK_UBLK);
+  unsigned char* rawq = dsm + (size_t)nkb * (MK_XBLK + NUR * MK_UBLK);
   constexpr int RAW_W = 2 + MK_EPI_WARPS;  // the raw-logit copy warp
   constexpr int EPI0 = 64;                 // first thread of the epilogue warps
   // Pair g (position kk, tile i)'s raw logits into stage g % nrs (one thread): boxes of
-  // 64 requests x 1 position x 64 columns.
+  // 64 requests x 1 position x 64 columns, box (hb, ch) at (2 hb + ch) x 8 KB for request
+  // block hb and column half ch.
   auto issue_raw = [&](int g, int kk, int i) {
     const int q = g & (nrs - 1);
     const int v0 = (blockIdx.x + i * gridDim.x) * MK_N;
     const uint64_t once = policy_evict_first();
     mbar_arrive_expect_tx(&rfull[q], static_cast<uint32_t>(rsb));
-    for (int h = 0; h * MK_RAWBOX < rsb; ++h)
-      tma_load_3d(rawq + (size_t)q * rsb + h * MK_RAWBOX, &tmL, v0, kk, g0 + 64 * h, &rfull[q],
-                  once);
+    for (int hb = 0; hb < nbox; ++hb)
+      for (int ch = 0; ch < 2; ++ch)
+        tma_load_3d(rawq + (size_t)q * rsb + (size_t)(2 * hb + ch) * MK_RAWBOX, &tmL,
+                    v0 + 64 * ch, kk, g0 + 64 * hb, &rfull[q], once);
   };
-  auto issue_u = [&](int g, int i) {  // U tile i into buffer g % MK_RING (one thread)
-    const int q = g & (MK_RING - 1);
+  auto issue_u = [&](int g, int i) {  // U tile i into buffer g % NUR (one thread)
+    const int q = g & (NUR - 1);
     const uint64_t keep = policy_evict_last();  // U is read again at every position
     mbar_arrive_expect_tx(&ufull[q], tile_bytes);
     const int t = blockIdx.x + i * gridDim.x;
@@ -323,24 +330,24 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   };
 
   if (tid == 0) {
-    for (int q = 0; q < MK_RING; ++q) {
+    for (int q = 0; q < NUR; ++q) {
       mbar_init(&ufull[q], 1);
       mbar_init(&uempty[q], 1);
     }
     for (int q = 0; q < MK_ACC; ++q) {
       mbar_init(&afull[q], 1);
-      mbar_init(&aempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
+      mbar_init(&aempty[q], MK_EPI_WARPS);
     }
     for (int q = 0; q < nrs; ++q) {
       mbar_init(&rfull[q], 1);
-      mbar_init(&rempty[q], dup ? MK_EPI_WARPS / 2 : MK_EPI_WARPS);
+      mbar_init(&rempty[q], MK_EPI_WARPS);
     }
     mbar_init(&xfull, 1);
     s_abort = 0;
     fence_mbar_init();
     // U does not depend on X: the first tiles of the ring start landing while X is
     // gathered (this thread is the TMA producer).
-    for (int g = 0; g < MK_RING && g < total; ++g) issue_u(g, g % nmine);
+    for (int g = 0; g < NUR && g < total; ++g) issue_u(g, g % nmine);
   }
   if (tid < MK_M) set_yrow(A.k, tid);  // one read of each request's previous token
   if (w == 0) {
@@ -366,16 +373,16 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   if (w == 0) {
     // U producer (lane 0): pair g's tile once its buffer's previous product is done.
     if (lane == 0) {
-      int g = MK_RING, i = MK_RING % max(nmine, 1);
+      int g = NUR, i = NUR % max(nmine, 1);
       for (; g < total; ++g) {
-        if (!mk_wait(&uempty[g & (MK_RING - 1)], static_cast<uint32_t>(((g >> 2) - 1) & 1), A))
+        if (!mk_wait(&uempty[g & (NUR - 1)], static_cast<uint32_t>(((g >> LGU) - 1) & 1), A))
           break;
         issue_u(g, i);
         if (++i == nmine) i = 0;
       }
       // After a timeout, let the copies already issued land before the CTA exits.
-      for (int j = max(0, min(g, total) - MK_RING); j < min(g, total); ++j)
-        mk_wait(&ufull[j & (MK_RING - 1)], static_cast<uint32_t>((j >> 2) & 1), A);
+      for (int j = max(0, min(g, total) - NUR); j < min(g, total); ++j)
+        mk_wait(&ufull[j & (NUR - 1)], static_cast<uint32_t>((j >> LGU) & 1), A);
     }
   } else if (w == 1) {
     // MMA issuer (lane 0): pair g's product into accumulator g % MK_ACC once its U tile
@@ -386,17 +393,17 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
       const int nk = r / 16;
       int i = 0, pos = 0;
       for (int g = 0; g < total; ++g) {
-        const int q = g & (MK_RING - 1), a = g & (MK_ACC - 1);
+        const int q = g & (NUR - 1), a = g & (MK_ACC - 1);
         if (i == 0 && pos > 0 && !mk_wait(&xfull, static_cast<uint32_t>((pos - 1) & 1), A)) break;
-        if (!mk_wait(&ufull[q], static_cast<uint32_t>((g >> 2) & 1), A)) break;
+        if (!mk_wait(&ufull[q], static_cast<uint32_t>((g >> LGU) & 1), A)) break;
         if (g >= MK_ACC && !mk_wait(&aempty[a], static_cast<uint32_t>(((g >> 2) - 1) & 1), A))
           break;
         tmem_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(a * MK_N);
         const uint64_t bd = sw128_desc(ubuf(q));
         for (int kk = 0; kk < nk; ++kk) {
-          // 16 elements = 32 bytes along K inside a 128-byte block; X's blocks are 16 KB
-          // apart, the U tile's 8 KB.
+          // 16 elements = 32 bytes along K inside a 128-byte block; X's blocks and the U
+          // tile's are 16 KB apart.
           const uint64_t sub = static_cast<uint64_t>((kk & 3) * 2);
           umma_bf16(d, ad + static_cast<uint64_t>((kk >> 2) * (MK_XBLK >> 4)) + sub,
                     bd + static_cast<uint64_t>((kk >> 2) * (MK_UBLK >> 4)) + sub, kk > 0 ? 1u : 0u);
@@ -411,13 +418,16 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     }
   } else if (w < 2 + MK_EPI_WARPS) {
     // Epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. request g0 + m,
-    // m = 32 (w % 4) + lane, and columns 32 h .. 32 h + 31 of each tile (h: which of the
-    // two warps of its lane group).
+    // m = 32 (w % 4) + lane, of every tile, in chunks of 32 columns: with the group
+    // doubled (rows 64..127 repeat 0..63) quadrants 0-1 take columns 0..63 and 2-3
+    // columns 64..127, 32 per warp; otherwise each warp takes 64 columns, as two chunks.
     const int m = 32 * (w & 3) + lane;        // TMEM lane (row of the product)
-    // With the group doubled, quadrants 0-1 take even pairs g and 2-3 odd ones.
-    const int par = dup ? ((w & 3) >> 1) : 0;
     const int mreq = dup ? (m & (MK_M / 2 - 1)) : m;
-    const int h = (w - 2) >> 2;
+    const int h = (w - 2) >> 2;               // which of the two warps of its lane group
+    const int nsub = dup ? 1 : 2;
+    const int cbase = dup ? 64 * ((w & 3) >> 1) + 32 * h : 64 * h;
+    const int rr = mreq & 63;                 // row of the request in its raw box
+    const int hb = dup ? 0 : (mreq >> 6);     // its request block
     const size_t KV = (size_t)A.K * V;
     const int b = g0 + mreq;
     const bool live = mreq < nb;
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         }
       };
       for (int i = 0; i < nmine; ++i, ++g) {
-        if ((dup && (g & 1) != par) || dead) continue;
+        if (dead) continue;
         const int a = g & (MK_ACC - 1), q = g & (nrs - 1);
         bool ok = true;
         if (lane == 0) ok = mk_wait(&afull[a], static_cast<uint32_t>((g >> 2) & 1), A);
@@ -449,26 +459,33 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
           continue;
         }
         tmem_fence_after();
-        const int vq = (blockIdx.x + i * gridDim.x) * MK_N + 32 * h;
+        for (int sb = 0; sb < nsub; ++sb) {
+        const int c0 = cbase + 32 * sb;  // the chunk's first column in the tile
+        const int vq = (blockIdx.x + i * gridDim.x) * MK_N + c0;
         const bool full = rt && live && vq + 32 <= V;
-        // This warp's 32 columns of the request's row in the stage: 16-byte chunks
-        // 4h .. 4h + 3 of row mreq, placed by the 128-byte swizzle.
+        // The chunk's 32 columns of the request's row in the stage: 16-byte chunks
+        // 4 ((c0 / 32) % 2) .. + 3 of row rr of box (hb, c0 / 64), placed by the 128-byte
+        // swizzle.
         uint4 raw[4];
         if (rt) {
-          const unsigned char* rp = rawq + (size_t)q * rsb + mreq * 128;
+          const unsigned char* rp =
+              rawq + (size_t)q * rsb + (size_t)(2 * hb + (c0 >> 6)) * MK_RAWBOX + rr * 128;
+          const int c4 = 4 * ((c0 >> 5) & 1);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            raw[j] = *reinterpret_cast<const uint4*>(rp + (((4 * h + j) ^ (mreq & 7)) << 4));
+            raw[j] = *reinterpret_cast<const uint4*>(rp + (((c4 + j) ^ (rr & 7)) << 4));
         }
         const uint32_t tcol = tmem + ((static_cast<uint32_t>(32 * (w & 3))) << 16) +
-                              static_cast<uint32_t>(a * MK_N + 32 * h);
+                              static_cast<uint32_t>(a * MK_N + c0);
         float acc[32];
         tmem_ld32(tcol, acc);
-        // The accumulator is in registers (tcgen05.wait::ld): release it to the MMA
-        // issuer.
-        tmem_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&aempty[a]);
+        if (sb == nsub - 1) {
+          // The accumulator is in registers (tcgen05.wait::ld): release it to the MMA
+          // issuer.
+          tmem_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&aempty[a]);
+        }
         if (full) {
           // Pairs of values: one packed fp32x2 add, one rounding to bf16x2 (round to
           // nearest even, as the per-value path), then the tile's maximum by packed
@@ -532,6 +549,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
             see(hv, vq + e);
           }
         }
+        }  // chunk
         // The raw-logit stage is released only once every lane has used its values: a
         // load whose result is still pending does not hold the stage, and a refill
         // issued on an earlier release could overwrite it before it is read.
@@ -637,11 +655,13 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
   static bool attr_set = false;
   if (!attr_set) {
     const int smax = (int)markov_smem_bytes(SV_MAX_MARKOV_R);
-    cudaError_t e = cudaFuncSetAttribute(sv_markov_step_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sv_markov_step_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+    const void* ks[4] = {reinterpret_cast<const void*>(sv_markov_step_kernel<false, 2>),
+                         reinterpret_cast<const void*>(sv_markov_step_kernel<false, 4>),
+                         reinterpret_cast<const void*>(sv_markov_step_kernel<true, 2>),
+                         reinterpret_cast<const void*>(sv_markov_step_kernel<true, 4>)};
+    cudaError_t e = cudaSuccess;
+    for (int j = 0; j < 4 && e == cudaSuccess; ++j)
+      e = cudaFuncSetAttribute(ks[j], cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -652,7 +672,7 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
   CUtensorMap tm;
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(r) * 2};
-  const cuuint32_t box[2] = {MK_KB, MK_N};  // 64 columns (128 bytes) x 64 rows
+  const cuuint32_t box[2] = {MK_KB, MK_N};  // 64 columns (128 bytes) x 128 rows
   const cuuint32_t estr[2] = {1, 1};
   if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(U), gdim, gstride, box,
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -669,7 +689,7 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t lstride[2] = {static_cast<cuuint64_t>(V) * 2,
                                    static_cast<cuuint64_t>(K) * static_cast<cuuint64_t>(V) * 2};
-    const cuuint32_t lbox[3] = {MK_N, 1, 64};
+    const cuuint32_t lbox[3] = {64, 1, 64};
     const cuuint32_t lestr[3] = {1, 1, 1};
     if (enc(&tl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(L), ldim, lstride,
             lbox, lestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -706,8 +726,11 @@ cudaError_t launch_markov(const uint16_t* L, const uint16_t* U, const uint16_t* 
     attr[0].val.cooperative = loop ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = ring ? cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<true>, A, tm, tl)
-             : cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<false>, A, tm, tl);
+    const bool u4 = mk_uring((r + MK_KB - 1) / MK_KB) == 4;
+    e = ring ? (u4 ? cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<true, 4>, A, tm, tl)
+                   : cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<true, 2>, A, tm, tl))
+             : (u4 ? cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<false, 4>, A, tm, tl)
+                   : cudaLaunchKernelEx(&cfg, sv_markov_step_kernel<false, 2>, A, tm, tl));
     if (e != cudaSuccess) return e;
   }
   sv_markov_finish_kernel<<<(B + 127) / 128, 128, 0, st>>>(A);
