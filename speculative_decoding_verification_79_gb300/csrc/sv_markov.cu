@@ -7,31 +7,30 @@
 // and the next token is drafted from L'_k (greedy here: the lowest-index argmax, as
 // in the page's sketch), so the positions run one after another.
 //
-// One launch per position. For a group of up to 128 requests the correction is the
-// product D = X U^T, X [128, r] the gathered rows Vm[y_b, :] (zero past the batch),
-// U [V, r]: a dense contraction on the fifth-generation tensor cores. A persistent CTA
-// per SM (and request group) gathers X once into shared memory in the canonical
-// K-major 128-byte-swizzled layout, then walks its vocabulary tiles of 64 rows with
-// three roles coupled only by mbarriers (a TMA warp, an MMA warp, eight epilogue warps):
-//  - U tiles of 64 rows come by 2-D tensor-map TMA (cp.async.bulk.tensor, 128-byte
-//    swizzle, one box of 64 rows x 64 columns per 64 of r; rows past V and columns past
-//    r are filled with zeros) into a ring of four shared-memory buffers, so three
-//    copies run ahead of the tile being multiplied;
+// For a group of up to 128 requests the correction is the product D = X U^T, X [128, r]
+// the gathered rows Vm[y_b, :] (zero past the batch), U [V, r]: a dense contraction on
+// the fifth-generation tensor cores. A persistent CTA per SM (and request group) gathers
+// X into shared memory in the canonical K-major 128-byte-swizzled layout, then walks its
+// vocabulary tiles of 128 rows with four roles coupled only by mbarriers:
+//  - one thread streams U tiles by 2-D tensor-map TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle, one box of 128 rows x 64 columns per 64 of r; rows past V and columns past
+//    r are filled with zeros) into a ring of four buffers (two at r > 128);
+//  - one thread copies the raw logits of each tile (the group's rows x 128 columns) by
+//    3-D tensor-map TMA into a second ring of stages, so that each SM keeps 32-64 KB of
+//    them in flight (loads held in registers one tile ahead kept only ~16 KB in flight
+//    and left the epilogue waiting on HBM latency); a stage is released only after its
+//    values have been used;
 //  - one thread issues the tile's tcgen05.mma (kind::f16, bf16 inputs, M = 128 requests,
-//    N = 64 vocabulary rows, K = 16 each) into one of four TMEM accumulators of 64 fp32
-//    columns and commits them to an mbarrier;
-//  - while the next tile multiplies, eight epilogue warps read the previous accumulator
-//    with tcgen05.ld (two warps per group of 32 TMEM lanes, 32 columns each: a thread
-//    holds 32 consecutive values of one request), add the raw logits, round once to
-//    bf16, store, and keep the request's running maximum and its first index;
-//  - a fourth role, one thread, copies the raw logits of each tile (the group's rows x 64
-//    columns) by 3-D tensor-map TMA into a second ring of stages, so that each SM keeps
-//    32-64 KB of them in flight (loads held in registers one tile ahead kept only
-//    ~16 KB in flight and left the epilogue waiting on HBM latency). A stage is released
-//    only after its values have been used.
-// A group of at most 64 requests
-//    fills X twice (rows 64..127 repeat rows 0..63), so that all four lane groups hold
-//    its products and the warps of lane groups 0-1 and 2-3 take alternate tiles.
+//    N = 128 vocabulary rows, K = 16 each) into one of four TMEM accumulators of 128 fp32
+//    columns (all 512) and commits them to mbarriers;
+//  - while the next tile multiplies, eight epilogue warps read the accumulator with
+//    tcgen05.ld (a thread holds 32 consecutive values of one request), add the raw
+//    logits, round once to bf16, store, and keep the request's running maximum and its
+//    first index. A group of at most 64 requests fills X twice (rows 64..127 repeat rows
+//    0..63), so that all four TMEM lane groups hold its products: lane groups 0-1 take
+//    the tile's columns 0..63 and 2-3 columns 64..127, 32 per warp.
+// At B <= 128 one cooperative launch runs all K positions, with a grid barrier between
+// positions (see the kernel); otherwise one launch per position.
 // key = (order-preserving bits of the bf16 value) << 32 | (0xffffffff - v): the largest
 // value wins and, among equal values, the lowest index. Each CTA ends with one
 // atomicMax per request; max is order-free, so results do not depend on scheduling.
