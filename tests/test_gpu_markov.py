@@ -134,3 +134,31 @@ def test_markov_deterministic(sv):
     a = sv.sv_markov_draft(d["logits"], d["U"], d["Vm"], d["prev"], ws)
     b = sv.sv_markov_draft(d["logits"], d["U"], d["Vm"], d["prev"], ws)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@needs_cuda
+def test_markov_shared_workspace_across_calls(sv):
+    """One workspace for calls of different shapes in a row: at most 128 requests all
+    positions run in one launch whose CTAs meet at a grid barrier counted in the
+    workspace header, and every call must leave that count at zero for the next (also
+    after a call that takes one launch per position, or reports invalid input)."""
+    ws = sv.Workspace(256, 8, 16)
+    shapes = [(8, 3, 2048, 64, 11), (64, 4, 4096, 128, 12), (130, 2, 1024, 64, 13),
+              (3, 5, 1000, 32, 14), (64, 4, 4096, 128, 12)]
+    for B, K, V, r, seed in shapes:
+        inp = synth.markov_inputs(B, K, V, r, seed=seed)
+        d = {k: v.cuda() for k, v in inp.items()}
+        corr, tok = sv.sv_markov_draft(d["logits"], d["U"], d["Vm"], d["prev"], ws)
+        assert ws.status(clear=True) == sv.SV_OK, (B, K, V, r)
+        _compare(inp, _bits(corr.cpu()), tok.cpu().numpy())
+    # A call with an invalid previous token reports it; the next call is unaffected.
+    inp = synth.markov_inputs(5, 3, 600, 64, seed=2)
+    inp["prev"][1] = -3
+    d = {k: v.cuda() for k, v in inp.items()}
+    sv.sv_markov_draft(d["logits"], d["U"], d["Vm"], d["prev"], ws)
+    assert ws.status(clear=True) == sv.SV_ERR_DEVICE_INPUT
+    inp = synth.markov_inputs(16, 6, 2048, 128, seed=15)
+    d = {k: v.cuda() for k, v in inp.items()}
+    corr, tok = sv.sv_markov_draft(d["logits"], d["U"], d["Vm"], d["prev"], ws)
+    assert ws.status(clear=True) == sv.SV_OK
+    _compare(inp, _bits(corr.cpu()), tok.cpu().numpy())
