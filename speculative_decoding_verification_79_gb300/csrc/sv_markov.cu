@@ -262,16 +262,16 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const uint32_t tile_bytes = static_cast<uint32_t>(nkb) * MK_UBLK;
   // A group of at most 64 requests is multiplied twice (rows 64..127 of X repeat rows
   // 0..63), so that the epilogue warps of all four TMEM lane quadrants hold its products
-  // and the two halves take alternate tiles.
+  // and the two halves take the two column halves of every tile.
   const bool dup = nb <= MK_M / 2;
   int nmine = 0;  // tiles of this CTA per position: blockIdx.x, blockIdx.x + gridDim.x, ...
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) ++nmine;
   const int npos = A.kend - A.k;
   const int total = npos * nmine;  // (position, tile) pairs, position-major
-  // Raw-logit stages: 64 rows of 128 bytes (64 requests x 64 columns) per tile, twice
-  // that for a group of more; the 128-byte swizzle puts row j's 16-byte chunk c at chunk
-  // c ^ (j & 7), so that the epilogue's reads of 32 rows spread over all banks. The
-  // number of stages is a power of two (2, 4 or 8).
+  // Raw-logit stages: per 64 requests two boxes of 64 rows x 128 bytes (the tile's two
+  // 64-column halves), twice that for a group of more; the 128-byte swizzle puts row j's
+  // 16-byte chunk c at chunk c ^ (j & 7), so that the epilogue's reads of 32 rows spread
+  // over all banks. The number of stages is a power of two (1, 2 or 4).
   constexpr bool rt = RING;
   constexpr int LGU = NUR == 4 ? 2 : 1;  // log2 of the U buffers
   static_assert(NUR == 2 || NUR == 4, "U ring");
